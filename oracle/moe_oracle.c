@@ -1,0 +1,242 @@
+/*
+ * Reference oracle for the int4 routed-MoE FFN step -- TEST INFRASTRUCTURE.
+ * Plain double-precision C; see moe_oracle.h for the sources each step
+ * follows.  Nothing here is blocked, fused or reordered beyond the plain
+ * definitions; OpenMP (when enabled) only splits independent output rows.
+ */
+#include "moe_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int oracle_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Section 06: element 2j is the low nibble of byte j, 2j+1 the high nibble;
+ * the stored nibble is q + 8. */
+static int nibble_at(const uint8_t *row, int i) {
+    uint8_t b = row[i >> 1];
+    int v = (i & 1) ? (b >> 4) : (b & 15);
+    return v - 8;
+}
+
+void oracle_unpack_int4(const uint8_t *row, int n, int *q) {
+    for (int i = 0; i < n; i++) q[i] = nibble_at(row, i);
+}
+
+/* Section 06 quantiser: per row amax, s = max(amax/7, 1e-8),
+ * q = clip(rint(w/s), -8, 7), pad value 0 (stored 8).  float32 as printed. */
+void oracle_quantize_int4(const float *w, int O, int I, uint8_t *q4, float *scale) {
+    const int qmax = 7, rb = (I + 1) / 2;
+    for (int o = 0; o < O; o++) {
+        const float *wr = w + (int64_t)o * I;
+        float amax = 0.f;
+        for (int i = 0; i < I; i++) {
+            float a = fabsf(wr[i]);
+            if (a > amax) amax = a;
+        }
+        float s = amax / (float)qmax;
+        if (s < 1e-8f) s = 1e-8f;
+        scale[o] = s;
+        uint8_t *qr = q4 + (int64_t)o * rb;
+        for (int j = 0; j < rb; j++) {
+            int v[2] = {0, 0};
+            for (int h = 0; h < 2; h++) {
+                int i = 2 * j + h;
+                if (i >= I) break;
+                long r = lrintf(wr[i] / s);   /* round half to even */
+                if (r > qmax) r = qmax;
+                if (r < -8) r = -8;
+                v[h] = (int)r;
+            }
+            qr[j] = (uint8_t)((v[0] + 8) | ((v[1] + 8) << 4));
+        }
+    }
+}
+
+double oracle_silu(double v) { return v / (1.0 + exp(-v)); }
+
+/* Section 04 RMSNorm with unit weight. */
+void oracle_rmsnorm(const double *x, int H, double eps, double *out) {
+    double ms = 0.0;
+    for (int i = 0; i < H; i++) ms += x[i] * x[i];
+    double r = 1.0 / sqrt(ms / H + eps);
+    for (int i = 0; i < H; i++) out[i] = x[i] * r;
+}
+
+/* out[o] = scale[o] * sum_i q[o,i] * v[i] over one packed [O, ceil(n/2)] matrix. */
+static void int4_matvec(const uint8_t *q4, const float *scale, int O, int n,
+                        const double *v, double *out) {
+    const int rb = (n + 1) / 2;
+#pragma omp parallel for schedule(static)
+    for (int o = 0; o < O; o++) {
+        const uint8_t *row = q4 + (int64_t)o * rb;
+        double acc = 0.0;
+        for (int i = 0; i < n; i++) acc += (double)nibble_at(row, i) * v[i];
+        out[o] = (double)scale[o] * acc;
+    }
+}
+
+/* Section 11 expert: g = W_g x, u = W_u x, h = silu(g) * u, d = W_d h. */
+void oracle_expert(int H, int I, const uint8_t *slab, const float *scale,
+                   const double *x, double *d_out, double *h_out) {
+    const int64_t rbH = (H + 1) / 2;
+    const uint8_t *qg = slab;
+    const uint8_t *qu = slab + (int64_t)I * rbH;
+    const uint8_t *qd = slab + 2 * (int64_t)I * rbH;
+    const float *sg = scale, *su = scale + I, *sd = scale + 2 * I;
+    double *g = (double *)malloc(sizeof(double) * I);
+    double *u = (double *)malloc(sizeof(double) * I);
+    double *h = (double *)malloc(sizeof(double) * I);
+    int4_matvec(qg, sg, I, H, x, g);
+    int4_matvec(qu, su, I, H, x, u);
+    for (int i = 0; i < I; i++) h[i] = oracle_silu(g[i]) * u[i];
+    int4_matvec(qd, sd, H, I, h, d_out);
+    if (h_out) memcpy(h_out, h, sizeof(double) * I);
+    free(g); free(u); free(h);
+}
+
+typedef struct { double c; int e; } scored;
+
+/* Order: larger selection score first; on equal scores the lower index first
+ * (what a strict '>' scan in ascending index order produces). */
+static int by_score_desc(const void *a, const void *b) {
+    const scored *p = (const scored *)a, *q = (const scored *)b;
+    if (p->c > q->c) return -1;
+    if (p->c < q->c) return 1;
+    return (p->e > q->e) - (p->e < q->e);
+}
+
+static int cfg_ok(const oracle_cfg *c) {
+    return c && c->H > 0 && c->E > 0 && c->K > 0 && c->K <= c->E && c->I > 0 &&
+           c->n_group == 1 && (c->n_shared == 0 || (c->n_shared == 1 && c->I_shared > 0));
+}
+
+static void router_scores(const oracle_cfg *c, const float *W, const float *b,
+                          const double *x, double *logit, double *sig, double *choice) {
+#pragma omp parallel for schedule(static)
+    for (int e = 0; e < c->E; e++) {
+        const float *wr = W + (int64_t)e * c->H;
+        double acc = 0.0;
+        for (int h = 0; h < c->H; h++) acc += (double)wr[h] * x[h];
+        logit[e] = acc;
+        sig[e] = 1.0 / (1.0 + exp(-acc));
+        choice[e] = sig[e] + (double)b[e];
+    }
+}
+
+static void weights_of(const oracle_cfg *c, const double *sig, const int *idx, double *w) {
+    double den = 0.0;
+    for (int k = 0; k < c->K; k++) den += sig[idx[k]];
+    den += 1e-20;
+    for (int k = 0; k < c->K; k++)
+        w[k] = c->norm_topk ? c->routed_scale * sig[idx[k]] / den
+                            : c->routed_scale * sig[idx[k]];
+}
+
+int oracle_route(const oracle_cfg *c, const float *router_w, const float *router_b,
+                 const double *x, int *idx, double *w, double *margin, double *scores) {
+    if (!cfg_ok(c)) return -1;
+    const int E = c->E, K = c->K;
+    double *logit = (double *)malloc(sizeof(double) * 3 * E);
+    double *sig = logit + E, *choice = logit + 2 * E;
+    router_scores(c, router_w, router_b, x, logit, sig, choice);
+    scored *s = (scored *)malloc(sizeof(scored) * E);
+    for (int e = 0; e < E; e++) { s[e].c = choice[e]; s[e].e = e; }
+    qsort(s, E, sizeof(scored), by_score_desc);
+    for (int k = 0; k < K; k++) idx[k] = s[k].e;
+    if (margin) *margin = (K < E) ? s[K - 1].c - s[K].c : INFINITY;
+    if (w) weights_of(c, sig, idx, w);
+    if (scores) memcpy(scores, logit, sizeof(double) * 3 * E);
+    free(s);
+    free(logit);
+    return 0;
+}
+
+int oracle_weights_for(const oracle_cfg *c, const float *router_w, const double *x,
+                       const int *idx, double *w) {
+    if (!cfg_ok(c)) return -1;
+    double *sig = (double *)malloc(sizeof(double) * c->E);
+    for (int e = 0; e < c->E; e++) {
+        const float *wr = router_w + (int64_t)e * c->H;
+        double acc = 0.0;
+        for (int h = 0; h < c->H; h++) acc += (double)wr[h] * x[h];
+        sig[e] = 1.0 / (1.0 + exp(-acc));
+    }
+    for (int k = 0; k < c->K; k++)
+        if (idx[k] < 0 || idx[k] >= c->E) { free(sig); return -1; }
+    weights_of(c, sig, idx, w);
+    free(sig);
+    return 0;
+}
+
+int oracle_moe_token(const oracle_cfg *c, const oracle_layer *L, const double *x,
+                     const int *forced_idx, double *y, int *idx_out, double *w_out,
+                     double *margin) {
+    if (!cfg_ok(c)) return -1;
+    const int H = c->H, K = c->K;
+    double *xin = (double *)malloc(sizeof(double) * H);
+    double *d = (double *)malloc(sizeof(double) * H);
+    double *acc = (double *)calloc(H, sizeof(double));
+    int *idx = (int *)malloc(sizeof(int) * K);
+    double *w = (double *)malloc(sizeof(double) * K);
+    int rc = 0;
+
+    if (c->prenorm_residual) oracle_rmsnorm(x, H, c->rms_eps, xin);
+    else memcpy(xin, x, sizeof(double) * H);
+
+    double mg = INFINITY;
+    if (forced_idx) {
+        memcpy(idx, forced_idx, sizeof(int) * K);
+        rc = oracle_weights_for(c, L->router_w, xin, idx, w);
+    } else {
+        rc = oracle_route(c, L->router_w, L->router_b, xin, idx, w, &mg, NULL);
+    }
+    if (rc == 0) {
+        /* routed experts in selection order, then the shared expert (weight 1) */
+        for (int k = 0; k < K && rc == 0; k++) {
+            const uint8_t *slab = L->slab[idx[k]];
+            const float *scale = L->scale[idx[k]];
+            if (!slab || !scale) { rc = -2; break; }
+            oracle_expert(H, c->I, slab, scale, xin, d, NULL);
+            for (int h = 0; h < H; h++) acc[h] += w[k] * d[h];
+        }
+        if (rc == 0 && c->n_shared) {
+            oracle_expert(H, c->I_shared, L->sh_slab, L->sh_scale, xin, d, NULL);
+            for (int h = 0; h < H; h++) acc[h] += d[h];
+        }
+        if (rc == 0) {
+            for (int h = 0; h < H; h++) y[h] = c->prenorm_residual ? x[h] + acc[h] : acc[h];
+            if (idx_out) memcpy(idx_out, idx, sizeof(int) * K);
+            if (w_out) memcpy(w_out, w, sizeof(double) * K);
+            if (margin) *margin = mg;
+        }
+    }
+    free(xin); free(d); free(acc); free(idx); free(w);
+    return rc;
+}
+
+int oracle_moe_forward(const oracle_cfg *c, const oracle_layer *L, const float *x, int T,
+                       double *y, int *idx, double *w, double *margin) {
+    if (!cfg_ok(c) || T < 0) return -1;
+    double *xd = (double *)malloc(sizeof(double) * c->H);
+    int rc = 0;
+    for (int t = 0; t < T && rc == 0; t++) {
+        for (int h = 0; h < c->H; h++) xd[h] = (double)x[(int64_t)t * c->H + h];
+        rc = oracle_moe_token(c, L, xd, NULL, y + (int64_t)t * c->H,
+                              idx ? idx + (int64_t)t * c->K : NULL,
+                              w ? w + (int64_t)t * c->K : NULL,
+                              margin ? margin + t : NULL);
+    }
+    free(xd);
+    return rc;
+}

@@ -1,0 +1,101 @@
+/*
+ * Reference oracle for the int4 routed-MoE FFN step -- TEST INFRASTRUCTURE.
+ *
+ * A plain, slow, double-precision CPU statement of what the step computes.
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg
+ * may load it; the GPU library never does, and the two share no code.
+ *
+ * Sources (page, section):
+ *  - "25GB 内存上运行 GLM 5.2 744B" (reader.mx), section 11 "MoE 路由与专家执行":
+ *    sigmoid(logit) + correction bias selects the top-K; the weight is the
+ *    un-biased sigmoid times routed_scale; greedy K-pass argmax, strict '>',
+ *    so the lowest index wins a tie; SwiGLU expert h = silu(g) * u, d = W_d h;
+ *    weighted accumulate of the expert outputs.
+ *  - same page, section 06 "从 FP8 到 int4": row-wise symmetric int4, qmax 7,
+ *    s = max(amax/7, 1e-8), q = clip(rint(w/s), -8, 7); stored q+8, element
+ *    2j in the low nibble, 2j+1 in the high nibble; row stride ceil(I/2)
+ *    bytes, pad nibble 8; one float32 scale per output row (".qs").
+ *  - same page, section 04 "手写的基础数学": RMSNorm and SiLU.
+ *  - Edge0 article (magicnetworld.com), section 七 "路由数学": renormalised
+ *    sigmoid weights w_i = s * sigma_i / (sum_{j in S} sigma_j + 1e-20).
+ *  - GLM-5.2 operator breakdown (devpress.csdn.net), section 2.3 and stage
+ *    "Step 6 (MoE)" 6a-6d: output = sum of routed outputs + shared expert.
+ *
+ * Every floating-point step is done in double, except the offline quantiser
+ * oracle_quantize_int4, which follows the page's float32 arithmetic because
+ * its output bytes are what the pages define.
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+    int H;            /* hidden size */
+    int E;            /* routed experts */
+    int K;            /* top-k */
+    int I;            /* routed expert intermediate size */
+    int n_shared;     /* 0 or 1 */
+    int I_shared;     /* shared expert intermediate size */
+    int n_group;      /* expert groups; only 1 is defined here */
+    int norm_topk;    /* 1: renormalise the selected sigmoid weights */
+    int prenorm_residual; /* 1: y = x + moe(rmsnorm(x)) */
+    double routed_scale;
+    double rms_eps;
+} oracle_cfg;
+
+typedef struct {
+    const float *router_w;            /* [E, H] */
+    const float *router_b;            /* [E] */
+    const uint8_t *const *slab;       /* E pointers: gate | up | down packed bytes */
+    const float *const *scale;        /* E pointers: sg[I] | su[I] | sd[H] */
+    const uint8_t *sh_slab;           /* shared expert, same layout with I_shared */
+    const float *sh_scale;
+} oracle_layer;
+
+/* int4 unpack of n values from one packed row: q[i] = nibble - 8. */
+void oracle_unpack_int4(const uint8_t *row, int n, int *q);
+
+/* Offline quantiser of section 06 (float32 arithmetic, as printed). */
+void oracle_quantize_int4(const float *w, int O, int I, uint8_t *q4, float *scale);
+
+double oracle_silu(double v);
+
+/* RMSNorm with unit weight: out = x / sqrt(mean(x^2) + eps). */
+void oracle_rmsnorm(const double *x, int H, double eps, double *out);
+
+/* One SwiGLU expert on one token: d[H] = W_d (silu(W_g x) * (W_u x)). */
+void oracle_expert(int H, int I, const uint8_t *slab, const float *scale,
+                   const double *x, double *d_out, double *h_out /* nullable, [I] */);
+
+/* Router for one token.  Returns 0, or -1 on an invalid config.
+ * idx[K] in descending selection-score order, w[K] routing weights,
+ * *margin = c_(K) - c_(K+1) (+inf when K == E), scores (nullable) [3*E]:
+ * logits | sigmoid | sigmoid + bias. */
+int oracle_route(const oracle_cfg *c, const float *router_w, const float *router_b,
+                 const double *x, int *idx, double *w, double *margin, double *scores);
+
+/* Routing weights of a given selection (used to re-score a GPU selection). */
+int oracle_weights_for(const oracle_cfg *c, const float *router_w, const double *x,
+                       const int *idx, double *w);
+
+/* One token through one layer.  forced_idx (nullable) replaces the top-k
+ * selection.  y[H]; idx[K], w[K], margin outputs may be NULL. */
+int oracle_moe_token(const oracle_cfg *c, const oracle_layer *L, const double *x,
+                     const int *forced_idx, double *y, int *idx, double *w, double *margin);
+
+/* T tokens of float32 input through one layer (loops oracle_moe_token). */
+int oracle_moe_forward(const oracle_cfg *c, const oracle_layer *L, const float *x, int T,
+                       double *y, int *idx, double *w, double *margin);
+
+/* Threads an OpenMP build would use (1 without OpenMP). */
+int oracle_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,357 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix.
+
+Each test checks the oracle against something other than itself: the values
+printed in the pages' worked example, closed forms, brute force on tiny
+inputs, special cases that reduce to a library routine (numpy matmul / sort,
+scipy's logistic), and exact invariants.  None needs a GPU.
+"""
+import itertools
+import math
+from pathlib import Path
+
+import numpy as np
+import pytest
+from scipy.special import expit
+
+import oracle
+import synth
+
+GOLDEN = Path(__file__).parent / "golden"
+
+
+def _golden(name):
+    out = {}
+    for line in (GOLDEN / name).read_text().splitlines():
+        if not line.strip() or line.startswith("#"):
+            continue
+        k, *v = line.split()
+        out[k] = v
+    return out
+
+
+# --- int4 storage format ("25GB 内存上运行 GLM 5.2 744B", section 06) --------
+
+def test_unpack_matches_printed_worked_example():
+    g = _golden("int4_unpack_gate_proj.txt")
+    raw = np.array([int(b, 16) for b in g["first_bytes"]], dtype=np.uint8)
+    q = oracle.unpack_int4(raw, 2 * raw.size)
+    # the page prints the low nibbles: they are the even-indexed elements
+    assert q[0::2].tolist() == [int(v) for v in g["low_nibbles"]]
+
+
+def test_size_identity_from_printed_tensor():
+    g = _golden("int4_unpack_gate_proj.txt")
+    rows, nbytes, cols = int(g["rows"][0]), int(g["packed_bytes"][0]), int(g["implied_cols"][0])
+    assert rows * ((cols + 1) // 2) == nbytes
+    assert nbytes * 2 // rows == cols
+
+
+def test_nibble_order_low_first():
+    # byte 0x4B: low nibble 0xB -> element 0 = 11 - 8 = 3; high nibble 4 -> element 1 = -4
+    assert oracle.unpack_int4(np.array([0x4B], np.uint8), 2).tolist() == [3, -4]
+    # stored value 8 is zero; 0 is -8; 15 is 7
+    assert oracle.unpack_int4(np.array([0x88, 0xF0], np.uint8), 4).tolist() == [0, 0, -8, 7]
+
+
+def test_expert_bytes_match_the_pages_19MB_figure():
+    # one GLM-5.2 expert: gate/up [2048, 6144], down [6144, 2048], int4 + per-row f32 scale
+    b = synth.slab_bytes(6144, 2048) + 4 * synth.scale_count(6144, 2048)
+    assert b == 18_915_328
+    assert abs(b / 1e6 - 19) < 0.2
+    # the survey's per-config figures for the other shapes
+    assert synth.slab_bytes(256, 128) + 4 * synth.scale_count(256, 128) == 51_200
+    assert synth.slab_bytes(2048, 1024) + 4 * synth.scale_count(2048, 1024) == 3_162_112
+    assert synth.slab_bytes(2048, 512) + 4 * synth.scale_count(2048, 512) == 1_585_152
+
+
+def test_quantize_roundtrip_exact_on_integer_rows():
+    rng = np.random.default_rng(7)
+    O, I = 6, 33
+    q = rng.integers(-7, 8, size=(O, I))
+    q[:, 0] = 7            # amax = 7 * s0 so the quantiser's scale is s0 exactly
+    s0 = 2.0 ** -rng.integers(3, 9, size=O)
+    w = (q * s0[:, None]).astype(np.float32)
+    q4, s = oracle.quantize_int4(w)
+    assert np.array_equal(s, s0.astype(np.float32))
+    for o in range(O):
+        assert oracle.unpack_int4(q4[o], I).tolist() == q[o].tolist()
+    # I odd: the pad nibble of the last byte is stored as 8 (value 0)
+    assert np.all(q4[:, -1] >> 4 == 8)
+
+
+def test_quantize_rounds_half_to_even_and_clips():
+    # amax = 7 -> s = 1: rint(2.5)=2, rint(3.5)=4, rint(-2.5)=-2, rint(0.5)=0
+    w = np.array([[2.5, 3.5, -2.5, 0.5, 7.0, -6.5]], np.float32)
+    q4, s = oracle.quantize_int4(w)
+    assert s[0] == 1.0
+    assert oracle.unpack_int4(q4[0], 6).tolist() == [2, 4, -2, 0, 7, -6]
+    # all-zero row: scale floor 1e-8, every stored nibble 8
+    q4, s = oracle.quantize_int4(np.zeros((1, 4), np.float32))
+    assert s[0] == np.float32(1e-8) and q4.tolist() == [[0x88, 0x88]]
+
+
+# --- SwiGLU expert (section 11 / section 04) ---------------------------------
+
+def test_silu_closed_forms():
+    assert oracle.silu(0.0) == 0.0
+    assert oracle.silu(1.0) == pytest.approx(1.0 / (1.0 + math.e ** -1), rel=1e-15)
+    assert oracle.silu(-1.0) == pytest.approx(-1.0 / (1.0 + math.e), rel=1e-15)
+    assert oracle.silu(40.0) == pytest.approx(40.0, rel=1e-15)
+    for v in (-7.5, -0.3, 0.2, 3.0):
+        assert oracle.silu(v) == pytest.approx(v * expit(v), rel=1e-14)
+
+
+def _pack(q_rows):
+    """Pack integer rows in [-8, 7] by hand (stored q+8, even element low)."""
+    q = np.asarray(q_rows)
+    O, n = q.shape
+    out = np.full((O, (n + 1) // 2), 0x88, np.uint8)
+    for o in range(O):
+        for i in range(n):
+            b = out[o, i // 2]
+            if i % 2 == 0:
+                out[o, i // 2] = (b & 0xF0) | (q[o, i] + 8)
+            else:
+                out[o, i // 2] = (b & 0x0F) | ((q[o, i] + 8) << 4)
+    return out
+
+
+def test_expert_hand_2x2():
+    # H = I = 2.  gate q = [[1,0],[0,-1]] sg=[1,.5]; up q = [[2,1],[-3,0]] su=[1,2];
+    # down q = [[1,1],[-1,2]] sd=[1,.25]; x = [1, 2].
+    # g = [1, -1], u = [4, -6], h = [4 silu(1), -6 silu(-1)] = [2.92423431452, 1.61364852822]
+    # d = [h0 + h1, (-h0 + 2 h1)/4] = [4.53788284274, 0.0757656854800]
+    slab = np.concatenate([_pack([[1, 0], [0, -1]]).ravel(), _pack([[2, 1], [-3, 0]]).ravel(),
+                           _pack([[1, 1], [-1, 2]]).ravel()])
+    scale = np.array([1, .5, 1, 2, 1, .25], np.float32)
+    d, h = oracle.expert(2, 2, slab, scale, np.array([1.0, 2.0]))
+    assert h == pytest.approx([2.9242343145200196, 1.6136485282199706], rel=1e-13)
+    assert d == pytest.approx([4.53788284273999, 0.07576568547998022], rel=1e-12)
+
+
+def _dequant(q4, scale, O, n):
+    q = np.stack([oracle.unpack_int4(q4[o], n) for o in range(O)]).astype(np.float64)
+    return q * scale.astype(np.float64)[:, None]
+
+
+def _dense_swiglu(H, I, slab, scale, x):
+    rb = (H + 1) // 2
+    g4 = slab[:I * rb].reshape(I, rb)
+    u4 = slab[I * rb:2 * I * rb].reshape(I, rb)
+    d4 = slab[2 * I * rb:].reshape(H, (I + 1) // 2)
+    Wg = _dequant(g4, scale[:I], I, H)
+    Wu = _dequant(u4, scale[I:2 * I], I, H)
+    Wd = _dequant(d4, scale[2 * I:], H, I)
+    g = Wg @ x
+    return Wd @ (g * expit(g) * (Wu @ x))
+
+
+@pytest.mark.parametrize("H,I", [(64, 32), (7, 5), (32, 96)])
+def test_expert_equals_dense_swiglu(H, I):
+    rng = np.random.default_rng(H * 100 + I)
+    slab = rng.integers(0, 256, synth.slab_bytes(H, I), dtype=np.uint8)
+    if H % 2:   # pad nibbles hold 8
+        rb = (H + 1) // 2
+        m = slab[:2 * I * rb].reshape(2 * I, rb)
+        m[:, -1] = (m[:, -1] & 0x0F) | 0x80
+    if I % 2:
+        d = slab[2 * I * ((H + 1) // 2):].reshape(H, (I + 1) // 2)
+        d[:, -1] = (d[:, -1] & 0x0F) | 0x80
+    scale = rng.uniform(0.005, 0.02, 2 * I + H).astype(np.float32)
+    x = rng.standard_normal(H)
+    d, _ = oracle.expert(H, I, slab, scale, x)
+    np.testing.assert_allclose(d, _dense_swiglu(H, I, slab, scale, x), rtol=1e-10, atol=1e-12)
+
+
+# --- router (section 11; Edge0 section 七) ------------------------------------
+
+def _route_scores(c_values, K, x=None):
+    """Route with W = 0, so sigmoid = 0.5 everywhere and selection score = 0.5 + b."""
+    E = len(c_values)
+    H = 4
+    cfg = oracle.make_cfg(H, E, K, 8, routed_scale=1.0)
+    W = np.zeros((E, H), np.float32)
+    b = (np.asarray(c_values, np.float64) - 0.5).astype(np.float32)
+    return oracle.route(cfg, W, b, np.ones(H) if x is None else x)
+
+
+def test_topk_equals_best_subset_bruteforce():
+    rng = np.random.default_rng(3)
+    for trial in range(40):
+        E = int(rng.integers(2, 9))
+        K = int(rng.integers(1, E + 1))
+        c = rng.uniform(-1, 1, E).astype(np.float32)
+        idx, _, margin, sc = _route_scores(c, K)
+        choice = sc[2]
+        best = max(itertools.combinations(range(E), K), key=lambda S: sum(choice[list(S)]))
+        assert sorted(idx.tolist()) == sorted(best)
+        assert all(choice[idx[i]] >= choice[idx[i + 1]] for i in range(K - 1))
+        if K < E:
+            srt = np.sort(choice)[::-1]
+            assert margin == srt[K - 1] - srt[K]
+        else:
+            assert margin == math.inf
+
+
+def test_topk_ties_lowest_index_wins():
+    c = [0.0, 0.2, 0.2, 0.1, 0.2]
+    assert _route_scores(c, 1)[0].tolist() == [1]
+    assert _route_scores(c, 2)[0].tolist() == [1, 2]
+    assert _route_scores(c, 3)[0].tolist() == [1, 2, 4]
+    assert _route_scores(c, 4)[0].tolist() == [1, 2, 4, 3]
+    assert _route_scores([0.3] * 6, 4)[0].tolist() == [0, 1, 2, 3]
+
+
+def test_topk_e_equals_k_selects_all():
+    idx, _, margin, _ = _route_scores([0.1, 0.4, -0.2, 0.3], 4)
+    assert idx.tolist() == [1, 3, 0, 2] and margin == math.inf
+
+
+def test_zero_bias_is_topk_of_logits_and_weights_use_unbiased_sigmoid():
+    rng = np.random.default_rng(11)
+    E, H, K, s = 32, 48, 4, 2.5
+    W = rng.normal(0, 0.3, (E, H)).astype(np.float32)
+    x = rng.standard_normal(H)
+    logits = W.astype(np.float64) @ x
+    cfg = oracle.make_cfg(H, E, K, 8, routed_scale=s)
+    idx, w, _, _ = oracle.route(cfg, W, np.zeros(E, np.float32), x)
+    assert idx.tolist() == np.argsort(-logits, kind="stable")[:K].tolist()
+    sig = expit(logits)
+    np.testing.assert_allclose(w, s * sig[idx] / (sig[idx].sum() + 1e-20), rtol=1e-12)
+    assert w.sum() == pytest.approx(s, rel=1e-12)
+    # a bias that keeps the same selection leaves the weights unchanged
+    b = np.zeros(E, np.float32)
+    b[idx] = 0.75
+    idx2, w2, _, _ = oracle.route(cfg, W, b, x)
+    assert sorted(idx2.tolist()) == sorted(idx.tolist())
+    np.testing.assert_allclose(np.sort(w2), np.sort(w), rtol=1e-14)
+    # a bias can change the selection; weights are still the plain sigmoid
+    b = np.zeros(E, np.float32)
+    lo = np.argsort(logits)[:K]
+    b[lo] = 5.0
+    idx3, w3, _, _ = oracle.route(cfg, W, b, x)
+    assert sorted(idx3.tolist()) == sorted(lo.tolist())
+    np.testing.assert_allclose(w3, s * sig[idx3] / (sig[idx3].sum() + 1e-20), rtol=1e-12)
+    # without renormalisation the weight is s * sigmoid
+    cfg0 = oracle.make_cfg(H, E, K, 8, routed_scale=s, norm_topk=0)
+    idx0, w0, _, _ = oracle.route(cfg0, W, np.zeros(E, np.float32), x)
+    np.testing.assert_allclose(w0, s * sig[idx0], rtol=1e-12)
+
+
+def test_invalid_group_config_rejected():
+    cfg = oracle.make_cfg(4, 4, 2, 8, n_group=2)
+    with pytest.raises(ValueError):
+        oracle.route(cfg, np.zeros((4, 4), np.float32), np.zeros(4, np.float32), np.ones(4))
+
+
+# --- whole layer ---------------------------------------------------------------
+
+def _small_layer(H=64, E=6, K=2, I=32, I_sh=48, s=2.5, seed=5, shared=True):
+    rng = np.random.default_rng(seed)
+    W = rng.normal(0, 0.1, (E, H)).astype(np.float32)
+    b = rng.uniform(-0.1, 0.1, E).astype(np.float32)
+    slabs = [rng.integers(0, 256, synth.slab_bytes(H, I), dtype=np.uint8) for _ in range(E)]
+    scales = [rng.uniform(0.005, 0.02, 2 * I + H).astype(np.float32) for _ in range(E)]
+    sh = rng.integers(0, 256, synth.slab_bytes(H, I_sh), dtype=np.uint8) if shared else None
+    shs = rng.uniform(0.005, 0.02, 2 * I_sh + H).astype(np.float32) if shared else None
+    cfg = oracle.make_cfg(H, E, K, I, int(shared), I_sh if shared else 0, routed_scale=s)
+    return cfg, W, b, slabs, scales, sh, shs
+
+
+def test_single_expert_layer_is_scaled_dense_swiglu():
+    H, I, s = 64, 32, 2.5
+    cfg, W, b, slabs, scales, _, _ = _small_layer(H=H, E=1, K=1, I=I, s=s, shared=False)
+    L = oracle.LayerRef(cfg, W, b, slabs, scales)
+    x = np.random.default_rng(1).standard_normal(H)
+    y, idx, w, _ = L.token(x)
+    assert idx.tolist() == [0] and w[0] == pytest.approx(s, rel=1e-15)
+    np.testing.assert_allclose(y, s * _dense_swiglu(H, I, slabs[0], scales[0], x), rtol=1e-10)
+
+
+def test_shared_only_is_dense_swiglu():
+    H, I_sh = 64, 48
+    cfg, W, b, slabs, scales, sh, shs = _small_layer(H=H, I_sh=I_sh, s=0.0)
+    L = oracle.LayerRef(cfg, W, b, slabs, scales, sh, shs)
+    x = np.random.default_rng(2).standard_normal(H)
+    y, _, w, _ = L.token(x)
+    assert np.all(w == 0)
+    np.testing.assert_allclose(y, _dense_swiglu(H, I_sh, sh, shs, x), rtol=1e-10)
+
+
+def test_layer_is_weighted_sum_plus_shared():
+    H, I, I_sh, K, s = 64, 32, 48, 2, 2.5
+    cfg, W, b, slabs, scales, sh, shs = _small_layer(H=H, I=I, I_sh=I_sh, K=K, s=s)
+    L = oracle.LayerRef(cfg, W, b, slabs, scales, sh, shs)
+    x = np.random.default_rng(4).standard_normal(H)
+    y, idx, w, _ = L.token(x)
+    ref = sum(w[k] * _dense_swiglu(H, I, slabs[idx[k]], scales[idx[k]], x) for k in range(K))
+    ref = ref + _dense_swiglu(H, I_sh, sh, shs, x)
+    np.testing.assert_allclose(y, ref, rtol=1e-10, atol=1e-12)
+
+
+def test_doubling_down_scales_doubles_output_exactly():
+    H, I, I_sh = 64, 32, 48
+    cfg, W, b, slabs, scales, sh, shs = _small_layer(H=H, I=I, I_sh=I_sh)
+    x = np.random.default_rng(6).standard_normal(H)
+    y1, *_ = oracle.LayerRef(cfg, W, b, slabs, scales, sh, shs).token(x)
+    sc2 = [s.copy() for s in scales]
+    for s in sc2:
+        s[2 * I:] *= 2
+    shs2 = shs.copy()
+    shs2[2 * I_sh:] *= 2
+    y2, *_ = oracle.LayerRef(cfg, W, b, slabs, sc2, sh, shs2).token(x)
+    assert np.array_equal(y2, 2 * y1)
+
+
+def test_forced_selection_rescored():
+    cfg, W, b, slabs, scales, sh, shs = _small_layer()
+    L = oracle.LayerRef(cfg, W, b, slabs, scales, sh, shs)
+    x = np.random.default_rng(8).standard_normal(cfg.H)
+    y, idx, w, _ = L.token(x)
+    yf, idxf, wf, _ = L.token(x, forced_idx=idx)
+    assert np.array_equal(y, yf) and np.array_equal(w, wf)
+    other = np.array([idx[1], idx[0]], np.int32)     # same set, other order
+    yo, _, wo, _ = L.token(x, forced_idx=other)
+    np.testing.assert_allclose(yo, y, rtol=1e-12)
+
+
+def test_missing_selected_expert_is_an_error():
+    cfg, W, b, slabs, scales, sh, shs = _small_layer()
+    L = oracle.LayerRef(cfg, W, b, [None] * cfg.E, [None] * cfg.E, sh, shs)
+    with pytest.raises(ValueError):
+        L.token(np.ones(cfg.H))
+
+
+def test_rmsnorm_closed_form():
+    out = oracle.rmsnorm(np.array([3.0, 4.0]), 0.0)
+    np.testing.assert_allclose(out, np.array([3.0, 4.0]) / math.sqrt(12.5), rtol=1e-15)
+    x = np.random.default_rng(9).standard_normal(100) * 3
+    eps = 1e-5
+    out = oracle.rmsnorm(x, eps)
+    ms = np.mean(x * x)
+    assert np.mean(out * out) == pytest.approx(ms / (ms + eps), rel=1e-12)
+
+
+def test_prenorm_residual_layer():
+    cfg, W, b, slabs, scales, sh, shs = _small_layer()
+    x = np.random.default_rng(10).standard_normal(cfg.H) * 4
+    y_plain, *_ = oracle.LayerRef(cfg, W, b, slabs, scales, sh, shs).token(oracle.rmsnorm(x, 1e-5))
+    cfg_r = oracle.make_cfg(cfg.H, cfg.E, cfg.K, cfg.I, 1, cfg.I_shared, routed_scale=2.5,
+                            prenorm_residual=1, rms_eps=1e-5)
+    y_res, *_ = oracle.LayerRef(cfg_r, W, b, slabs, scales, sh, shs).token(x)
+    np.testing.assert_allclose(y_res, x + y_plain, rtol=1e-13, atol=1e-13)
+    # with nothing routed and no shared expert the residual stream is unchanged
+    cfg_0 = oracle.make_cfg(cfg.H, cfg.E, cfg.K, cfg.I, 0, 0, routed_scale=0.0,
+                            prenorm_residual=1)
+    y0, *_ = oracle.LayerRef(cfg_0, W, b, slabs, scales).token(x)
+    assert np.array_equal(y0, x)
+
+
+def test_forward_loops_tokens():
+    cfg, W, b, slabs, scales, sh, shs = _small_layer()
+    L = oracle.LayerRef(cfg, W, b, slabs, scales, sh, shs)
+    X = np.random.default_rng(12).standard_normal((5, cfg.H)).astype(np.float32)
+    Y, I_, Wt, M = L.forward(X)
+    for t in range(5):
+        y, idx, w, m = L.token(X[t].astype(np.float64))
+        assert np.array_equal(Y[t], y) and np.array_equal(I_[t], idx) and M[t] == m
