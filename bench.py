@@ -1,0 +1,455 @@
+#!/usr/bin/env python
+"""Benchmark of the int4 routed-MoE FFN step on GB300.
+
+One step = one moe_forward call (router, top-k, gate/up + SwiGLU, down +
+combine + shared expert) on one batch of synthetic tokens, default the
+GLM-5.2 MoE layer at decode (T=1, H=6144, E=256, top-8, inter 2048, one
+shared expert, int4 per-row weights, all 256 experts resident in HBM).
+
+Timing: W warm-up steps, then exactly K steps, each bracketed by CUDA events
+on the launching stream; L2 is flushed before every step (a 256 MiB write,
+then a 256 MiB read of another buffer, so the cache is cold and clean) and
+the flush is outside the events.  Inputs rotate over 16 token vectors, so
+the routed experts change from step to step.  value = tokens / sum of step
+times (whole job; max over ranks under torchrun).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+import numpy as np
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer decode tokens/s and achieved HBM GB/s vs ~8 TB/s (GLM-5.2 shape)"
+N_X = 16                      # distinct token batches rotated through the steps
+FLUSH_BYTES = 256 << 20       # > 129 MB L2
+PROFILE_FILE = ROOT / "profiles" / "traffic_gateup_decode_glm.txt"
+
+
+# --------------------------------------------------------------------------- helpers
+
+def expert_bytes(H: int, I: int) -> int:
+    """Packed int4 gate/up/down bytes + float32 per-row scales of one expert."""
+    return synth.slab_bytes(H, I) + 4 * synth.scale_count(H, I)
+
+
+def gateup_bytes(H: int, I: int) -> int:
+    """Bytes the gate/up kernel must read for one expert: two [I, H/2] int4
+    matrices and their 2I float32 scales."""
+    return 2 * I * ((H + 1) // 2) + 8 * I
+
+
+def step_bytes(wl, T: int, touched: int) -> int:
+    """Algorithmic HBM bytes of one step: router weight and bias, every routed
+    expert the batch touches (each read once), the shared expert, x and y."""
+    b = wl.E * wl.H * 4 + wl.E * 4 + touched * expert_bytes(wl.H, wl.I)
+    if wl.n_shared:
+        b += expert_bytes(wl.H, wl.I_shared)
+    return b + 2 * T * wl.H * 4
+
+
+def workload_desc(wl) -> str:
+    s = (f"{wl.name}: T={wl.T}, H={wl.H}, E={wl.E} routed, top-{wl.K}, moe_inter={wl.I}, "
+         f"{wl.n_shared} shared (inter {wl.I_shared}), sigmoid+bias noaux_tc n_group=1, "
+         f"norm_topk, routed_scale={wl.routed_scale}, int4 per-row weights, seed {wl.seed}")
+    if wl.n_layers > 1:
+        s += f", {wl.n_layers} chained layers x <- x + moe(rmsnorm(x))"
+    return s
+
+
+def rank_streams(rank: int, world: int, n: int) -> list[int]:
+    """Token-stream ids of one rank: disjoint across ranks (weak scaling, no
+    data exchange: each rank runs its own copy of the layer on its own tokens)."""
+    return [rank * 100_000 + i for i in range(n)]
+
+
+def reduce_max(value: float, dist_on: bool) -> float:
+    if not dist_on:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist_on: bool):
+    if dist_on:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        time.sleep(0.1)
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        rows = []
+        for l in self.lines:
+            f = [v.strip() for v in l.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                rows.append(dict(sm=float(f[1]), smax=float(f[2]), util=float(f[4]),
+                                 hw=f[6], hwt=f[7], swt=f[8], pcap=f[9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        load = [r for r in rows if r["util"] > 0] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["smax"] for r in rows), "reasons": sorted(reasons),
+                "samples": len(load)}
+
+
+def measured_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the gate/up kernel from the committed ncu
+    summary, or None when the kernel source changed since the capture."""
+    if not PROFILE_FILE.exists():
+        return None
+    kv = {}
+    for line in PROFILE_FILE.read_text().splitlines():
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    src = ROOT / "int4_moe_expert_gb300" / "csrc" / "moe_kernels.cu"
+    sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
+    if kv.get("kernel_source_sha256_16") != sha or "traffic_bytes_per_launch" not in kv:
+        return None
+    return float(kv["traffic_bytes_per_launch"])
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank, dist_on):
+    import torch
+    import int4_moe_expert_gb300 as moe
+
+    wl = synth.WORKLOADS[args.workload]
+    if wl.n_layers > 1:
+        raise SystemExit("bench.py times single-layer workloads; the stack is a parity case")
+    T = wl.T
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    li = synth.layer_inputs(wl)
+    cfg = moe.make_config(wl.H, wl.E, wl.K, wl.I, wl.n_shared, wl.I_shared, wl.routed_scale,
+                          wl.norm_topk, False, wl.rms_eps)
+    layer = moe.MoeLayer(cfg, li.router_w, li.router_b, li.slabs, li.scales, li.sh_slab,
+                         li.sh_scale, max_tokens=T)
+    streams = rank_streams(rank, world, N_X)
+    xs_host = [synth.tokens(wl, T=T, stream=s) for s in streams]
+    xs = [torch.from_numpy(x).to(dev) for x in xs_host]
+    y = torch.empty((T, wl.H), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    flush_w = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sink = torch.empty(1, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, keepdim=True, out=sink)
+
+    # routing of each rotated batch (for the algorithmic byte count)
+    touched = []
+    for x in xs:
+        _, idx, _ = layer.forward_debug(x)
+        touched.append(len(set(idx.cpu().numpy().ravel().tolist())))
+    torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        flush()
+        layer.forward(xs[i % N_X], y)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    n_prof = min(K, 4096)
+    moe.moe_profile_start(layer.handle, n_prof)
+    barrier(dist_on)
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        for i in range(K):
+            flush()
+            ev0[i].record(stream)
+            moe.moe_forward(layer.handle, xs[i % N_X], T, y, stream)
+            ev1[i].record(stream)
+        torch.cuda.synchronize()
+    barrier(dist_on)
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    total_ms = reduce_max(sum(step_ms), dist_on)
+    n_calls, stage_ms = moe.moe_profile_read(layer.handle)
+    moe.moe_profile_start(layer.handle, 0)
+    kernels_per_step = 3 if T == 1 else 4
+
+    # end to end through the host entry point (pinned host buffers)
+    xh = [torch.from_numpy(x).pin_memory() for x in xs_host]
+    yh = torch.empty((T, wl.H), dtype=torch.float32).pin_memory()
+    for i in range(min(args.warmup, 10)):
+        moe.moe_forward_host(layer.handle, xh[i % N_X], T, yh, stream)
+    barrier(dist_on)
+    e2e_s = 0.0
+    for i in range(K):
+        flush()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        moe.moe_forward_host(layer.handle, xh[i % N_X], T, yh, stream)
+        e2e_s += time.perf_counter() - t0
+    e2e_s = reduce_max(e2e_s, dist_on)
+    barrier(dist_on)
+
+    tokens = world * K * T
+    value = tokens / (total_ms / 1e3)
+    ms_per_step = total_ms / K
+    mean_touched = float(np.mean(touched))
+    bytes_step = float(np.mean([step_bytes(wl, T, t) for t in touched]))
+    peak, peak_kind = measured_peaks()
+    # dominant kernel: gate/up + SwiGLU, K routed experts + the shared one per launch (T = 1)
+    units = (mean_touched if T > 1 else wl.K) + wl.n_shared
+    gu_bytes = (mean_touched if T > 1 else wl.K) * gateup_bytes(wl.H, wl.I) + \
+        (gateup_bytes(wl.H, wl.I_shared) if wl.n_shared else 0)
+    gu_ms = stage_ms["gate_up"]
+    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+    out = None
+    if rank == 0:
+        out = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "tokens/s",
+            "n_gpus": world,
+            "steps": K,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 6),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f32 (int4 weights dequantised exactly, fp32 accumulation)",
+            "data": "synthetic (seeded SplitMix64; shapes and distributions of the workload)",
+            "config": {
+                "workload": workload_desc(wl),
+                "tokens_per_step": T,
+                "experts_resident_GB": round(wl.E * expert_bytes(wl.H, wl.I) / 1e9, 3),
+                "l2": "flushed before every step (256 MiB write + 256 MiB read), outside the events",
+                "x_rotation": N_X,
+                "parallelism": f"{world} independent replicas (no collective on the data path)",
+            },
+            "hbm": {
+                "algorithmic_bytes_per_step": int(bytes_step),
+                "achieved_gbs_per_step": round(bytes_step / (ms_per_step / 1e3) / 1e9, 1),
+                "vs_8tbs": round(bytes_step / (ms_per_step / 1e3) / 8e12, 4),
+                "vs_measured_peak": round(bytes_step / (ms_per_step / 1e3) / 1e9 / peak, 4),
+                "mean_routed_experts_touched": mean_touched,
+            },
+            "roofline": {
+                "kernel": "gateup (int4 dequant GEMV + SwiGLU), T=%d" % T,
+                "bound": "hbm",
+                "achieved": round(achieved, 1),
+                "peak": peak,
+                "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy)" if peak_kind == "measured" else peak_kind,
+                "unit": "GB/s",
+                "frac": round(achieved / peak, 4),
+                "traffic": recorded_traffic(),
+                "algorithmic_bytes_per_launch": int(gu_bytes),
+                "units_per_launch": units,
+                "launch_ms": round(gu_ms, 6),
+            },
+            "stages_ms": {k: round(v, 6) for k, v in stage_ms.items()},
+            "stages_calls": n_calls,
+            "e2e": {
+                "value": round(tokens / e2e_s, 2),
+                "unit": "tokens/s",
+                "h2d_bytes_per_step": T * wl.H * 4,
+                "d2h_bytes_per_step": T * wl.H * 4,
+                "api": "moe_forward_host (pinned host x/y, copies + step + stream sync)",
+            },
+            "gpu_launches": world * K * kernels_per_step,
+            "clocks": clk.summary(),
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(wl, li, xs_host, args.cpu_seconds)
+    layer.close()
+    return out
+
+
+def cpu_baseline(wl, li, xs_host, seconds):
+    """The oracle, as it stands, on this host's cores over a bounded sample of
+    the same workload (whole tokens through the layer in double precision)."""
+    import oracle
+    ref = oracle.LayerRef.from_inputs(oracle.cfg_from_workload(wl), li)
+    n_tok, t0 = 0, time.perf_counter()
+    i = 0
+    while True:
+        ref.forward(xs_host[i % len(xs_host)])
+        n_tok += xs_host[0].shape[0]
+        i += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or i >= 4096:
+            break
+    return {"value": round(n_tok / el, 4), "unit": "tokens/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": f"{n_tok} tokens ({i} calls of T={xs_host[0].shape[0]}) of the same layer "
+                      f"through the double-precision C oracle, OpenMP over output rows, {el:.1f} s"}
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args, world):
+    """The oracle on the host cores, same workload and metric.  One step is one
+    expert of one token (router included in a token's first step), so K steps
+    stay within minutes; tokens = steps / (K + n_shared)."""
+    import oracle
+    wl = synth.WORKLOADS[args.workload]
+    T = 1
+    J = wl.K + wl.n_shared
+    cfg = oracle.cfg_from_workload(wl)
+    li = synth.layer_inputs(wl)
+    ref = oracle.LayerRef.from_inputs(cfg, li)
+    xs = [synth.tokens(wl, T=1, stream=s)[0].astype(np.float64) for s in range(N_X)]
+
+    state = {"idx": None}
+
+    def step(s):
+        u, j = divmod(s, J)
+        x = xs[u % N_X]
+        if j == 0:
+            state["idx"], _, _, _ = oracle.route(cfg, ref.router_w, ref.router_b, x)
+        if j < wl.K:
+            e = int(state["idx"][j])
+            oracle.expert(wl.H, wl.I, li.slabs[e], li.scales[e], x)
+        else:
+            oracle.expert(wl.H, wl.I_shared, li.sh_slab, li.sh_scale, x)
+
+    for s in range(args.warmup):
+        step(s)
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(s)
+    el = time.perf_counter() - t0
+    tokens = args.steps / J * T
+    value = tokens / el
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64; shapes and distributions of the workload)",
+        "config": {"workload": workload_desc(wl), "tokens_per_step": 1.0 / J,
+                   "step": f"one of the {J} experts of one token (router on the token's first step)"},
+        "cpu_baseline": {"kind": "oracle", "cores": oracle.threads(), "value": round(value, 4),
+                         "unit": "tokens/s",
+                         "sample": f"{args.steps} steps = {tokens:.1f} tokens of the layer in the "
+                                   f"double-precision C oracle"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+# --------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="glm_decode",
+                    choices=[k for k, w in synth.WORKLOADS.items() if w.n_layers == 1])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world)), flush=True)
+        return
+
+    dist_on = world > 1
+    if dist_on:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    out = run_ours(args, rank, world, local_rank, dist_on)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist_on:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

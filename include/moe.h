@@ -1,0 +1,150 @@
+/*
+ * moe.h -- C ABI of the GB300 int4 routed-MoE FFN step.
+ *
+ * One call computes, for T tokens x[T,H] (float32, device memory),
+ *
+ *     y[t] = sum_{k<K} w[t,k] * FFN_{e[t,k]}(x[t]) + FFN_shared(x[t])
+ *
+ * where FFN_e(v) = W_d,e (silu(W_g,e v) * (W_u,e v)) is a SwiGLU expert whose
+ * three matrices are row-quantised int4, and (e[t,.], w[t,.]) is the router's
+ * choice.  Sources, by page and section:
+ *
+ *  - Router ("25GB 内存上运行 GLM 5.2 744B", reader.mx, section 11 "MoE 路由与
+ *    专家执行"): logit = W_r x (float32, W_r [E,H]); sigma = sigmoid(logit);
+ *    the top-K of sigma + bias[e] (e_score_correction_bias) is selected; the
+ *    weight uses the un-biased sigma, times routed_scaling_factor.  A tie is
+ *    won by the lower expert index; the K choices come out in descending
+ *    score order.
+ *  - Renormalisation (Edge0 article, magicnetworld.com, section 七 "路由数学",
+ *    sigmoid family): w = s * sigma / (sum_{selected} sigma + 1e-20).
+ *  - Expert format (reader.mx page, section 06 "从 FP8 到 int4"): each row of a
+ *    matrix [O, n] is ceil(n/2) bytes, element 2j in the low nibble of byte j
+ *    and 2j+1 in the high nibble, stored as q+8 with q in [-8, 7]; one float32
+ *    scale per output row, so W[o,i] = (nibble - 8) * scale[o].
+ *  - Composition (GLM-5.2 operator breakdown, devpress.csdn.net, "Step 6 (MoE)"
+ *    sub-steps 6a-6d): 8 routed experts plus one always-active shared expert,
+ *    whose output is added with weight 1.
+ *  - Optional pre-norm + residual (reader.mx page, section 04): with
+ *    MOE_FLAG_PRENORM_RESIDUAL the call computes y = x + moe(rmsnorm(x)),
+ *    rmsnorm(x) = x / sqrt(mean(x^2) + rms_eps) with unit weight.
+ *
+ * Everything runs on the current CUDA device, on the caller's stream, with
+ * no host synchronisation (except moe_forward_host, which is synchronous by
+ * design).  There is no CPU fallback: every failure is a status code.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+/* y = x + moe(rmsnorm(x)) instead of y = moe(x). */
+#define MOE_FLAG_PRENORM_RESIDUAL 1u
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID = 1,      /* bad argument or config; nothing was launched */
+    MOE_ERR_CUDA = 2,         /* a CUDA call failed; see moe_last_error() */
+    MOE_ERR_NOMEM = 3,        /* device allocation failed */
+    MOE_ERR_UNSUPPORTED = 4   /* well-formed but outside what the kernels cover */
+} moe_status;
+
+typedef struct moe_config {
+    int32_t hidden;        /* H: multiple of 32, 32..16384 */
+    int32_t n_experts;     /* E: 1..1024 */
+    int32_t top_k;         /* K: 1..min(E, 32) */
+    int32_t moe_inter;     /* I: multiple of 32, 32..16384 */
+    int32_t n_shared;      /* 0 or 1 */
+    int32_t shared_inter;  /* I_sh: multiple of 32 when n_shared == 1 */
+    int32_t n_group;       /* must be 1 (group-limited routing is not implemented) */
+    int32_t norm_topk;     /* 1: renormalise the selected weights (see above); 0: w = s * sigma */
+    float routed_scale;    /* s, routed_scaling_factor */
+    float rms_eps;         /* used with MOE_FLAG_PRENORM_RESIDUAL */
+    uint32_t flags;        /* MOE_FLAG_* */
+} moe_config;
+
+/*
+ * Weights are BORROWED device pointers: the caller allocates them, keeps them
+ * alive and unchanged until moe_destroy, and frees them afterwards.  The two
+ * per-expert pointer arrays themselves are HOST arrays of E entries; they are
+ * copied at moe_init and not referenced afterwards.
+ *
+ * Expert slab (one per routed expert, and one for the shared expert):
+ *     gate q4 [I, H/2] | up q4 [I, H/2] | down q4 [H, I/2]     uint8, row-major
+ * Expert scales:
+ *     gate s [I] | up s [I] | down s [H]                        float32
+ * Every slab and scale pointer must be 16-byte aligned.
+ */
+typedef struct moe_weights {
+    const float *router_w;                  /* [E, H] float32, row-major */
+    const float *router_bias;               /* [E] float32 (selection only) */
+    const uint8_t *const *expert_slab;      /* host array of E device pointers */
+    const float *const *expert_scale;       /* host array of E device pointers */
+    const uint8_t *shared_slab;             /* NULL when n_shared == 0 */
+    const float *shared_scale;              /* NULL when n_shared == 0 */
+} moe_weights;
+
+typedef struct moe_handle moe_handle;
+
+/* Validates cfg and weights, allocates the handle's device workspace (sized
+ * for max_tokens tokens per call) on the current device, and returns the
+ * handle in *out.  On error *out is NULL and nothing stays allocated. */
+moe_status moe_init(const moe_config *cfg, const moe_weights *w, int32_t max_tokens,
+                    moe_handle **out);
+
+/* y[T,H] = step(x[T,H]); x and y are device float32, row-major, must not
+ * overlap, and y is overwritten.  0 <= T <= max_tokens (T == 0 does nothing).
+ * Launches on `stream` (a cudaStream_t; NULL = legacy default stream) and
+ * returns without waiting.  Calls on one handle must not overlap on the GPU:
+ * they share the handle's workspace. */
+moe_status moe_forward(moe_handle *h, const float *x, int32_t T, float *y, void *stream);
+
+/* As moe_forward, and also writes the router's choice: topk_idx[T,K] int32
+ * (descending selection score), topk_w[T,K] float32, and, when not NULL,
+ * expert_counts[E] int32 = tokens routed to each expert.  Device pointers. */
+moe_status moe_forward_debug(moe_handle *h, const float *x, int32_t T, float *y,
+                             int32_t *topk_idx, float *topk_w, int32_t *expert_counts,
+                             void *stream);
+
+/* Host-memory variant: copies x_host[T,H] to the device, runs the step on
+ * `stream`, copies y back to y_host[T,H] and waits for the stream.  Host
+ * buffers may be pageable; pinned buffers make the copies asynchronous. */
+moe_status moe_forward_host(moe_handle *h, const float *x_host, int32_t T, float *y_host,
+                            void *stream);
+
+/* Frees the workspace and the handle (waits for the device first).  NULL is a no-op. */
+moe_status moe_destroy(moe_handle *h);
+
+/*
+ * Per-kernel timing.  moe_profile_start(h, n) makes the next n forward calls
+ * on h record a CUDA event on their stream before the first kernel and after
+ * each kernel (n <= 4096; n == 0 stops recording and frees the events).
+ * moe_profile_read waits for those events and returns, for each stage s,
+ * stage_ms[s] = mean time from the event before stage s to the event after
+ * it over the recorded calls.  Stages: 0 router (+ top-k, buckets),
+ * 1 gate/up + SwiGLU, 2 down (+ combine for T == 1), 3 combine (T > 1 only;
+ * 0 otherwise).  *n_calls = calls recorded.  stage_ms has MOE_PROFILE_STAGES
+ * entries.
+ */
+#define MOE_PROFILE_STAGES 4
+moe_status moe_profile_start(moe_handle *h, int32_t max_calls);
+moe_status moe_profile_read(moe_handle *h, int32_t *n_calls, float *stage_ms);
+
+/* Device workspace moe_init would allocate for this config (0 if invalid). */
+size_t moe_workspace_bytes(const moe_config *cfg, int32_t max_tokens);
+
+/* Message of the last failure on this thread ("" if none). */
+const char *moe_last_error(void);
+
+int32_t moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,70 @@
+// Internal declarations shared by the C-ABI layer (moe_abi.cu) and the
+// kernels (moe_kernels.cu).  Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+// Problem constants of one handle (validated by moe_init).
+struct Dims {
+    int H, E, K, I, n_shared, I_sh;
+    int I_max;          // max(I, I_sh)
+    int norm_topk;
+    int prenorm;        // MOE_FLAG_PRENORM_RESIDUAL
+    float scale;        // routed_scale
+    float eps;          // rms_eps
+    int max_tokens;
+};
+
+// Device workspace owned by a handle.  Vectors marked "perm" are stored in
+// the chunk-permuted order described in moe_kernels.cu (perm_pos).
+struct Workspace {
+    float *rnorm;        // [maxT] 1/rms(x_t) (1 when no pre-norm)
+    float *xperm;        // [maxT, H] perm, x_t * rnorm_t
+    float *logits;       // [maxT, E] raw router logits
+    int *topk_idx;       // [maxT, K]
+    float *topk_w;       // [maxT, K]
+    unsigned *counters;  // [16] last-block tickets, reset by the last block
+    float *h;            // [(maxT*K + maxT), I_max] perm, SwiGLU activations
+    int *cnt;            // [E]
+    int *off;            // [E+1]
+    int *perm;           // [maxT*K] pair ids (t*K+k) grouped by expert, stable
+    int *inv;            // [maxT*K] position of pair p in perm
+    int *slot_expert;    // [E] active experts, ascending id
+    int *n_slots;        // [1]
+    float *dbuf;         // [(maxT*K + maxT), H] unweighted down outputs (T > 1)
+};
+
+// Everything a kernel needs, passed by value.
+struct Params {
+    Dims d;
+    const float *router_w;
+    const float *router_b;
+    const uint8_t *const *slabs;    // device array [E]
+    const float *const *scales;     // device array [E]
+    const uint8_t *sh_slab;
+    const float *sh_scale;
+    Workspace ws;
+};
+
+size_t workspace_bytes(const Dims &d);
+void carve_workspace(const Dims &d, void *base, Workspace *ws);
+
+// Per-config kernel attributes (dynamic shared memory limits); once per handle.
+cudaError_t prepare_kernels(const Dims &d);
+
+constexpr int kStages = 4;   // router, gate/up, down, combine
+
+// Launch the whole step for T >= 1 tokens on `stream`.  want_buckets forces
+// the token -> expert histogram (ws.cnt) even for T == 1.  When ev is not
+// NULL, ev[0] is recorded before the first kernel and ev[s+1] after stage s
+// (kStages + 1 events; stages a path does not run get back-to-back events).
+// Returns the first launch error (cudaSuccess when all launches were issued).
+cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cudaStream_t stream,
+                           bool want_buckets, cudaEvent_t *ev);
+
+}  // namespace moe

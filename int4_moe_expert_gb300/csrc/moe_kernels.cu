@@ -1,0 +1,774 @@
+// Kernels of the int4 routed-MoE FFN step (sm_103a).
+//
+// Step order (GLM-5.2 operator breakdown, devpress.csdn.net, "Step 6 (MoE)"
+// 6a-6d; reader.mx "25GB 内存上运行 GLM 5.2 744B", section 11):
+//   router    logits = W_r x, sigma, + bias, top-K, renormalised weights
+//   buckets   (T > 1) tokens grouped per expert, each expert read once per
+//             batch (the batch union of section 11)
+//   gate/up   g = s_g (Q_g x), u = s_u (Q_u x), h = silu(g) * u
+//   down      d = s_d (Q_d h), y = sum_k w_k d_k + d_shared
+//
+// Vectors that feed an int4 dot product (x and h) are kept in a
+// "chunk-permuted" order so that one 16-byte weight load (32 int4 values)
+// meets its 32 activations as eight float4 loads that are contiguous across
+// the lanes of a warp; see perm_pos.
+#include <math.h>
+#include <stdint.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kGemvMaxT = 8;       // router GEMV handles up to this many tokens
+
+// ---------------------------------------------------------------------------
+// Layout helpers
+// ---------------------------------------------------------------------------
+
+// Position of element i of a length-L vector (L % 32 == 0) in chunk-permuted
+// order.  Chunk c holds elements 32c..32c+31.  Within a chunk, the 16 packed
+// bytes are four 32-bit words; word m holds elements 8m..8m+7, with element
+// 8m+2b in the low nibble and 8m+2b+1 in the high nibble of byte b.  The
+// permuted vector is an array of float4: float4 (k*C + c) for k = 2m holds
+// the even elements 8m+{0,2,4,6} of chunk c and k = 2m+1 the odd ones
+// 8m+{1,3,5,7}.
+__host__ __device__ __forceinline__ int perm_pos(int i, int L) {
+    const int C = L >> 5;
+    const int c = i >> 5, j = i & 31, m = j >> 3, e = j & 7;
+    const int k = 2 * m + (e & 1), r = e >> 1;
+    return ((k * C + c) << 2) + r;
+}
+
+// 16-byte streaming load of weights: read-only path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const void *ptr) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(ptr));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// One int4 nibble (already isolated in byte b of v) to its exact float value
+// q = nibble - 8: the byte becomes the low mantissa byte of 2^23 (0x4B000000),
+// giving 2^23 + nibble exactly, then 2^23 + 8 is subtracted exactly.
+__device__ __forceinline__ float nib(uint32_t v, uint32_t b) {
+    return __uint_as_float(__byte_perm(v, 0x4B000000u, 0x7440u | b)) - 8388616.0f;
+}
+
+// acc + sum over the 8 values of one packed word, against their activations:
+// xe = elements 0,2,4,6 and xo = elements 1,3,5,7 of the word.
+__device__ __forceinline__ float dot_word(uint32_t w, float4 xe, float4 xo, float acc) {
+    const uint32_t lo = w & 0x0F0F0F0Fu;
+    const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;
+    acc = fmaf(nib(lo, 0), xe.x, acc);
+    acc = fmaf(nib(hi, 0), xo.x, acc);
+    acc = fmaf(nib(lo, 1), xe.y, acc);
+    acc = fmaf(nib(hi, 1), xo.y, acc);
+    acc = fmaf(nib(lo, 2), xe.z, acc);
+    acc = fmaf(nib(hi, 2), xo.z, acc);
+    acc = fmaf(nib(lo, 3), xe.w, acc);
+    acc = fmaf(nib(hi, 3), xo.w, acc);
+    return acc;
+}
+
+// acc + dot(one 16-byte chunk of 32 int4 weights, its 32 permuted activations)
+__device__ __forceinline__ float dot_chunk(uint4 w, const float4 (&xv)[8], float acc) {
+    acc = dot_word(w.x, xv[0], xv[1], acc);
+    acc = dot_word(w.y, xv[2], xv[3], acc);
+    acc = dot_word(w.z, xv[4], xv[5], acc);
+    acc = dot_word(w.w, xv[6], xv[7], acc);
+    return acc;
+}
+
+__device__ __forceinline__ void load_chunk_act(const float *vec_perm, int C, int c, float4 (&xv)[8]) {
+    const float4 *p4 = reinterpret_cast<const float4 *>(vec_perm);
+#pragma unroll
+    for (int k = 0; k < 8; k++) xv[k] = __ldg(p4 + k * C + c);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return g / (1.0f + expf(-g)) * u;
+}
+
+// ---------------------------------------------------------------------------
+// Router: top-K selection and token -> expert buckets (last block of the
+// router grid; no block ever waits on another)
+// ---------------------------------------------------------------------------
+
+// Order of the router's selection: larger score first, then lower index
+// (the greedy strict-'>' scan of section 11 makes the lowest index win a tie).
+__device__ __forceinline__ bool ranks_before(float v, int e, float bv, int be) {
+    return v > bv || (v == bv && e < be);
+}
+
+// Top-K for tokens [0, T): one warp per token.  Scores live in shared memory
+// (sig and choice, E floats per warp).  NaN scores rank last, so an index in
+// [0, E) is always produced.
+__device__ void topk_phase(const Params &p, int T, float *smem) {
+    const int E = p.d.E, K = p.d.K;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float *sig = smem + warp * 2 * E;
+    float *choice = sig + E;
+    for (int t = warp; t < T; t += kWarps) {
+        for (int e = lane; e < E; e += 32) {
+            const float l = __ldcg(p.ws.logits + (size_t)t * E + e);
+            const float s = 1.0f / (1.0f + expf(-l));
+            float c = s + p.router_b[e];
+            if (isnan(c)) c = -INFINITY;
+            sig[e] = s;
+            choice[e] = c;
+        }
+        __syncwarp();
+        uint32_t taken = 0;       // bit i: expert lane + 32 i already chosen
+        float sum_sig = 0.0f;
+        for (int kk = 0; kk < K; kk++) {
+            float bv = -INFINITY;
+            int be = 0x7fffffff;
+            for (int i = 0; i * 32 + lane < E; i++) {
+                if ((taken >> i) & 1u) continue;
+                const int e = i * 32 + lane;
+                const float v = choice[e];
+                if (ranks_before(v, e, bv, be)) { bv = v; be = e; }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                if (ranks_before(ov, oe, bv, be)) { bv = ov; be = oe; }
+            }
+            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+            const float s = sig[be];
+            sum_sig += s;
+            if (lane == 0) {
+                p.ws.topk_idx[(size_t)t * K + kk] = be;
+                p.ws.topk_w[(size_t)t * K + kk] = s;   // rescaled below
+            }
+        }
+        __syncwarp();
+        if (lane == 0) {
+            const float den = sum_sig + 1e-20f;
+            for (int kk = 0; kk < K; kk++) {
+                float *wp = p.ws.topk_w + (size_t)t * K + kk;
+                *wp = p.d.norm_topk ? p.d.scale * (*wp) / den : p.d.scale * (*wp);
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// Token -> expert buckets for T tokens (whole block).  cnt[e], exclusive
+// offsets off[e], the pair ids p = t*K + k of each expert in ascending p
+// (stable), inv[p], and the list of experts with at least one token.
+__device__ void bucket_phase(const Params &p, int T, int *ismem) {
+    const int E = p.d.E, K = p.d.K, P = T * K;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    int *cnt = ismem;               // [E]
+    int *run = cnt + E;             // [E] next free position per expert
+    int *wcnt = run + E;            // [kWarps][E] per-warp counts in a chunk
+    for (int e = tid; e < E; e += kThreads) cnt[e] = 0;
+    for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
+    __syncthreads();
+    for (int q = tid; q < P; q += kThreads) atomicAdd(&cnt[p.ws.topk_idx[q]], 1);
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scans of counts and of "active" flags, E <= 1024
+        const int per = (E + 31) / 32;
+        const int b = lane * per;
+        int s = 0, a = 0;
+        for (int i = 0; i < per; i++) {
+            const int e = b + i;
+            if (e < E) { s += cnt[e]; a += cnt[e] > 0; }
+        }
+        int ps = s, pa = a;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int vs = __shfl_up_sync(0xffffffffu, ps, o);
+            const int va = __shfl_up_sync(0xffffffffu, pa, o);
+            if (lane >= o) { ps += vs; pa += va; }
+        }
+        int off = ps - s, act = pa - a;
+        for (int i = 0; i < per; i++) {
+            const int e = b + i;
+            if (e < E) {
+                p.ws.cnt[e] = cnt[e];
+                p.ws.off[e] = off;
+                run[e] = off;
+                if (cnt[e] > 0) p.ws.slot_expert[act++] = e;
+                off += cnt[e];
+            }
+        }
+        if (lane == 31) { p.ws.off[E] = ps; *p.ws.n_slots = pa; }
+    }
+    __syncthreads();
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int base = 0; base < P; base += kThreads) {
+        const int q = base + tid;
+        const int e = q < P ? p.ws.topk_idx[q] : -1;
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        const int lrank = __popc(same & lt_mask);
+        if (e >= 0 && lrank == 0) wcnt[warp * E + e] = __popc(same);
+        __syncthreads();
+        if (e >= 0) {
+            int pre = 0;
+            for (int w = 0; w < warp; w++) pre += wcnt[w * E + e];
+            const int pos = run[e] + pre + lrank;
+            p.ws.perm[pos] = q;
+            p.ws.inv[q] = pos;
+        }
+        __syncthreads();
+        for (int e2 = tid; e2 < E; e2 += kThreads) {
+            int s = 0;
+            for (int w = 0; w < kWarps; w++) { s += wcnt[w * E + e2]; wcnt[w * E + e2] = 0; }
+            run[e2] += s;
+        }
+        __syncthreads();
+    }
+}
+
+// Shared tail of both router kernels: every block signs in; the last one to
+// arrive sees all logits and runs top-K (and the buckets when asked).
+__device__ void router_tail(const Params &p, int T, int buckets, unsigned nblocks, float *smem) {
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned prev = atomicAdd(p.ws.counters, 1u);
+        s_last = (prev == nblocks - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    topk_phase(p, T, smem);
+    __syncthreads();
+    if (buckets) bucket_phase(p, T, reinterpret_cast<int *>(smem));
+    if (threadIdx.x == 0) *p.ws.counters = 0u;     // ready for the next call
+}
+
+// Router for T <= kGemvMaxT tokens: one warp per expert row.  Also writes
+// rnorm and the permuted (and pre-normed) activations used by gate/up.
+__global__ void __launch_bounds__(kThreads) router_gemv_kernel(Params p, const float *__restrict__ x,
+                                                               int T, int buckets) {
+    extern __shared__ float smem[];
+    __shared__ float s_r[kGemvMaxT];
+    const int H = p.d.H, E = p.d.E;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < T) {
+        float ss = 0.0f;
+        if (p.d.prenorm) {
+            const float4 *x4 = reinterpret_cast<const float4 *>(x + (size_t)warp * H);
+            for (int i = lane; i < H / 4; i += 32) {
+                const float4 v = __ldg(x4 + i);
+                ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
+                ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+            }
+            ss = warp_sum(ss);
+        }
+        const float r = p.d.prenorm ? 1.0f / sqrtf(ss / (float)H + p.d.eps) : 1.0f;
+        if (lane == 0) {
+            s_r[warp] = r;
+            if (blockIdx.x == 0) p.ws.rnorm[warp] = r;
+        }
+    }
+    __syncthreads();
+    for (int i = blockIdx.x * kThreads + threadIdx.x; i < T * H; i += gridDim.x * kThreads) {
+        const int t = i / H, c = i - t * H;
+        p.ws.xperm[(size_t)t * H + perm_pos(c, H)] = x[i] * s_r[t];
+    }
+    const int e = blockIdx.x * kWarps + warp;
+    if (e < E) {
+        float acc[kGemvMaxT];
+#pragma unroll
+        for (int t = 0; t < kGemvMaxT; t++) acc[t] = 0.0f;
+        const float4 *w4 = reinterpret_cast<const float4 *>(p.router_w + (size_t)e * H);
+        for (int i = lane; i < H / 4; i += 32) {
+            const float4 wv = __ldg(w4 + i);
+#pragma unroll
+            for (int t = 0; t < kGemvMaxT; t++) {
+                if (t < T) {
+                    const float4 xv = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H) + i);
+                    acc[t] = fmaf(wv.x, xv.x, acc[t]);
+                    acc[t] = fmaf(wv.y, xv.y, acc[t]);
+                    acc[t] = fmaf(wv.z, xv.z, acc[t]);
+                    acc[t] = fmaf(wv.w, xv.w, acc[t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kGemvMaxT; t++) {
+            if (t < T) {
+                const float v = warp_sum(acc[t]);
+                if (lane == 0) p.ws.logits[(size_t)t * E + e] = v * s_r[t];
+            }
+        }
+    }
+    router_tail(p, T, buckets, gridDim.x, smem);
+}
+
+// Router for larger T: a 32 (experts) x 32 (tokens) tile per block, k-loop
+// over H in steps of 32 through shared memory.
+__global__ void __launch_bounds__(kThreads) router_tiled_kernel(Params p, const float *__restrict__ x,
+                                                                int T, int buckets) {
+    extern __shared__ float smem[];
+    __shared__ float Ws[32][33];
+    __shared__ float Xs[32][33];
+    __shared__ float s_r[32];
+    const int H = p.d.H, E = p.d.E;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int e0 = blockIdx.x * 32, t0 = blockIdx.y * 32;
+    const int ty = tid >> 4, tx = tid & 15;
+    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    float ss[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = 0; k0 < H; k0 += 32) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int row = warp + 8 * i;      // tile row handled by this warp
+            const int e = e0 + row, t = t0 + row;
+            Ws[row][lane] = e < E ? __ldg(p.router_w + (size_t)e * H + k0 + lane) : 0.0f;
+            const float xv = t < T ? __ldg(x + (size_t)t * H + k0 + lane) : 0.0f;
+            Xs[row][lane] = xv;
+            ss[i] = fmaf(xv, xv, ss[i]);
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int kk = 0; kk < 32; kk++) {
+            const float a0 = Ws[ty * 2][kk], a1 = Ws[ty * 2 + 1][kk];
+            const float b0 = Xs[tx * 2][kk], b1 = Xs[tx * 2 + 1][kk];
+            acc[0][0] = fmaf(a0, b0, acc[0][0]);
+            acc[0][1] = fmaf(a0, b1, acc[0][1]);
+            acc[1][0] = fmaf(a1, b0, acc[1][0]);
+            acc[1][1] = fmaf(a1, b1, acc[1][1]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; i++) {
+        const float s = warp_sum(ss[i]);
+        if (lane == 0)
+            s_r[warp + 8 * i] = p.d.prenorm ? 1.0f / sqrtf(s / (float)H + p.d.eps) : 1.0f;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int a = 0; a < 2; a++)
+#pragma unroll
+        for (int b = 0; b < 2; b++) {
+            const int e = e0 + ty * 2 + a, tl = tx * 2 + b, t = t0 + tl;
+            if (e < E && t < T) p.ws.logits[(size_t)t * E + e] = acc[a][b] * s_r[tl];
+        }
+    if (blockIdx.x == 0) {
+        for (int tl = warp; tl < 32 && t0 + tl < T; tl += kWarps) {
+            const int t = t0 + tl;
+            if (lane == 0) p.ws.rnorm[t] = s_r[tl];
+            for (int i = lane; i < H; i += 32)
+                p.ws.xperm[(size_t)t * H + perm_pos(i, H)] = x[(size_t)t * H + i] * s_r[tl];
+        }
+    }
+    router_tail(p, T, buckets, gridDim.x * gridDim.y, smem);
+}
+
+// ---------------------------------------------------------------------------
+// Decode (T == 1): slot j < K is the j-th routed choice, slot K the shared expert
+// ---------------------------------------------------------------------------
+
+template <int RPW>
+__global__ void __launch_bounds__(kThreads) gateup_decode_kernel(Params p) {
+    const int H = p.d.H, C = H >> 5;
+    const int slot = blockIdx.y;
+    const uint8_t *slab;
+    const float *sc;
+    int Is;
+    if (slot < p.d.K) {
+        const int e = p.ws.topk_idx[slot];
+        slab = p.slabs[e];
+        sc = p.scales[e];
+        Is = p.d.I;
+    } else {
+        slab = p.sh_slab;
+        sc = p.sh_scale;
+        Is = p.d.I_sh;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = (blockIdx.x * kWarps + warp) * RPW;
+    if (row0 >= Is) return;
+    const size_t rb = (size_t)(H >> 1);
+    const uint8_t *g0 = slab + (size_t)row0 * rb;
+    const uint8_t *u0 = slab + ((size_t)Is + row0) * rb;
+    float ag[RPW], au[RPW];
+#pragma unroll
+    for (int r = 0; r < RPW; r++) { ag[r] = 0.f; au[r] = 0.f; }
+#pragma unroll 2
+    for (int c = lane; c < C; c += 32) {
+        uint4 wg[RPW], wu[RPW];
+#pragma unroll
+        for (int r = 0; r < RPW; r++) {
+            wg[r] = ld_stream(g0 + r * rb + (size_t)c * 16);
+            wu[r] = ld_stream(u0 + r * rb + (size_t)c * 16);
+        }
+        float4 xv[8];
+        load_chunk_act(p.ws.xperm, C, c, xv);
+#pragma unroll
+        for (int r = 0; r < RPW; r++) {
+            ag[r] = dot_chunk(wg[r], xv, ag[r]);
+            au[r] = dot_chunk(wu[r], xv, au[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RPW; r++) {
+        const float g = warp_sum(ag[r]);
+        const float u = warp_sum(au[r]);
+        if (lane == r) {
+            const int o = row0 + r;
+            const float hv = silu_mul(sc[o] * g, sc[Is + o] * u);
+            p.ws.h[(size_t)slot * p.d.I_max + perm_pos(o, Is)] = hv;
+        }
+    }
+}
+
+constexpr int kMaxSlots = 33;   // K <= 32 routed + 1 shared
+
+template <int RPW>
+__global__ void __launch_bounds__(kThreads) down_decode_kernel(Params p, const float *__restrict__ x,
+                                                               float *__restrict__ y) {
+    __shared__ const uint8_t *s_slab[kMaxSlots];
+    __shared__ const float *s_sc[kMaxSlots];
+    __shared__ float s_w[kMaxSlots];
+    const int H = p.d.H, K = p.d.K, I = p.d.I, Ish = p.d.I_sh;
+    const int J = K + p.d.n_shared;
+    if (threadIdx.x < J) {
+        const int j = threadIdx.x;
+        if (j < K) {
+            const int e = p.ws.topk_idx[j];
+            s_slab[j] = p.slabs[e];
+            s_sc[j] = p.scales[e];
+            s_w[j] = p.ws.topk_w[j];
+        } else {
+            s_slab[j] = p.sh_slab;
+            s_sc[j] = p.sh_scale;
+            s_w[j] = 1.0f;
+        }
+    }
+    __syncthreads();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = (blockIdx.x * kWarps + warp) * RPW;
+    if (row0 >= H) return;
+    const int C = I >> 5, Csh = Ish >> 5;
+    const int Qr = K * C;
+    const int Q = Qr + (p.d.n_shared ? Csh : 0);
+    float acc[RPW];
+#pragma unroll
+    for (int r = 0; r < RPW; r++) acc[r] = 0.f;
+    // (slot, chunk) items strided over the lanes; every item adds
+    // w_j * s_d[o] * dot(Q_d[o, chunk], h_j[chunk]) to row o.
+#pragma unroll 2
+    for (int q = lane; q < Q; q += 32) {
+        int j, c, Ij;
+        if (q < Qr) { j = q / C; c = q - j * C; Ij = I; }
+        else { j = K; c = q - Qr; Ij = Ish; }
+        const size_t rbI = (size_t)(Ij >> 1);
+        const uint8_t *d0 = s_slab[j] + 2 * (size_t)Ij * (size_t)(H >> 1) + (size_t)row0 * rbI + (size_t)c * 16;
+        uint4 wv[RPW];
+#pragma unroll
+        for (int r = 0; r < RPW; r++) wv[r] = ld_stream(d0 + r * rbI);
+        float4 hv[8];
+        load_chunk_act(p.ws.h + (size_t)j * p.d.I_max, Ij >> 5, c, hv);
+        const float *sd = s_sc[j] + 2 * Ij;
+        const float wj = s_w[j];
+#pragma unroll
+        for (int r = 0; r < RPW; r++) {
+            const float part = dot_chunk(wv[r], hv, 0.0f);
+            acc[r] = fmaf(wj * sd[row0 + r], part, acc[r]);
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RPW; r++) {
+        const float v = warp_sum(acc[r]);
+        if (lane == r) {
+            const int o = row0 + r;
+            y[o] = p.d.prenorm ? x[o] + v : v;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Batched (T > 1): slot s < n_slots is the s-th active expert with its tokens,
+// slot n_slots the shared expert over all T tokens.
+// ---------------------------------------------------------------------------
+
+struct SlotInfo {
+    const uint8_t *slab;
+    const float *sc;
+    int Is;          // intermediate size of this expert
+    int n;           // tokens in the slot
+    int base;        // first position in perm (routed) or -1 (shared)
+    bool valid;
+};
+
+__device__ __forceinline__ SlotInfo slot_info(const Params &p, int T, int slot) {
+    SlotInfo s;
+    const int ns = *p.ws.n_slots;
+    s.valid = true;
+    if (slot < ns) {
+        const int e = p.ws.slot_expert[slot];
+        s.slab = p.slabs[e];
+        s.sc = p.scales[e];
+        s.Is = p.d.I;
+        s.n = p.ws.cnt[e];
+        s.base = p.ws.off[e];
+    } else if (slot == ns && p.d.n_shared) {
+        s.slab = p.sh_slab;
+        s.sc = p.sh_scale;
+        s.Is = p.d.I_sh;
+        s.n = T;
+        s.base = -1;
+    } else {
+        s.valid = false;
+        s.slab = nullptr; s.sc = nullptr; s.Is = 0; s.n = 0; s.base = 0;
+    }
+    return s;
+}
+
+// token index and h/d row of the u-th token of a slot
+__device__ __forceinline__ void slot_token(const Params &p, const SlotInfo &s, int T, int u,
+                                           int *tok, int *row) {
+    if (s.base < 0) { *tok = u; *row = T * p.d.K + u; }
+    else { const int pos = s.base + u; *tok = p.ws.perm[pos] / p.d.K; *row = pos; }
+}
+
+template <int RPW, int NT>
+__global__ void __launch_bounds__(kThreads) gateup_batched_kernel(Params p, int T) {
+    const SlotInfo s = slot_info(p, T, blockIdx.y);
+    if (!s.valid) return;
+    const int H = p.d.H, C = H >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = (blockIdx.x * kWarps + warp) * RPW;
+    if (row0 >= s.Is) return;
+    const size_t rb = (size_t)(H >> 1);
+    const uint8_t *g0 = s.slab + (size_t)row0 * rb;
+    const uint8_t *u0 = s.slab + ((size_t)s.Is + row0) * rb;
+    for (int tb = 0; tb < s.n; tb += NT) {
+        int tok[NT], hrow[NT];
+#pragma unroll
+        for (int u = 0; u < NT; u++) {
+            if (tb + u < s.n) slot_token(p, s, T, tb + u, &tok[u], &hrow[u]);
+            else { tok[u] = 0; hrow[u] = -1; }
+        }
+        float ag[NT][RPW], au[NT][RPW];
+#pragma unroll
+        for (int u = 0; u < NT; u++)
+#pragma unroll
+            for (int r = 0; r < RPW; r++) { ag[u][r] = 0.f; au[u][r] = 0.f; }
+        for (int c = lane; c < C; c += 32) {
+            uint4 wg[RPW], wu[RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; r++) {
+                wg[r] = ld_stream(g0 + r * rb + (size_t)c * 16);
+                wu[r] = ld_stream(u0 + r * rb + (size_t)c * 16);
+            }
+#pragma unroll
+            for (int u = 0; u < NT; u++) {
+                if (hrow[u] < 0) continue;
+                float4 xv[8];
+                load_chunk_act(p.ws.xperm + (size_t)tok[u] * H, C, c, xv);
+#pragma unroll
+                for (int r = 0; r < RPW; r++) {
+                    ag[u][r] = dot_chunk(wg[r], xv, ag[u][r]);
+                    au[u][r] = dot_chunk(wu[r], xv, au[u][r]);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NT; u++) {
+#pragma unroll
+            for (int r = 0; r < RPW; r++) {
+                const float g = warp_sum(ag[u][r]);
+                const float uu = warp_sum(au[u][r]);
+                if (lane == r && hrow[u] >= 0) {
+                    const int o = row0 + r;
+                    p.ws.h[(size_t)hrow[u] * p.d.I_max + perm_pos(o, s.Is)] =
+                        silu_mul(s.sc[o] * g, s.sc[s.Is + o] * uu);
+                }
+            }
+        }
+    }
+}
+
+template <int RPW, int NT>
+__global__ void __launch_bounds__(kThreads) down_batched_kernel(Params p, int T) {
+    const SlotInfo s = slot_info(p, T, blockIdx.y);
+    if (!s.valid) return;
+    const int H = p.d.H, Cj = s.Is >> 5;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int row0 = (blockIdx.x * kWarps + warp) * RPW;
+    if (row0 >= H) return;
+    const size_t rbI = (size_t)(s.Is >> 1);
+    const uint8_t *d0 = s.slab + 2 * (size_t)s.Is * (size_t)(H >> 1) + (size_t)row0 * rbI;
+    const float *sd = s.sc + 2 * s.Is;
+    for (int tb = 0; tb < s.n; tb += NT) {
+        int tok[NT], hrow[NT];
+#pragma unroll
+        for (int u = 0; u < NT; u++) {
+            if (tb + u < s.n) slot_token(p, s, T, tb + u, &tok[u], &hrow[u]);
+            else { tok[u] = 0; hrow[u] = -1; }
+        }
+        float acc[NT][RPW];
+#pragma unroll
+        for (int u = 0; u < NT; u++)
+#pragma unroll
+            for (int r = 0; r < RPW; r++) acc[u][r] = 0.f;
+        for (int c = lane; c < Cj; c += 32) {
+            uint4 wv[RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; r++) wv[r] = ld_stream(d0 + r * rbI + (size_t)c * 16);
+#pragma unroll
+            for (int u = 0; u < NT; u++) {
+                if (hrow[u] < 0) continue;
+                float4 hv[8];
+                load_chunk_act(p.ws.h + (size_t)hrow[u] * p.d.I_max, Cj, c, hv);
+#pragma unroll
+                for (int r = 0; r < RPW; r++) acc[u][r] = dot_chunk(wv[r], hv, acc[u][r]);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NT; u++) {
+#pragma unroll
+            for (int r = 0; r < RPW; r++) {
+                const float v = warp_sum(acc[u][r]);
+                if (lane == r && hrow[u] >= 0) {
+                    const int o = row0 + r;
+                    p.ws.dbuf[(size_t)hrow[u] * H + o] = sd[o] * v;
+                }
+            }
+        }
+    }
+}
+
+// y[t] = sum_k w[t,k] d[(t,k)] (k ascending) + d_shared[t] (+ x[t] with pre-norm residual)
+__global__ void __launch_bounds__(kThreads) combine_kernel(Params p, const float *__restrict__ x,
+                                                           float *__restrict__ y, int T) {
+    const int t = blockIdx.x, H = p.d.H, K = p.d.K;
+    for (int o = threadIdx.x; o < H; o += kThreads) {
+        float v = 0.0f;
+        for (int k = 0; k < K; k++) {
+            const int q = t * K + k;
+            v = fmaf(p.ws.topk_w[q], p.ws.dbuf[(size_t)p.ws.inv[q] * H + o], v);
+        }
+        if (p.d.n_shared) v += p.ws.dbuf[(size_t)(T * K + t) * H + o];
+        if (p.d.prenorm) v += x[(size_t)t * H + o];
+        y[(size_t)t * H + o] = v;
+    }
+}
+
+size_t router_smem_bytes(const Dims &d) {
+    const size_t topk = (size_t)kWarps * 2 * d.E * sizeof(float);
+    const size_t bucket = (size_t)(2 + kWarps) * d.E * sizeof(int);
+    return topk > bucket ? topk : bucket;
+}
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Workspace
+// ---------------------------------------------------------------------------
+
+size_t workspace_bytes(const Dims &d) {
+    Workspace ws;
+    carve_workspace(d, nullptr, &ws);
+    return reinterpret_cast<size_t>(ws.dbuf) +
+           align_up((size_t)(d.max_tokens * d.K + d.max_tokens) * d.H * sizeof(float), 256);
+}
+
+void carve_workspace(const Dims &d, void *base, Workspace *ws) {
+    char *b = static_cast<char *>(base);
+    size_t o = 0;
+    auto take = [&](size_t bytes) { char *r = b + o; o += align_up(bytes, 256); return r; };
+    const size_t T = d.max_tokens, P = T * d.K;
+    ws->rnorm = reinterpret_cast<float *>(take(T * sizeof(float)));
+    ws->xperm = reinterpret_cast<float *>(take(T * d.H * sizeof(float)));
+    ws->logits = reinterpret_cast<float *>(take(T * d.E * sizeof(float)));
+    ws->topk_idx = reinterpret_cast<int *>(take(P * sizeof(int)));
+    ws->topk_w = reinterpret_cast<float *>(take(P * sizeof(float)));
+    ws->counters = reinterpret_cast<unsigned *>(take(16 * sizeof(unsigned)));
+    ws->h = reinterpret_cast<float *>(take((P + T) * d.I_max * sizeof(float)));
+    ws->cnt = reinterpret_cast<int *>(take(d.E * sizeof(int)));
+    ws->off = reinterpret_cast<int *>(take((d.E + 1) * sizeof(int)));
+    ws->perm = reinterpret_cast<int *>(take(P * sizeof(int)));
+    ws->inv = reinterpret_cast<int *>(take(P * sizeof(int)));
+    ws->slot_expert = reinterpret_cast<int *>(take(d.E * sizeof(int)));
+    ws->n_slots = reinterpret_cast<int *>(take(sizeof(int)));
+    ws->dbuf = reinterpret_cast<float *>(take(0));
+}
+
+// ---------------------------------------------------------------------------
+// Launch
+// ---------------------------------------------------------------------------
+
+cudaError_t prepare_kernels(const Dims &d) {
+    const int smem = (int)router_smem_bytes(d);
+    cudaError_t e = cudaFuncSetAttribute(router_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(router_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+
+cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cudaStream_t st,
+                           bool want_buckets, cudaEvent_t *ev) {
+    const Dims &d = p.d;
+    const size_t smem = router_smem_bytes(d);
+    const int buckets = (T > 1 || want_buckets) ? 1 : 0;
+    cudaError_t e = cudaSuccess;
+    auto mark = [&](int i) {
+        if (ev && e == cudaSuccess) e = cudaEventRecord(ev[i], st);
+    };
+    auto check = [&]() {
+        if (e == cudaSuccess) e = cudaGetLastError();
+    };
+    mark(0);
+    if (T <= kGemvMaxT) {
+        const int grid = (d.E + kWarps - 1) / kWarps;
+        router_gemv_kernel<<<grid, kThreads, smem, st>>>(p, x, T, buckets);
+    } else {
+        const dim3 grid((d.E + 31) / 32, (T + 31) / 32);
+        router_tiled_kernel<<<grid, kThreads, smem, st>>>(p, x, T, buckets);
+    }
+    check();
+    mark(1);
+    if (T == 1) {
+        constexpr int RPW_GU = 2, RPW_D = 4;
+        const dim3 g1((d.I_max + kWarps * RPW_GU - 1) / (kWarps * RPW_GU), d.K + d.n_shared);
+        gateup_decode_kernel<RPW_GU><<<g1, kThreads, 0, st>>>(p);
+        check();
+        mark(2);
+        const int g2 = (d.H + kWarps * RPW_D - 1) / (kWarps * RPW_D);
+        down_decode_kernel<RPW_D><<<g2, kThreads, 0, st>>>(p, x, y);
+        check();
+        mark(3);
+        mark(4);
+        return e;
+    }
+    constexpr int RPW_GU = 2, RPW_D = 4, NT = 4;
+    const int slots = (d.E < T * d.K ? d.E : T * d.K) + d.n_shared;
+    const dim3 g1((d.I_max + kWarps * RPW_GU - 1) / (kWarps * RPW_GU), slots);
+    gateup_batched_kernel<RPW_GU, NT><<<g1, kThreads, 0, st>>>(p, T);
+    check();
+    mark(2);
+    const dim3 g2((d.H + kWarps * RPW_D - 1) / (kWarps * RPW_D), slots);
+    down_batched_kernel<RPW_D, NT><<<g2, kThreads, 0, st>>>(p, T);
+    check();
+    mark(3);
+    combine_kernel<<<T, kThreads, 0, st>>>(p, x, y, T);
+    check();
+    mark(4);
+    return e;
+}
+
+}  // namespace moe

@@ -1,0 +1,73 @@
+"""Helpers shared by the GPU parity tests: upload a synthetic layer, compare a
+GPU call with the oracle under the selection-margin rule."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+
+MARGIN = 1e-5      # selection must match exactly when c_(K) - c_(K+1) > MARGIN
+REL_TOL = 2e-3     # per token: max|y - y_ref| / max|y_ref|
+W_RTOL = 1e-4      # routing weights, per expert id (float32 sigmoid vs double)
+
+
+def gpu_config(moe, wl):
+    return moe.make_config(wl.H, wl.E, wl.K, wl.I, wl.n_shared, wl.I_shared, wl.routed_scale,
+                           wl.norm_topk, wl.prenorm_residual, wl.rms_eps)
+
+
+def upload(moe, wl, li, max_tokens):
+    return moe.MoeLayer(gpu_config(moe, wl), li.router_w, li.router_b, li.slabs, li.scales,
+                        li.sh_slab, li.sh_scale, max_tokens=max_tokens)
+
+
+def oracle_layer(wl, li, experts=None):
+    return oracle.LayerRef.from_inputs(oracle.cfg_from_workload(wl), li, experts)
+
+
+def rel_err(y, y_ref):
+    den = np.abs(y_ref).max()
+    return float(np.abs(y - y_ref).max() / (den if den > 0 else 1.0))
+
+
+def check_token(wl, ref: oracle.LayerRef, x_t, y_gpu, idx_gpu, w_gpu, where=""):
+    """Check one token.  Returns (rel_err, near_tie)."""
+    x64 = np.asarray(x_t, dtype=np.float64)
+    xin = oracle.rmsnorm(x64, wl.rms_eps) if wl.prenorm_residual else x64
+    idx_ref, w_ref, margin, scores = oracle.route(ref.cfg, ref.router_w, ref.router_b, xin)
+    choice = scores[2]
+    idx_gpu = np.asarray(idx_gpu, dtype=np.int64)
+    assert np.all((idx_gpu >= 0) & (idx_gpu < wl.E)), (where, idx_gpu)
+    assert len(set(idx_gpu.tolist())) == wl.K, (where, idx_gpu)
+    near_tie = margin <= MARGIN
+    if not near_tie:
+        assert sorted(idx_gpu.tolist()) == sorted(idx_ref.tolist()), (where, idx_gpu, idx_ref, margin)
+        forced = None
+    else:
+        kth = choice[idx_ref[-1]]
+        assert np.all(choice[idx_gpu] >= kth - MARGIN), (where, idx_gpu, idx_ref, margin)
+        forced = idx_gpu.astype(np.int32)
+    # GPU order is descending selection score (up to float32 rounding)
+    c = choice[idx_gpu]
+    assert np.all(c[:-1] >= c[1:] - MARGIN), (where, c)
+    y_ref, idx_used, w_used, _ = ref.token(x64, forced_idx=forced)
+    # weights compared per expert id
+    ref_w = dict(zip(idx_used.tolist(), w_used.tolist()))
+    for e, w in zip(idx_gpu.tolist(), np.asarray(w_gpu, dtype=np.float64).tolist()):
+        assert abs(w - ref_w[e]) <= W_RTOL * max(abs(ref_w[e]), 1e-30), (where, e, w, ref_w[e])
+    err = rel_err(np.asarray(y_gpu, dtype=np.float64), y_ref)
+    assert err <= REL_TOL, (where, err)
+    return err, near_tie
+
+
+def selected_experts(wl, li, x, experts_hint=None):
+    """Experts the oracle needs for these tokens (its own choice plus any hint)."""
+    ref = oracle_layer(wl, li, experts=[])
+    need = set(experts_hint or [])
+    for t in range(x.shape[0]):
+        x64 = x[t].astype(np.float64)
+        xin = oracle.rmsnorm(x64, wl.rms_eps) if wl.prenorm_residual else x64
+        idx, _, _, _ = oracle.route(ref.cfg, ref.router_w, ref.router_b, xin)
+        need.update(idx.tolist())
+    return need

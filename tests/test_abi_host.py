@@ -1,0 +1,93 @@
+"""The C-ABI library loads, exports every symbol include/moe.h declares, and
+rejects bad configurations and arguments on the host (no GPU needed)."""
+import ctypes as C
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import __graft_entry__
+    __graft_entry__.build()
+    import int4_moe_expert_gb300 as m
+    return m
+
+
+def declared_functions():
+    text = (ROOT / "include" / "moe.h").read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("moe_init", "moe_forward", "moe_forward_debug", "moe_forward_host", "moe_destroy",
+              "moe_last_error", "moe_workspace_bytes", "moe_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(moe):
+    L = C.CDLL(str(moe.library_path()))
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_config_struct_layout_matches_header(moe):
+    # eleven 4-byte fields, no padding
+    assert C.sizeof(moe.MoeConfig) == 44
+    assert C.sizeof(moe.MoeWeights) == 6 * C.sizeof(C.c_void_p)
+
+
+def test_workspace_bytes_validates_config(moe):
+    good = moe.make_config(6144, 256, 8, 2048, 1, 2048, 2.5)
+    assert moe.moe_workspace_bytes(good, 1) > 0
+    assert moe.moe_workspace_bytes(good, 512) > moe.moe_workspace_bytes(good, 1)
+    bad = [
+        moe.make_config(6144, 256, 0, 2048, 1, 2048),        # K = 0
+        moe.make_config(6144, 4, 8, 2048, 1, 2048),          # K > E
+        moe.make_config(6144, 256, 33, 2048, 1, 2048),       # K > 32
+        moe.make_config(6100, 256, 8, 2048, 1, 2048),        # H not a multiple of 32
+        moe.make_config(6144, 256, 8, 2000, 1, 2048),        # I not a multiple of 32
+        moe.make_config(6144, 256, 8, 2048, 1, 100),         # I_shared not a multiple of 32
+        moe.make_config(6144, 256, 8, 2048, 2, 2048),        # two shared experts
+        moe.make_config(6144, 256, 8, 2048, 1, 2048, n_group=8),
+        moe.make_config(6144, 2048, 8, 2048, 1, 2048),       # E > 1024
+        moe.make_config(6144, 256, 8, 2048, 1, 2048, routed_scale=float("inf")),
+    ]
+    for cfg in bad:
+        assert moe.moe_workspace_bytes(cfg, 1) == 0
+    assert moe.moe_workspace_bytes(good, 0) == 0
+    assert moe.moe_workspace_bytes(good, 1 << 20) == 0
+
+
+def test_null_arguments_are_errors_not_crashes(moe):
+    L = moe.lib()
+    cfg = moe.make_config(256, 16, 2, 128, 1, 128, 2.5)
+    h = C.c_void_p(123)
+    assert L.moe_init(C.byref(cfg), None, 1, C.byref(h)) == moe.MOE_ERR_INVALID
+    assert h.value is None
+    assert "weights" in moe.moe_last_error()
+    assert L.moe_init(None, None, 1, C.byref(h)) == moe.MOE_ERR_INVALID
+    assert L.moe_forward(None, None, 1, None, None) == moe.MOE_ERR_INVALID
+    assert L.moe_forward_host(None, None, 1, None, None) == moe.MOE_ERR_INVALID
+    assert L.moe_destroy(None) == moe.MOE_OK
+    cfg_bad = moe.make_config(256, 16, 2, 128, 1, 128, n_group=4)
+    assert L.moe_init(C.byref(cfg_bad), None, 1, C.byref(h)) == moe.MOE_ERR_UNSUPPORTED
+    assert "n_group" in moe.moe_last_error()
+    with pytest.raises(moe.MoeError):
+        moe.moe_forward(0, None, 1, None, stream=0)
+
+
+def test_abi_version(moe):
+    assert moe.moe_abi_version() == 1
+
+
+def test_product_path_does_not_reference_the_oracle():
+    pkg = ROOT / "int4_moe_expert_gb300"
+    for f in list(pkg.rglob("*.py")) + list(pkg.rglob("*.cu")) + list(pkg.rglob("*.h")):
+        text = f.read_text()
+        assert "oracle" not in text.lower(), f

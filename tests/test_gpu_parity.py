@@ -1,0 +1,281 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the
+double-precision oracle on the same seeded inputs.
+
+Bar: expert selection identical whenever the oracle's K-th/(K+1)-th score
+margin exceeds 1e-5 (otherwise the GPU's set must be within 1e-5 of the
+K-th score and the output is checked against the oracle re-run with that
+set); per token max|y - y_ref| / max|y_ref| <= 2e-3; routing weights within
+1e-4 relative per expert id.
+"""
+import numpy as np
+import pytest
+
+import synth
+from parity_util import (MARGIN, REL_TOL, check_token, oracle_layer, rel_err, upload)
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import int4_moe_expert_gb300 as m
+    return m
+
+
+_LAYERS = {}
+
+
+def layer_for(moe, name, max_tokens):
+    """Upload each workload once per module (GLM-size layers are ~4.9 GB);
+    a new workload evicts the previous one."""
+    key = (name, max_tokens)
+    if key not in _LAYERS:
+        for k in list(_LAYERS):
+            _LAYERS.pop(k)[2].close()
+        wl = synth.WORKLOADS[name]
+        li = synth.layer_inputs(wl)
+        _LAYERS[key] = (wl, li, upload(moe, wl, li, max_tokens))
+    return _LAYERS[key]
+
+
+def run_and_check(moe, wl, li, layer, x, where):
+    xd = torch.from_numpy(x).cuda()
+    y, idx, w = layer.forward_debug(xd)
+    torch.cuda.synchronize()
+    y, idx, w = y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+    ref = oracle_layer(wl, li)
+    errs = []
+    for t in range(x.shape[0]):
+        err, _ = check_token(wl, ref, x[t], y[t], idx[t], w[t], where=f"{where} t={t}")
+        errs.append(err)
+    return max(errs), y
+
+
+# --- decode (T = 1) -------------------------------------------------------------
+
+@pytest.mark.parametrize("name,streams", [("tiny", 16), ("olmoe", 8)])
+def test_decode_small_configs(moe, name, streams):
+    wl, li, layer = layer_for(moe, name, 64)
+    for s in range(streams):
+        run_and_check(moe, wl, li, layer, synth.tokens(wl, T=1, stream=s), f"{name} stream {s}")
+
+
+def test_decode_glm(moe):
+    wl, li, layer = layer_for(moe, "glm_decode", 1)
+    worst = 0.0
+    for s in range(4):
+        err, _ = run_and_check(moe, wl, li, layer, synth.tokens(wl, T=1, stream=s), f"glm s={s}")
+        worst = max(worst, err)
+    print(f"glm decode worst rel err {worst:.3e}")
+
+
+def test_decode_is_deterministic(moe):
+    wl, li, layer = layer_for(moe, "glm_decode", 1)
+    x = torch.from_numpy(synth.tokens(wl, T=1, stream=7)).cuda()
+    a = layer.forward(x).clone()
+    b = layer.forward(x).clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_host_entry_point_matches_device_call(moe):
+    wl, li, layer = layer_for(moe, "olmoe", 64)
+    x = synth.tokens(wl, T=3, stream=11)
+    y_dev = layer.forward(torch.from_numpy(x).cuda()).cpu().numpy()
+    y_host = layer.forward_host(x)
+    assert np.array_equal(y_dev, y_host)
+    pinned = torch.from_numpy(x).pin_memory()
+    out = torch.empty_like(pinned).pin_memory()
+    moe.moe_forward_host(layer.handle, pinned, 3, out)
+    assert np.array_equal(out.numpy(), y_dev)
+
+
+# --- batched (T > 1) --------------------------------------------------------------
+
+@pytest.mark.parametrize("name,T", [("tiny", 2), ("tiny", 7), ("tiny", 33), ("olmoe", 3),
+                                    ("olmoe", 17), ("olmoe", 64)])
+def test_batched_small_configs_ragged(moe, name, T):
+    wl, li, layer = layer_for(moe, name, 64)
+    run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=100 + T), f"{name} T={T}")
+
+
+def test_batched_glm_512_sampled(moe):
+    """Full-size batched layer: all 512 routing decisions, outputs on a sample."""
+    wl, li, layer = layer_for(moe, "glm_batched", 512)
+    x = synth.tokens(wl, T=512, stream=0)
+    xd = torch.from_numpy(x).cuda()
+    y, idx, w, cnt = layer.forward_debug(xd, counts=True)
+    torch.cuda.synchronize()
+    y, idx, w, cnt = y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy(), cnt.cpu().numpy()
+    # bucketing: a histogram of the routing decisions
+    assert cnt.sum() == 512 * wl.K
+    assert np.array_equal(cnt, np.bincount(idx.ravel(), minlength=wl.E))
+    ref = oracle_layer(wl, li)
+    import oracle
+    n_tie = 0
+    for t in range(512):
+        ridx, _, margin, scores = oracle.route(ref.cfg, ref.router_w, ref.router_b,
+                                               x[t].astype(np.float64))
+        if margin > MARGIN:
+            assert sorted(idx[t].tolist()) == sorted(ridx.tolist()), t
+        else:
+            n_tie += 1
+            assert np.all(scores[2][idx[t]] >= scores[2][ridx[-1]] - MARGIN), t
+    # load is uneven, as the workload asks (bias ~ N(0, 0.5))
+    assert cnt.max() >= 2 * cnt[cnt > 0].mean()
+    rng = np.random.default_rng(0)
+    sample = sorted(set([0, 1, 255, 511] + rng.choice(512, 20, replace=False).tolist()))
+    worst = 0.0
+    for t in sample:
+        err, _ = check_token(wl, ref, x[t], y[t], idx[t], w[t], where=f"glm512 t={t}")
+        worst = max(worst, err)
+    print(f"glm batched: worst sampled rel err {worst:.3e}, near ties {n_tie}")
+
+
+def test_batched_is_deterministic_and_token_independent(moe):
+    wl, li, layer = layer_for(moe, "olmoe", 64)
+    x = synth.tokens(wl, T=40, stream=3)
+    xd = torch.from_numpy(x).cuda()
+    a = layer.forward(xd).clone()
+    b = layer.forward(xd).clone()
+    assert torch.equal(a, b)
+    # a token's output does not depend on the rest of the batch beyond rounding
+    c = layer.forward(xd[5:6].contiguous())
+    torch.cuda.synchronize()
+    assert rel_err(c.cpu().numpy()[0].astype(np.float64), a[5].cpu().numpy().astype(np.float64)) < 1e-5
+
+
+# --- 40-layer stack (x <- x + moe(rmsnorm(x))) -------------------------------------
+
+def test_stack_35b_40_layers(moe):
+    wl = synth.WORKLOADS["stack35b"]
+    x0 = synth.tokens(wl, T=1, stream=0)
+    x_gpu = torch.from_numpy(x0).cuda()
+    x_ref = x0[0].astype(np.float64)
+    chain_ok = True
+    worst_tf = 0.0
+    for l in range(wl.n_layers):
+        li = synth.layer_inputs(wl, layer=l)
+        layer = upload(moe, wl, li, 1)
+        x_in = x_gpu.cpu().numpy()
+        y, idx, w = layer.forward_debug(x_gpu)
+        torch.cuda.synchronize()
+        ref = oracle_layer(wl, li)
+        # teacher-forced: the oracle gets this layer's GPU input
+        err, tie = check_token(wl, ref, x_in[0], y.cpu().numpy()[0], idx.cpu().numpy()[0],
+                               w.cpu().numpy()[0], where=f"stack layer {l}")
+        worst_tf = max(worst_tf, err)
+        # free-running oracle chain
+        y_ref, _, _, margin = ref.token(x_ref)
+        chain_ok &= margin > MARGIN
+        x_ref = y_ref
+        x_gpu = y
+        layer.close()
+        del li
+    final = x_gpu.cpu().numpy()[0].astype(np.float64)
+    chain_err = rel_err(final, x_ref)
+    print(f"stack: worst teacher-forced layer err {worst_tf:.3e}, chained err {chain_err:.3e}")
+    if chain_ok:
+        assert chain_err <= REL_TOL
+
+
+# --- edge cases -------------------------------------------------------------------
+
+def small_workload(**kw):
+    base = dict(name="edge", T=1, H=64, E=8, K=2, I=32, n_shared=1, I_shared=64,
+                routed_scale=2.5, seed=77)
+    base.update(kw)
+    return synth.Workload(**base)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(E=4, K=4),                        # E == K: every expert selected
+    dict(K=1),
+    dict(n_shared=0, I_shared=0),
+    dict(I_shared=96),                     # shared inter != routed inter
+    dict(norm_topk=0, routed_scale=1.5),   # no renormalisation
+    dict(E=1, K=1, n_shared=0, I_shared=0),
+    dict(E=300, K=32, H=96),               # K at its limit, E not a multiple of 32
+    dict(n_layers=2),                      # pre-norm + residual flag (one layer here)
+])
+def test_edge_configs(moe, kw):
+    wl = small_workload(**kw)
+    li = synth.layer_inputs(wl)
+    layer = upload(moe, wl, li, 40)
+    for T in (1, 2, 37):
+        run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=T), f"{kw} T={T}")
+    layer.close()
+
+
+def test_empty_and_oversized_calls(moe):
+    wl = small_workload()
+    li = synth.layer_inputs(wl)
+    layer = upload(moe, wl, li, 4)
+    y = torch.full((4, wl.H), 7.0, device="cuda")
+    x = torch.zeros((4, wl.H), device="cuda")
+    moe.moe_forward(layer.handle, x, 0, y)          # T = 0 does nothing
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_forward(layer.handle, x, 5, y)
+    assert e.value.status == moe.MOE_ERR_INVALID
+    with pytest.raises(moe.MoeError):
+        moe.moe_forward(layer.handle, x, 2, x)      # y overlaps x
+    with pytest.raises(moe.MoeError):
+        moe.moe_forward(layer.handle, x[:, 1:], 1, y)  # misaligned
+    layer.close()
+
+
+def _weights_struct(moe, rw, rb, slab_ptrs, scale_ptrs, sh, shs):
+    import ctypes as C
+    E = len(slab_ptrs)
+    slabs = (C.c_void_p * E)(*slab_ptrs)
+    scales = (C.c_void_p * E)(*scale_ptrs)
+    w = moe.MoeWeights(rw.data_ptr(), rb.data_ptr(), C.cast(slabs, C.POINTER(C.c_void_p)),
+                       C.cast(scales, C.POINTER(C.c_void_p)), sh.data_ptr(), shs.data_ptr())
+    return w, (slabs, scales)
+
+
+def test_init_rejects_host_and_misaligned_weights(moe):
+    wl = small_workload()
+    li = synth.layer_inputs(wl)
+    cfg = moe.make_config(wl.H, wl.E, wl.K, wl.I, wl.n_shared, wl.I_shared, wl.routed_scale)
+    rw = torch.from_numpy(li.router_w).cuda()
+    rb = torch.from_numpy(li.router_b).cuda()
+    sh = torch.from_numpy(li.sh_slab).cuda()
+    shs = torch.from_numpy(li.sh_scale).cuda()
+    # host memory where device pointers are required
+    w, keep = _weights_struct(moe, rw, rb, [li.slabs[e].ctypes.data for e in range(wl.E)],
+                              [li.scales[e].ctypes.data for e in range(wl.E)], sh, shs)
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_init(cfg, w, 1)
+    assert e.value.status == moe.MOE_ERR_INVALID
+    # a slab pointer off a 16-byte boundary
+    dev_slabs = torch.from_numpy(li.slabs).cuda()
+    dev_scales = torch.from_numpy(li.scales).cuda()
+    sp = [dev_slabs.data_ptr() + e * dev_slabs.stride(0) for e in range(wl.E)]
+    sp[3] += 8
+    cp = [dev_scales.data_ptr() + e * dev_scales.stride(0) * 4 for e in range(wl.E)]
+    w, keep = _weights_struct(moe, rw, rb, sp, cp, sh, shs)
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_init(cfg, w, 1)
+    assert e.value.status == moe.MOE_ERR_INVALID and "aligned" in str(e.value)
+
+
+def test_nan_input_gives_valid_indices(moe):
+    wl = small_workload()
+    li = synth.layer_inputs(wl)
+    layer = upload(moe, wl, li, 2)
+    x = torch.from_numpy(synth.tokens(wl, T=2, stream=1)).cuda()
+    x[0, 5] = float("nan")
+    y, idx, w = layer.forward_debug(x)
+    torch.cuda.synchronize()
+    assert bool(((idx >= 0) & (idx < wl.E)).all())
+    assert torch.isnan(y[0]).all() and torch.isfinite(y[1]).all()
+    layer.close()
