@@ -144,6 +144,47 @@ const char *moe_last_error(void);
 
 int32_t moe_abi_version(void);
 
+/*
+ * Router only, with no device allocation.  (The pages have no counterpart:
+ * this is a convenience of this library.)
+ *
+ * Some callers may not allocate device memory: a host framework whose device
+ * memory all belongs to its own pool allocator, or a serving loop that must
+ * not call cudaMalloc/cudaFree because those calls can synchronise the device
+ * and can fail under memory pressure.  They cannot create a moe_handle, whose
+ * moe_init allocates a workspace.  This call computes, for T tokens x[T,H]
+ * (device float32), exactly what moe_forward_debug returns in topk_idx[T,K]
+ * (int32, descending selection score) and topk_w[T,K] (float32): router
+ * logits W_r x (with 1/rms(x) applied when cfg->flags has
+ * MOE_FLAG_PRENORM_RESIDUAL), sigmoid + bias top-K, renormalised weights.
+ * Only cfg's hidden, n_experts, top_k, n_group, norm_topk, routed_scale,
+ * rms_eps and flags are read.
+ *
+ * Scratch: one fixed static device array in the library (logits of up to
+ * MOE_ROUTE_NOALLOC_MAX_TOKENS x MOE_ROUTE_NOALLOC_MAX_EXPERTS floats plus a
+ * ticket counter, about 32 KB), held by every GPU that loads the library
+ * until the process exits.  The caller passes all inputs and outputs; the
+ * call allocates nothing (no cudaMalloc, no cudaFree).  The first call on a
+ * device looks the array's device address up with that device current (and
+ * sets the kernel's shared-memory limit); make that first call before any
+ * stream capture.  Every call shares the array: calls that overlap on the GPU
+ * (other streams, other host threads on the same device) race and must be
+ * serialised by the caller.  The call clears the ticket counter on `stream`
+ * before its kernel; logits are rewritten in full every call.
+ *
+ * Errors: MOE_ERR_INVALID for NULL or misaligned pointers (router_w and x
+ * 16-byte aligned), T outside 0..MOE_ROUTE_NOALLOC_MAX_TOKENS, bad top_k or
+ * norm_topk; MOE_ERR_UNSUPPORTED for hidden not a multiple of 32 in
+ * [32, 16384], n_experts outside 1..MOE_ROUTE_NOALLOC_MAX_EXPERTS, or
+ * n_group != 1; MOE_ERR_CUDA if a CUDA call fails.  T == 0 does nothing.
+ * This call does not set moe_last_error's message.
+ */
+#define MOE_ROUTE_NOALLOC_MAX_TOKENS 8
+#define MOE_ROUTE_NOALLOC_MAX_EXPERTS 1024
+moe_status moe_route_noalloc(const moe_config *cfg, const float *router_w, const float *router_bias,
+                             const float *x, int32_t T, int32_t *topk_idx, float *topk_w,
+                             void *stream);
+
 #ifdef __cplusplus
 }
 #endif

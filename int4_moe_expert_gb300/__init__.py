@@ -17,7 +17,7 @@ __all__ = [
     "MOE_FLAG_PRENORM_RESIDUAL", "MoeError", "MoeConfig", "MoeWeights", "MoeLayer",
     "lib", "library_path", "moe_init", "moe_forward", "moe_forward_debug", "moe_forward_host",
     "moe_destroy", "moe_last_error", "moe_workspace_bytes", "moe_abi_version",
-    "moe_profile_start", "moe_profile_read",
+    "moe_profile_start", "moe_profile_read", "moe_route_noalloc",
 ]
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_CUDA, MOE_ERR_NOMEM, MOE_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
@@ -80,6 +80,8 @@ def lib():
         L.moe_profile_start.restype = C.c_int
         L.moe_profile_read.argtypes = [vp, C.POINTER(i32), C.POINTER(C.c_float)]
         L.moe_profile_read.restype = C.c_int
+        L.moe_route_noalloc.argtypes = [C.POINTER(MoeConfig), vp, vp, vp, i32, vp, vp, vp]
+        L.moe_route_noalloc.restype = C.c_int
         _lib = L
     return _lib
 
@@ -154,6 +156,21 @@ def moe_profile_read(handle: int):
     ms = (C.c_float * MOE_PROFILE_STAGES)()
     _check(lib().moe_profile_read(handle, C.byref(n), ms), "moe_profile_read")
     return n.value, dict(zip(PROFILE_STAGE_NAMES, list(ms)))
+
+
+MOE_ROUTE_NOALLOC_MAX_TOKENS = 8
+MOE_ROUTE_NOALLOC_MAX_EXPERTS = 1024
+
+
+def moe_route_noalloc(cfg: MoeConfig, router_w, router_bias, x, T: int, topk_idx, topk_w,
+                      stream=None) -> None:
+    """Router + top-k without any device allocation by the library (its
+    scratch is a fixed static device array); see moe.h.  All tensors are
+    caller-owned device memory."""
+    status = lib().moe_route_noalloc(C.byref(cfg), _ptr(router_w), _ptr(router_bias), _ptr(x), T,
+                                     _ptr(topk_idx), _ptr(topk_w), _stream_handle(stream))
+    if status != MOE_OK:
+        raise MoeError(status, "moe_route_noalloc", "rejected (see moe.h for the limits)")
 
 
 def moe_destroy(handle: int) -> None:

@@ -15,6 +15,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "moe_internal.h"
 
 namespace moe {
@@ -772,3 +774,139 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Router without any device allocation (moe_route_noalloc in moe.h).
+//
+// For callers that may not allocate device memory themselves: for example a
+// host framework whose device memory all belongs to its own pool allocator,
+// or a serving loop that must never call cudaMalloc/cudaFree because those
+// calls can synchronise the device and can fail under memory pressure.  Such
+// a caller cannot create a moe_handle (moe_init allocates the workspace), so
+// this entry point takes the router weights and buffers directly and keeps
+// its scratch (router logits and the last-block ticket) in one fixed static
+// device array.  Every GPU that loads this library holds that array until
+// the process exits.
+// ---------------------------------------------------------------------------
+
+#define MOE_NOALLOC_LOGITS (MOE_ROUTE_NOALLOC_MAX_TOKENS * MOE_ROUTE_NOALLOC_MAX_EXPERTS)
+
+// [0, 64): ticket counter (and padding); [64, 64 + MOE_NOALLOC_LOGITS): logits
+static __device__ __align__(256) float g_route_scratch[64 + MOE_NOALLOC_LOGITS];
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(kThreads) router_noalloc_kernel(Params p, const float *__restrict__ x,
+                                                                  int T) {
+    extern __shared__ float smem[];
+    __shared__ float s_r[kGemvMaxT];
+    const int H = p.d.H, E = p.d.E;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (warp < T) {
+        float ss = 0.0f;
+        if (p.d.prenorm) {
+            const float4 *x4 = reinterpret_cast<const float4 *>(x + (size_t)warp * H);
+            for (int i = lane; i < H / 4; i += 32) {
+                const float4 v = __ldg(x4 + i);
+                ss = fmaf(v.x, v.x, ss); ss = fmaf(v.y, v.y, ss);
+                ss = fmaf(v.z, v.z, ss); ss = fmaf(v.w, v.w, ss);
+            }
+            ss = warp_sum(ss);
+        }
+        if (lane == 0) s_r[warp] = p.d.prenorm ? 1.0f / sqrtf(ss / (float)H + p.d.eps) : 1.0f;
+    }
+    __syncthreads();
+    const int e = blockIdx.x * kWarps + warp;
+    if (e < E) {
+        float acc[kGemvMaxT];
+#pragma unroll
+        for (int t = 0; t < kGemvMaxT; t++) acc[t] = 0.0f;
+        const float4 *w4 = reinterpret_cast<const float4 *>(p.router_w + (size_t)e * H);
+        for (int i = lane; i < H / 4; i += 32) {
+            const float4 wv = __ldg(w4 + i);
+#pragma unroll
+            for (int t = 0; t < kGemvMaxT; t++) {
+                if (t < T) {
+                    const float4 xv = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H) + i);
+                    acc[t] = fmaf(wv.x, xv.x, acc[t]);
+                    acc[t] = fmaf(wv.y, xv.y, acc[t]);
+                    acc[t] = fmaf(wv.z, xv.z, acc[t]);
+                    acc[t] = fmaf(wv.w, xv.w, acc[t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < kGemvMaxT; t++) {
+            if (t < T) {
+                const float v = warp_sum(acc[t]);
+                if (lane == 0) p.ws.logits[(size_t)t * E + e] = v * s_r[t];
+            }
+        }
+    }
+    router_tail(p, T, 0, gridDim.x, smem);
+}
+
+constexpr int kMaxDevices = 64;
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status moe_route_noalloc(const moe_config *cfg, const float *router_w,
+                                        const float *router_bias, const float *x, int32_t T,
+                                        int32_t *topk_idx, float *topk_w, void *stream) {
+    using namespace moe;
+    // Device address of the static scratch array, looked up once per device
+    // with that device current (the host-side symbol is only a stand-in).
+    static float *s_scratch[kMaxDevices] = {};
+    static bool s_ready[kMaxDevices] = {};
+    static std::mutex s_setup;
+    if (!cfg || !router_w || !router_bias || !x || !topk_idx || !topk_w) return MOE_ERR_INVALID;
+    if (cfg->hidden < 32 || cfg->hidden > 16384 || cfg->hidden % 32) return MOE_ERR_UNSUPPORTED;
+    if (cfg->n_experts < 1 || cfg->n_experts > MOE_ROUTE_NOALLOC_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED;
+    if (cfg->top_k < 1 || cfg->top_k > cfg->n_experts || cfg->top_k > 32) return MOE_ERR_INVALID;
+    if (cfg->n_group != 1) return MOE_ERR_UNSUPPORTED;
+    if (cfg->norm_topk != 0 && cfg->norm_topk != 1) return MOE_ERR_INVALID;
+    if (T < 0 || T > MOE_ROUTE_NOALLOC_MAX_TOKENS) return MOE_ERR_INVALID;
+    if ((reinterpret_cast<uintptr_t>(router_w) | reinterpret_cast<uintptr_t>(x)) & 15u) return MOE_ERR_INVALID;
+    if (T == 0) return MOE_OK;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    Dims d = {};
+    d.H = cfg->hidden;
+    d.E = cfg->n_experts;
+    d.K = cfg->top_k;
+    d.norm_topk = cfg->norm_topk;
+    d.prenorm = (cfg->flags & MOE_FLAG_PRENORM_RESIDUAL) ? 1 : 0;
+    d.scale = cfg->routed_scale;
+    d.eps = cfg->rms_eps;
+    d.max_tokens = MOE_ROUTE_NOALLOC_MAX_TOKENS;
+    const size_t smem = router_smem_bytes(d);
+    std::unique_lock<std::mutex> lock(s_setup);
+    if (!s_ready[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_route_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
+        const int max_smem = (int)((size_t)kWarps * 2 * MOE_ROUTE_NOALLOC_MAX_EXPERTS * sizeof(float));
+        if (cudaFuncSetAttribute(router_noalloc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 max_smem) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        s_scratch[dev] = static_cast<float *>(ptr);
+        s_ready[dev] = true;
+    }
+    float *scratch = s_scratch[dev];
+    lock.unlock();
+    Params p = {};
+    p.d = d;
+    p.router_w = router_w;
+    p.router_b = router_bias;
+    p.ws.counters = reinterpret_cast<unsigned *>(scratch);
+    p.ws.logits = scratch + 64;
+    p.ws.topk_idx = topk_idx;
+    p.ws.topk_w = topk_w;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The ticket must start at zero; logits are fully rewritten by every call.
+    if (cudaMemsetAsync(p.ws.counters, 0, sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
+    const int grid = (d.E + kWarps - 1) / kWarps;
+    router_noalloc_kernel<<<grid, kThreads, smem, st>>>(p, x, T);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
