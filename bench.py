@@ -186,6 +186,10 @@ def run_ours(args, rank, world, local_rank, dist_on):
     wl = synth.WORKLOADS[args.workload]
     if wl.n_layers > 1:
         raise SystemExit("bench.py times single-layer workloads; the stack is a parity case")
+    if args.resident_experts:
+        # profiling captures: same per-launch expert work, fewer experts resident
+        import dataclasses
+        wl = dataclasses.replace(wl, E=args.resident_experts, name=wl.name + f"_e{args.resident_experts}")
     T = wl.T
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
@@ -422,6 +426,8 @@ def main():
                     choices=[k for k, w in synth.WORKLOADS.items() if w.n_layers == 1])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--resident-experts", type=int, default=0,
+                    help="profiling only: keep this many routed experts resident instead of E")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
