@@ -193,11 +193,15 @@ def run_ours(args, rank, world, local_rank, dist_on):
     T = wl.T
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    li = synth.layer_inputs(wl)
+    li = synth.layer_inputs(wl, experts=[0] if args.alias_experts else None)
     cfg = moe.make_config(wl.H, wl.E, wl.K, wl.I, wl.n_shared, wl.I_shared, wl.routed_scale,
                           wl.norm_topk, False, wl.rms_eps)
-    layer = moe.MoeLayer(cfg, li.router_w, li.router_b, li.slabs, li.scales, li.sh_slab,
-                         li.sh_scale, max_tokens=T)
+    slabs, scales = li.slabs, li.scales
+    if args.alias_experts:
+        # profiling only: every expert pointer aliases expert 0's slab
+        slabs, scales = li.slabs[:1], li.scales[:1]
+    layer = moe.MoeLayer(cfg, li.router_w, li.router_b, slabs, scales, li.sh_slab,
+                         li.sh_scale, max_tokens=T, expert_rows=[0] * wl.E if args.alias_experts else None)
     streams = rank_streams(rank, world, N_X)
     xs_host = [synth.tokens(wl, T=T, stream=s) for s in streams]
     xs = [torch.from_numpy(x).to(dev) for x in xs_host]
@@ -226,8 +230,6 @@ def run_ours(args, rank, world, local_rank, dist_on):
     K = args.steps
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    n_prof = min(K, 4096)
-    moe.moe_profile_start(layer.handle, n_prof)
     barrier(dist_on)
     torch.cuda.synchronize()
     with ClockSampler(local_rank) as clk:
@@ -240,9 +242,29 @@ def run_ours(args, rank, world, local_rank, dist_on):
     barrier(dist_on)
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     total_ms = reduce_max(sum(step_ms), dist_on)
+    assert moe.moe_device_error(layer.handle) == 0
+
+    # Per-kernel times: the same steps again with the library recording an
+    # event at every kernel boundary (those events add GPU time and stop the
+    # kernels overlapping, so this pass is kept out of the timed one above).
+    n_prof = min(K, 4096)
+    moe.moe_profile_start(layer.handle, n_prof)
+    for i in range(n_prof):
+        flush()
+        moe.moe_forward(layer.handle, xs[i % N_X], T, y, stream)
+    torch.cuda.synchronize()
     n_calls, stage_ms = moe.moe_profile_read(layer.handle)
     moe.moe_profile_start(layer.handle, 0)
-    kernels_per_step = 3 if T == 1 else 4
+    # GPU time one event boundary adds (two events back to back, cold L2)
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(200)]
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(200)]
+    for i in range(200):
+        flush()
+        ea[i].record(stream)
+        eb[i].record(stream)
+    torch.cuda.synchronize()
+    event_ms = statistics.median(a.elapsed_time(b) for a, b in zip(ea, eb))
+    kernels_per_step = 4
 
     # end to end through the host entry point (pinned host buffers)
     xh = [torch.from_numpy(x).pin_memory() for x in xs_host]
@@ -270,7 +292,7 @@ def run_ours(args, rank, world, local_rank, dist_on):
     units = (mean_touched if T > 1 else wl.K) + wl.n_shared
     gu_bytes = (mean_touched if T > 1 else wl.K) * gateup_bytes(wl.H, wl.I) + \
         (gateup_bytes(wl.H, wl.I_shared) if wl.n_shared else 0)
-    gu_ms = stage_ms["gate_up"]
+    gu_ms = stage_ms["gate_up"] - event_ms
     achieved = gu_bytes / (gu_ms / 1e3) / 1e9
     out = None
     if rank == 0:
@@ -316,6 +338,10 @@ def run_ours(args, rank, world, local_rank, dist_on):
                 "launch_ms": round(gu_ms, 6),
             },
             "stages_ms": {k: round(v, 6) for k, v in stage_ms.items()},
+            "stages_note": ("separate pass with an event at each kernel boundary; "
+                            "event_boundary_ms (two events back to back) is subtracted from "
+                            "roofline.launch_ms"),
+            "event_boundary_ms": round(event_ms, 6),
             "stages_calls": n_calls,
             "e2e": {
                 "value": round(tokens / e2e_s, 2),
@@ -426,6 +452,8 @@ def main():
                     choices=[k for k, w in synth.WORKLOADS.items() if w.n_layers == 1])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--alias-experts", action="store_true",
+                    help="profiling only: all routed experts share one slab (router captures)")
     ap.add_argument("--resident-experts", type=int, default=0,
                     help="profiling only: keep this many routed experts resident instead of E")
     args = ap.parse_args()

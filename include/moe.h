@@ -136,6 +136,17 @@ moe_status moe_destroy(moe_handle *h);
 moe_status moe_profile_start(moe_handle *h, int32_t max_calls);
 moe_status moe_profile_read(moe_handle *h, int32_t *n_calls, float *stage_ms);
 
+/* Waits for the device, then reads and clears the handle's device error
+ * word.  Kernels never wait without bound: a pipeline wait that runs out sets
+ * a flag bit and the kernel returns early (its output is then invalid).
+ * *flags = the bits seen (0: none); returns MOE_ERR_CUDA when any was set. */
+moe_status moe_device_error(moe_handle *h, uint32_t *flags);
+
+/* 1 if T == 1 calls on this handle use the streaming decode kernels (bulk
+ * copies through shared memory, fixed-point activations, dp4a), 0 if they
+ * use the generic kernels (shapes outside the streaming kernels' limits). */
+int32_t moe_uses_streaming_decode(const moe_handle *h);
+
 /* Device workspace moe_init would allocate for this config (0 if invalid). */
 size_t moe_workspace_bytes(const moe_config *cfg, int32_t max_tokens);
 

@@ -17,7 +17,8 @@ __all__ = [
     "MOE_FLAG_PRENORM_RESIDUAL", "MoeError", "MoeConfig", "MoeWeights", "MoeLayer",
     "lib", "library_path", "moe_init", "moe_forward", "moe_forward_debug", "moe_forward_host",
     "moe_destroy", "moe_last_error", "moe_workspace_bytes", "moe_abi_version",
-    "moe_profile_start", "moe_profile_read", "moe_route_noalloc",
+    "moe_profile_start", "moe_profile_read", "moe_route_noalloc", "moe_device_error",
+    "moe_uses_streaming_decode",
 ]
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_CUDA, MOE_ERR_NOMEM, MOE_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
@@ -80,6 +81,10 @@ def lib():
         L.moe_profile_start.restype = C.c_int
         L.moe_profile_read.argtypes = [vp, C.POINTER(i32), C.POINTER(C.c_float)]
         L.moe_profile_read.restype = C.c_int
+        L.moe_device_error.argtypes = [vp, C.POINTER(C.c_uint32)]
+        L.moe_device_error.restype = C.c_int
+        L.moe_uses_streaming_decode.argtypes = [vp]
+        L.moe_uses_streaming_decode.restype = i32
         L.moe_route_noalloc.argtypes = [C.POINTER(MoeConfig), vp, vp, vp, i32, vp, vp, vp]
         L.moe_route_noalloc.restype = C.c_int
         _lib = L
@@ -173,6 +178,17 @@ def moe_route_noalloc(cfg: MoeConfig, router_w, router_bias, x, T: int, topk_idx
         raise MoeError(status, "moe_route_noalloc", "rejected (see moe.h for the limits)")
 
 
+def moe_device_error(handle: int) -> int:
+    """Device error flags since the last check (0 = none); raises if any."""
+    f = C.c_uint32()
+    _check(lib().moe_device_error(handle, C.byref(f)), "moe_device_error")
+    return f.value
+
+
+def moe_uses_streaming_decode(handle: int) -> bool:
+    return bool(lib().moe_uses_streaming_decode(handle))
+
+
 def moe_destroy(handle: int) -> None:
     _check(lib().moe_destroy(handle), "moe_destroy")
 
@@ -189,11 +205,12 @@ class MoeLayer:
 
     Uploads host arrays (router [E,H] f32, bias [E] f32, slabs [E, nbytes] u8,
     scales [E, 2I+H] f32, optional shared slab/scale) into device tensors it
-    owns, and holds a library handle that borrows them.
+    owns, and holds a library handle that borrows them.  expert_rows (optional)
+    maps each expert to a row of slabs/scales, so experts may share storage.
     """
 
     def __init__(self, cfg: MoeConfig, router_w, router_b, slabs, scales, sh_slab=None,
-                 sh_scale=None, max_tokens: int = 1, device=None):
+                 sh_scale=None, max_tokens: int = 1, device=None, expert_rows=None):
         import torch
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
         self.cfg = cfg
@@ -217,8 +234,9 @@ class MoeLayer:
         cp = self.scales.data_ptr()
         sb = self.slabs.stride(0)
         cb = self.scales.stride(0) * 4
-        self._slab_ptrs = (C.c_void_p * E)(*[sp + e * sb for e in range(E)])
-        self._scale_ptrs = (C.c_void_p * E)(*[cp + e * cb for e in range(E)])
+        rows = list(range(E)) if expert_rows is None else list(expert_rows)   # expert -> row
+        self._slab_ptrs = (C.c_void_p * E)(*[sp + r * sb for r in rows])
+        self._scale_ptrs = (C.c_void_p * E)(*[cp + r * cb for r in rows])
         self.weights = MoeWeights(_ptr(self.router_w), _ptr(self.router_b),
                                   C.cast(self._slab_ptrs, C.POINTER(C.c_void_p)),
                                   C.cast(self._scale_ptrs, C.POINTER(C.c_void_p)),

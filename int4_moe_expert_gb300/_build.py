@@ -12,7 +12,7 @@ ROOT = PKG.parent
 CSRC = PKG / "csrc"
 BUILD = PKG / "_build"
 LIB = PKG / "libmoe_gb300.so"
-SOURCES = ["moe_kernels.cu", "moe_abi.cu"]
+SOURCES = ["moe_kernels.cu", "moe_decode.cu", "moe_abi.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -82,6 +82,7 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
     d->scale = c->routed_scale;
     d->eps = c->rms_eps;
     d->max_tokens = max_tokens;
+    d->fast_decode = moe::decode_fast_supported(*d) ? 1 : 0;
     return MOE_OK;
 }
 
@@ -312,6 +313,20 @@ moe_status moe_profile_read(moe_handle *h, int32_t *n_calls, float *stage_ms) {
     for (int s = 0; s < moe::kStages; s++) stage_ms[s] = (float)(sum[s] / h->prof_n);
     return MOE_OK;
 }
+
+moe_status moe_device_error(moe_handle *h, uint32_t *flags) {
+    if (!h || !flags) return fail(MOE_ERR_INVALID, "NULL argument");
+    unsigned v = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&v, h->p.ws.err, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && v) e = cudaMemset(h->p.ws.err, 0, sizeof(unsigned));
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    *flags = v;
+    if (v) return fail(MOE_ERR_CUDA, "a kernel gave up waiting (flags 0x%x)", v);
+    return MOE_OK;
+}
+
+int32_t moe_uses_streaming_decode(const moe_handle *h) { return h ? h->p.d.fast_decode : 0; }
 
 moe_status moe_destroy(moe_handle *h) {
     if (!h) return MOE_OK;

@@ -18,6 +18,7 @@ struct Dims {
     float scale;        // routed_scale
     float eps;          // rms_eps
     int max_tokens;
+    int fast_decode;    // T == 1 runs the streaming kernels (moe_decode.cu)
 };
 
 // Device workspace owned by a handle.  Vectors marked "perm" are stored in
@@ -37,7 +38,16 @@ struct Workspace {
     int *slot_expert;    // [E] active experts, ascending id
     int *n_slots;        // [1]
     float *dbuf;         // [(maxT*K + maxT), H] unweighted down outputs (T > 1)
+    // decode (T == 1) streaming path
+    unsigned *hmax;      // [kMaxSlots] bits of max |h| per slot (reset by the down kernel)
+    unsigned *rb_ticket; // [H / 8] per row-block arrivals in the down kernel
+    unsigned *err;       // [4] device error word: bounded waits that ran out
+    float *dpart;        // [kMaxSlots, H] down outputs per slot (times the routing weight)
+    float *dscore;       // [2, E] decode router: sigmoid | selection score (sigmoid + bias)
+    size_t total_bytes;  // size of the carved region
 };
+
+constexpr int kMaxSlots = 33;   // K <= 32 routed + 1 shared
 
 // Everything a kernel needs, passed by value.
 struct Params {
@@ -58,6 +68,11 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws);
 cudaError_t prepare_kernels(const Dims &d);
 
 constexpr int kStages = 4;   // router, gate/up, down, combine
+
+// Decode streaming path (moe_decode.cu): T == 1 only.
+bool decode_fast_supported(const Dims &d);
+cudaError_t prepare_decode_fast(const Dims &d);
+cudaError_t launch_decode_fast(const Params &p, const float *x, float *y, cudaStream_t st, cudaEvent_t *ev);
 
 // Launch the whole step for T >= 1 tokens on `stream`.  want_buckets forces
 // the token -> expert histogram (ws.cnt) even for T == 1.  When ev is not

@@ -122,17 +122,30 @@ __device__ void topk_phase(const Params &p, int T, float *smem) {
     float *sig = smem + warp * 2 * E;
     float *choice = sig + E;
     for (int t = warp; t < T; t += kWarps) {
-        for (int e = lane; e < E; e += 32) {
-            const float l = __ldcg(p.ws.logits + (size_t)t * E + e);
-            const float s = 1.0f / (1.0f + expf(-l));
-            float c = s + p.router_b[e];
-            if (isnan(c)) c = -INFINITY;
-            sig[e] = s;
-            choice[e] = c;
+        for (int base = 0; base < E; base += 256) {     // loads issued 8 at a time
+            float lv[8], bv8[8];
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int e = base + lane + 32 * i;
+                lv[i] = e < E ? __ldcg(p.ws.logits + (size_t)t * E + e) : 0.0f;
+                bv8[i] = e < E ? p.router_b[e] : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int e = base + lane + 32 * i;
+                if (e < E) {
+                    const float s = 1.0f / (1.0f + expf(-lv[i]));
+                    float c = s + bv8[i];
+                    if (isnan(c)) c = -INFINITY;
+                    sig[e] = s;
+                    choice[e] = c;
+                }
+            }
         }
         __syncwarp();
         uint32_t taken = 0;       // bit i: expert lane + 32 i already chosen
-        float sum_sig = 0.0f;
+        float sum_sig = 0.0f, my_sig = 0.0f;
+        int my_e = 0;
         for (int kk = 0; kk < K; kk++) {
             float bv = -INFINITY;
             int be = 0x7fffffff;
@@ -150,27 +163,19 @@ __device__ void topk_phase(const Params &p, int T, float *smem) {
             }
             if ((be & 31) == lane) taken |= 1u << (be >> 5);
             const float s = sig[be];
-            sum_sig += s;
-            if (lane == 0) {
-                p.ws.topk_idx[(size_t)t * K + kk] = be;
-                p.ws.topk_w[(size_t)t * K + kk] = s;   // rescaled below
-            }
+            sum_sig += s;               // same order in every lane
+            if (lane == kk) { my_e = be; my_sig = s; }
         }
-        __syncwarp();
-        if (lane == 0) {
+        // lane kk holds choice kk (K <= 32)
+        if (lane < K) {
             const float den = sum_sig + 1e-20f;
-            for (int kk = 0; kk < K; kk++) {
-                float *wp = p.ws.topk_w + (size_t)t * K + kk;
-                *wp = p.d.norm_topk ? p.d.scale * (*wp) / den : p.d.scale * (*wp);
-            }
+            p.ws.topk_idx[(size_t)t * K + lane] = my_e;
+            p.ws.topk_w[(size_t)t * K + lane] = p.d.norm_topk ? p.d.scale * my_sig / den : p.d.scale * my_sig;
         }
         __syncwarp();
     }
 }
 
-// Token -> expert buckets for T tokens (whole block).  cnt[e], exclusive
-// offsets off[e], the pair ids p = t*K + k of each expert in ascending p
-// (stable), inv[p], and the list of experts with at least one token.
 __device__ void bucket_phase(const Params &p, int T, int *ismem) {
     const int E = p.d.E, K = p.d.K, P = T * K;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -316,6 +321,121 @@ __global__ void __launch_bounds__(kThreads) router_gemv_kernel(Params p, const f
     router_tail(p, T, buckets, gridDim.x, smem);
 }
 
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+    acc = fmaf(a.x, b.x, acc);
+    acc = fmaf(a.y, b.y, acc);
+    acc = fmaf(a.z, b.z, acc);
+    return fmaf(a.w, b.w, acc);
+}
+
+// Top-K for one token from per-expert (sigmoid, selection score) pairs in
+// ws.dscore, by one warp: every lane loads its experts e = lane + 32 i at once
+// and the K argmax rounds run on registers.  Lane k then writes choice k.
+__device__ void topk_decode_warp(const Params &p, int lane) {
+    const int E = p.d.E, K = p.d.K;
+    constexpr int kPer = 32;                       // E <= 1024
+    float c[kPer], sg[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; i++) {
+        const int e = lane + 32 * i;
+        sg[i] = e < E ? __ldcg(p.ws.dscore + e) : 0.0f;
+        c[i] = e < E ? __ldcg(p.ws.dscore + E + e) : -INFINITY;
+    }
+    uint32_t taken = 0;
+    float sum_sig = 0.0f, my_sig = 0.0f;
+    int my_e = 0;
+    for (int kk = 0; kk < K; kk++) {
+        float bv = -INFINITY, bs = 0.0f;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < kPer; i++) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u) && ranks_before(c[i], e, bv, be)) { bv = c[i]; be = e; bs = sg[i]; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+            if (ranks_before(ov, oe, bv, be)) { bv = ov; be = oe; bs = os; }
+        }
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        sum_sig += bs;
+        if (lane == kk) { my_e = be; my_sig = bs; }
+    }
+    if (lane < K) {
+        const float den = sum_sig + 1e-20f;
+        p.ws.topk_idx[lane] = my_e;
+        p.ws.topk_w[lane] = p.d.norm_topk ? p.d.scale * my_sig / den : p.d.scale * my_sig;
+    }
+}
+
+// Router for one token on the streaming decode path: two expert rows per
+// block, each row split over all threads, so ~E/2 blocks keep enough loads
+// in flight.  Each block turns its logits into (sigmoid, sigmoid + bias); the
+// last block to finish picks the top K.  It lets the dependent gate/up grid
+// launch at once; that grid waits for this one before it reads the routing.
+__global__ void __launch_bounds__(kThreads) router_decode_kernel(Params p, const float *__restrict__ x,
+                                                                 int buckets) {
+    extern __shared__ float smem[];
+    __shared__ float s_part[kWarps][3];
+    __shared__ int s_last;
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int H = p.d.H, E = p.d.E, H4 = H / 4;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int e0 = blockIdx.x * 2;
+    const bool has1 = e0 + 1 < E;
+    const float4 *x4 = reinterpret_cast<const float4 *>(x);
+    const float4 *w0 = reinterpret_cast<const float4 *>(p.router_w + (size_t)e0 * H);
+    const float4 *w1 = reinterpret_cast<const float4 *>(p.router_w + (size_t)(has1 ? e0 + 1 : e0) * H);
+    const float b0 = p.router_b[e0], b1 = p.router_b[has1 ? e0 + 1 : e0];
+    float a0 = 0.0f, a1 = 0.0f, ss = 0.0f;
+#pragma unroll 8
+    for (int i = tid; i < H4; i += kThreads) {
+        const float4 xv = __ldg(x4 + i);
+        a0 = dot4(__ldg(w0 + i), xv, a0);
+        a1 = dot4(__ldg(w1 + i), xv, a1);
+        ss = dot4(xv, xv, ss);
+    }
+    a0 = warp_sum(a0);
+    a1 = warp_sum(a1);
+    ss = warp_sum(ss);
+    if (lane == 0) {
+        s_part[warp][0] = a0;
+        s_part[warp][1] = a1;
+        s_part[warp][2] = ss;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float A0 = 0.0f, A1 = 0.0f, S = 0.0f;
+        for (int w = 0; w < kWarps; w++) { A0 += s_part[w][0]; A1 += s_part[w][1]; S += s_part[w][2]; }
+        const float r = p.d.prenorm ? 1.0f / sqrtf(S / (float)H + p.d.eps) : 1.0f;
+        const float l0 = A0 * r, l1 = A1 * r;
+        const float s0 = 1.0f / (1.0f + expf(-l0)), s1 = 1.0f / (1.0f + expf(-l1));
+        float c0 = s0 + b0, c1 = s1 + b1;
+        if (isnan(c0)) c0 = -INFINITY;
+        if (isnan(c1)) c1 = -INFINITY;
+        p.ws.logits[e0] = l0;
+        p.ws.dscore[e0] = s0;
+        p.ws.dscore[E + e0] = c0;
+        if (has1) {
+            p.ws.logits[e0 + 1] = l1;
+            p.ws.dscore[e0 + 1] = s1;
+            p.ws.dscore[E + e0 + 1] = c1;
+        }
+        if (blockIdx.x == 0) p.ws.rnorm[0] = r;
+        __threadfence();
+        s_last = (atomicAdd(p.ws.counters, 1u) == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (warp == 0) topk_decode_warp(p, lane);
+    __syncthreads();
+    if (buckets) bucket_phase(p, 1, reinterpret_cast<int *>(smem));
+    if (tid == 0) *p.ws.counters = 0u;
+}
+
 // Router for larger T: a 32 (experts) x 32 (tokens) tile per block, k-loop
 // over H in steps of 32 through shared memory.
 __global__ void __launch_bounds__(kThreads) router_tiled_kernel(Params p, const float *__restrict__ x,
@@ -435,7 +555,6 @@ __global__ void __launch_bounds__(kThreads) gateup_decode_kernel(Params p) {
     }
 }
 
-constexpr int kMaxSlots = 33;   // K <= 32 routed + 1 shared
 
 template <int RPW>
 __global__ void __launch_bounds__(kThreads) down_decode_kernel(Params p, const float *__restrict__ x,
@@ -686,8 +805,7 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 size_t workspace_bytes(const Dims &d) {
     Workspace ws;
     carve_workspace(d, nullptr, &ws);
-    return reinterpret_cast<size_t>(ws.dbuf) +
-           align_up((size_t)(d.max_tokens * d.K + d.max_tokens) * d.H * sizeof(float), 256);
+    return ws.total_bytes;
 }
 
 void carve_workspace(const Dims &d, void *base, Workspace *ws) {
@@ -708,7 +826,13 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
     ws->inv = reinterpret_cast<int *>(take(P * sizeof(int)));
     ws->slot_expert = reinterpret_cast<int *>(take(d.E * sizeof(int)));
     ws->n_slots = reinterpret_cast<int *>(take(sizeof(int)));
-    ws->dbuf = reinterpret_cast<float *>(take(0));
+    ws->hmax = reinterpret_cast<unsigned *>(take(kMaxSlots * sizeof(unsigned)));
+    ws->rb_ticket = reinterpret_cast<unsigned *>(take((d.H / 8 + 1) * sizeof(unsigned)));
+    ws->err = reinterpret_cast<unsigned *>(take(4 * sizeof(unsigned)));
+    ws->dpart = reinterpret_cast<float *>(take((size_t)kMaxSlots * d.H * sizeof(float)));
+    ws->dscore = reinterpret_cast<float *>(take(2 * (size_t)d.E * sizeof(float)));
+    ws->dbuf = reinterpret_cast<float *>(take((P + T) * d.H * sizeof(float)));
+    ws->total_bytes = o;
 }
 
 // ---------------------------------------------------------------------------
@@ -718,8 +842,12 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
 cudaError_t prepare_kernels(const Dims &d) {
     const int smem = (int)router_smem_bytes(d);
     cudaError_t e = cudaFuncSetAttribute(router_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(router_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(router_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(router_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess && d.fast_decode) e = prepare_decode_fast(d);
+    return e;
 }
 
 cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cudaStream_t st,
@@ -735,6 +863,13 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
         if (e == cudaSuccess) e = cudaGetLastError();
     };
     mark(0);
+    if (T == 1 && d.fast_decode) {
+        router_decode_kernel<<<(d.E + 1) / 2, kThreads, smem, st>>>(p, x, buckets);
+        check();
+        mark(1);
+        if (e == cudaSuccess) e = launch_decode_fast(p, x, y, st, ev);
+        return e;
+    }
     if (T <= kGemvMaxT) {
         const int grid = (d.E + kWarps - 1) / kWarps;
         router_gemv_kernel<<<grid, kThreads, smem, st>>>(p, x, T, buckets);

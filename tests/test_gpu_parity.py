@@ -47,7 +47,7 @@ def layer_for(moe, name, max_tokens):
 def run_and_check(moe, wl, li, layer, x, where):
     xd = torch.from_numpy(x).cuda()
     y, idx, w = layer.forward_debug(xd)
-    torch.cuda.synchronize()
+    assert moe.moe_device_error(layer.handle) == 0
     y, idx, w = y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
     ref = oracle_layer(wl, li)
     errs = []
@@ -73,6 +73,12 @@ def test_decode_glm(moe):
         err, _ = run_and_check(moe, wl, li, layer, synth.tokens(wl, T=1, stream=s), f"glm s={s}")
         worst = max(worst, err)
     print(f"glm decode worst rel err {worst:.3e}")
+
+
+@pytest.mark.parametrize("name", ["tiny", "olmoe", "glm_decode"])
+def test_streaming_decode_path_is_used(moe, name):
+    wl, li, layer = layer_for(moe, name, 1 if name == "glm_decode" else 64)
+    assert moe.moe_uses_streaming_decode(layer.handle)
 
 
 def test_decode_is_deterministic(moe):
@@ -165,7 +171,8 @@ def test_stack_35b_40_layers(moe):
         layer = upload(moe, wl, li, 1)
         x_in = x_gpu.cpu().numpy()
         y, idx, w = layer.forward_debug(x_gpu)
-        torch.cuda.synchronize()
+        assert moe.moe_device_error(layer.handle) == 0
+        assert moe.moe_uses_streaming_decode(layer.handle)
         ref = oracle_layer(wl, li)
         # teacher-forced: the oracle gets this layer's GPU input
         err, tie = check_token(wl, ref, x_in[0], y.cpu().numpy()[0], idx.cpu().numpy()[0],
@@ -203,6 +210,9 @@ def small_workload(**kw):
     dict(E=1, K=1, n_shared=0, I_shared=0),
     dict(E=300, K=32, H=96),               # K at its limit, E not a multiple of 32
     dict(n_layers=2),                      # pre-norm + residual flag (one layer here)
+    dict(I_shared=32, K=8, E=64),          # streaming decode: small rows, lanes idle
+    dict(I_shared=32, n_shared=0, E=40, K=32, H=96),   # streaming decode: 32 slots, H = 96
+    dict(I_shared=32, n_layers=2, H=1056, I=160),      # streaming decode, odd chunk counts
 ])
 def test_edge_configs(moe, kw):
     wl = small_workload(**kw)
