@@ -137,14 +137,18 @@ moe_status moe_profile_start(moe_handle *h, int32_t max_calls);
 moe_status moe_profile_read(moe_handle *h, int32_t *n_calls, float *stage_ms);
 
 /* Waits for the device, then reads and clears the handle's device error
- * word.  Kernels never wait without bound: a pipeline wait that runs out sets
- * a flag bit and the kernel returns early (its output is then invalid).
- * *flags = the bits seen (0: none); returns MOE_ERR_CUDA when any was set. */
+ * word.  Kernels never wait without bound: a wait that runs out (a pipeline
+ * stage, or a grid-wide barrier of the T == 1 kernel) sets a flag bit and the
+ * kernel returns early; that call's output is then invalid.  *flags = the bits
+ * seen (0: none); returns MOE_ERR_CUDA when any was set, after resetting the
+ * handle's barrier state so that later calls are valid again. */
 moe_status moe_device_error(moe_handle *h, uint32_t *flags);
 
-/* 1 if T == 1 calls on this handle use the streaming decode kernels (bulk
- * copies through shared memory, fixed-point activations, dp4a), 0 if they
- * use the generic kernels (shapes outside the streaming kernels' limits). */
+/* 1 if T == 1 calls on this handle run the single persistent decode kernel
+ * (a cooperative launch; weights streamed through shared memory with
+ * cp.async; fixed-point activations and dp4a), 0 if they use the generic
+ * kernels (shapes outside its limits: H, I multiples of 32, I == I_shared,
+ * I <= 2048, H <= 8192, E <= 1024, K + n_shared <= 32). */
 int32_t moe_uses_streaming_decode(const moe_handle *h);
 
 /* Device workspace moe_init would allocate for this config (0 if invalid). */

@@ -1,13 +1,26 @@
-// Decode (T == 1) streaming path: gate/up + SwiGLU and down as persistent
-// kernels in which every warp streams its own units of expert rows into
-// shared memory with cp.async (two buffers per warp: one is computed while
-// the next one lands), followed by a small combine kernel.  The three are
-// chained with programmatic dependent launch after the router.
+// Decode (T == 1): the whole MoE step as one persistent kernel.
 //
-// What is computed is the same as the generic kernels (reader.mx
-// "25GB 内存上运行 GLM 5.2 744B" section 11; devpress GLM-5.2 breakdown
-// "Step 6 (MoE)" 6b-6d):  g = s_g (Q_g x), u = s_u (Q_u x), h = silu(g) u,
-// d = s_d (Q_d h), y = sum_k w_k d_k + d_shared.
+// One block per SM (a cooperative launch, so every block is resident), eight
+// warps.  The step's four parts run as phases separated by grid-wide
+// barriers; while a block waits at a barrier its warps have already started
+// fetching the next phase's weights, so HBM keeps streaming from the first
+// router byte to the last down byte:
+//   phase 0  one batch of loads (x chunk and this block's two router rows);
+//            router logits -> sigmoid and selection score (sigmoid + bias);
+//            x digits                                           -> barrier 1
+//            (meanwhile: shared-expert gate/up rows stream in)
+//   routing  warp 0 of every block selects the top K (K rounds of a warp max)
+//   phase 1  gate/up + SwiGLU, units of two (gate, up) row pairs
+//            (each warp then starts fetching its first down rows) -> barrier 2
+//   phase 2  down: each warp serves one slot; d_j = w_j * s_d * (Q_d h_j)
+//                                                              -> barrier 3
+//   phase 3  y = sum_k d_k + d_shared (k ascending; + x with pre-norm residual)
+//
+// What is computed (reader.mx "25GB 内存上运行 GLM 5.2 744B" section 11;
+// devpress GLM-5.2 breakdown "Step 6 (MoE)" 6a-6d; Edge0 article section 七):
+// l = W_r x, sigma = sigmoid(l), top-K of sigma + bias (lower index wins a
+// tie), w = s sigma / (sum sigma + 1e-20); g = s_g (Q_g x), u = s_u (Q_u x),
+// h = silu(g) u, d = s_d (Q_d h), y = sum_k w_k d_k + d_shared.
 //
 // Arithmetic.  An activation vector v (x, or one expert's h) is held as
 // 24-bit fixed point with one scale per vector: X_i = rint(v_i / s),
@@ -21,16 +34,16 @@
 // are floating point.  The representation error of v is at most
 // max|v| * 2^-24 per element, the same order as one float32 rounding.
 //
-// Layout of a vector's digits (shared memory): for chunk c (elements
-// 32c..32c+31, one 16-byte weight load) and q = 2p + lh, the uint4 at
-// [q * C + c] holds, in word m, the plane-p digits of elements 8m+{0,2,4,6}
-// (lh = 0: the low nibbles of word m) or 8m+{1,3,5,7} (lh = 1: the high
-// nibbles), one per byte, matching the nibble order of the weight word.
+// Digits in shared memory: for chunk c (elements 32c..32c+31, one 16-byte
+// weight load) and q = 2p + lh, the uint4 at [q * C + c] holds, in word m,
+// the plane-p digits of elements 8m+{0,2,4,6} (lh = 0: the low nibbles of
+// word m) or 8m+{1,3,5,7} (lh = 1: the high nibbles), one per byte.
 //
-// Why cp.async and not bulk (TMA) copies: measured on this GPU, one block
-// issuing 1-D bulk copies completes about one copy per 0.27 us whatever its
-// size, so 6-12 KB units capped a block at 23-45 GB/s; per-lane 16-byte
-// asynchronous copies from eight warps keep enough bytes in flight.
+// Weights move with per-lane 16-byte cp.async copies into per-warp buffers;
+// each lane reads back exactly the pieces it copied, so a warp needs no
+// synchronisation with any other to consume its own units.  (Measured on this
+// GPU: one block issuing 1-D bulk copies completes about one copy per 0.27 us
+// whatever its size, which capped 6-12 KB units at 23-45 GB/s per SM.)
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -44,11 +57,16 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kGuRows = 2;          // row pairs (gate + up) per gate/up unit
+constexpr int kGuBufs = 2;          // gate/up buffers per warp
 constexpr int kDnRows = 8;          // output rows per down unit
-constexpr int kBufs = 2;            // gate/up buffers per warp
-constexpr int kGuSmemBudget = 220 * 1024;
-constexpr int kDnSmemBudget = 220 * 1024;
+constexpr int kDnBufs = 3;          // down buffers per warp
+constexpr int kSmemBudget = 220 * 1024;
+constexpr unsigned kSpinLimit = 1u << 22;   // bounded waits (about 0.1-1 s)
 constexpr float kQMax = 8355711.0f;         // 0x7F7F7F
+constexpr int kSwWords = (kMaxSlots + 3) / 4 * 4;   // s_w padded to 16 bytes
+static_assert(kMaxSlots * 16 % 16 == 0 && kSwWords >= kMaxSlots, "shared-memory carving");
+
+enum : unsigned { kErrGrid = 8u };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -57,16 +75,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_2() { asm volatile("cp.async.wait_group 2;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
     return v;
 }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ void dp4a_us(int &acc, uint32_t nib, uint32_t dig) {
     asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"(nib), "r"(dig));
@@ -76,75 +89,74 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int m) {
     return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
 }
 
-// acc[p] += sum over the 32 weights of one 16-byte chunk of nibble * digit(p)
-__device__ __forceinline__ void dot_chunk(const uint4 w, const uint4 (&dig)[6], int (&acc)[3]) {
-#pragma unroll
-    for (int m = 0; m < 4; m++) {
-        const uint32_t word = word_of(w, m);
-        const uint32_t lo = word & 0x0F0F0F0Fu;
-        const uint32_t hi = (word >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-        for (int p = 0; p < 3; p++) {
-            dp4a_us(acc[p], lo, word_of(dig[2 * p], m));
-            dp4a_us(acc[p], hi, word_of(dig[2 * p + 1], m));
-        }
-    }
-}
-
-// Same sums with the high nibbles kept in place (byte value 16 n): acc_lo
-// collects n * d for the low nibbles, acc_hi 16 n * d for the high ones, so
-// the total is acc_lo + acc_hi / 16 (exact: acc_hi is a multiple of 16).
-__device__ __forceinline__ void dot_chunk_lh(const uint4 w, const uint4 (&dig)[6], int (&lo_acc)[3],
-                                             int (&hi_acc)[3]) {
-#pragma unroll
-    for (int m = 0; m < 4; m++) {
-        const uint32_t word = word_of(w, m);
-        const uint32_t lo = word & 0x0F0F0F0Fu;
-        const uint32_t hi = word & 0xF0F0F0F0u;
-#pragma unroll
-        for (int p = 0; p < 3; p++) {
-            dp4a_us(lo_acc[p], lo, word_of(dig[2 * p], m));
-            dp4a_us(hi_acc[p], hi, word_of(dig[2 * p + 1], m));
-        }
-    }
-}
-
 __device__ __forceinline__ float planes_lh_to_float(const int (&lo)[3], const int (&hi)[3]) {
     const int a0 = lo[0] + (hi[0] >> 4), a1 = lo[1] + (hi[1] >> 4), a2 = lo[2] + (hi[2] >> 4);
     return fmaf(__int2float_rn(a2), 65536.0f, fmaf(__int2float_rn(a1), 256.0f, __int2float_rn(a0)));
 }
 
-__device__ __forceinline__ float planes_to_float(const int (&a)[3]) {
-    return fmaf(__int2float_rn(a[2]), 65536.0f, fmaf(__int2float_rn(a[1]), 256.0f, __int2float_rn(a[0])));
-}
-
 // Digits of the 32 values of one chunk (natural order) scaled by inv = 1/s;
-// dsum[p] = sum of the plane-p digits.
+// dsum[p] = sum of the plane-p digits.  With U = X + 0x808080 (>= 0), byte p
+// of U minus 128 is the balanced digit d_p, i.e. byte p of U xor 0x80 read
+// as a signed byte; bytes are gathered into words with byte permutes.
 __device__ __forceinline__ void quant_chunk(const float (&v)[32], float inv, uint4 (&dig)[6], int (&dsum)[3]) {
-    uint32_t w[6][4];
-#pragma unroll
-    for (int q = 0; q < 6; q++)
-#pragma unroll
-        for (int m = 0; m < 4; m++) w[q][m] = 0u;
-    dsum[0] = dsum[1] = dsum[2] = 0;
+    uint32_t U[32];
 #pragma unroll
     for (int i = 0; i < 32; i++) {
-        int X = __float2int_rn(v[i] * inv);
-        X = min(max(X, -8355711), 8355711);
-        const int d0 = ((X + 128) & 255) - 128;
-        const int X1 = (X - d0) >> 8;
-        const int d1 = ((X1 + 128) & 255) - 128;
-        const int d2 = (X1 - d1) >> 8;
-        const int m = i >> 3, e = i & 7, lh = e & 1, b = e >> 1;
-        w[0 + lh][m] |= (uint32_t)(d0 & 255) << (8 * b);
-        w[2 + lh][m] |= (uint32_t)(d1 & 255) << (8 * b);
-        w[4 + lh][m] |= (uint32_t)(d2 & 255) << (8 * b);
-        dsum[0] += d0;
-        dsum[1] += d1;
-        dsum[2] += d2;
+        const int X = min(max(__float2int_rn(v[i] * inv), -8355711), 8355711);
+        U[i] = (uint32_t)(X + 0x808080);
+    }
+    uint32_t w[6][4];
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+#pragma unroll
+        for (int lh = 0; lh < 2; lh++) {
+            const int e0 = 8 * m + lh;       // elements e0, e0 + 2, e0 + 4, e0 + 6
+#pragma unroll
+            for (int p = 0; p < 3; p++) {
+                const uint32_t sel = (uint32_t)p | ((uint32_t)(4 + p) << 4);
+                const uint32_t a = __byte_perm(U[e0], U[e0 + 2], sel);
+                const uint32_t b = __byte_perm(U[e0 + 4], U[e0 + 6], sel);
+                w[2 * p + lh][m] = __byte_perm(a, b, 0x5410) ^ 0x80808080u;
+            }
+        }
     }
 #pragma unroll
     for (int q = 0; q < 6; q++) dig[q] = make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]);
+#pragma unroll
+    for (int p = 0; p < 3; p++) {
+        int t = 0;
+#pragma unroll
+        for (int m = 0; m < 4; m++) {
+            t = __dp4a((int)w[2 * p][m], 0x01010101, t);
+            t = __dp4a((int)w[2 * p + 1][m], 0x01010101, t);
+        }
+        dsum[p] = t;
+    }
+}
+
+// lo[rr][p] += low-nibble sums, hi[rr][p] += 16 x high-nibble sums for NR
+// rows of one chunk, issued so that consecutive dp4a go to different rows.
+template <int NR>
+__device__ __forceinline__ void dot_rows(const uint4 (&w)[NR], const uint4 (&dig)[6], int (&lo)[NR][3],
+                                         int (&hi)[NR][3]) {
+#pragma unroll
+    for (int m = 0; m < 4; m++) {
+        uint32_t l[NR], h[NR];
+#pragma unroll
+        for (int rr = 0; rr < NR; rr++) {
+            const uint32_t word = word_of(w[rr], m);
+            l[rr] = word & 0x0F0F0F0Fu;
+            h[rr] = word & 0xF0F0F0F0u;
+        }
+#pragma unroll
+        for (int p = 0; p < 3; p++) {
+            const uint32_t dl = word_of(dig[2 * p], m), dh = word_of(dig[2 * p + 1], m);
+#pragma unroll
+            for (int rr = 0; rr < NR; rr++) dp4a_us(lo[rr][p], l[rr], dl);
+#pragma unroll
+            for (int rr = 0; rr < NR; rr++) dp4a_us(hi[rr][p], h[rr], dh);
+        }
+    }
 }
 
 // Reduce NV floats per lane over the warp so that lane l ends holding the
@@ -168,220 +180,383 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[NV], int lane) {
     return r;
 }
 
+// Unsigned key with the order of the float (no NaN; -0 not used); every
+// float, -inf included, maps above 0, which marks a removed entry.
+__device__ __forceinline__ unsigned order_key(float f) {
+    const unsigned u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
+__device__ __forceinline__ void cp_async_wait_n(int n) {     // n = groups allowed to stay pending
+    if (n <= 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
+    else if (n == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else asm volatile("cp.async.wait_group 2;" ::: "memory");
+}
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+// Single thread: wait until *ctr has reached target (counters only grow;
+// wrap-safe).  false if the bounded wait ran out.
+__device__ bool spin_until(const unsigned *ctr, unsigned target) {
+    for (unsigned i = 0; i < kSpinLimit; i++) {
+        if ((int)(ld_acquire(ctr) - target) >= 0) return true;
+        __nanosleep(32);
+    }
+    return false;
+}
+// Whole block: every block adds one to *ctr, then waits for all of them.
+__device__ bool grid_barrier(unsigned *ctr, unsigned target, unsigned *err, volatile int *s_ok) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(ctr, 1u);
+        const bool ok = spin_until(ctr, target);
+        if (!ok) atomicOr(err, kErrGrid);
+        *s_ok = ok ? 1 : 0;
+    }
+    __syncthreads();
+    return *s_ok != 0;
+}
 
-// ---------------------------------------------------------------------------
-// gate/up + SwiGLU
-// ---------------------------------------------------------------------------
 
-struct GuShape {
-    int C;            // chunks per row = H / 32
-    int rowbytes;     // H / 2
-    int unit_bytes;   // 2 * kGuRows * rowbytes
-    int U_sh, U_r;    // units of the shared expert, units per routed expert
-    int units;
+struct FusedShape {
+    // gate/up
+    int C;             // chunks per row = H / 32
+    int rowbytes;      // H / 2
+    int gu_unit;       // bytes of one unit: 2 * kGuRows rows
+    int U_sh, U_r;     // units of the shared expert, units per routed expert
+    int gu_units;
+    // down
+    int Cd;            // chunks per row = I / 32
+    int drowbytes;     // I / 2
+    int dn_unit;       // kDnRows rows
+    int J;             // slots = K + n_shared
+    int RB;            // row blocks = H / kDnRows
+    int warp_bytes;    // per-warp buffer region
     size_t smem;
 };
 
-// smem: [kWarps][kBufs][unit_bytes] | xdig [6][C] uint4 | xdsum [C] int4 | red
-__host__ __device__ inline GuShape gu_shape(const Dims &d) {
-    GuShape s;
+__host__ __device__ inline FusedShape fused_shape(const Dims &d) {
+    FusedShape s;
     s.C = d.H / 32;
     s.rowbytes = d.H / 2;
-    s.unit_bytes = 2 * kGuRows * s.rowbytes;
+    s.gu_unit = 2 * kGuRows * s.rowbytes;
     s.U_sh = d.n_shared ? d.I_sh / kGuRows : 0;
     s.U_r = d.I / kGuRows;
-    s.units = s.U_sh + d.K * s.U_r;
-    s.smem = (size_t)kWarps * kBufs * s.unit_bytes + (size_t)7 * s.C * 16 + 64 * sizeof(float);
+    s.gu_units = s.U_sh + d.K * s.U_r;
+    s.Cd = d.I / 32;
+    s.drowbytes = d.I / 2;
+    s.dn_unit = kDnRows * s.drowbytes;
+    s.J = d.K + d.n_shared;
+    s.RB = d.H / kDnRows;
+    const int gu = kGuBufs * s.gu_unit, dn = kDnBufs * s.dn_unit;
+    s.warp_bytes = gu > dn ? gu : dn;
+    // buffers | xdig | xdsum | red[64] | slab[33] | scale[33] | w[36] | flags[4] | score keys[E] | idx[32]
+    // (every part starts on a 16-byte boundary)
+    s.smem = (size_t)kWarps * s.warp_bytes + (size_t)7 * s.C * 16 + 64 * 4 + kMaxSlots * 16 + kSwWords * 4 + 16 +
+             (size_t)(d.E + 3) / 4 * 16 + 32 * 4;
     return s;
 }
 
-// Pointers of slot j (j < K: the j-th routed choice; j == K: shared expert)
-// for lane j of the calling warp; read after the routing is final.
-struct SlotPtr {
-    const uint8_t *slab;
-    const float *scale;
-};
-__device__ __forceinline__ SlotPtr lane_slot(const Params &p, int lane) {
-    SlotPtr r{nullptr, nullptr};
-    if (lane < p.d.K) {
-        const int e = __ldcg(p.ws.topk_idx + lane);
-        r.slab = p.slabs[e];
-        r.scale = p.scales[e];
-    } else if (lane == p.d.K && p.d.n_shared) {
-        r.slab = p.sh_slab;
-        r.scale = p.sh_scale;
-    }
-    return r;
-}
-__device__ __forceinline__ const void *shfl_ptr(const void *ptr, int src) {
-    const unsigned long long v = reinterpret_cast<unsigned long long>(ptr);
-    return reinterpret_cast<const void *>(__shfl_sync(0xffffffffu, v, src));
-}
-
-// CPL = chunks per lane = ceil(C / 32); lane l owns chunks l + 32 k.
-template <int CPL>
-__global__ void __launch_bounds__(kThreads, 1) gateup_stream_kernel(Params p, const float *__restrict__ x,
-                                                                    GuShape sh) {
+template <int CPLH, int CPLI>
+__global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, const float *__restrict__ x,
+                                                                   float *__restrict__ y, FusedShape sh,
+                                                                   unsigned gen, int want_counts) {
     extern __shared__ __align__(128) unsigned char smem[];
-    uint4 *xdig = reinterpret_cast<uint4 *>(smem + (size_t)kWarps * kBufs * sh.unit_bytes);
+    uint4 *xdig = reinterpret_cast<uint4 *>(smem + (size_t)kWarps * sh.warp_bytes);
     int4 *xdsum = reinterpret_cast<int4 *>(xdig + 6 * sh.C);
     float *red = reinterpret_cast<float *>(xdsum + sh.C);
+    const uint8_t **s_slab = reinterpret_cast<const uint8_t **>(red + 64);
+    const float **s_scale = reinterpret_cast<const float **>(s_slab + kMaxSlots);
+    float *s_w = reinterpret_cast<float *>(s_scale + kMaxSlots);
+    volatile int *s_flags = reinterpret_cast<volatile int *>(s_w + kSwWords);   // [0] ok [1] abort
+    unsigned *s_key = reinterpret_cast<unsigned *>(const_cast<int *>(s_flags + 4));   // [E] (+pad)
+    int *s_sel = reinterpret_cast<int *>(s_key + (p.d.E + 3) / 4 * 4);                // [32]
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const Dims &d = p.d;
-    const int H = d.H, C = sh.C;
-    const bool full_lanes = (C % 32) == 0;
-    const uint32_t wbuf = smem_u32(smem + (size_t)warp * kBufs * sh.unit_bytes) + (uint32_t)(lane * 16);
+    const int H = d.H, E = d.E, K = d.K, J = sh.J, C = sh.C, Cd = sh.Cd;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int G = gridDim.x, nw = G * kWarps, gw = blockIdx.x * kWarps + warp;
+    const unsigned target = gen * (unsigned)G;
+    unsigned *bar1 = p.ws.counters + 4, *bar2 = p.ws.counters + 5, *bar3 = p.ws.counters + 6;
+    const uint32_t wbuf = smem_u32(smem + (size_t)warp * sh.warp_bytes) + (uint32_t)(lane * 16);
+    const bool fullH = (C % 32) == 0, fullI = (Cd % 32) == 0;
 
-    // units of this warp: u = gw, gw + nw, ...; the shared expert's come first
-    const int nw = gridDim.x * kWarps;
-    const int gw = blockIdx.x * kWarps + warp;
-    bool routed_ready = false;
-    SlotPtr mine{nullptr, nullptr};
-
-    auto unit_src = [&](int u, int &slot, int &rb, const uint8_t *&slab, const float *&scale, int &Ij) {
+    // ---- gate/up units of this warp: u = gw + n * nw; the shared expert's first --------
+    const int n_gu = gw < sh.gu_units ? (sh.gu_units - 1 - gw) / nw + 1 : 0;
+    int gu_issued = 0;
+    bool routed = false;          // routing known to this block
+    auto gu_src = [&](int u, int &slot, int &rb, const uint8_t *&slab, int &Ij) {
         if (u < sh.U_sh) {
-            slot = d.K; rb = u; slab = p.sh_slab; scale = p.sh_scale; Ij = d.I_sh;
+            slot = K; rb = u; slab = p.sh_slab; Ij = d.I_sh;
         } else {
-            if (!routed_ready) {
-                pdl_wait();
-                mine = lane_slot(p, lane);
-                routed_ready = true;
-            }
             const int v = u - sh.U_sh;
             slot = v / sh.U_r;
             rb = v - slot * sh.U_r;
-            slab = static_cast<const uint8_t *>(shfl_ptr(mine.slab, slot));
-            scale = static_cast<const float *>(shfl_ptr(mine.scale, slot));
+            slab = s_slab[slot];
             Ij = d.I;
         }
     };
-    // each lane copies the 16-byte pieces it will read itself
-    auto issue = [&](int u, int buf) {
+    auto issue_gu = [&](int n) {
         int slot, rb, Ij;
         const uint8_t *slab;
-        const float *scale;
-        unit_src(u, slot, rb, slab, scale, Ij);
-        const uint32_t dst = wbuf + (uint32_t)(buf * sh.unit_bytes);
+        gu_src(gw + n * nw, slot, rb, slab, Ij);
+        const uint32_t dst = wbuf + (uint32_t)((n % kGuBufs) * sh.gu_unit);
         const uint8_t *gsrc = slab + (size_t)rb * kGuRows * sh.rowbytes + lane * 16;
         const uint8_t *usrc = slab + ((size_t)Ij + (size_t)rb * kGuRows) * sh.rowbytes + lane * 16;
 #pragma unroll
         for (int rr = 0; rr < 2 * kGuRows; rr++) {
-            const uint8_t *src = (rr < kGuRows ? gsrc + rr * sh.rowbytes : usrc + (rr - kGuRows) * sh.rowbytes);
+            const uint8_t *src = rr < kGuRows ? gsrc + rr * sh.rowbytes : usrc + (rr - kGuRows) * sh.rowbytes;
             const uint32_t drow = dst + (uint32_t)(rr * sh.rowbytes);
 #pragma unroll
-            for (int k = 0; k < CPL; k++)
-                if (full_lanes || lane + 32 * k < C) cp_async16(drow + 512 * k, src + 512 * k);
+            for (int k = 0; k < CPLH; k++)
+                if (fullH || lane + 32 * k < C) cp_async16(drow + 512 * k, src + 512 * k);
         }
     };
-
-#pragma unroll
-    for (int b = 0; b < kBufs; b++) {
-        if (gw + b * nw < sh.units) issue(gw + b * nw, b);
-        cp_async_commit();
-    }
-
-    // ---- quantise x once per block ----------------------------------------------
-    float amax = 0.0f, ss = 0.0f;
+    // issue the next units, up to kGuBufs ahead of `done`; routed ones only once routing is known
+    auto gu_fill = [&](int done) {
+        while (gu_issued < n_gu && gu_issued < done + kGuBufs) {
+            if (gw + gu_issued * nw >= sh.U_sh && !routed) return;
+            issue_gu(gu_issued);
+            cp_async_commit();
+            gu_issued++;
+        }
+    };
+    // ---- phase 0: one batch of loads: x chunk `tid`, the same chunk of this block's two router rows
+    // (issued before the shared-expert prefetch: routing is on the critical path)
+    const int e0 = 2 * blockIdx.x;
+    const bool has0 = e0 < E, has1 = e0 + 1 < E;
+    float xv[32];
+    float a0 = 0.0f, a1 = 0.0f, amax = 0.0f, ss = 0.0f;
     bool bad = false;
-    for (int c = threadIdx.x; c < C; c += kThreads) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(x + (size_t)c * 32);
+    float4 u0[8], u1[8];
+    if (tid < C) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(x + (size_t)tid * 32);
+        const float4 *w0 = reinterpret_cast<const float4 *>(p.router_w + (size_t)(has0 ? e0 : 0) * H + (size_t)tid * 32);
+        const float4 *w1 = reinterpret_cast<const float4 *>(p.router_w + (size_t)(has1 ? e0 + 1 : 0) * H + (size_t)tid * 32);
 #pragma unroll
         for (int k = 0; k < 8; k++) {
-            const float4 v = __ldg(x4 + k);
-            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-            ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
-            bad |= !(isfinite(v.x) && isfinite(v.y) && isfinite(v.z) && isfinite(v.w));
+            const float4 f = __ldg(x4 + k);
+            xv[4 * k] = f.x; xv[4 * k + 1] = f.y; xv[4 * k + 2] = f.z; xv[4 * k + 3] = f.w;
+            u0[k] = has0 ? __ldg(w0 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+            u1[k] = has1 ? __ldg(w1 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    gu_fill(0);
+    if (tid < C) {
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            a0 = fmaf(u0[k].x, xv[4 * k], fmaf(u0[k].y, xv[4 * k + 1], fmaf(u0[k].z, xv[4 * k + 2], fmaf(u0[k].w, xv[4 * k + 3], a0))));
+            a1 = fmaf(u1[k].x, xv[4 * k], fmaf(u1[k].y, xv[4 * k + 1], fmaf(u1[k].z, xv[4 * k + 2], fmaf(u1[k].w, xv[4 * k + 3], a1))));
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i++) {
+            amax = fmaxf(amax, fabsf(xv[i]));
+            ss = fmaf(xv[i], xv[i], ss);
+            bad |= !isfinite(xv[i]);
         }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+        a1 += __shfl_xor_sync(0xffffffffu, a1, o);
     }
     bad = __any_sync(0xffffffffu, bad);
     if (lane == 0) {
         red[warp] = amax;
-        red[kWarps + warp] = ss;
-        red[2 * kWarps + warp] = bad ? 1.0f : 0.0f;
+        red[8 + warp] = ss;
+        red[16 + warp] = bad ? 1.0f : 0.0f;
+        red[24 + warp] = a0;
+        red[32 + warp] = a1;
     }
     __syncthreads();
     amax = 0.0f;
     ss = 0.0f;
     bad = false;
+    float A0 = 0.0f, A1 = 0.0f;
     for (int w = 0; w < kWarps; w++) {
         amax = fmaxf(amax, red[w]);
-        ss += red[kWarps + w];
-        bad |= red[2 * kWarps + w] != 0.0f;
+        ss += red[8 + w];
+        bad |= red[16 + w] != 0.0f;
+        A0 += red[24 + w];
+        A1 += red[32 + w];
     }
     const float r = d.prenorm ? 1.0f / sqrtf(ss / (float)H + d.eps) : 1.0f;
+    auto put_score = [&](int e, float raw) {
+        const float l = raw * r;
+        const float sg = 1.0f / (1.0f + expf(-l));
+        float c = sg + p.router_b[e] + 0.0f;   // + 0: no negative zero
+        if (isnan(c)) c = -INFINITY;
+        p.ws.logits[e] = l;
+        p.ws.dscore[e] = sg;
+        p.ws.dscore[E + e] = c;
+    };
+    if (tid == 0) {
+        if (has0) put_score(e0, A0);
+        if (has1) put_score(e0 + 1, A1);
+    }
+    // more experts than 2 per block: further pairs, rows split over all threads
+    for (int ep = e0 + 2 * G; ep < E; ep += 2 * G) {
+        const bool h1 = ep + 1 < E;
+        const float4 *x4 = reinterpret_cast<const float4 *>(x);
+        const float4 *w0 = reinterpret_cast<const float4 *>(p.router_w + (size_t)ep * H);
+        const float4 *w1 = reinterpret_cast<const float4 *>(p.router_w + (size_t)(h1 ? ep + 1 : ep) * H);
+        float b0 = 0.0f, b1 = 0.0f;
+        for (int i = tid; i < H / 4; i += kThreads) {
+            const float4 xq = __ldg(x4 + i), v0 = __ldg(w0 + i), v1 = __ldg(w1 + i);
+            b0 = fmaf(v0.x, xq.x, fmaf(v0.y, xq.y, fmaf(v0.z, xq.z, fmaf(v0.w, xq.w, b0))));
+            b1 = fmaf(v1.x, xq.x, fmaf(v1.y, xq.y, fmaf(v1.z, xq.z, fmaf(v1.w, xq.w, b1))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            b0 += __shfl_xor_sync(0xffffffffu, b0, o);
+            b1 += __shfl_xor_sync(0xffffffffu, b1, o);
+        }
+        __syncthreads();
+        if (lane == 0) { red[40 + warp] = b0; red[48 + warp] = b1; }
+        __syncthreads();
+        if (tid == 0) {
+            float B0 = 0.0f, B1 = 0.0f;
+            for (int w = 0; w < kWarps; w++) { B0 += red[40 + w]; B1 += red[48 + w]; }
+            put_score(ep, B0);
+            if (h1) put_score(ep + 1, B1);
+        }
+    }
+
+    // x digits (pre-normed when asked), from the registers already loaded
     const float m = amax * r;
     const float s_x = bad ? __int_as_float(0x7fc00000) : m / kQMax;
     const float inv = (m > 0.0f && !bad) ? kQMax / m : 0.0f;
-    for (int c = threadIdx.x; c < C; c += kThreads) {
+    if (tid < C) {
         float v[32];
-        const float4 *x4 = reinterpret_cast<const float4 *>(x + (size_t)c * 32);
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-            const float4 f = __ldg(x4 + k);
-            v[4 * k] = f.x * r; v[4 * k + 1] = f.y * r; v[4 * k + 2] = f.z * r; v[4 * k + 3] = f.w * r;
-        }
+        for (int i = 0; i < 32; i++) v[i] = xv[i] * r;
         uint4 dig[6];
         int ds[3];
         quant_chunk(v, inv, dig, ds);
 #pragma unroll
-        for (int q = 0; q < 6; q++) xdig[q * C + c] = dig[q];
-        xdsum[c] = make_int4(ds[0], ds[1], ds[2], 0);
+        for (int q = 0; q < 6; q++) xdig[q * C + tid] = dig[q];
+        xdsum[tid] = make_int4(ds[0], ds[1], ds[2], 0);
+    }
+
+    // ---- barrier 1: every block's scores are written; then the block picks the top K -----
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        atomicAdd(bar1, 1u);
+        const bool ok = spin_until(bar1, target);
+        if (!ok) atomicOr(p.ws.err, kErrGrid);
+        s_flags[0] = ok ? 1 : 0;
+        s_flags[1] = 0;
     }
     __syncthreads();
-    // per-lane correction: -8 * (sum of digits over this lane's chunks)
+    if (!s_flags[0]) {
+        cp_async_wait_n(0);
+        return;
+    }
+    // top K by (score desc, index asc), one warp: K rounds of a warp-wide max
+    // over each lane's best remaining expert (lane l holds experts l + 32 i)
+    if (warp == 0) {
+        unsigned best = 0u;
+        int bidx = 0x7fffffff;
+        for (int e = lane; e < E; e += 32) {
+            const unsigned k = order_key(__ldcg(p.ws.dscore + E + e));
+            s_key[e] = k;
+            if (k > best) { best = k; bidx = e; }
+        }
+        for (int r = 0; r < K; r++) {
+            const unsigned mx = __reduce_max_sync(0xffffffffu, best);
+            const unsigned win = __reduce_min_sync(0xffffffffu, best == mx ? (unsigned)bidx : 0xffffffffu);
+            if (lane == 0) s_sel[r] = (int)win;
+            if (lane == (int)(win & 31u)) {          // the winner's lane removes it and rescans
+                s_key[win] = 0u;
+                best = 0u;
+                bidx = 0x7fffffff;
+                for (int e = lane; e < E; e += 32) {
+                    const unsigned k = s_key[e];
+                    if (k > best) { best = k; bidx = e; }
+                }
+            }
+        }
+        __syncwarp();
+    }
+    if (warp == 0) {
+        const int me = lane < K ? s_sel[lane] : 0;   // written by lane 0 of this warp
+        const float sg = lane < K ? __ldcg(p.ws.dscore + me) : 0.0f;
+        float sum = sg;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        const float mw = d.norm_topk ? d.scale * sg / (sum + 1e-20f) : d.scale * sg;
+        if (lane < K) {
+            s_slab[lane] = p.slabs[me];
+            s_scale[lane] = p.scales[me];
+            s_w[lane] = mw;
+        } else if (lane == K && d.n_shared) {
+            s_slab[lane] = p.sh_slab;
+            s_scale[lane] = p.sh_scale;
+            s_w[lane] = 1.0f;
+        }
+        if (blockIdx.x == 0) {
+            if (want_counts) {
+                for (int e = lane; e < E; e += 32) p.ws.cnt[e] = 0;
+                __syncwarp();
+            }
+            if (lane < K) {
+                p.ws.topk_idx[lane] = me;
+                p.ws.topk_w[lane] = mw;
+                if (want_counts) p.ws.cnt[me] = 1;
+            }
+        }
+    }
+    __syncthreads();
+    routed = true;
+
+    // ---- phase 1: gate/up + SwiGLU ------------------------------------------------------
+    gu_fill(0);
     int corr[3] = {0, 0, 0};
 #pragma unroll
-    for (int k = 0; k < CPL; k++) {
-        if (full_lanes || lane + 32 * k < C) {
+    for (int k = 0; k < CPLH; k++) {
+        if (fullH || lane + 32 * k < C) {
             const int4 t = xdsum[lane + 32 * k];
             corr[0] -= 8 * t.x; corr[1] -= 8 * t.y; corr[2] -= 8 * t.z;
         }
     }
     const uint32_t xdig_a = smem_u32(xdig) + (uint32_t)(lane * 16);
-
-    // ---- stream units ---------------------------------------------------------------
-    // lane l ends with row l / 8 of the unit: rows 0..kGuRows-1 gate, then up
-    const bool writer = lane < 16 && (lane & 7) == 0;
-    int buf = 0;
-    for (int u = gw; u < sh.units; u += nw, buf = (buf + 1 == kBufs) ? 0 : buf + 1) {
+    const bool gu_writer = lane < 16 && (lane & 7) == 0;   // lane l ends with row l / 8
+    for (int n = 0; n < n_gu; n++) {
+        cp_async_wait_n(gu_issued - n - 1);
         int slot, rb, Ij;
         const uint8_t *slab;
-        const float *scale;
-        unit_src(u, slot, rb, slab, scale, Ij);
+        gu_src(gw + n * nw, slot, rb, slab, Ij);
+        const float *scale = slot < K ? s_scale[slot] : p.sh_scale;
         const int o = rb * kGuRows + (lane >> 3);
         float sg = 0.0f, su = 0.0f;
-        if (writer) {            // issued now, needed after the dot products
+        if (gu_writer) {          // issued now, needed after the dot products
             sg = __ldg(scale + o);
             su = __ldg(scale + Ij + o);
         }
-        cp_async_wait_1();       // this unit's copies (this lane's own pieces) have landed
-        const uint32_t st = wbuf + (uint32_t)(buf * sh.unit_bytes);
+        const uint32_t st = wbuf + (uint32_t)((n % kGuBufs) * sh.gu_unit);
         int lo[2 * kGuRows][3], hi[2 * kGuRows][3];
-        static_assert(kBufs == 2, "wait_group count below assumes two buffers");
 #pragma unroll
         for (int rr = 0; rr < 2 * kGuRows; rr++) {
             lo[rr][0] = corr[0]; lo[rr][1] = corr[1]; lo[rr][2] = corr[2];
             hi[rr][0] = 0; hi[rr][1] = 0; hi[rr][2] = 0;
         }
 #pragma unroll
-        for (int k = 0; k < CPL; k++) {
-            if (full_lanes || lane + 32 * k < C) {
-                uint4 dig[6];
+        for (int k = 0; k < CPLH; k++) {
+            if (fullH || lane + 32 * k < C) {
+                uint4 dig[6], w[2 * kGuRows];
 #pragma unroll
                 for (int q = 0; q < 6; q++) dig[q] = lds128(xdig_a + (uint32_t)(q * C * 16 + 512 * k));
 #pragma unroll
-                for (int rr = 0; rr < 2 * kGuRows; rr++) {
-                    const uint4 w = lds128(st + (uint32_t)(rr * sh.rowbytes + 512 * k));
-                    dot_chunk_lh(w, dig, lo[rr], hi[rr]);
-                }
+                for (int rr = 0; rr < 2 * kGuRows; rr++) w[rr] = lds128(st + (uint32_t)(rr * sh.rowbytes + 512 * k));
+                dot_rows<2 * kGuRows>(w, dig, lo, hi);
             }
         }
         float v[2 * kGuRows];
@@ -389,99 +564,55 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_stream_kernel(Params p, co
         for (int rr = 0; rr < 2 * kGuRows; rr++) v[rr] = planes_lh_to_float(lo[rr], hi[rr]);
         const float tot = reduce_scatter<2 * kGuRows>(v, lane);
         const float up = __shfl_down_sync(0xffffffffu, tot, 16);   // up row of the same output
-        if (writer) {
+        if (gu_writer) {
             const float hv = silu_mul(tot * s_x * sg, up * s_x * su);
             p.ws.h[(size_t)slot * d.I_max + o] = hv;
             atomicMax(p.ws.hmax + slot, __float_as_uint(fabsf(hv)));
         }
-        // this buffer is free again: fetch the unit kBufs ahead into it
-        if (u + kBufs * nw < sh.units) issue(u + kBufs * nw, buf);
-        cp_async_commit();
+        gu_fill(n + 1);   // the buffer just read takes the unit kGuBufs ahead
     }
-    cp_async_wait_0();
-    if (!routed_ready) pdl_wait();
-    pdl_trigger();
-}
+    cp_async_wait_n(0);
 
-// ---------------------------------------------------------------------------
-// down: per-slot outputs times the routing weight, combined after.  Each warp
-// works on one slot only, so its lanes keep that slot's h digits in registers.
-// ---------------------------------------------------------------------------
-
-constexpr int kDnBufs = 3;         // down buffers per warp
-
-struct DnShape {
-    int C;            // chunks per row = I / 32
-    int rowbytes;     // I / 2
-    int unit_bytes;   // kDnRows * rowbytes
-    int J;            // slots (K + n_shared)
-    int RB;           // row blocks = H / kDnRows
-    size_t smem;
-};
-
-// smem: [kWarps][kDnBufs][unit_bytes]
-__host__ __device__ inline DnShape dn_shape(const Dims &d) {
-    DnShape s;
-    s.C = d.I / 32;
-    s.rowbytes = d.I / 2;
-    s.unit_bytes = kDnRows * s.rowbytes;
-    s.J = d.K + d.n_shared;
-    s.RB = d.H / kDnRows;
-    s.smem = (size_t)kWarps * kDnBufs * s.unit_bytes + 64;
-    return s;
-}
-
-template <int CPL>
-__global__ void __launch_bounds__(kThreads, 1) down_stream_kernel(Params p, DnShape sh) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const Dims &d = p.d;
-    const int H = d.H, K = d.K, J = sh.J, C = sh.C;
-    const bool full_lanes = (C % 32) == 0;
-    const uint32_t wbuf = smem_u32(smem + (size_t)warp * kDnBufs * sh.unit_bytes) + (uint32_t)(lane * 16);
-
-    // warp gw serves slot j = gw % J; the warps of one slot split its row blocks
-    const int nw = gridDim.x * kWarps;
-    const int gw = blockIdx.x * kWarps + warp;
+    // ---- down units of this warp: slot j = gw % J, row blocks q, q + nq, ... ---------------
     const int j = gw % J;
     const int q = gw / J;
-    const int nq = (nw - j + J - 1) / J;    // warps serving slot j
-
-    pdl_trigger();   // the combine grid may launch; it waits for this one
-    // Routing was final before the gate/up grid let this grid start, so the
-    // weights can stream while the SwiGLU activations are still being made.
-    const SlotPtr mine = lane_slot(p, lane);
-    const uint8_t *dslab = static_cast<const uint8_t *>(shfl_ptr(mine.slab, j)) + (size_t)d.I * d.H + lane * 16;
-    const float *sd = static_cast<const float *>(shfl_ptr(mine.scale, j)) + 2 * d.I;
-    auto issue = [&](int rb, int buf) {
-        const uint8_t *src = dslab + (size_t)rb * kDnRows * sh.rowbytes;
-        const uint32_t dst = wbuf + (uint32_t)(buf * sh.unit_bytes);
+    const int nq = (nw - j + J - 1) / J;
+    const int n_dn = q < sh.RB ? (sh.RB - 1 - q) / nq + 1 : 0;
+    const uint8_t *dslab = n_dn > 0 ? s_slab[j] + (size_t)d.I * d.H + lane * 16 : nullptr;
+    auto issue_dn = [&](int n) {
+        const int rb = q + n * nq;
+        const uint8_t *src = dslab + (size_t)rb * kDnRows * sh.drowbytes;
+        const uint32_t dst = wbuf + (uint32_t)((n % kDnBufs) * sh.dn_unit);
 #pragma unroll
         for (int rr = 0; rr < kDnRows; rr++)
 #pragma unroll
-            for (int k = 0; k < CPL; k++)
-                if (full_lanes || lane + 32 * k < C)
-                    cp_async16(dst + (uint32_t)(rr * sh.rowbytes + 512 * k), src + (size_t)rr * sh.rowbytes + 512 * k);
+            for (int k = 0; k < CPLI; k++)
+                if (fullI || lane + 32 * k < Cd)
+                    cp_async16(dst + (uint32_t)(rr * sh.drowbytes + 512 * k), src + (size_t)rr * sh.drowbytes + 512 * k);
     };
-#pragma unroll
-    for (int b = 0; b < kDnBufs; b++) {
-        if (q + b * nq < sh.RB) issue(q + b * nq, b);
+    int dn_issued = 0;
+    for (; dn_issued < n_dn && dn_issued < kDnBufs; dn_issued++) {
+        issue_dn(dn_issued);
         cp_async_commit();
     }
 
-    // ---- wait for gate/up; this lane's chunks of slot j's h as digits --------------
-    pdl_wait();
+    // ---- barrier 2: every SwiGLU activation and its maximum are written ------------------
+    if (!grid_barrier(bar2, target, p.ws.err, s_flags + 1)) {
+        cp_async_wait_n(0);
+        return;
+    }
+
+    // ---- phase 2: down; this lane's chunks of slot j's h as digits in registers ------------
     const float hmax = __uint_as_float(__ldcg(p.ws.hmax + j));
     const float hs = hmax / kQMax;                    // NaN propagates
-    const float inv = (hs > 0.0f && isfinite(hs)) ? 1.0f / hs : 0.0f;
-    const float wj = (j < K) ? __ldcg(p.ws.topk_w + j) : 1.0f;
-    const float coef_j = wj * hs;
-    uint4 dig[CPL][6];
-    int corr[3] = {0, 0, 0};
+    const float hinv = (hs > 0.0f && isfinite(hs)) ? 1.0f / hs : 0.0f;
+    const float coef_j = s_w[j] * hs;
+    uint4 hdig[CPLI][6];
+    int dcorr[3] = {0, 0, 0};
 #pragma unroll
-    for (int k = 0; k < CPL; k++) {
+    for (int k = 0; k < CPLI; k++) {
         const int c = lane + 32 * k;
-        if (full_lanes || c < C) {
+        if (n_dn > 0 && (fullI || c < Cd)) {
             const float4 *h4 = reinterpret_cast<const float4 *>(p.ws.h + (size_t)j * d.I_max + (size_t)c * 32);
             float v[32];
 #pragma unroll
@@ -490,117 +621,100 @@ __global__ void __launch_bounds__(kThreads, 1) down_stream_kernel(Params p, DnSh
                 v[4 * t] = f.x; v[4 * t + 1] = f.y; v[4 * t + 2] = f.z; v[4 * t + 3] = f.w;
             }
             int ds[3];
-            quant_chunk(v, inv, dig[k], ds);
-            corr[0] -= 8 * ds[0]; corr[1] -= 8 * ds[1]; corr[2] -= 8 * ds[2];
+            quant_chunk(v, hinv, hdig[k], ds);
+            dcorr[0] -= 8 * ds[0]; dcorr[1] -= 8 * ds[1]; dcorr[2] -= 8 * ds[2];
         } else {
 #pragma unroll
-            for (int t = 0; t < 6; t++) dig[k][t] = make_uint4(0u, 0u, 0u, 0u);
+            for (int t = 0; t < 6; t++) hdig[k][t] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    // every block has read hmax: the last one to get here clears it for the next call
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        if (atomicAdd(p.ws.counters + 2, 1u) == gridDim.x - 1) {
-            for (int jj = 0; jj < J; jj++) p.ws.hmax[jj] = 0u;
-            p.ws.counters[2] = 0u;
-        }
-    }
-
-    // ---- stream row blocks --------------------------------------------------------
-    // lane l ends with row l / 4 of the unit
-    const bool writer = (lane & 3) == 0;
-    int buf = 0;
-    for (int rb = q; rb < sh.RB; rb += nq, buf = (buf + 1 == kDnBufs) ? 0 : buf + 1) {
+    const float *sd = n_dn > 0 ? s_scale[j] + 2 * d.I : nullptr;
+    const bool dn_writer = (lane & 3) == 0;                // lane l ends with row l / 4
+    for (int n = 0; n < n_dn; n++) {
+        const int rb = q + n * nq;
         const int o = rb * kDnRows + (lane >> 2);
-        const float coef = writer ? coef_j * __ldg(sd + o) : 0.0f;   // issued before the wait
-        static_assert(kDnBufs == 3, "wait_group count below assumes three buffers");
-        cp_async_wait_2();
-        const uint32_t st = wbuf + (uint32_t)(buf * sh.unit_bytes);
+        const float coef = dn_writer ? coef_j * __ldg(sd + o) : 0.0f;   // issued before the wait
+        cp_async_wait_n(dn_issued - n - 1);
+        const uint32_t st = wbuf + (uint32_t)((n % kDnBufs) * sh.dn_unit);
         int lo[kDnRows][3], hi[kDnRows][3];
 #pragma unroll
         for (int rr = 0; rr < kDnRows; rr++) {
-            lo[rr][0] = corr[0]; lo[rr][1] = corr[1]; lo[rr][2] = corr[2];
+            lo[rr][0] = dcorr[0]; lo[rr][1] = dcorr[1]; lo[rr][2] = dcorr[2];
             hi[rr][0] = 0; hi[rr][1] = 0; hi[rr][2] = 0;
         }
 #pragma unroll
-        for (int k = 0; k < CPL; k++) {
-            if (full_lanes || lane + 32 * k < C) {
+        for (int k = 0; k < CPLI; k++) {
+            if (fullI || lane + 32 * k < Cd) {
+                uint4 w[kDnRows];
 #pragma unroll
-                for (int rr = 0; rr < kDnRows; rr++) {
-                    const uint4 w = lds128(st + (uint32_t)(rr * sh.rowbytes + 512 * k));
-                    dot_chunk_lh(w, dig[k], lo[rr], hi[rr]);
-                }
+                for (int rr = 0; rr < kDnRows; rr++) w[rr] = lds128(st + (uint32_t)(rr * sh.drowbytes + 512 * k));
+                dot_rows<kDnRows>(w, hdig[k], lo, hi);
             }
         }
         float v[kDnRows];
 #pragma unroll
         for (int rr = 0; rr < kDnRows; rr++) v[rr] = planes_lh_to_float(lo[rr], hi[rr]);
         const float tot = reduce_scatter<kDnRows>(v, lane);
-        if (writer) p.ws.dpart[(size_t)j * H + o] = tot * coef;
-        if (rb + kDnBufs * nq < sh.RB) issue(rb + kDnBufs * nq, buf);
-        cp_async_commit();
+        if (dn_writer) p.ws.dpart[(size_t)j * H + o] = tot * coef;
+        if (dn_issued < n_dn) {            // the buffer just read takes the unit kDnBufs ahead
+            issue_dn(dn_issued);
+            cp_async_commit();
+            dn_issued++;
+        }
     }
-    cp_async_wait_0();
-}
+    cp_async_wait_n(0);
 
-// y = sum_k (w_k d_k) over k ascending, then + d_shared (and + x with pre-norm
-// residual); runs once the down grid has finished.
-__global__ void __launch_bounds__(256) combine_decode_kernel(Params p, const float *__restrict__ x,
-                                                             float *__restrict__ y) {
-    pdl_wait();
-    const int o = blockIdx.x * 256 + threadIdx.x;
-    const Dims &d = p.d;
-    if (o >= d.H) return;
-    float acc = 0.0f;
-    for (int k = 0; k < d.K; k++) acc += __ldcg(p.ws.dpart + (size_t)k * d.H + o);
-    if (d.n_shared) acc += __ldcg(p.ws.dpart + (size_t)d.K * d.H + o);
-    y[o] = d.prenorm ? x[o] + acc : acc;
+    // ---- barrier 3, then phase 3: combine ---------------------------------------------------
+    if (!grid_barrier(bar3, target, p.ws.err, s_flags + 1)) return;
+    for (int o = blockIdx.x * kThreads + tid; o < H; o += G * kThreads) {
+        float acc = 0.0f;
+        for (int k = 0; k < K; k++) acc += __ldcg(p.ws.dpart + (size_t)k * H + o);
+        if (d.n_shared) acc += __ldcg(p.ws.dpart + (size_t)K * H + o);
+        y[o] = d.prenorm ? x[o] + acc : acc;
+    }
+    // every block has read hmax (before barrier 3): clear it for the next call
+    if (blockIdx.x == 0 && tid < J) p.ws.hmax[tid] = 0u;
 }
 
 int g_sms = 0;
+int g_blocks = 0;   // co-resident blocks the cooperative launch uses
 
-constexpr int kMaxCpl = 8;     // gate/up: H up to 8192
-constexpr int kMaxCplDn = 3;   // down: I up to 3072 (digits of more chunks do not fit in registers)
+constexpr int kMaxCplH = 8;   // H up to 8192
+constexpr int kMaxCplI = 2;   // I up to 2048 (digits of more chunks do not fit in registers)
 
-template <int CPL>
-cudaError_t launch_gu(cudaLaunchConfig_t &cfg, const Params &p, const float *x, const GuShape &gs) {
-    return cudaLaunchKernelEx(&cfg, gateup_stream_kernel<CPL>, p, x, gs);
-}
-template <int CPL>
-cudaError_t launch_dn(cudaLaunchConfig_t &cfg, const Params &p, const DnShape &ds) {
-    return cudaLaunchKernelEx(&cfg, down_stream_kernel<CPL>, p, ds);
+template <int A, int B>
+cudaError_t launch_t(cudaLaunchConfig_t &cfg, const Params &p, const float *x, float *y, const FusedShape &s,
+                     unsigned gen, int counts) {
+    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<A, B>, p, x, y, s, gen, counts);
 }
 
-cudaError_t dispatch_gu(int cpl, cudaLaunchConfig_t &cfg, const Params &p, const float *x, const GuShape &gs) {
-    switch (cpl) {
-        case 1: return launch_gu<1>(cfg, p, x, gs);
-        case 2: return launch_gu<2>(cfg, p, x, gs);
-        case 3: return launch_gu<3>(cfg, p, x, gs);
-        case 4: return launch_gu<4>(cfg, p, x, gs);
-        case 5: return launch_gu<5>(cfg, p, x, gs);
-        case 6: return launch_gu<6>(cfg, p, x, gs);
-        case 7: return launch_gu<7>(cfg, p, x, gs);
-        case 8: return launch_gu<8>(cfg, p, x, gs);
-    }
-    return cudaErrorInvalidValue;
-}
-cudaError_t dispatch_dn(int cpl, cudaLaunchConfig_t &cfg, const Params &p, const DnShape &ds) {
-    switch (cpl) {
-        case 1: return launch_dn<1>(cfg, p, ds);
-        case 2: return launch_dn<2>(cfg, p, ds);
-        case 3: return launch_dn<3>(cfg, p, ds);
+template <int B>
+cudaError_t launch_h(int a, cudaLaunchConfig_t &cfg, const Params &p, const float *x, float *y,
+                     const FusedShape &s, unsigned gen, int counts) {
+    switch (a) {
+        case 1: return launch_t<1, B>(cfg, p, x, y, s, gen, counts);
+        case 2: return launch_t<2, B>(cfg, p, x, y, s, gen, counts);
+        case 3: return launch_t<3, B>(cfg, p, x, y, s, gen, counts);
+        case 4: return launch_t<4, B>(cfg, p, x, y, s, gen, counts);
+        case 6: return launch_t<6, B>(cfg, p, x, y, s, gen, counts);
+        case 8: return launch_t<8, B>(cfg, p, x, y, s, gen, counts);
     }
     return cudaErrorInvalidValue;
 }
 
-template <int CPL>
-cudaError_t set_smem_attr() {
-    cudaError_t e = cudaFuncSetAttribute(gateup_stream_kernel<CPL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kGuSmemBudget);
-    if (e == cudaSuccess && CPL <= kMaxCplDn)
-        e = cudaFuncSetAttribute(down_stream_kernel<(CPL <= kMaxCplDn ? CPL : 1)>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kDnSmemBudget);
+int cpl_h(const Dims &d) {
+    const int c = (d.H / 32 + 31) / 32;
+    return c == 5 ? 6 : (c == 7 ? 8 : c);       // instantiated: 1, 2, 3, 4, 6, 8
+}
+
+template <int A, int B>
+cudaError_t attr_t() {
+    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<A, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemBudget);
+    int nb = 0;
+    if (e == cudaSuccess)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, decode_fused_kernel<A, B>, kThreads, kSmemBudget);
+    if (e == cudaSuccess && nb < 1) e = cudaErrorInvalidConfiguration;
     return e;
 }
 
@@ -609,66 +723,60 @@ cudaError_t set_smem_attr() {
 bool decode_fast_supported(const Dims &d) {
     if (d.H % kDnRows != 0 || d.H % 32 != 0 || d.I % 32 != 0 || d.I % kGuRows != 0) return false;
     if (d.n_shared && d.I_sh != d.I) return false;
-    if (d.K + d.n_shared > kMaxSlots || d.K + d.n_shared > 32) return false;
-    if ((d.H / 32 + 31) / 32 > kMaxCpl || (d.I / 32 + 31) / 32 > kMaxCplDn) return false;
-    return gu_shape(d).smem <= (size_t)kGuSmemBudget && dn_shape(d).smem <= (size_t)kDnSmemBudget;
+    if (d.K + d.n_shared > kMaxSlots || d.K + d.n_shared > 32 || d.E > 1024) return false;
+    if ((d.H / 32 + 31) / 32 > kMaxCplH || (d.I / 32 + 31) / 32 > kMaxCplI) return false;
+    return fused_shape(d).smem <= (size_t)kSmemBudget;
 }
 
 cudaError_t prepare_decode_fast(const Dims &d) {
     if (!decode_fast_supported(d)) return cudaSuccess;
-    int dev = 0;
+    int dev = 0, coop = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    // the largest any supported shape asks for, so handles of different shapes coexist
-    if (e == cudaSuccess) e = set_smem_attr<1>();
-    if (e == cudaSuccess) e = set_smem_attr<2>();
-    if (e == cudaSuccess) e = set_smem_attr<3>();
-    if (e == cudaSuccess) e = set_smem_attr<4>();
-    if (e == cudaSuccess) e = set_smem_attr<5>();
-    if (e == cudaSuccess) e = set_smem_attr<6>();
-    if (e == cudaSuccess) e = set_smem_attr<7>();
-    if (e == cudaSuccess) e = set_smem_attr<8>();
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+    if (e == cudaSuccess && !coop) e = cudaErrorNotSupported;
+    // every instantiation gets the same (largest) shared-memory limit, so
+    // handles of different shapes coexist
+    const int b = (d.I / 32 + 31) / 32;
+    if (e == cudaSuccess) {
+        switch (cpl_h(d) * 16 + b) {
+#define MOE_ATTR(A, B) case A * 16 + B: e = attr_t<A, B>(); break;
+            MOE_ATTR(1, 1) MOE_ATTR(2, 1) MOE_ATTR(3, 1) MOE_ATTR(4, 1) MOE_ATTR(6, 1) MOE_ATTR(8, 1)
+            MOE_ATTR(1, 2) MOE_ATTR(2, 2) MOE_ATTR(3, 2) MOE_ATTR(4, 2) MOE_ATTR(6, 2) MOE_ATTR(8, 2)
+#undef MOE_ATTR
+            default: e = cudaErrorInvalidValue;
+        }
+    }
+    // every slot needs at least one warp in the down phase
+    if (e == cudaSuccess && g_sms * kWarps < d.K + d.n_shared) e = cudaErrorNotSupported;
+    g_blocks = g_sms;
     return e;
 }
 
-// The router has been launched already (it lets these kernels start early).
-// ev (optional): ev[2] after gate/up, ev[3] after down, ev[4] after the combine.
-cudaError_t launch_decode_fast(const Params &p, const float *x, float *y, cudaStream_t st, cudaEvent_t *ev) {
-    const GuShape gs = gu_shape(p.d);
-    const DnShape ds = dn_shape(p.d);
-    const int sms = g_sms > 0 ? g_sms : 148;
+// One cooperative launch for the whole T == 1 step.  ev (optional): ev[0],
+// ev[1] before the kernel, ev[2..4] after it (stage 1 = the fused kernel).
+cudaError_t launch_decode_fast(const Params &p, const float *x, float *y, cudaStream_t st, cudaEvent_t *ev,
+                               bool want_counts) {
+    const FusedShape s = fused_shape(p.d);
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
     cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g_blocks > 0 ? g_blocks : 148);
     cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = s.smem;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-
-    const int gu_blocks = (gs.units + kWarps - 1) / kWarps;
-    cfg.gridDim = dim3(gu_blocks < sms ? gu_blocks : sms);
-    cfg.dynamicSmemBytes = gs.smem;
-    cudaError_t e = dispatch_gu((gs.C + 31) / 32, cfg, p, x, gs);
-    if (e == cudaSuccess && ev) e = cudaEventRecord(ev[2], st);
+    cudaError_t e = cudaSuccess;
+    if (ev) e = cudaEventRecord(ev[0], st);
+    if (e == cudaSuccess && ev) e = cudaEventRecord(ev[1], st);
     if (e != cudaSuccess) return e;
-
-    // at least one warp per slot; otherwise one block per SM
-    const int dn_units = ds.RB * ds.J;
-    const int dn_blocks = (dn_units + kWarps - 1) / kWarps;
-    int nb = dn_blocks < sms ? dn_blocks : sms;
-    if (nb * kWarps < ds.J) nb = (ds.J + kWarps - 1) / kWarps;
-    cfg.gridDim = dim3(nb);
-    cfg.dynamicSmemBytes = ds.smem;
-    e = dispatch_dn((ds.C + 31) / 32, cfg, p, ds);
-    if (e == cudaSuccess && ev) e = cudaEventRecord(ev[3], st);
-    if (e != cudaSuccess) return e;
-
-    cfg.gridDim = dim3((p.d.H + 255) / 256);
-    cfg.blockDim = dim3(256);
-    cfg.dynamicSmemBytes = 0;
-    e = cudaLaunchKernelEx(&cfg, combine_decode_kernel, p, x, y);
-    if (e == cudaSuccess && ev) e = cudaEventRecord(ev[4], st);
+    const int b = (p.d.I / 32 + 31) / 32;
+    const int counts = want_counts ? 1 : 0;
+    e = b == 1 ? launch_h<1>(cpl_h(p.d), cfg, p, x, y, s, p.gen, counts)
+               : launch_h<2>(cpl_h(p.d), cfg, p, x, y, s, p.gen, counts);
+    for (int i = 2; ev && e == cudaSuccess && i < 5; i++) e = cudaEventRecord(ev[i], st);
     return e;
 }
 

@@ -59,6 +59,7 @@ struct Params {
     const uint8_t *sh_slab;
     const float *sh_scale;
     Workspace ws;
+    unsigned gen;                   // call number on this handle (grid barrier targets)
 };
 
 size_t workspace_bytes(const Dims &d);
@@ -69,10 +70,13 @@ cudaError_t prepare_kernels(const Dims &d);
 
 constexpr int kStages = 4;   // router, gate/up, down, combine
 
-// Decode streaming path (moe_decode.cu): T == 1 only.
+// Decode path (moe_decode.cu): T == 1 as one persistent cooperative kernel.
+// ws.counters[4..6] are its grid barriers: they only grow, by gridDim per
+// call; p.gen numbers the calls from 1.
 bool decode_fast_supported(const Dims &d);
 cudaError_t prepare_decode_fast(const Dims &d);
-cudaError_t launch_decode_fast(const Params &p, const float *x, float *y, cudaStream_t st, cudaEvent_t *ev);
+cudaError_t launch_decode_fast(const Params &p, const float *x, float *y, cudaStream_t st, cudaEvent_t *ev,
+                               bool want_counts);
 
 // Launch the whole step for T >= 1 tokens on `stream`.  want_buckets forces
 // the token -> expert histogram (ws.cnt) even for T == 1.  When ev is not

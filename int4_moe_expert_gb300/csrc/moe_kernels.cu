@@ -853,6 +853,7 @@ cudaError_t prepare_kernels(const Dims &d) {
 cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cudaStream_t st,
                            bool want_buckets, cudaEvent_t *ev) {
     const Dims &d = p.d;
+    if (T == 1 && d.fast_decode) return launch_decode_fast(p, x, y, st, ev, want_buckets);
     const size_t smem = router_smem_bytes(d);
     const int buckets = (T > 1 || want_buckets) ? 1 : 0;
     cudaError_t e = cudaSuccess;
@@ -863,13 +864,6 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
         if (e == cudaSuccess) e = cudaGetLastError();
     };
     mark(0);
-    if (T == 1 && d.fast_decode) {
-        router_decode_kernel<<<(d.E + 1) / 2, kThreads, smem, st>>>(p, x, buckets);
-        check();
-        mark(1);
-        if (e == cudaSuccess) e = launch_decode_fast(p, x, y, st, ev);
-        return e;
-    }
     if (T <= kGemvMaxT) {
         const int grid = (d.E + kWarps - 1) / kWarps;
         router_gemv_kernel<<<grid, kThreads, smem, st>>>(p, x, T, buckets);
