@@ -37,7 +37,11 @@ import synth  # noqa: E402
 METRIC = "MoE-layer decode tokens/s and achieved HBM GB/s vs ~8 TB/s (GLM-5.2 shape)"
 N_X = 16                      # distinct token batches rotated through the steps
 FLUSH_BYTES = 256 << 20       # > 129 MB L2
-PROFILE_FILE = ROOT / "profiles" / "traffic_gateup_decode_glm.txt"
+# committed ncu traffic summaries: dominant kernel -> (summary file, the source it was taken from)
+TRAFFIC_FILES = {
+    "fused": ("traffic_decode_fused_glm_decode.txt", "moe_decode.cu"),
+    "gate_up": ("traffic_gateup_batched_glm.txt", "moe_kernels.cu"),
+}
 
 
 # --------------------------------------------------------------------------- helpers
@@ -160,17 +164,20 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def recorded_traffic():
-    """DRAM bytes per launch of the gate/up kernel from the committed ncu
-    summary, or None when the kernel source changed since the capture."""
-    if not PROFILE_FILE.exists():
+def recorded_traffic(kind: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary (already scaled to the bench workload), or None when the kernel
+    source changed since the capture."""
+    name, src_name = TRAFFIC_FILES[kind]
+    f = ROOT / "profiles" / name
+    if not f.exists():
         return None
     kv = {}
-    for line in PROFILE_FILE.read_text().splitlines():
+    for line in f.read_text().splitlines():
         if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             kv[k.strip()] = v.strip()
-    src = ROOT / "int4_moe_expert_gb300" / "csrc" / "moe_kernels.cu"
+    src = ROOT / "int4_moe_expert_gb300" / "csrc" / src_name
     sha = hashlib.sha256(src.read_bytes()).hexdigest()[:16]
     if kv.get("kernel_source_sha256_16") != sha or "traffic_bytes_per_launch" not in kv:
         return None
@@ -244,27 +251,32 @@ def run_ours(args, rank, world, local_rank, dist_on):
     total_ms = reduce_max(sum(step_ms), dist_on)
     assert moe.moe_device_error(layer.handle) == 0
 
-    # Per-kernel times: the same steps again with the library recording an
-    # event at every kernel boundary (those events add GPU time and stop the
-    # kernels overlapping, so this pass is kept out of the timed one above).
-    n_prof = min(K, 4096)
-    moe.moe_profile_start(layer.handle, n_prof)
-    for i in range(n_prof):
-        flush()
-        moe.moe_forward(layer.handle, xs[i % N_X], T, y, stream)
-    torch.cuda.synchronize()
-    n_calls, stage_ms = moe.moe_profile_read(layer.handle)
-    moe.moe_profile_start(layer.handle, 0)
-    # GPU time one event boundary adds (two events back to back, cold L2)
-    ea = [torch.cuda.Event(enable_timing=True) for _ in range(200)]
-    eb = [torch.cuda.Event(enable_timing=True) for _ in range(200)]
-    for i in range(200):
-        flush()
-        ea[i].record(stream)
-        eb[i].record(stream)
-    torch.cuda.synchronize()
-    event_ms = statistics.median(a.elapsed_time(b) for a, b in zip(ea, eb))
-    kernels_per_step = 4
+    # One cooperative launch per step on the decode path (the step events
+    # bracket exactly that kernel); otherwise router, gate/up, down (+ combine).
+    fused = T == 1 and moe.moe_uses_streaming_decode(layer.handle)
+    kernels_per_step = 1 if fused else (3 if T == 1 else 4)
+    stage_ms, n_calls, event_ms = None, 0, 0.0
+    if not fused:
+        # Per-kernel times: the same steps again with the library recording an
+        # event at every kernel boundary (those events add GPU time and stop the
+        # kernels overlapping, so this pass is kept out of the timed one above).
+        n_prof = min(K, 4096)
+        moe.moe_profile_start(layer.handle, n_prof)
+        for i in range(n_prof):
+            flush()
+            moe.moe_forward(layer.handle, xs[i % N_X], T, y, stream)
+        torch.cuda.synchronize()
+        n_calls, stage_ms = moe.moe_profile_read(layer.handle)
+        moe.moe_profile_start(layer.handle, 0)
+        # GPU time one event boundary adds (two events back to back, cold L2)
+        ea = [torch.cuda.Event(enable_timing=True) for _ in range(200)]
+        eb = [torch.cuda.Event(enable_timing=True) for _ in range(200)]
+        for i in range(200):
+            flush()
+            ea[i].record(stream)
+            eb[i].record(stream)
+        torch.cuda.synchronize()
+        event_ms = statistics.median(a.elapsed_time(b) for a, b in zip(ea, eb))
 
     # end to end through the host entry point (pinned host buffers)
     xh = [torch.from_numpy(x).pin_memory() for x in xs_host]
@@ -288,12 +300,23 @@ def run_ours(args, rank, world, local_rank, dist_on):
     mean_touched = float(np.mean(touched))
     bytes_step = float(np.mean([step_bytes(wl, T, t) for t in touched]))
     peak, peak_kind = measured_peaks()
-    # dominant kernel: gate/up + SwiGLU, K routed experts + the shared one per launch (T = 1)
-    units = (mean_touched if T > 1 else wl.K) + wl.n_shared
-    gu_bytes = (mean_touched if T > 1 else wl.K) * gateup_bytes(wl.H, wl.I) + \
-        (gateup_bytes(wl.H, wl.I_shared) if wl.n_shared else 0)
-    gu_ms = stage_ms["gate_up"] - event_ms
-    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+    if fused:
+        # dominant (only) kernel: the whole step; its bytes are the step's bytes
+        dom_kind = "fused"
+        dom_name = ("decode_fused_kernel: router + top-k + gate/up + SwiGLU + down + combine, "
+                    "one cooperative launch, T=1")
+        dom_bytes = bytes_step
+        dom_ms = statistics.mean(step_ms)
+        units = wl.K + wl.n_shared
+    else:
+        # dominant kernel: gate/up + SwiGLU over the touched experts + the shared one
+        dom_kind = "gate_up"
+        dom_name = "gate/up + SwiGLU (int4 GEMV/GEMM), T=%d" % T
+        n_r = mean_touched if T > 1 else wl.K
+        units = n_r + wl.n_shared
+        dom_bytes = n_r * gateup_bytes(wl.H, wl.I) + (gateup_bytes(wl.H, wl.I_shared) if wl.n_shared else 0)
+        dom_ms = stage_ms["gate_up"] - event_ms
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     out = None
     if rank == 0:
         out = {
@@ -307,7 +330,7 @@ def run_ours(args, rank, world, local_rank, dist_on):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f32 (int4 weights dequantised exactly, fp32 accumulation)",
+            "dtype": "int4 x fx24 -> s32 (exact dp4a sums), f32 router/scales/SwiGLU/combine",
             "data": "synthetic (seeded SplitMix64; shapes and distributions of the workload)",
             "config": {
                 "workload": workload_desc(wl),
@@ -325,24 +348,20 @@ def run_ours(args, rank, world, local_rank, dist_on):
                 "mean_routed_experts_touched": mean_touched,
             },
             "roofline": {
-                "kernel": "gateup (int4 dequant GEMV + SwiGLU), T=%d" % T,
+                "kernel": dom_name,
                 "bound": "hbm",
                 "achieved": round(achieved, 1),
                 "peak": peak,
                 "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy)" if peak_kind == "measured" else peak_kind,
                 "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": recorded_traffic(),
-                "algorithmic_bytes_per_launch": int(gu_bytes),
-                "units_per_launch": units,
-                "launch_ms": round(gu_ms, 6),
+                "traffic": recorded_traffic(dom_kind),
+                "algorithmic_bytes_per_launch": int(dom_bytes),
+                "experts_per_launch": units,
+                "launch_ms": round(dom_ms, 6),
+                "launch_ms_source": ("mean of the timed steps' CUDA events (one launch each)" if fused else
+                                     "profiled pass, event boundary time subtracted"),
             },
-            "stages_ms": {k: round(v, 6) for k, v in stage_ms.items()},
-            "stages_note": ("separate pass with an event at each kernel boundary; "
-                            "event_boundary_ms (two events back to back) is subtracted from "
-                            "roofline.launch_ms"),
-            "event_boundary_ms": round(event_ms, 6),
-            "stages_calls": n_calls,
             "e2e": {
                 "value": round(tokens / e2e_s, 2),
                 "unit": "tokens/s",
@@ -353,6 +372,13 @@ def run_ours(args, rank, world, local_rank, dist_on):
             "gpu_launches": world * K * kernels_per_step,
             "clocks": clk.summary(),
         }
+        if stage_ms is not None:
+            out["stages_ms"] = {k: round(v, 6) for k, v in stage_ms.items()}
+            out["stages_note"] = ("separate pass with an event at each kernel boundary; "
+                                  "event_boundary_ms (two events back to back) is subtracted from "
+                                  "roofline.launch_ms")
+            out["event_boundary_ms"] = round(event_ms, 6)
+            out["stages_calls"] = n_calls
         if world == 1 and not args.no_cpu_baseline:
             out["cpu_baseline"] = cpu_baseline(wl, li, xs_host, args.cpu_seconds)
     layer.close()

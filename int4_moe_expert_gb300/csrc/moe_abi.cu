@@ -321,11 +321,11 @@ moe_status moe_device_error(moe_handle *h, uint32_t *flags) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = cudaMemcpy(&v, h->p.ws.err, sizeof(v), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess && v) {
-        // a kernel gave up part-way: start the barrier counters and the
-        // SwiGLU maxima afresh so the next call is consistent again
+        // a kernel gave up part-way: start the barrier and work counters
+        // afresh so the next call is consistent again
         e = cudaMemset(h->p.ws.err, 0, sizeof(unsigned));
         if (e == cudaSuccess) e = cudaMemset(h->p.ws.counters, 0, 16 * sizeof(unsigned));
-        if (e == cudaSuccess) e = cudaMemset(h->p.ws.hmax, 0, moe::kMaxSlots * sizeof(unsigned));
+        if (e == cudaSuccess) e = cudaMemset(h->p.ws.claims, 0, moe::kClaimWords * sizeof(unsigned));
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
         h->p.gen = 0;
     }

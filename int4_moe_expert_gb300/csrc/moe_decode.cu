@@ -58,8 +58,10 @@ constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr int kGuRows = 2;          // row pairs (gate + up) per gate/up unit
 constexpr int kGuBufs = 2;          // gate/up buffers per warp
+constexpr int kGuPre = 1;           // 1: a first claimed unit of the shared expert is fetched before routing
 constexpr int kDnRows = 8;          // output rows per down unit
 constexpr int kDnBufs = 3;          // down buffers per warp
+constexpr int kDnPre = 1;           // down units a warp fetches before the SwiGLU barrier
 constexpr int kSmemBudget = 220 * 1024;
 constexpr unsigned kSpinLimit = 1u << 22;   // bounded waits (about 0.1-1 s)
 constexpr float kQMax = 8355711.0f;         // 0x7F7F7F
@@ -73,6 +75,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
 }
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ float lds32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -194,6 +204,9 @@ __device__ __forceinline__ void cp_async_wait_n(int n) {     // n = groups allow
     else if (n == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
     else asm volatile("cp.async.wait_group 2;" ::: "memory");
 }
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -227,16 +240,17 @@ struct FusedShape {
     // gate/up
     int C;             // chunks per row = H / 32
     int rowbytes;      // H / 2
-    int gu_unit;       // bytes of one unit: 2 * kGuRows rows
+    int gu_unit;       // bytes of one unit: 2 * kGuRows rows + their scales (16 B)
     int U_sh, U_r;     // units of the shared expert, units per routed expert
     int gu_units;
     // down
     int Cd;            // chunks per row = I / 32
     int drowbytes;     // I / 2
-    int dn_unit;       // kDnRows rows
+    int dn_unit;       // kDnRows rows + their scales (32 B)
     int J;             // slots = K + n_shared
     int RB;            // row blocks = H / kDnRows
     int warp_bytes;    // per-warp buffer region
+    int dig_bytes;     // digit region: x (7 C uint4) in phase 0/1, two slots' h (2 x 7 Cd uint4) in phase 2
     size_t smem;
 };
 
@@ -244,21 +258,21 @@ __host__ __device__ inline FusedShape fused_shape(const Dims &d) {
     FusedShape s;
     s.C = d.H / 32;
     s.rowbytes = d.H / 2;
-    s.gu_unit = 2 * kGuRows * s.rowbytes;
+    s.gu_unit = 2 * kGuRows * s.rowbytes + 16;
     s.U_sh = d.n_shared ? d.I_sh / kGuRows : 0;
     s.U_r = d.I / kGuRows;
     s.gu_units = s.U_sh + d.K * s.U_r;
     s.Cd = d.I / 32;
     s.drowbytes = d.I / 2;
-    s.dn_unit = kDnRows * s.drowbytes;
+    s.dn_unit = kDnRows * s.drowbytes + 32;
     s.J = d.K + d.n_shared;
     s.RB = d.H / kDnRows;
     const int gu = kGuBufs * s.gu_unit, dn = kDnBufs * s.dn_unit;
     s.warp_bytes = gu > dn ? gu : dn;
-    // buffers | xdig | xdsum | red[64] | slab[33] | scale[33] | w[36] | flags[4] | score keys[E] | idx[32]
-    // (every part starts on a 16-byte boundary)
-    s.smem = (size_t)kWarps * s.warp_bytes + (size_t)7 * s.C * 16 + 64 * 4 + kMaxSlots * 16 + kSwWords * 4 + 16 +
-             (size_t)(d.E + 3) / 4 * 16 + 32 * 4;
+    s.dig_bytes = 7 * 16 * (s.C > 2 * s.Cd ? s.C : 2 * s.Cd);
+    // buffers | digits | red[64] | slab[33] | scale[33] | w[36] | flags[4] | score keys[E] | idx[32] | ring[8][4]
+    s.smem = (size_t)kWarps * s.warp_bytes + (size_t)s.dig_bytes + 64 * 4 + kMaxSlots * 16 + kSwWords * 4 + 16 +
+             (size_t)(d.E + 3) / 4 * 16 + 32 * 4 + kWarps * 4 * 4;
     return s;
 }
 
@@ -269,26 +283,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     extern __shared__ __align__(128) unsigned char smem[];
     uint4 *xdig = reinterpret_cast<uint4 *>(smem + (size_t)kWarps * sh.warp_bytes);
     int4 *xdsum = reinterpret_cast<int4 *>(xdig + 6 * sh.C);
-    float *red = reinterpret_cast<float *>(xdsum + sh.C);
+    float *red = reinterpret_cast<float *>(smem + (size_t)kWarps * sh.warp_bytes + sh.dig_bytes);
     const uint8_t **s_slab = reinterpret_cast<const uint8_t **>(red + 64);
     const float **s_scale = reinterpret_cast<const float **>(s_slab + kMaxSlots);
     float *s_w = reinterpret_cast<float *>(s_scale + kMaxSlots);
     volatile int *s_flags = reinterpret_cast<volatile int *>(s_w + kSwWords);   // [0] ok [1] abort
     unsigned *s_key = reinterpret_cast<unsigned *>(const_cast<int *>(s_flags + 4));   // [E] (+pad)
     int *s_sel = reinterpret_cast<int *>(s_key + (p.d.E + 3) / 4 * 4);                // [32]
+    int *s_ring = s_sel + 32;                                                          // [kWarps][4]
 
     const Dims &d = p.d;
     const int H = d.H, E = d.E, K = d.K, J = sh.J, C = sh.C, Cd = sh.Cd;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    const int G = gridDim.x, nw = G * kWarps, gw = blockIdx.x * kWarps + warp;
+    const int G = gridDim.x;
     const unsigned target = gen * (unsigned)G;
     unsigned *bar1 = p.ws.counters + 4, *bar2 = p.ws.counters + 5, *bar3 = p.ws.counters + 6;
     const uint32_t wbuf = smem_u32(smem + (size_t)warp * sh.warp_bytes) + (uint32_t)(lane * 16);
     const bool fullH = (C % 32) == 0, fullI = (Cd % 32) == 0;
 
-    // ---- gate/up units of this warp: u = gw + n * nw; the shared expert's first --------
-    const int n_gu = gw < sh.gu_units ? (sh.gu_units - 1 - gw) / nw + 1 : 0;
-    int gu_issued = 0;
+    // ---- gate/up units: unit u (shared expert's first, then slot by slot) is taken by the
+    // warp that claims it from a grid-wide counter, so faster SMs do more of them
+    const unsigned kFull = 0xffffffffu;
+    const int U_total = sh.gu_units;
+    unsigned *gu_ctr = p.ws.claims;
     bool routed = false;          // routing known to this block
     auto gu_src = [&](int u, int &slot, int &rb, const uint8_t *&slab, int &Ij) {
         if (u < sh.U_sh) {
@@ -301,11 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             Ij = d.I;
         }
     };
-    auto issue_gu = [&](int n) {
+    auto issue_gu = [&](int u, int b) {
         int slot, rb, Ij;
         const uint8_t *slab;
-        gu_src(gw + n * nw, slot, rb, slab, Ij);
-        const uint32_t dst = wbuf + (uint32_t)((n % kGuBufs) * sh.gu_unit);
+        gu_src(u, slot, rb, slab, Ij);
+        const uint32_t dst = wbuf + (uint32_t)(b * sh.gu_unit);
         const uint8_t *gsrc = slab + (size_t)rb * kGuRows * sh.rowbytes + lane * 16;
         const uint8_t *usrc = slab + ((size_t)Ij + (size_t)rb * kGuRows) * sh.rowbytes + lane * 16;
 #pragma unroll
@@ -316,16 +333,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             for (int k = 0; k < CPLH; k++)
                 if (fullH || lane + 32 * k < C) cp_async16(drow + 512 * k, src + 512 * k);
         }
-    };
-    // issue the next units, up to kGuBufs ahead of `done`; routed ones only once routing is known
-    auto gu_fill = [&](int done) {
-        while (gu_issued < n_gu && gu_issued < done + kGuBufs) {
-            if (gw + gu_issued * nw >= sh.U_sh && !routed) return;
-            issue_gu(gu_issued);
-            cp_async_commit();
-            gu_issued++;
+        // the row scales travel with the rows: writer lane 8r copies (s_g, s_u) of row r into
+        // the unit's last 16 bytes, so it can read them back after its own wait
+        if (lane < 8 * kGuRows && (lane & 7) == 0) {
+            const int r = lane >> 3;
+            const float *scale = slot < K ? s_scale[slot] : p.sh_scale;
+            const uint32_t sdst = dst - (uint32_t)(lane * 16) + (uint32_t)(2 * kGuRows * sh.rowbytes + 8 * r);
+            cp_async4(sdst, scale + rb * kGuRows + r);
+            cp_async4(sdst + 4, scale + Ij + rb * kGuRows + r);
         }
+        cp_async_commit();
     };
+    // a claim is an atomic issued early; taking it (a shuffle of lane 0's result) waits for it
+    auto take = [&](unsigned c, unsigned limit) -> int {
+        const unsigned u = __shfl_sync(kFull, c, 0);
+        return u < limit ? (int)u : -1;
+    };
+    unsigned c_first = 0, c_second = 0;
+    if (lane == 0) {
+        c_first = atomicAdd(gu_ctr, 1u);
+        c_second = atomicAdd(gu_ctr, 1u);
+    }
+
     // ---- phase 0: one batch of loads: x chunk `tid`, the same chunk of this block's two router rows
     // (issued before the shared-expert prefetch: routing is on the critical path)
     const int e0 = 2 * blockIdx.x;
@@ -334,6 +363,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     float a0 = 0.0f, a1 = 0.0f, amax = 0.0f, ss = 0.0f;
     bool bad = false;
     float4 u0[8], u1[8];
+    float bias0 = 0.0f, bias1 = 0.0f;
+    if (tid == 0) {
+        if (has0) bias0 = __ldg(p.router_b + e0);
+        if (has1) bias1 = __ldg(p.router_b + e0 + 1);
+    }
     if (tid < C) {
         const float4 *x4 = reinterpret_cast<const float4 *>(x + (size_t)tid * 32);
         const float4 *w0 = reinterpret_cast<const float4 *>(p.router_w + (size_t)(has0 ? e0 : 0) * H + (size_t)tid * 32);
@@ -346,7 +380,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             u1[k] = has1 ? __ldg(w1 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    gu_fill(0);
+    // the first unit goes out now if it is the shared expert's (routing not needed)
+    const int uA = take(c_first, (unsigned)U_total);
+    int n_iss = 0;
+    if (uA >= 0 && uA < sh.U_sh && kGuPre > 0) {
+        issue_gu(uA, 0);
+        n_iss = 1;
+    }
     if (tid < C) {
 #pragma unroll
         for (int k = 0; k < 8; k++) {
@@ -388,18 +428,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         A1 += red[32 + w];
     }
     const float r = d.prenorm ? 1.0f / sqrtf(ss / (float)H + d.eps) : 1.0f;
-    auto put_score = [&](int e, float raw) {
+    auto put_score = [&](int e, float raw, float bias) {
         const float l = raw * r;
         const float sg = 1.0f / (1.0f + expf(-l));
-        float c = sg + p.router_b[e] + 0.0f;   // + 0: no negative zero
+        float c = sg + bias + 0.0f;   // + 0: no negative zero
         if (isnan(c)) c = -INFINITY;
         p.ws.logits[e] = l;
         p.ws.dscore[e] = sg;
         p.ws.dscore[E + e] = c;
     };
     if (tid == 0) {
-        if (has0) put_score(e0, A0);
-        if (has1) put_score(e0 + 1, A1);
+        if (has0) put_score(e0, A0, bias0);
+        if (has1) put_score(e0 + 1, A1, bias1);
     }
     // more experts than 2 per block: further pairs, rows split over all threads
     for (int ep = e0 + 2 * G; ep < E; ep += 2 * G) {
@@ -424,8 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         if (tid == 0) {
             float B0 = 0.0f, B1 = 0.0f;
             for (int w = 0; w < kWarps; w++) { B0 += red[40 + w]; B1 += red[48 + w]; }
-            put_score(ep, B0);
-            if (h1) put_score(ep + 1, B1);
+            put_score(ep, B0, __ldg(p.router_b + ep));
+            if (h1) put_score(ep + 1, B1, __ldg(p.router_b + ep + 1));
         }
     }
 
@@ -518,7 +558,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     routed = true;
 
     // ---- phase 1: gate/up + SwiGLU ------------------------------------------------------
-    gu_fill(0);
+    // Units sit in the warp's buffers in claim order (unit m in buffer m % 2); one more claim
+    // is always in flight so the next unit can be issued as soon as a buffer frees.
+    int ub0 = uA, ub1 = -1;
+    if (uA >= 0 && n_iss == 0) {
+        issue_gu(uA, 0);
+        n_iss = 1;
+    }
+    const int uB = take(c_second, (unsigned)U_total);
+    if (uA >= 0 && uB >= 0) {
+        issue_gu(uB, 1);
+        ub1 = uB;
+        n_iss = 2;
+    }
+    unsigned c_next = 0;
+    bool pending = false;
+    if (n_iss == 2) {
+        if (lane == 0) c_next = atomicAdd(gu_ctr, 1u);
+        pending = true;
+    }
     int corr[3] = {0, 0, 0};
 #pragma unroll
     for (int k = 0; k < CPLH; k++) {
@@ -529,19 +587,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     }
     const uint32_t xdig_a = smem_u32(xdig) + (uint32_t)(lane * 16);
     const bool gu_writer = lane < 16 && (lane & 7) == 0;   // lane l ends with row l / 8
-    for (int n = 0; n < n_gu; n++) {
-        cp_async_wait_n(gu_issued - n - 1);
+    for (int m = 0; m < n_iss; m++) {
+        cp_async_wait_n(n_iss - m - 1);
+        const int b = m & 1;
+        const int u = b ? ub1 : ub0;
         int slot, rb, Ij;
         const uint8_t *slab;
-        gu_src(gw + n * nw, slot, rb, slab, Ij);
-        const float *scale = slot < K ? s_scale[slot] : p.sh_scale;
+        gu_src(u, slot, rb, slab, Ij);
         const int o = rb * kGuRows + (lane >> 3);
-        float sg = 0.0f, su = 0.0f;
-        if (gu_writer) {          // issued now, needed after the dot products
-            sg = __ldg(scale + o);
-            su = __ldg(scale + Ij + o);
-        }
-        const uint32_t st = wbuf + (uint32_t)((n % kGuBufs) * sh.gu_unit);
+        const uint32_t st = wbuf + (uint32_t)(b * sh.gu_unit);
         int lo[2 * kGuRows][3], hi[2 * kGuRows][3];
 #pragma unroll
         for (int rr = 0; rr < 2 * kGuRows; rr++) {
@@ -563,79 +617,153 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
 #pragma unroll
         for (int rr = 0; rr < 2 * kGuRows; rr++) v[rr] = planes_lh_to_float(lo[rr], hi[rr]);
         const float tot = reduce_scatter<2 * kGuRows>(v, lane);
-        const float up = __shfl_down_sync(0xffffffffu, tot, 16);   // up row of the same output
-        if (gu_writer) {
-            const float hv = silu_mul(tot * s_x * sg, up * s_x * su);
-            p.ws.h[(size_t)slot * d.I_max + o] = hv;
-            atomicMax(p.ws.hmax + slot, __float_as_uint(fabsf(hv)));
+        const float up = __shfl_down_sync(kFull, tot, 16);   // up row of the same output
+        if (gu_writer) {          // the scales this lane copied with the unit
+            const uint32_t sa = st - (uint32_t)(lane * 16) + (uint32_t)(2 * kGuRows * sh.rowbytes + 8 * (lane >> 3));
+            const float sg = lds32(sa), su = lds32(sa + 4);
+            p.ws.h[(size_t)slot * d.I_max + o] = silu_mul(tot * s_x * sg, up * s_x * su);
         }
-        gu_fill(n + 1);   // the buffer just read takes the unit kGuBufs ahead
+        if (pending) {            // the buffer just read takes the next claimed unit
+            pending = false;
+            const int un = take(c_next, (unsigned)U_total);
+            if (un >= 0) {
+                issue_gu(un, b);
+                if (b) ub1 = un; else ub0 = un;
+                n_iss++;
+                if (lane == 0) c_next = atomicAdd(gu_ctr, 1u);
+                pending = true;
+            }
+        }
     }
     cp_async_wait_n(0);
 
-    // ---- down units of this warp: slot j = gw % J, row blocks q, q + nq, ... ---------------
-    const int j = gw % J;
-    const int q = gw / J;
-    const int nq = (nw - j + J - 1) / J;
-    const int n_dn = q < sh.RB ? (sh.RB - 1 - q) / nq + 1 : 0;
-    const uint8_t *dslab = n_dn > 0 ? s_slab[j] + (size_t)d.I * d.H + lane * 16 : nullptr;
-    auto issue_dn = [&](int n) {
-        const int rb = q + n * nq;
+    // ---- down: half-block hb (warps 4 hb .. 4 hb + 3) serves slot j; its rows are claimed
+    // from the slot's counter.  The first unit goes out before barrier 2.
+    const int hb = warp >> 2;
+    const int j = (2 * blockIdx.x + hb) % J;
+    unsigned *dn_ctr = p.ws.claims + 1 + j;
+    const uint8_t *dslab = s_slab[j] + (size_t)d.I * d.H + lane * 16;
+    const float *sd = s_scale[j] + 2 * d.I;
+    const bool dn_writer = (lane & 3) == 0;                // lane l ends with row l / 4
+    int *ring = s_ring + warp * 4;                         // row block of each buffer
+    auto issue_dn = [&](int rb, int b) {
         const uint8_t *src = dslab + (size_t)rb * kDnRows * sh.drowbytes;
-        const uint32_t dst = wbuf + (uint32_t)((n % kDnBufs) * sh.dn_unit);
+        const uint32_t dst = wbuf + (uint32_t)(b * sh.dn_unit);
 #pragma unroll
         for (int rr = 0; rr < kDnRows; rr++)
 #pragma unroll
             for (int k = 0; k < CPLI; k++)
                 if (fullI || lane + 32 * k < Cd)
                     cp_async16(dst + (uint32_t)(rr * sh.drowbytes + 512 * k), src + (size_t)rr * sh.drowbytes + 512 * k);
-    };
-    int dn_issued = 0;
-    for (; dn_issued < n_dn && dn_issued < kDnBufs; dn_issued++) {
-        issue_dn(dn_issued);
+        // writer lane 4r copies the scale of row r into the unit's last 32 bytes
+        if (dn_writer)
+            cp_async4(dst - (uint32_t)(lane * 16) + (uint32_t)(kDnRows * sh.drowbytes + lane),
+                      sd + rb * kDnRows + (lane >> 2));
         cp_async_commit();
+        ring[b] = rb;             // every lane stores the same value
+    };
+    unsigned dc[kDnBufs] = {};
+    if (lane == 0)
+#pragma unroll
+        for (int i = 0; i < kDnBufs; i++) dc[i] = atomicAdd(dn_ctr, 1u);
+    int nd = 0;
+    const int rb0 = take(dc[0], (unsigned)sh.RB);
+    if (rb0 >= 0 && kDnPre > 0) {
+        issue_dn(rb0, 0);
+        nd = 1;
     }
 
-    // ---- barrier 2: every SwiGLU activation and its maximum are written ------------------
+    // ---- barrier 2: every SwiGLU activation is written ------------------------------------
     if (!grid_barrier(bar2, target, p.ws.err, s_flags + 1)) {
         cp_async_wait_n(0);
         return;
     }
 
-    // ---- phase 2: down; this lane's chunks of slot j's h as digits in registers ------------
-    const float hmax = __uint_as_float(__ldcg(p.ws.hmax + j));
+    // ---- phase 2: the half-block loads slot j's h (thread t of the half: chunk t), takes
+    // max |h|, and writes the digits to shared memory; the loads go out before the rest of
+    // the warp's first down units so they do not queue behind them
+    const int ht = tid & 127;
+    const bool hchunk = ht < Cd;
+    float hv[32];
+    {
+        const float4 *h4 = reinterpret_cast<const float4 *>(p.ws.h + (size_t)j * d.I_max + (size_t)(hchunk ? ht : 0) * 32);
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+            const float4 f = hchunk ? __ldcg(h4 + t) : make_float4(0.f, 0.f, 0.f, 0.f);
+            hv[4 * t] = f.x; hv[4 * t + 1] = f.y; hv[4 * t + 2] = f.z; hv[4 * t + 3] = f.w;
+        }
+    }
+    if (rb0 >= 0 && nd == 0) {
+        issue_dn(rb0, 0);
+        nd = 1;
+    }
+#pragma unroll
+    for (int i = 1; i < kDnBufs; i++) {
+        const int rbi = take(dc[i], (unsigned)sh.RB);
+        if (rb0 >= 0 && nd == i && rbi >= 0) {
+            issue_dn(rbi, i);
+            nd = i + 1;
+        }
+    }
+    unsigned c_dn = 0;
+    bool dn_pending = false;
+    if (nd == kDnBufs) {
+        if (lane == 0) c_dn = atomicAdd(dn_ctr, 1u);
+        dn_pending = true;
+    }
+    float hm = 0.0f;
+    bool hnan = false;
+#pragma unroll
+    for (int i = 0; i < 32; i++) {
+        hm = fmaxf(hm, fabsf(hv[i]));
+        hnan |= isnan(hv[i]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) hm = fmaxf(hm, __shfl_xor_sync(kFull, hm, o));
+    hnan = __any_sync(kFull, hnan);
+    if (lane == 0) red[56 + warp] = hnan ? __int_as_float(0x7fc00000) : hm;
+    named_barrier(1 + hb, 128);
+    float hmax = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 4; w++) {
+        const float r4 = red[56 + 4 * hb + w];
+        hmax = (isnan(r4) || isnan(hmax)) ? r4 + hmax : fmaxf(hmax, r4);
+    }
     const float hs = hmax / kQMax;                    // NaN propagates
     const float hinv = (hs > 0.0f && isfinite(hs)) ? 1.0f / hs : 0.0f;
     const float coef_j = s_w[j] * hs;
+    uint4 *hd = xdig + (size_t)hb * 7 * Cd;           // x digits are no longer read
+    if (hchunk) {
+        uint4 dig[6];
+        int ds[3];
+        quant_chunk(hv, hinv, dig, ds);
+#pragma unroll
+        for (int q = 0; q < 6; q++) hd[q * Cd + ht] = dig[q];
+        hd[6 * Cd + ht] = make_uint4((unsigned)ds[0], (unsigned)ds[1], (unsigned)ds[2], 0u);
+    }
+    named_barrier(1 + hb, 128);
     uint4 hdig[CPLI][6];
     int dcorr[3] = {0, 0, 0};
 #pragma unroll
     for (int k = 0; k < CPLI; k++) {
         const int c = lane + 32 * k;
-        if (n_dn > 0 && (fullI || c < Cd)) {
-            const float4 *h4 = reinterpret_cast<const float4 *>(p.ws.h + (size_t)j * d.I_max + (size_t)c * 32);
-            float v[32];
+        if (fullI || c < Cd) {
 #pragma unroll
-            for (int t = 0; t < 8; t++) {
-                const float4 f = __ldcg(h4 + t);
-                v[4 * t] = f.x; v[4 * t + 1] = f.y; v[4 * t + 2] = f.z; v[4 * t + 3] = f.w;
-            }
-            int ds[3];
-            quant_chunk(v, hinv, hdig[k], ds);
-            dcorr[0] -= 8 * ds[0]; dcorr[1] -= 8 * ds[1]; dcorr[2] -= 8 * ds[2];
+            for (int q = 0; q < 6; q++) hdig[k][q] = hd[q * Cd + c];
+            const uint4 t = hd[6 * Cd + c];
+            dcorr[0] -= 8 * (int)t.x; dcorr[1] -= 8 * (int)t.y; dcorr[2] -= 8 * (int)t.z;
         } else {
 #pragma unroll
-            for (int t = 0; t < 6; t++) hdig[k][t] = make_uint4(0u, 0u, 0u, 0u);
+            for (int q = 0; q < 6; q++) hdig[k][q] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    const float *sd = n_dn > 0 ? s_scale[j] + 2 * d.I : nullptr;
-    const bool dn_writer = (lane & 3) == 0;                // lane l ends with row l / 4
-    for (int n = 0; n < n_dn; n++) {
-        const int rb = q + n * nq;
+    __syncwarp();
+    for (int m = 0; m < nd; m++) {
+        cp_async_wait_n(nd - m - 1);
+        const int b = m % kDnBufs;
+        const int rb = ring[b];
         const int o = rb * kDnRows + (lane >> 2);
-        const float coef = dn_writer ? coef_j * __ldg(sd + o) : 0.0f;   // issued before the wait
-        cp_async_wait_n(dn_issued - n - 1);
-        const uint32_t st = wbuf + (uint32_t)((n % kDnBufs) * sh.dn_unit);
+        const uint32_t st = wbuf + (uint32_t)(b * sh.dn_unit);
         int lo[kDnRows][3], hi[kDnRows][3];
 #pragma unroll
         for (int rr = 0; rr < kDnRows; rr++) {
@@ -655,11 +783,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
 #pragma unroll
         for (int rr = 0; rr < kDnRows; rr++) v[rr] = planes_lh_to_float(lo[rr], hi[rr]);
         const float tot = reduce_scatter<kDnRows>(v, lane);
-        if (dn_writer) p.ws.dpart[(size_t)j * H + o] = tot * coef;
-        if (dn_issued < n_dn) {            // the buffer just read takes the unit kDnBufs ahead
-            issue_dn(dn_issued);
-            cp_async_commit();
-            dn_issued++;
+        if (dn_writer) {          // the row scale this lane copied with the unit
+            const float coef = coef_j * lds32(st - (uint32_t)(lane * 16) + (uint32_t)(kDnRows * sh.drowbytes + lane));
+            p.ws.dpart[(size_t)j * H + o] = tot * coef;
+        }
+        __syncwarp();             // every lane has read ring[b] before it is rewritten
+        if (dn_pending) {         // the buffer just read takes the next claimed row block
+            dn_pending = false;
+            const int rn = take(c_dn, (unsigned)sh.RB);
+            if (rn >= 0) {
+                issue_dn(rn, b);
+                nd++;
+                if (lane == 0) c_dn = atomicAdd(dn_ctr, 1u);
+                dn_pending = true;
+            }
         }
     }
     cp_async_wait_n(0);
@@ -672,8 +809,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         if (d.n_shared) acc += __ldcg(p.ws.dpart + (size_t)K * H + o);
         y[o] = d.prenorm ? x[o] + acc : acc;
     }
-    // every block has read hmax (before barrier 3): clear it for the next call
-    if (blockIdx.x == 0 && tid < J) p.ws.hmax[tid] = 0u;
+    // every claim was taken before barrier 3: clear the counters for the next call
+    if (blockIdx.x == 0 && tid <= J) p.ws.claims[tid] = 0u;
 }
 
 int g_sms = 0;
@@ -747,8 +884,8 @@ cudaError_t prepare_decode_fast(const Dims &d) {
             default: e = cudaErrorInvalidValue;
         }
     }
-    // every slot needs at least one warp in the down phase
-    if (e == cudaSuccess && g_sms * kWarps < d.K + d.n_shared) e = cudaErrorNotSupported;
+    // every slot needs at least one half-block in the down phase
+    if (e == cudaSuccess && 2 * g_sms < d.K + d.n_shared) e = cudaErrorNotSupported;
     g_blocks = g_sms;
     return e;
 }

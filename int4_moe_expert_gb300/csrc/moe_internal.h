@@ -39,8 +39,8 @@ struct Workspace {
     int *n_slots;        // [1]
     float *dbuf;         // [(maxT*K + maxT), H] unweighted down outputs (T > 1)
     // decode (T == 1) streaming path
-    unsigned *hmax;      // [kMaxSlots] bits of max |h| per slot (reset by the down kernel)
-    unsigned *rb_ticket; // [H / 8] per row-block arrivals in the down kernel
+    unsigned *claims;    // [kClaimWords] work counters: [0] gate/up units, [1 + j] down rows of
+                         // slot j; each call's last barrier is followed by their reset to 0
     unsigned *err;       // [4] device error word: bounded waits that ran out
     float *dpart;        // [kMaxSlots, H] down outputs per slot (times the routing weight)
     float *dscore;       // [2, E] decode router: sigmoid | selection score (sigmoid + bias)
@@ -48,6 +48,7 @@ struct Workspace {
 };
 
 constexpr int kMaxSlots = 33;   // K <= 32 routed + 1 shared
+constexpr int kClaimWords = 64;  // >= 1 + kMaxSlots
 
 // Everything a kernel needs, passed by value.
 struct Params {

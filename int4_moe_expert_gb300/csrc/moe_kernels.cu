@@ -826,8 +826,7 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
     ws->inv = reinterpret_cast<int *>(take(P * sizeof(int)));
     ws->slot_expert = reinterpret_cast<int *>(take(d.E * sizeof(int)));
     ws->n_slots = reinterpret_cast<int *>(take(sizeof(int)));
-    ws->hmax = reinterpret_cast<unsigned *>(take(kMaxSlots * sizeof(unsigned)));
-    ws->rb_ticket = reinterpret_cast<unsigned *>(take((d.H / 8 + 1) * sizeof(unsigned)));
+    ws->claims = reinterpret_cast<unsigned *>(take(kClaimWords * sizeof(unsigned)));
     ws->err = reinterpret_cast<unsigned *>(take(4 * sizeof(unsigned)));
     ws->dpart = reinterpret_cast<float *>(take((size_t)kMaxSlots * d.H * sizeof(float)));
     ws->dscore = reinterpret_cast<float *>(take(2 * (size_t)d.E * sizeof(float)));
