@@ -112,7 +112,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -249,6 +249,11 @@ def run_ours(args, rank, world, local_rank, dist_on):
     barrier(dist_on)
     step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     total_ms = reduce_max(sum(step_ms), dist_on)
+    step_sorted = sorted(step_ms)
+    step_stats = {"median_us": round(1e3 * statistics.median(step_ms), 2),
+                  "p10_us": round(1e3 * step_sorted[len(step_sorted) // 10], 2),
+                  "p90_us": round(1e3 * step_sorted[(9 * len(step_sorted)) // 10], 2),
+                  "max_us": round(1e3 * step_sorted[-1], 2)}
     assert moe.moe_device_error(layer.handle) == 0
 
     # One cooperative launch per step on the decode path (the step events
@@ -327,6 +332,7 @@ def run_ours(args, rank, world, local_rank, dist_on):
             "steps": K,
             "warmup": args.warmup,
             "ms_per_step": round(ms_per_step, 6),
+            "step_time_distribution": step_stats,
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,

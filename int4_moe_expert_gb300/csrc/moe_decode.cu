@@ -2,18 +2,19 @@
 //
 // One block per SM (a cooperative launch, so every block is resident), eight
 // warps.  The step's four parts run as phases separated by grid-wide
-// barriers; while a block waits at a barrier its warps have already started
-// fetching the next phase's weights, so HBM keeps streaming from the first
-// router byte to the last down byte:
+// barriers:
 //   phase 0  one batch of loads (x chunk and this block's two router rows);
 //            router logits -> sigmoid and selection score (sigmoid + bias);
 //            x digits                                           -> barrier 1
-//            (meanwhile: shared-expert gate/up rows stream in)
+//            (a warp whose first unit is the shared expert's starts its loads)
 //   routing  warp 0 of every block selects the top K (K rounds of a warp max)
-//   phase 1  gate/up + SwiGLU, units of two (gate, up) row pairs
-//            (each warp then starts fetching its first down rows) -> barrier 2
-//   phase 2  down: each warp serves one slot; d_j = w_j * s_d * (Q_d h_j)
-//                                                              -> barrier 3
+//   phase 1  gate/up + SwiGLU: warp gw computes units gw, gw + nw, ... (nw =
+//            warps in the grid); a unit is the (gate row, up row) pair of one
+//            output, the shared expert's units first, then slot by slot
+//            (each warp then starts loading its first down unit) -> barrier 2
+//   phase 2  down: each half-block (4 warps) serves one slot, quantises that
+//            slot's h once into shared memory, and its warps take units of
+//            four output rows; d_j = w_j * s_d * (Q_d h_j)          -> barrier 3
 //   phase 3  y = sum_k d_k + d_shared (k ascending; + x with pre-norm residual)
 //
 // What is computed (reader.mx "25GB 内存上运行 GLM 5.2 744B" section 11;
@@ -39,11 +40,13 @@
 // the plane-p digits of elements 8m+{0,2,4,6} (lh = 0: the low nibbles of
 // word m) or 8m+{1,3,5,7} (lh = 1: the high nibbles), one per byte.
 //
-// Weights move with per-lane 16-byte cp.async copies into per-warp buffers;
-// each lane reads back exactly the pieces it copied, so a warp needs no
-// synchronisation with any other to consume its own units.  (Measured on this
-// GPU: one block issuing 1-D bulk copies completes about one copy per 0.27 us
-// whatever its size, which capped 6-12 KB units at 23-45 GB/s per SM.)
+// Weights go straight from HBM into registers with 16-byte non-caching loads:
+// lane l holds chunks l, l + 32, ... of every row of its unit, which is the
+// layout the dp4a loop reads, and the next unit's loads are in flight while
+// the current one is computed.  (Measured on this GPU, streaming 105 MB with
+// 8 warps per SM: per-warp units loaded into registers ran at 5.8 TB/s, the
+// same units through cp.async or 1-D bulk copies into shared memory at
+// 5.0-5.1 TB/s, with or without compute.)
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -56,14 +59,9 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kGuRows = 2;          // row pairs (gate + up) per gate/up unit
-constexpr int kGuBufs = 2;          // gate/up buffers per warp
-constexpr int kGuPre = 1;           // 1: a first claimed unit of the shared expert is fetched before routing
-constexpr int kDnRows = 8;          // output rows per down unit
-constexpr int kDnBufs = 3;          // down buffers per warp
-constexpr int kDnPre = 1;           // down units a warp fetches before the SwiGLU barrier
-constexpr int kSmemBudget = 220 * 1024;
-constexpr unsigned kSpinLimit = 1u << 22;   // bounded waits (about 0.1-1 s)
+constexpr int kDnRows = 4;          // output rows per down unit
+constexpr int kSmemBudget = 64 * 1024;
+constexpr unsigned long long kWaitNs = 500ull * 1000 * 1000;   // every wait gives up after 0.5 s
 constexpr float kQMax = 8355711.0f;         // 0x7F7F7F
 constexpr int kSwWords = (kMaxSlots + 3) / 4 * 4;   // s_w padded to 16 bytes
 static_assert(kMaxSlots * 16 % 16 == 0 && kSwWords >= kMaxSlots, "shared-memory carving");
@@ -73,18 +71,6 @@ enum : unsigned { kErrGrid = 8u };
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ float lds32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-    return v;
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -199,11 +185,6 @@ __device__ __forceinline__ unsigned order_key(float f) {
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
-__device__ __forceinline__ void cp_async_wait_n(int n) {     // n = groups allowed to stay pending
-    if (n <= 0) asm volatile("cp.async.wait_group 0;" ::: "memory");
-    else if (n == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
-    else asm volatile("cp.async.wait_group 2;" ::: "memory");
-}
 __device__ __forceinline__ void named_barrier(int id, int threads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -212,14 +193,22 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
+__device__ __forceinline__ unsigned long long now_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
 // Single thread: wait until *ctr has reached target (counters only grow;
-// wrap-safe).  false if the bounded wait ran out.
+// wrap-safe).  false if the wait ran out (kWaitNs).
 __device__ bool spin_until(const unsigned *ctr, unsigned target) {
-    for (unsigned i = 0; i < kSpinLimit; i++) {
-        if ((int)(ld_acquire(ctr) - target) >= 0) return true;
-        __nanosleep(32);
+    const unsigned long long t0 = now_ns();
+    for (;;) {
+        for (int i = 0; i < 32; i++) {
+            if ((int)(ld_acquire(ctr) - target) >= 0) return true;
+            __nanosleep(32);
+        }
+        if (now_ns() - t0 > kWaitNs) return false;
     }
-    return false;
 }
 // Whole block: every block adds one to *ctr, then waits for all of them.
 __device__ bool grid_barrier(unsigned *ctr, unsigned target, unsigned *err, volatile int *s_ok) {
@@ -237,20 +226,17 @@ __device__ bool grid_barrier(unsigned *ctr, unsigned target, unsigned *err, vola
 
 
 struct FusedShape {
-    // gate/up
+    // gate/up: a unit is one (gate row, up row) pair of one slot
     int C;             // chunks per row = H / 32
     int rowbytes;      // H / 2
-    int gu_unit;       // bytes of one unit: 2 * kGuRows rows + their scales (16 B)
     int U_sh, U_r;     // units of the shared expert, units per routed expert
     int gu_units;
-    // down
+    // down: a unit is kDnRows consecutive output rows of one slot
     int Cd;            // chunks per row = I / 32
     int drowbytes;     // I / 2
-    int dn_unit;       // kDnRows rows + their scales (32 B)
     int J;             // slots = K + n_shared
     int RB;            // row blocks = H / kDnRows
-    int warp_bytes;    // per-warp buffer region
-    int dig_bytes;     // digit region: x (7 C uint4) in phase 0/1, two slots' h (2 x 7 Cd uint4) in phase 2
+    int dig_bytes;     // digits: x (7 C uint4) in phases 0/1, two slots' h (2 x 7 Cd uint4) in phase 2
     size_t smem;
 };
 
@@ -258,22 +244,25 @@ __host__ __device__ inline FusedShape fused_shape(const Dims &d) {
     FusedShape s;
     s.C = d.H / 32;
     s.rowbytes = d.H / 2;
-    s.gu_unit = 2 * kGuRows * s.rowbytes + 16;
-    s.U_sh = d.n_shared ? d.I_sh / kGuRows : 0;
-    s.U_r = d.I / kGuRows;
+    s.U_sh = d.n_shared ? d.I_sh : 0;
+    s.U_r = d.I;
     s.gu_units = s.U_sh + d.K * s.U_r;
     s.Cd = d.I / 32;
     s.drowbytes = d.I / 2;
-    s.dn_unit = kDnRows * s.drowbytes + 32;
     s.J = d.K + d.n_shared;
     s.RB = d.H / kDnRows;
-    const int gu = kGuBufs * s.gu_unit, dn = kDnBufs * s.dn_unit;
-    s.warp_bytes = gu > dn ? gu : dn;
     s.dig_bytes = 7 * 16 * (s.C > 2 * s.Cd ? s.C : 2 * s.Cd);
-    // buffers | digits | red[64] | slab[33] | scale[33] | w[36] | flags[4] | score keys[E] | idx[32] | ring[8][4]
-    s.smem = (size_t)kWarps * s.warp_bytes + (size_t)s.dig_bytes + 64 * 4 + kMaxSlots * 16 + kSwWords * 4 + 16 +
-             (size_t)(d.E + 3) / 4 * 16 + 32 * 4 + kWarps * 4 * 4;
+    // digits | red[64] | slab[33] | scale[33] | w[36] | flags[4] | score keys[E] | sel[32]
+    s.smem = (size_t)s.dig_bytes + 64 * 4 + kMaxSlots * 16 + kSwWords * 4 + 16 + (size_t)(d.E + 3) / 4 * 16 + 32 * 4;
     return s;
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {   // weights: read once, keep out of L1
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 template <int CPLH, int CPLI>
@@ -281,79 +270,61 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
                                                                    float *__restrict__ y, FusedShape sh,
                                                                    unsigned gen, int want_counts) {
     extern __shared__ __align__(128) unsigned char smem[];
-    uint4 *xdig = reinterpret_cast<uint4 *>(smem + (size_t)kWarps * sh.warp_bytes);
+    uint4 *xdig = reinterpret_cast<uint4 *>(smem);
     int4 *xdsum = reinterpret_cast<int4 *>(xdig + 6 * sh.C);
-    float *red = reinterpret_cast<float *>(smem + (size_t)kWarps * sh.warp_bytes + sh.dig_bytes);
+    float *red = reinterpret_cast<float *>(smem + sh.dig_bytes);
     const uint8_t **s_slab = reinterpret_cast<const uint8_t **>(red + 64);
     const float **s_scale = reinterpret_cast<const float **>(s_slab + kMaxSlots);
     float *s_w = reinterpret_cast<float *>(s_scale + kMaxSlots);
     volatile int *s_flags = reinterpret_cast<volatile int *>(s_w + kSwWords);   // [0] ok [1] abort
     unsigned *s_key = reinterpret_cast<unsigned *>(const_cast<int *>(s_flags + 4));   // [E] (+pad)
     int *s_sel = reinterpret_cast<int *>(s_key + (p.d.E + 3) / 4 * 4);                // [32]
-    int *s_ring = s_sel + 32;                                                          // [kWarps][4]
 
     const Dims &d = p.d;
     const int H = d.H, E = d.E, K = d.K, J = sh.J, C = sh.C, Cd = sh.Cd;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
-    const int G = gridDim.x;
+    const int G = gridDim.x, nw = G * kWarps, gw = blockIdx.x * kWarps + warp;
     const unsigned target = gen * (unsigned)G;
+    const unsigned kFull = 0xffffffffu;
     unsigned *bar1 = p.ws.counters + 4, *bar2 = p.ws.counters + 5, *bar3 = p.ws.counters + 6;
-    const uint32_t wbuf = smem_u32(smem + (size_t)warp * sh.warp_bytes) + (uint32_t)(lane * 16);
     const bool fullH = (C % 32) == 0, fullI = (Cd % 32) == 0;
 
-    // ---- gate/up units: unit u (shared expert's first, then slot by slot) is taken by the
-    // warp that claims it from a grid-wide counter, so faster SMs do more of them
-    const unsigned kFull = 0xffffffffu;
+    // ---- gate/up units (the shared expert's first, then slot by slot): warp gw takes units
+    // gw, gw + nw, gw + 2 nw, ...  A unit's rows go straight into registers (lane l: chunks
+    // l + 32 k of the gate row, then of the up row); the next unit's loads are in flight
+    // while the current one is computed.
     const int U_total = sh.gu_units;
-    unsigned *gu_ctr = p.ws.claims;
-    bool routed = false;          // routing known to this block
-    auto gu_src = [&](int u, int &slot, int &rb, const uint8_t *&slab, int &Ij) {
+    auto load_gu = [&](int u, uint4 (&w)[2 * CPLH], float &sg, float &su) {
+        int slot, o, Ij;
+        const uint8_t *slab;
+        const float *scale;
         if (u < sh.U_sh) {
-            slot = K; rb = u; slab = p.sh_slab; Ij = d.I_sh;
+            slot = K; o = u; Ij = d.I_sh; slab = p.sh_slab; scale = p.sh_scale;
         } else {
             const int v = u - sh.U_sh;
             slot = v / sh.U_r;
-            rb = v - slot * sh.U_r;
-            slab = s_slab[slot];
+            o = v - slot * sh.U_r;
             Ij = d.I;
+            slab = s_slab[slot];
+            scale = s_scale[slot];
         }
-    };
-    auto issue_gu = [&](int u, int b) {
-        int slot, rb, Ij;
-        const uint8_t *slab;
-        gu_src(u, slot, rb, slab, Ij);
-        const uint32_t dst = wbuf + (uint32_t)(b * sh.gu_unit);
-        const uint8_t *gsrc = slab + (size_t)rb * kGuRows * sh.rowbytes + lane * 16;
-        const uint8_t *usrc = slab + ((size_t)Ij + (size_t)rb * kGuRows) * sh.rowbytes + lane * 16;
+        const uint4 *g = reinterpret_cast<const uint4 *>(slab + (size_t)o * sh.rowbytes) + lane;
+        const uint4 *up = reinterpret_cast<const uint4 *>(slab + (size_t)(Ij + o) * sh.rowbytes) + lane;
 #pragma unroll
-        for (int rr = 0; rr < 2 * kGuRows; rr++) {
-            const uint8_t *src = rr < kGuRows ? gsrc + rr * sh.rowbytes : usrc + (rr - kGuRows) * sh.rowbytes;
-            const uint32_t drow = dst + (uint32_t)(rr * sh.rowbytes);
-#pragma unroll
-            for (int k = 0; k < CPLH; k++)
-                if (fullH || lane + 32 * k < C) cp_async16(drow + 512 * k, src + 512 * k);
+        for (int k = 0; k < CPLH; k++) {
+            if (fullH || lane + 32 * k < C) {
+                w[k] = ldg_stream(g + 32 * k);
+                w[CPLH + k] = ldg_stream(up + 32 * k);
+            }
         }
-        // the row scales travel with the rows: writer lane 8r copies (s_g, s_u) of row r into
-        // the unit's last 16 bytes, so it can read them back after its own wait
-        if (lane < 8 * kGuRows && (lane & 7) == 0) {
-            const int r = lane >> 3;
-            const float *scale = slot < K ? s_scale[slot] : p.sh_scale;
-            const uint32_t sdst = dst - (uint32_t)(lane * 16) + (uint32_t)(2 * kGuRows * sh.rowbytes + 8 * r);
-            cp_async4(sdst, scale + rb * kGuRows + r);
-            cp_async4(sdst + 4, scale + Ij + rb * kGuRows + r);
+        if (lane == 0) {
+            sg = __ldg(scale + o);
+            su = __ldg(scale + Ij + o);
         }
-        cp_async_commit();
     };
-    // a claim is an atomic issued early; taking it (a shuffle of lane 0's result) waits for it
-    auto take = [&](unsigned c, unsigned limit) -> int {
-        const unsigned u = __shfl_sync(kFull, c, 0);
-        return u < limit ? (int)u : -1;
-    };
-    unsigned c_first = 0, c_second = 0;
-    if (lane == 0) {
-        c_first = atomicAdd(gu_ctr, 1u);
-        c_second = atomicAdd(gu_ctr, 1u);
-    }
+    uint4 wa[2 * CPLH], wb[2 * CPLH];
+    float sga = 0.0f, sua = 0.0f, sgb = 0.0f, sub = 0.0f;
+    bool loaded = false;          // wa holds the warp's first unit
 
     // ---- phase 0: one batch of loads: x chunk `tid`, the same chunk of this block's two router rows
     // (issued before the shared-expert prefetch: routing is on the critical path)
@@ -380,12 +351,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             u1[k] = has1 ? __ldg(w1 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    // the first unit goes out now if it is the shared expert's (routing not needed)
-    const int uA = take(c_first, (unsigned)U_total);
-    int n_iss = 0;
-    if (uA >= 0 && uA < sh.U_sh && kGuPre > 0) {
-        issue_gu(uA, 0);
-        n_iss = 1;
+    // the first unit's loads go out now if it is the shared expert's (routing not needed)
+    if (gw < sh.U_sh) {
+        load_gu(gw, wa, sga, sua);
+        loaded = true;
     }
     if (tid < C) {
 #pragma unroll
@@ -402,12 +371,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        a0 += __shfl_xor_sync(0xffffffffu, a0, o);
-        a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+        amax = fmaxf(amax, __shfl_xor_sync(kFull, amax, o));
+        ss += __shfl_xor_sync(kFull, ss, o);
+        a0 += __shfl_xor_sync(kFull, a0, o);
+        a1 += __shfl_xor_sync(kFull, a1, o);
     }
-    bad = __any_sync(0xffffffffu, bad);
+    bad = __any_sync(kFull, bad);
     if (lane == 0) {
         red[warp] = amax;
         red[8 + warp] = ss;
@@ -496,10 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         s_flags[1] = 0;
     }
     __syncthreads();
-    if (!s_flags[0]) {
-        cp_async_wait_n(0);
-        return;
-    }
+    if (!s_flags[0]) return;
     // top K by (score desc, index asc), one warp: K rounds of a warp-wide max
     // over each lane's best remaining expert (lane l holds experts l + 32 i)
     if (warp == 0) {
@@ -555,28 +521,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         }
     }
     __syncthreads();
-    routed = true;
 
     // ---- phase 1: gate/up + SwiGLU ------------------------------------------------------
-    // Units sit in the warp's buffers in claim order (unit m in buffer m % 2); one more claim
-    // is always in flight so the next unit can be issued as soon as a buffer frees.
-    int ub0 = uA, ub1 = -1;
-    if (uA >= 0 && n_iss == 0) {
-        issue_gu(uA, 0);
-        n_iss = 1;
-    }
-    const int uB = take(c_second, (unsigned)U_total);
-    if (uA >= 0 && uB >= 0) {
-        issue_gu(uB, 1);
-        ub1 = uB;
-        n_iss = 2;
-    }
-    unsigned c_next = 0;
-    bool pending = false;
-    if (n_iss == 2) {
-        if (lane == 0) c_next = atomicAdd(gu_ctr, 1u);
-        pending = true;
-    }
     int corr[3] = {0, 0, 0};
 #pragma unroll
     for (int k = 0; k < CPLH; k++) {
@@ -586,102 +532,79 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         }
     }
     const uint32_t xdig_a = smem_u32(xdig) + (uint32_t)(lane * 16);
-    const bool gu_writer = lane < 16 && (lane & 7) == 0;   // lane l ends with row l / 8
-    for (int m = 0; m < n_iss; m++) {
-        cp_async_wait_n(n_iss - m - 1);
-        const int b = m & 1;
-        const int u = b ? ub1 : ub0;
-        int slot, rb, Ij;
-        const uint8_t *slab;
-        gu_src(u, slot, rb, slab, Ij);
-        const int o = rb * kGuRows + (lane >> 3);
-        const uint32_t st = wbuf + (uint32_t)(b * sh.gu_unit);
-        int lo[2 * kGuRows][3], hi[2 * kGuRows][3];
+    auto gu_compute = [&](int u, const uint4 (&w2)[2 * CPLH], float sg, float su) {
+        int slot, o;
+        if (u < sh.U_sh) {
+            slot = K; o = u;
+        } else {
+            const int v = u - sh.U_sh;
+            slot = v / sh.U_r;
+            o = v - slot * sh.U_r;
+        }
+        int lo[2][3], hi[2][3];
 #pragma unroll
-        for (int rr = 0; rr < 2 * kGuRows; rr++) {
+        for (int rr = 0; rr < 2; rr++) {
             lo[rr][0] = corr[0]; lo[rr][1] = corr[1]; lo[rr][2] = corr[2];
             hi[rr][0] = 0; hi[rr][1] = 0; hi[rr][2] = 0;
         }
 #pragma unroll
         for (int k = 0; k < CPLH; k++) {
             if (fullH || lane + 32 * k < C) {
-                uint4 dig[6], w[2 * kGuRows];
+                uint4 dig[6];
 #pragma unroll
                 for (int q = 0; q < 6; q++) dig[q] = lds128(xdig_a + (uint32_t)(q * C * 16 + 512 * k));
-#pragma unroll
-                for (int rr = 0; rr < 2 * kGuRows; rr++) w[rr] = lds128(st + (uint32_t)(rr * sh.rowbytes + 512 * k));
-                dot_rows<2 * kGuRows>(w, dig, lo, hi);
+                const uint4 w[2] = {w2[k], w2[CPLH + k]};
+                dot_rows<2>(w, dig, lo, hi);
             }
         }
-        float v[2 * kGuRows];
+        float v[2] = {planes_lh_to_float(lo[0], hi[0]), planes_lh_to_float(lo[1], hi[1])};
+        const float tot = reduce_scatter<2>(v, lane);            // lane < 16: gate, else up
+        const float up = __shfl_down_sync(kFull, tot, 16);
+        if (lane == 0) p.ws.h[(size_t)slot * d.I_max + o] = silu_mul(tot * s_x * sg, up * s_x * su);
+    };
+    // the next unit's loads are in flight while this one is computed; the loop is kept
+    // rolled (its body is large: unrolling it only grows the instruction footprint)
+    if (!loaded && gw < U_total) load_gu(gw, wa, sga, sua);
+#pragma unroll 1
+    for (int u = gw; u < U_total; u += nw) {
+        const int un = u + nw;
+        if (un < U_total) load_gu(un, wb, sgb, sub);
+        gu_compute(u, wa, sga, sua);
 #pragma unroll
-        for (int rr = 0; rr < 2 * kGuRows; rr++) v[rr] = planes_lh_to_float(lo[rr], hi[rr]);
-        const float tot = reduce_scatter<2 * kGuRows>(v, lane);
-        const float up = __shfl_down_sync(kFull, tot, 16);   // up row of the same output
-        if (gu_writer) {          // the scales this lane copied with the unit
-            const uint32_t sa = st - (uint32_t)(lane * 16) + (uint32_t)(2 * kGuRows * sh.rowbytes + 8 * (lane >> 3));
-            const float sg = lds32(sa), su = lds32(sa + 4);
-            p.ws.h[(size_t)slot * d.I_max + o] = silu_mul(tot * s_x * sg, up * s_x * su);
-        }
-        if (pending) {            // the buffer just read takes the next claimed unit
-            pending = false;
-            const int un = take(c_next, (unsigned)U_total);
-            if (un >= 0) {
-                issue_gu(un, b);
-                if (b) ub1 = un; else ub0 = un;
-                n_iss++;
-                if (lane == 0) c_next = atomicAdd(gu_ctr, 1u);
-                pending = true;
-            }
-        }
+        for (int k = 0; k < 2 * CPLH; k++) wa[k] = wb[k];
+        sga = sgb;
+        sua = sub;
     }
-    cp_async_wait_n(0);
 
-    // ---- down: half-block hb (warps 4 hb .. 4 hb + 3) serves slot j; its rows are claimed
-    // from the slot's counter.  The first unit goes out before barrier 2.
+    // ---- down: half-block hb (warps 4 hb .. 4 hb + 3) serves slot j; warp wl of the slot's
+    // nwj warps takes row blocks wl, wl + nwj, ...  The first unit's loads go out before
+    // barrier 2 (weights do not depend on h).
     const int hb = warp >> 2;
-    const int j = (2 * blockIdx.x + hb) % J;
-    unsigned *dn_ctr = p.ws.claims + 1 + j;
-    const uint8_t *dslab = s_slab[j] + (size_t)d.I * d.H + lane * 16;
+    const int hbg = 2 * blockIdx.x + hb;
+    const int j = hbg % J;
+    const int wl = (hbg / J) * 4 + (warp & 3);
+    const int nwj = 4 * ((2 * G - 1 - j) / J + 1);
+    const uint8_t *dslab = s_slab[j] + (size_t)d.I * d.H;
     const float *sd = s_scale[j] + 2 * d.I;
-    const bool dn_writer = (lane & 3) == 0;                // lane l ends with row l / 4
-    int *ring = s_ring + warp * 4;                         // row block of each buffer
-    auto issue_dn = [&](int rb, int b) {
-        const uint8_t *src = dslab + (size_t)rb * kDnRows * sh.drowbytes;
-        const uint32_t dst = wbuf + (uint32_t)(b * sh.dn_unit);
+    const bool dn_writer = (lane & 7) == 0;                // lane l ends with row l / 8
+    auto load_dn = [&](int rb, uint4 (&w)[kDnRows * CPLI], float &sc) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(dslab + (size_t)rb * kDnRows * sh.drowbytes) + lane;
 #pragma unroll
         for (int rr = 0; rr < kDnRows; rr++)
 #pragma unroll
             for (int k = 0; k < CPLI; k++)
-                if (fullI || lane + 32 * k < Cd)
-                    cp_async16(dst + (uint32_t)(rr * sh.drowbytes + 512 * k), src + (size_t)rr * sh.drowbytes + 512 * k);
-        // writer lane 4r copies the scale of row r into the unit's last 32 bytes
-        if (dn_writer)
-            cp_async4(dst - (uint32_t)(lane * 16) + (uint32_t)(kDnRows * sh.drowbytes + lane),
-                      sd + rb * kDnRows + (lane >> 2));
-        cp_async_commit();
-        ring[b] = rb;             // every lane stores the same value
+                if (fullI || lane + 32 * k < Cd) w[rr * CPLI + k] = ldg_stream(src + rr * (sh.drowbytes / 16) + 32 * k);
+        if (dn_writer) sc = __ldg(sd + rb * kDnRows + (lane >> 3));
     };
-    unsigned dc[kDnBufs] = {};
-    if (lane == 0)
-#pragma unroll
-        for (int i = 0; i < kDnBufs; i++) dc[i] = atomicAdd(dn_ctr, 1u);
-    int nd = 0;
-    const int rb0 = take(dc[0], (unsigned)sh.RB);
-    if (rb0 >= 0 && kDnPre > 0) {
-        issue_dn(rb0, 0);
-        nd = 1;
-    }
+    uint4 da[kDnRows * CPLI], db[kDnRows * CPLI];
+    float sca = 0.0f, scb = 0.0f;
+    if (wl < sh.RB) load_dn(wl, da, sca);
 
     // ---- barrier 2: every SwiGLU activation is written ------------------------------------
-    if (!grid_barrier(bar2, target, p.ws.err, s_flags + 1)) {
-        cp_async_wait_n(0);
-        return;
-    }
+    if (!grid_barrier(bar2, target, p.ws.err, s_flags + 1)) return;
 
     // ---- phase 2: the half-block loads slot j's h (thread t of the half: chunk t), takes
-    // max |h|, and writes the digits to shared memory; the loads go out before the rest of
-    // the warp's first down units so they do not queue behind them
+    // max |h|, and writes the digits to shared memory (x digits are no longer read)
     const int ht = tid & 127;
     const bool hchunk = ht < Cd;
     float hv[32];
@@ -692,24 +615,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             const float4 f = hchunk ? __ldcg(h4 + t) : make_float4(0.f, 0.f, 0.f, 0.f);
             hv[4 * t] = f.x; hv[4 * t + 1] = f.y; hv[4 * t + 2] = f.z; hv[4 * t + 3] = f.w;
         }
-    }
-    if (rb0 >= 0 && nd == 0) {
-        issue_dn(rb0, 0);
-        nd = 1;
-    }
-#pragma unroll
-    for (int i = 1; i < kDnBufs; i++) {
-        const int rbi = take(dc[i], (unsigned)sh.RB);
-        if (rb0 >= 0 && nd == i && rbi >= 0) {
-            issue_dn(rbi, i);
-            nd = i + 1;
-        }
-    }
-    unsigned c_dn = 0;
-    bool dn_pending = false;
-    if (nd == kDnBufs) {
-        if (lane == 0) c_dn = atomicAdd(dn_ctr, 1u);
-        dn_pending = true;
     }
     float hm = 0.0f;
     bool hnan = false;
@@ -732,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     const float hs = hmax / kQMax;                    // NaN propagates
     const float hinv = (hs > 0.0f && isfinite(hs)) ? 1.0f / hs : 0.0f;
     const float coef_j = s_w[j] * hs;
-    uint4 *hd = xdig + (size_t)hb * 7 * Cd;           // x digits are no longer read
+    uint4 *hd = xdig + (size_t)hb * 7 * Cd;
     if (hchunk) {
         uint4 dig[6];
         int ds[3];
@@ -757,13 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             for (int q = 0; q < 6; q++) hdig[k][q] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    __syncwarp();
-    for (int m = 0; m < nd; m++) {
-        cp_async_wait_n(nd - m - 1);
-        const int b = m % kDnBufs;
-        const int rb = ring[b];
-        const int o = rb * kDnRows + (lane >> 2);
-        const uint32_t st = wbuf + (uint32_t)(b * sh.dn_unit);
+    auto dn_compute = [&](int rb, const uint4 (&w2)[kDnRows * CPLI], float sc) {
         int lo[kDnRows][3], hi[kDnRows][3];
 #pragma unroll
         for (int rr = 0; rr < kDnRows; rr++) {
@@ -775,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             if (fullI || lane + 32 * k < Cd) {
                 uint4 w[kDnRows];
 #pragma unroll
-                for (int rr = 0; rr < kDnRows; rr++) w[rr] = lds128(st + (uint32_t)(rr * sh.drowbytes + 512 * k));
+                for (int rr = 0; rr < kDnRows; rr++) w[rr] = w2[rr * CPLI + k];
                 dot_rows<kDnRows>(w, hdig[k], lo, hi);
             }
         }
@@ -783,23 +682,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
 #pragma unroll
         for (int rr = 0; rr < kDnRows; rr++) v[rr] = planes_lh_to_float(lo[rr], hi[rr]);
         const float tot = reduce_scatter<kDnRows>(v, lane);
-        if (dn_writer) {          // the row scale this lane copied with the unit
-            const float coef = coef_j * lds32(st - (uint32_t)(lane * 16) + (uint32_t)(kDnRows * sh.drowbytes + lane));
-            p.ws.dpart[(size_t)j * H + o] = tot * coef;
-        }
-        __syncwarp();             // every lane has read ring[b] before it is rewritten
-        if (dn_pending) {         // the buffer just read takes the next claimed row block
-            dn_pending = false;
-            const int rn = take(c_dn, (unsigned)sh.RB);
-            if (rn >= 0) {
-                issue_dn(rn, b);
-                nd++;
-                if (lane == 0) c_dn = atomicAdd(dn_ctr, 1u);
-                dn_pending = true;
-            }
-        }
+        if (dn_writer) p.ws.dpart[(size_t)j * H + rb * kDnRows + (lane >> 3)] = tot * coef_j * sc;
+    };
+#pragma unroll 1
+    for (int rb = wl; rb < sh.RB; rb += nwj) {
+        const int rn = rb + nwj;
+        if (rn < sh.RB) load_dn(rn, db, scb);             // in flight during this unit
+        dn_compute(rb, da, sca);
+#pragma unroll
+        for (int k = 0; k < kDnRows * CPLI; k++) da[k] = db[k];
+        sca = scb;
     }
-    cp_async_wait_n(0);
 
     // ---- barrier 3, then phase 3: combine ---------------------------------------------------
     if (!grid_barrier(bar3, target, p.ws.err, s_flags + 1)) return;
@@ -809,8 +702,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         if (d.n_shared) acc += __ldcg(p.ws.dpart + (size_t)K * H + o);
         y[o] = d.prenorm ? x[o] + acc : acc;
     }
-    // every claim was taken before barrier 3: clear the counters for the next call
-    if (blockIdx.x == 0 && tid <= J) p.ws.claims[tid] = 0u;
 }
 
 int g_sms = 0;
@@ -858,7 +749,7 @@ cudaError_t attr_t() {
 }  // namespace
 
 bool decode_fast_supported(const Dims &d) {
-    if (d.H % kDnRows != 0 || d.H % 32 != 0 || d.I % 32 != 0 || d.I % kGuRows != 0) return false;
+    if (d.H % kDnRows != 0 || d.H % 32 != 0 || d.I % 32 != 0) return false;
     if (d.n_shared && d.I_sh != d.I) return false;
     if (d.K + d.n_shared > kMaxSlots || d.K + d.n_shared > 32 || d.E > 1024) return false;
     if ((d.H / 32 + 31) / 32 > kMaxCplH || (d.I / 32 + 31) / 32 > kMaxCplI) return false;
