@@ -278,6 +278,30 @@ def test_init_rejects_host_and_misaligned_weights(moe):
     assert e.value.status == moe.MOE_ERR_INVALID and "aligned" in str(e.value)
 
 
+def test_nan_input_decode_path(moe):
+    """T = 1 through the fused decode kernel: a NaN in x makes every output
+    NaN, and the selected indices stay valid (NaN scores rank last)."""
+    wl = synth.WORKLOADS["tiny"]
+    li = synth.layer_inputs(wl)
+    layer = upload(moe, wl, li, 1)
+    assert moe.moe_uses_streaming_decode(layer.handle)
+    for pos in (0, 5, wl.H - 1):
+        x = torch.from_numpy(synth.tokens(wl, T=1, stream=2)).cuda()
+        x[0, pos] = float("nan")
+        y, idx, w = layer.forward_debug(x)
+        torch.cuda.synchronize()
+        assert bool(((idx >= 0) & (idx < wl.E)).all())
+        assert len(set(idx[0].tolist())) == wl.K
+        assert torch.isnan(y[0]).all()
+    # the next finite call is unaffected
+    x = torch.from_numpy(synth.tokens(wl, T=1, stream=3)).cuda()
+    y, idx, w = layer.forward_debug(x)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y).all()
+    assert moe.moe_device_error(layer.handle) == 0
+    layer.close()
+
+
 def test_nan_input_gives_valid_indices(moe):
     wl = small_workload()
     li = synth.layer_inputs(wl)
