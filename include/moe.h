@@ -46,6 +46,9 @@ extern "C" {
 
 /* y = x + moe(rmsnorm(x)) instead of y = moe(x). */
 #define MOE_FLAG_PRENORM_RESIDUAL 1u
+/* Record the timeline of every T == 1 call on the single-kernel decode path
+ * (see moe_trace_read); results are identical with and without it. */
+#define MOE_FLAG_TRACE 2u
 
 typedef enum {
     MOE_OK = 0,
@@ -145,11 +148,30 @@ moe_status moe_profile_read(moe_handle *h, int32_t *n_calls, float *stage_ms);
 moe_status moe_device_error(moe_handle *h, uint32_t *flags);
 
 /* 1 if T == 1 calls on this handle run the single persistent decode kernel
- * (a cooperative launch; weights streamed through shared memory with
- * cp.async; fixed-point activations and dp4a), 0 if they use the generic
- * kernels (shapes outside its limits: H, I multiples of 32, I == I_shared,
+ * (a cooperative launch; weights streamed from HBM into registers;
+ * fixed-point activations and dp4a), 0 if they use the generic kernels
+ * (shapes outside its limits: H, I multiples of 32, I == I_shared,
  * I <= 2048, H <= 8192, E <= 1024, K + n_shared <= 32). */
 int32_t moe_uses_streaming_decode(const moe_handle *h);
+
+/*
+ * Timeline of the last T == 1 call on a handle created with MOE_FLAG_TRACE
+ * (decode kernel only; a diagnostic of this library, not a step of the
+ * method).  Waits for the device, then copies to out[b * MOE_TRACE_SLOTS + i]
+ * (host memory, capacity_blocks * MOE_TRACE_SLOTS uint64 values) the GPU
+ * global-timer readings, in nanoseconds, that block b of the decode launch
+ * took at:
+ *   0 its start            1 router scores and x digits written
+ *   2 routing known        3 past the SwiGLU barrier
+ *   4 its slots' h digits  5 past the down barrier      6 its end
+ *   8 + i  warp 0 finished its i-th gate/up unit (i < 32)
+ *   40 + i warp 0 finished its i-th down unit (i < 24)
+ * Unreached entries are 0.  *n_blocks = blocks of the launch (copied:
+ * min(*n_blocks, capacity_blocks)).  MOE_ERR_UNSUPPORTED if the handle was
+ * created without MOE_FLAG_TRACE or does not use the decode kernel.
+ */
+#define MOE_TRACE_SLOTS 64
+moe_status moe_trace_read(moe_handle *h, uint64_t *out, int32_t capacity_blocks, int32_t *n_blocks);
 
 /* Device workspace moe_init would allocate for this config (0 if invalid). */
 size_t moe_workspace_bytes(const moe_config *cfg, int32_t max_tokens);

@@ -14,7 +14,7 @@ import numpy as np
 
 __all__ = [
     "MOE_OK", "MOE_ERR_INVALID", "MOE_ERR_CUDA", "MOE_ERR_NOMEM", "MOE_ERR_UNSUPPORTED",
-    "MOE_FLAG_PRENORM_RESIDUAL", "MoeError", "MoeConfig", "MoeWeights", "MoeLayer",
+    "MOE_FLAG_PRENORM_RESIDUAL", "MOE_FLAG_TRACE", "MOE_TRACE_SLOTS", "moe_trace_read", "MoeError", "MoeConfig", "MoeWeights", "MoeLayer",
     "lib", "library_path", "moe_init", "moe_forward", "moe_forward_debug", "moe_forward_host",
     "moe_destroy", "moe_last_error", "moe_workspace_bytes", "moe_abi_version",
     "moe_profile_start", "moe_profile_read", "moe_route_noalloc", "moe_device_error",
@@ -23,6 +23,8 @@ __all__ = [
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_CUDA, MOE_ERR_NOMEM, MOE_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
 MOE_FLAG_PRENORM_RESIDUAL = 1
+MOE_FLAG_TRACE = 2
+MOE_TRACE_SLOTS = 64
 _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CUDA", 3: "MOE_ERR_NOMEM",
            4: "MOE_ERR_UNSUPPORTED"}
 
@@ -87,6 +89,8 @@ def lib():
         L.moe_uses_streaming_decode.restype = i32
         L.moe_route_noalloc.argtypes = [C.POINTER(MoeConfig), vp, vp, vp, i32, vp, vp, vp]
         L.moe_route_noalloc.restype = C.c_int
+        L.moe_trace_read.argtypes = [vp, vp, i32, C.POINTER(i32)]
+        L.moe_trace_read.restype = C.c_int
         _lib = L
     return _lib
 
@@ -194,10 +198,20 @@ def moe_destroy(handle: int) -> None:
 
 
 def make_config(H, E, K, I, n_shared=0, I_shared=0, routed_scale=1.0, norm_topk=1,
-                prenorm_residual=False, rms_eps=1e-5, n_group=1) -> MoeConfig:
+                prenorm_residual=False, rms_eps=1e-5, n_group=1, trace=False) -> MoeConfig:
+    flags = (MOE_FLAG_PRENORM_RESIDUAL if prenorm_residual else 0) | (MOE_FLAG_TRACE if trace else 0)
     return MoeConfig(H, E, K, I, n_shared, I_shared if n_shared else 0, n_group, norm_topk,
-                     float(routed_scale), float(rms_eps),
-                     MOE_FLAG_PRENORM_RESIDUAL if prenorm_residual else 0)
+                     float(routed_scale), float(rms_eps), flags)
+
+
+def moe_trace_read(handle: int, capacity_blocks: int = 1024):
+    """Timeline of the last decode call (handle made with trace=True): a uint64
+    numpy array [blocks, MOE_TRACE_SLOTS] of global-timer nanoseconds, 0 where
+    a point was not reached (slot meanings in include/moe.h)."""
+    out = np.zeros((capacity_blocks, MOE_TRACE_SLOTS), dtype=np.uint64)
+    n = C.c_int32(0)
+    _check(lib().moe_trace_read(handle, out.ctypes.data, capacity_blocks, C.byref(n)), "moe_trace_read")
+    return out[:min(n.value, capacity_blocks)]
 
 
 class MoeLayer:

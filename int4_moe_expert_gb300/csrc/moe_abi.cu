@@ -65,7 +65,8 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
     if (c->norm_topk != 0 && c->norm_topk != 1)
         return fail(MOE_ERR_INVALID, "norm_topk=%d: need 0 or 1", c->norm_topk);
     if (!isfinite(c->routed_scale)) return fail(MOE_ERR_INVALID, "routed_scale is not finite");
-    if (c->flags & ~MOE_FLAG_PRENORM_RESIDUAL) return fail(MOE_ERR_INVALID, "unknown flags 0x%x", c->flags);
+    if (c->flags & ~(MOE_FLAG_PRENORM_RESIDUAL | MOE_FLAG_TRACE))
+        return fail(MOE_ERR_INVALID, "unknown flags 0x%x", c->flags);
     if ((c->flags & MOE_FLAG_PRENORM_RESIDUAL) && !(c->rms_eps >= 0.0f && isfinite(c->rms_eps)))
         return fail(MOE_ERR_INVALID, "rms_eps must be finite and >= 0");
     if (max_tokens < 1 || max_tokens > kMaxTokens)
@@ -83,6 +84,7 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
     d->eps = c->rms_eps;
     d->max_tokens = max_tokens;
     d->fast_decode = moe::decode_fast_supported(*d) ? 1 : 0;
+    d->trace = (c->flags & MOE_FLAG_TRACE) ? 1 : 0;
     return MOE_OK;
 }
 
@@ -336,6 +338,20 @@ moe_status moe_device_error(moe_handle *h, uint32_t *flags) {
 }
 
 int32_t moe_uses_streaming_decode(const moe_handle *h) { return h ? h->p.d.fast_decode : 0; }
+
+moe_status moe_trace_read(moe_handle *h, uint64_t *out, int32_t capacity_blocks, int32_t *n_blocks) {
+    if (!h || !out || !n_blocks || capacity_blocks < 0) return fail(MOE_ERR_INVALID, "NULL argument or negative capacity");
+    if (!h->p.d.trace || !h->p.d.fast_decode)
+        return fail(MOE_ERR_UNSUPPORTED, "the handle records no trace (MOE_FLAG_TRACE and the decode kernel needed)");
+    const int g = moe::decode_grid_blocks();
+    const int n = g < capacity_blocks ? g : capacity_blocks;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess && n > 0)
+        e = cudaMemcpy(out, h->p.ws.trace, (size_t)n * MOE_TRACE_SLOTS * sizeof(uint64_t), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the trace");
+    *n_blocks = g;
+    return MOE_OK;
+}
 
 moe_status moe_destroy(moe_handle *h) {
     if (!h) return MOE_OK;

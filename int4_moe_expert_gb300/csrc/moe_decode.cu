@@ -288,6 +288,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     const unsigned kFull = 0xffffffffu;
     unsigned *bar1 = p.ws.counters + 4, *bar2 = p.ws.counters + 5, *bar3 = p.ws.counters + 6;
     const bool fullH = (C % 32) == 0, fullI = (Cd % 32) == 0;
+    // timeline (MOE_FLAG_TRACE): block b's record of MOE_TRACE_SLOTS global-timer readings
+    const bool trace = p.d.trace != 0 && blockIdx.x < kTraceBlocks;
+    unsigned long long *tr = p.ws.trace + (size_t)blockIdx.x * MOE_TRACE_SLOTS;
+    auto mark = [&](int slot) {
+        if (trace && tid == 0) tr[slot] = now_ns();
+    };
+    if (trace && tid < MOE_TRACE_SLOTS) tr[tid] = 0ull;
+    mark(0);
 
     // ---- gate/up units (the shared expert's first, then slot by slot): warp gw takes units
     // gw, gw + nw, gw + 2 nw, ...  A unit's rows go straight into registers (lane l: chunks
@@ -455,6 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     }
 
     // ---- barrier 1: every block's scores are written; then the block picks the top K -----
+    mark(1);
     __syncthreads();
     if (tid == 0) {
         __threadfence();
@@ -523,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     __syncthreads();
 
     // ---- phase 1: gate/up + SwiGLU ------------------------------------------------------
+    mark(2);
     int corr[3] = {0, 0, 0};
 #pragma unroll
     for (int k = 0; k < CPLH; k++) {
@@ -574,6 +584,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         for (int k = 0; k < 2 * CPLH; k++) wa[k] = wb[k];
         sga = sgb;
         sua = sub;
+        if (trace && warp == 0 && lane == 0) {
+            const int i = (u - gw) / nw;
+            if (i < 32) tr[8 + i] = now_ns();
+        }
     }
 
     // ---- down: half-block hb (warps 4 hb .. 4 hb + 3) serves slot j; warp wl of the slot's
@@ -602,6 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
 
     // ---- barrier 2: every SwiGLU activation is written ------------------------------------
     if (!grid_barrier(bar2, target, p.ws.err, s_flags + 1)) return;
+    mark(3);
 
     // ---- phase 2: the half-block loads slot j's h (thread t of the half: chunk t), takes
     // max |h|, and writes the digits to shared memory (x digits are no longer read)
@@ -647,6 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         hd[6 * Cd + ht] = make_uint4((unsigned)ds[0], (unsigned)ds[1], (unsigned)ds[2], 0u);
     }
     named_barrier(1 + hb, 128);
+    mark(4);
     uint4 hdig[CPLI][6];
     int dcorr[3] = {0, 0, 0};
 #pragma unroll
@@ -692,16 +708,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
 #pragma unroll
         for (int k = 0; k < kDnRows * CPLI; k++) da[k] = db[k];
         sca = scb;
+        if (trace && warp == 0 && lane == 0) {
+            const int i = (rb - wl) / nwj;
+            if (i < 24) tr[40 + i] = now_ns();
+        }
     }
 
     // ---- barrier 3, then phase 3: combine ---------------------------------------------------
     if (!grid_barrier(bar3, target, p.ws.err, s_flags + 1)) return;
+    mark(5);
     for (int o = blockIdx.x * kThreads + tid; o < H; o += G * kThreads) {
         float acc = 0.0f;
         for (int k = 0; k < K; k++) acc += __ldcg(p.ws.dpart + (size_t)k * H + o);
         if (d.n_shared) acc += __ldcg(p.ws.dpart + (size_t)K * H + o);
         y[o] = d.prenorm ? x[o] + acc : acc;
     }
+    mark(6);
 }
 
 int g_sms = 0;
@@ -747,6 +769,8 @@ cudaError_t attr_t() {
 }
 
 }  // namespace
+
+int decode_grid_blocks() { return g_blocks; }
 
 bool decode_fast_supported(const Dims &d) {
     if (d.H % kDnRows != 0 || d.H % 32 != 0 || d.I % 32 != 0) return false;

@@ -19,6 +19,7 @@ struct Dims {
     float eps;          // rms_eps
     int max_tokens;
     int fast_decode;    // T == 1 runs the streaming kernels (moe_decode.cu)
+    int trace;          // MOE_FLAG_TRACE: the decode kernel records its timeline
 };
 
 // Device workspace owned by a handle.  Vectors marked "perm" are stored in
@@ -44,11 +45,13 @@ struct Workspace {
     unsigned *err;       // [4] device error word: bounded waits that ran out
     float *dpart;        // [kMaxSlots, H] down outputs per slot (times the routing weight)
     float *dscore;       // [2, E] decode router: sigmoid | selection score (sigmoid + bias)
+    unsigned long long *trace;   // [kTraceBlocks, MOE_TRACE_SLOTS] decode timeline (MOE_FLAG_TRACE)
     size_t total_bytes;  // size of the carved region
 };
 
 constexpr int kMaxSlots = 33;   // K <= 32 routed + 1 shared
 constexpr int kClaimWords = 64;  // >= 1 + kMaxSlots
+constexpr int kTraceBlocks = 1024;   // decode blocks the trace buffer holds
 
 // Everything a kernel needs, passed by value.
 struct Params {
@@ -76,6 +79,7 @@ constexpr int kStages = 4;   // router, gate/up, down, combine
 // call; p.gen numbers the calls from 1.
 bool decode_fast_supported(const Dims &d);
 cudaError_t prepare_decode_fast(const Dims &d);
+int decode_grid_blocks();   // blocks of the decode launch (0 before prepare)
 cudaError_t launch_decode_fast(const Params &p, const float *x, float *y, cudaStream_t st, cudaEvent_t *ev,
                                bool want_counts);
 

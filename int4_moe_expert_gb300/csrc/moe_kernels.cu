@@ -830,6 +830,8 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
     ws->err = reinterpret_cast<unsigned *>(take(4 * sizeof(unsigned)));
     ws->dpart = reinterpret_cast<float *>(take((size_t)kMaxSlots * d.H * sizeof(float)));
     ws->dscore = reinterpret_cast<float *>(take(2 * (size_t)d.E * sizeof(float)));
+    ws->trace = reinterpret_cast<unsigned long long *>(
+        take(d.trace ? (size_t)kTraceBlocks * MOE_TRACE_SLOTS * sizeof(unsigned long long) : 0));
     ws->dbuf = reinterpret_cast<float *>(take((P + T) * d.H * sizeof(float)));
     ws->total_bytes = o;
 }

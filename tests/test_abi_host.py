@@ -58,8 +58,14 @@ def test_workspace_bytes_validates_config(moe):
         moe.make_config(6144, 2048, 8, 2048, 1, 2048),       # E > 1024
         moe.make_config(6144, 256, 8, 2048, 1, 2048, routed_scale=float("inf")),
     ]
+    unknown_flag = moe.make_config(6144, 256, 8, 2048, 1, 2048)
+    unknown_flag.flags = 4
+    bad.append(unknown_flag)
     for cfg in bad:
         assert moe.moe_workspace_bytes(cfg, 1) == 0
+    # the trace flag is accepted and adds the trace buffer (1024 blocks x 64 x 8 B)
+    traced = moe.make_config(6144, 256, 8, 2048, 1, 2048, 2.5, trace=True)
+    assert moe.moe_workspace_bytes(traced, 1) >= moe.moe_workspace_bytes(good, 1) + 1024 * 64 * 8
     assert moe.moe_workspace_bytes(good, 0) == 0
     assert moe.moe_workspace_bytes(good, 1 << 20) == 0
 

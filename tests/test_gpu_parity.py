@@ -278,6 +278,45 @@ def test_init_rejects_host_and_misaligned_weights(moe):
     assert e.value.status == moe.MOE_ERR_INVALID and "aligned" in str(e.value)
 
 
+def test_trace_decode_path(moe):
+    """MOE_FLAG_TRACE records the decode kernel's timeline without changing
+    its results: outputs are bit-identical to an untraced handle, every block's
+    phase marks are ordered, and each warp-0 unit time lies inside its phase."""
+    wl = synth.WORKLOADS["tiny"]
+    li = synth.layer_inputs(wl)
+    cfg_kw = dict(H=wl.H, E=wl.E, K=wl.K, I=wl.I, n_shared=wl.n_shared, I_shared=wl.I_shared,
+                  routed_scale=wl.routed_scale)
+    plain = moe.MoeLayer(moe.make_config(**cfg_kw), li.router_w, li.router_b, li.slabs, li.scales,
+                         li.sh_slab, li.sh_scale, max_tokens=1)
+    traced = moe.MoeLayer(moe.make_config(**cfg_kw, trace=True), li.router_w, li.router_b, li.slabs,
+                          li.scales, li.sh_slab, li.sh_scale, max_tokens=1)
+    assert moe.moe_uses_streaming_decode(traced.handle)
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_trace_read(plain.handle)
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+    for s in range(3):
+        x = torch.from_numpy(synth.tokens(wl, T=1, stream=10 + s)).cuda()
+        y0 = plain.forward(x)
+        y1 = traced.forward(x)
+        torch.cuda.synchronize()
+        assert torch.equal(y0, y1)
+        tr = moe.moe_trace_read(traced.handle).astype(np.int64)
+        assert tr.shape[1] == moe.MOE_TRACE_SLOTS and tr.shape[0] > 0
+        ph = tr[:, [0, 1, 2, 3, 4, 5, 6]]
+        assert (ph > 0).all(), "a block missed a phase mark"
+        assert (np.diff(ph, axis=1) >= 0).all(), "phase marks out of order"
+        for b in range(tr.shape[0]):
+            gu = tr[b, 8:40][tr[b, 8:40] > 0]
+            dn = tr[b, 40:64][tr[b, 40:64] > 0]
+            assert (np.diff(gu) >= 0).all() and (np.diff(dn) >= 0).all()
+            assert ((gu >= tr[b, 0]) & (gu <= tr[b, 3])).all()
+            assert ((dn >= tr[b, 4]) & (dn <= tr[b, 5])).all()
+        assert (tr[:, 8] > 0).any() and (tr[:, 40] > 0).any()
+    assert moe.moe_device_error(traced.handle) == 0
+    plain.close()
+    traced.close()
+
+
 def test_nan_input_decode_path(moe):
     """T = 1 through the fused decode kernel: a NaN in x makes every output
     NaN, and the selected indices stay valid (NaN scores rank last)."""
