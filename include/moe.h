@@ -164,6 +164,7 @@ int32_t moe_uses_streaming_decode(const moe_handle *h);
  *   0 its start            1 router scores and x digits written
  *   2 routing known        3 past the SwiGLU barrier
  *   4 its slots' h digits  5 past the down barrier      6 its end
+ *   7 past the router-score barrier
  *   8 + i  warp 0 finished its i-th gate/up unit (i < 32)
  *   40 + i warp 0 finished its i-th down unit (i < 24)
  * Unreached entries are 0.  *n_blocks = blocks of the launch (copied:

@@ -296,12 +296,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     };
     if (trace && tid < MOE_TRACE_SLOTS) tr[tid] = 0ull;
     mark(0);
+    if (tid == 0) s_flags[2] = 0;     // routing not known yet (read after the first __syncthreads)
 
-    // ---- gate/up units (the shared expert's first, then slot by slot): warp gw takes units
-    // gw, gw + nw, gw + 2 nw, ...  A unit's rows go straight into registers (lane l: chunks
-    // l + 32 k of the gate row, then of the up row); the next unit's loads are in flight
-    // while the current one is computed.
+    // ---- gate/up units: unit u < U_sh is row u of the shared expert, unit U_sh + v is row
+    // v mod I of slot v / I.  The shared expert's units go to warps 1..7 (their share
+    // sw = 7 block + warp - 1, sw + nsw, ... with nsw = 7 G), since warp 0 spends that time
+    // routing; then every warp takes routed units U_sh + gw, U_sh + gw + nw, ...  A unit's
+    // rows go straight into registers (lane l: chunks l + 32 k of the gate row, then of
+    // the up row); the next unit's loads are in flight while the current one is computed.
     const int U_total = sh.gu_units;
+    const int nsw = 7 * G, sw = 7 * blockIdx.x + warp - 1;
+    const int u_first = (warp > 0 && sw < sh.U_sh) ? sw : sh.U_sh + gw;
+    auto next_unit = [&](int u) -> int {
+        if (u < sh.U_sh) {
+            const int n = u + nsw;
+            return n < sh.U_sh ? n : sh.U_sh + gw;
+        }
+        return u + nw;
+    };
     auto load_gu = [&](int u, uint4 (&w)[2 * CPLH], float &sg, float &su) {
         int slot, o, Ij;
         const uint8_t *slab;
@@ -360,8 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         }
     }
     // the first unit's loads go out now if it is the shared expert's (routing not needed)
-    if (gw < sh.U_sh) {
-        load_gu(gw, wa, sga, sua);
+    if (u_first < sh.U_sh) {
+        load_gu(u_first, wa, sga, sua);
         loaded = true;
     }
     if (tid < C) {
@@ -462,22 +474,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         xdsum[tid] = make_int4(ds[0], ds[1], ds[2], 0);
     }
 
-    // ---- barrier 1: every block's scores are written; then the block picks the top K -----
+    // ---- barrier 1 and routing: warp 0 waits for every block's scores and picks the top K
+    // while warps 1..7 compute the shared expert's units (those need no routing);
+    // s_flags[2] then tells the block: 1 routing known (slot tables written), 2 failed
     mark(1);
-    __syncthreads();
-    if (tid == 0) {
-        __threadfence();
-        atomicAdd(bar1, 1u);
-        const bool ok = spin_until(bar1, target);
-        if (!ok) atomicOr(p.ws.err, kErrGrid);
-        s_flags[0] = ok ? 1 : 0;
-        s_flags[1] = 0;
-    }
-    __syncthreads();
-    if (!s_flags[0]) return;
-    // top K by (score desc, index asc), one warp: K rounds of a warp-wide max
-    // over each lane's best remaining expert (lane l holds experts l + 32 i)
+    __syncthreads();              // this block's scores and x digits are written
     if (warp == 0) {
+        bool ok = true;
+        if (lane == 0) {
+            __threadfence();
+            atomicAdd(bar1, 1u);
+            ok = spin_until(bar1, target);
+            if (!ok) atomicOr(p.ws.err, kErrGrid);
+        }
+        ok = __shfl_sync(kFull, ok ? 1 : 0, 0) != 0;
+        if (!ok) {
+            if (lane == 0) s_flags[2] = 2;
+            return;
+        }
+        if (trace && lane == 0) tr[7] = now_ns();
+        // top K by (score desc, index asc): K rounds of a warp-wide max over each
+        // lane's best remaining expert (lane l holds experts l + 32 i)
         unsigned best = 0u;
         int bidx = 0x7fffffff;
         for (int e = lane; e < E; e += 32) {
@@ -486,8 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             if (k > best) { best = k; bidx = e; }
         }
         for (int r = 0; r < K; r++) {
-            const unsigned mx = __reduce_max_sync(0xffffffffu, best);
-            const unsigned win = __reduce_min_sync(0xffffffffu, best == mx ? (unsigned)bidx : 0xffffffffu);
+            const unsigned mx = __reduce_max_sync(kFull, best);
+            const unsigned win = __reduce_min_sync(kFull, best == mx ? (unsigned)bidx : 0xffffffffu);
             if (lane == 0) s_sel[r] = (int)win;
             if (lane == (int)(win & 31u)) {          // the winner's lane removes it and rescans
                 s_key[win] = 0u;
@@ -500,13 +517,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             }
         }
         __syncwarp();
-    }
-    if (warp == 0) {
         const int me = lane < K ? s_sel[lane] : 0;   // written by lane 0 of this warp
         const float sg = lane < K ? __ldcg(p.ws.dscore + me) : 0.0f;
         float sum = sg;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
         const float mw = d.norm_topk ? d.scale * sg / (sum + 1e-20f) : d.scale * sg;
         if (lane < K) {
             s_slab[lane] = p.slabs[me];
@@ -517,6 +532,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             s_scale[lane] = p.sh_scale;
             s_w[lane] = 1.0f;
         }
+        __syncwarp();
+        if (lane == 0) {          // release the slot tables to the block
+            __threadfence_block();
+            s_flags[2] = 1;
+        }
+        mark(2);
         if (blockIdx.x == 0) {
             if (want_counts) {
                 for (int e = lane; e < E; e += 32) p.ws.cnt[e] = 0;
@@ -529,7 +550,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             }
         }
     }
-    __syncthreads();
+    // warps 1..7: wait (bounded) for the slot tables before the first routed unit
+    bool routed = warp == 0;
+    auto wait_routing = [&]() -> bool {
+        if (routed) return true;
+        int v = 1;
+        if (lane == 0) {
+            const unsigned long long t0 = now_ns();
+            while ((v = s_flags[2]) == 0) {
+                __nanosleep(64);
+                if (now_ns() - t0 > kWaitNs) break;
+            }
+            if (v == 0) atomicOr(p.ws.err, kErrGrid);
+        }
+        v = __shfl_sync(kFull, v, 0);
+        __threadfence_block();
+        routed = v == 1;
+        return routed;
+    };
 
     // ---- phase 1: gate/up + SwiGLU ------------------------------------------------------
     mark(2);
@@ -574,18 +612,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     };
     // the next unit's loads are in flight while this one is computed; the loop is kept
     // rolled (its body is large: unrolling it only grows the instruction footprint)
-    if (!loaded && gw < U_total) load_gu(gw, wa, sga, sua);
+    if (!loaded && u_first < U_total) {
+        if (!wait_routing()) return;
+        load_gu(u_first, wa, sga, sua);
+    }
 #pragma unroll 1
-    for (int u = gw; u < U_total; u += nw) {
-        const int un = u + nw;
-        if (un < U_total) load_gu(un, wb, sgb, sub);
+    for (int u = u_first, un; u < U_total; u = un) {
+        un = next_unit(u);
+        if (un < U_total) {
+            if (un >= sh.U_sh && !wait_routing()) return;
+            load_gu(un, wb, sgb, sub);
+        }
         gu_compute(u, wa, sga, sua);
 #pragma unroll
         for (int k = 0; k < 2 * CPLH; k++) wa[k] = wb[k];
         sga = sgb;
         sua = sub;
-        if (trace && warp == 0 && lane == 0) {
-            const int i = (u - gw) / nw;
+        if (trace && warp == 0 && lane == 0) {    // warp 0 has routed units only
+            const int i = (u - sh.U_sh - gw) / nw;
             if (i < 32) tr[8 + i] = now_ns();
         }
     }
@@ -593,6 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     // ---- down: half-block hb (warps 4 hb .. 4 hb + 3) serves slot j; warp wl of the slot's
     // nwj warps takes row blocks wl, wl + nwj, ...  The first unit's loads go out before
     // barrier 2 (weights do not depend on h).
+    if (!wait_routing()) return;     // the slot tables (on failure every warp returns here)
     const int hb = warp >> 2;
     const int hbg = 2 * blockIdx.x + hb;
     const int j = hbg % J;
