@@ -304,30 +304,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     // routing; then every warp takes routed units U_sh + gw, U_sh + gw + nw, ...  A unit's
     // rows go straight into registers (lane l: chunks l + 32 k of the gate row, then of
     // the up row); the next unit's loads are in flight while the current one is computed.
-    const int U_total = sh.gu_units;
+    // A unit is held as (pos, o): pos -1 the shared expert, 0..K-1 a routed slot; o its row.
+    // Units are stepped incrementally (no division per unit).
+    struct Unit { int pos, o; };
     const int nsw = 7 * G, sw = 7 * blockIdx.x + warp - 1;
-    const int u_first = (warp > 0 && sw < sh.U_sh) ? sw : sh.U_sh + gw;
-    auto next_unit = [&](int u) -> int {
-        if (u < sh.U_sh) {
-            const int n = u + nsw;
-            return n < sh.U_sh ? n : sh.U_sh + gw;
+    const Unit r_first = {gw / d.I, gw % d.I};       // routed unit U_sh + gw
+    const Unit u_first = (warp > 0 && sw < sh.U_sh) ? Unit{-1, sw} : r_first;
+    auto next_unit = [&](Unit u) -> Unit {
+        if (u.pos < 0) {
+            const int n = u.o + nsw;
+            return n < sh.U_sh ? Unit{-1, n} : r_first;
         }
-        return u + nw;
+        int pos = u.pos, o = u.o + nw;
+        while (o >= d.I) { o -= d.I; pos++; }
+        return Unit{pos, o};
     };
-    auto load_gu = [&](int u, uint4 (&w)[2 * CPLH], float &sg, float &su) {
-        int slot, o, Ij;
-        const uint8_t *slab;
-        const float *scale;
-        if (u < sh.U_sh) {
-            slot = K; o = u; Ij = d.I_sh; slab = p.sh_slab; scale = p.sh_scale;
-        } else {
-            const int v = u - sh.U_sh;
-            slot = v / sh.U_r;
-            o = v - slot * sh.U_r;
-            Ij = d.I;
-            slab = s_slab[slot];
-            scale = s_scale[slot];
-        }
+    auto load_gu = [&](Unit u, uint4 (&w)[2 * CPLH], float &sg, float &su) {
+        const int o = u.o;
+        const int Ij = u.pos < 0 ? d.I_sh : d.I;
+        const uint8_t *slab = u.pos < 0 ? p.sh_slab : s_slab[u.pos];
+        const float *scale = u.pos < 0 ? p.sh_scale : s_scale[u.pos];
         const uint4 *g = reinterpret_cast<const uint4 *>(slab + (size_t)o * sh.rowbytes) + lane;
         const uint4 *up = reinterpret_cast<const uint4 *>(slab + (size_t)(Ij + o) * sh.rowbytes) + lane;
 #pragma unroll
@@ -372,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         }
     }
     // the first unit's loads go out now if it is the shared expert's (routing not needed)
-    if (u_first < sh.U_sh) {
+    if (u_first.pos < 0) {
         load_gu(u_first, wa, sga, sua);
         loaded = true;
     }
@@ -580,15 +576,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         }
     }
     const uint32_t xdig_a = smem_u32(xdig) + (uint32_t)(lane * 16);
-    auto gu_compute = [&](int u, const uint4 (&w2)[2 * CPLH], float sg, float su) {
-        int slot, o;
-        if (u < sh.U_sh) {
-            slot = K; o = u;
-        } else {
-            const int v = u - sh.U_sh;
-            slot = v / sh.U_r;
-            o = v - slot * sh.U_r;
-        }
+    auto gu_compute = [&](Unit u, const uint4 (&w2)[2 * CPLH], float sg, float su) {
+        const int slot = u.pos < 0 ? K : u.pos, o = u.o;
         int lo[2][3], hi[2][3];
 #pragma unroll
         for (int rr = 0; rr < 2; rr++) {
@@ -612,15 +601,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     };
     // the next unit's loads are in flight while this one is computed; the loop is kept
     // rolled (its body is large: unrolling it only grows the instruction footprint)
-    if (!loaded && u_first < U_total) {
+    if (!loaded && u_first.pos < K) {
         if (!wait_routing()) return;
         load_gu(u_first, wa, sga, sua);
     }
 #pragma unroll 1
-    for (int u = u_first, un; u < U_total; u = un) {
+    for (Unit u = u_first, un; u.pos < K; u = un) {
         un = next_unit(u);
-        if (un < U_total) {
-            if (un >= sh.U_sh && !wait_routing()) return;
+        if (un.pos < K) {
+            if (un.pos >= 0 && !wait_routing()) return;
             load_gu(un, wb, sgb, sub);
         }
         gu_compute(u, wa, sga, sua);
@@ -629,7 +618,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         sga = sgb;
         sua = sub;
         if (trace && warp == 0 && lane == 0) {    // warp 0 has routed units only
-            const int i = (u - sh.U_sh - gw) / nw;
+            const int i = (u.pos * d.I + u.o - gw) / nw;
             if (i < 32) tr[8 + i] = now_ns();
         }
     }
