@@ -336,7 +336,7 @@ def run_ours(args, rank, world, local_rank, dist_on):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "int4 x fx24 -> s32 (exact dp4a sums), f32 router/scales/SwiGLU/combine",
+            "dtype": "int4 x fx16 -> s32 (exact dp4a sums), f32 router/scales/SwiGLU/combine",
             "data": "synthetic (seeded SplitMix64; shapes and distributions of the workload)",
             "config": {
                 "workload": workload_desc(wl),

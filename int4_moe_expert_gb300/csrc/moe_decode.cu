@@ -24,19 +24,20 @@
 // h = silu(g) u, d = s_d (Q_d h), y = sum_k w_k d_k + d_shared.
 //
 // Arithmetic.  An activation vector v (x, or one expert's h) is held as
-// 24-bit fixed point with one scale per vector: X_i = rint(v_i / s),
-// s = max|v| / 8355711, |X_i| <= 8355711 = 0x7F7F7F, written as three signed
-// base-256 digits X = d2 65536 + d1 256 + d0, each in [-128, 127].  A packed
-// int4 weight byte holds two unsigned nibbles n = q + 8 (section 06 format),
-// so one row's dot product is
+// 16-bit fixed point with one scale per vector: X_i = rint(v_i / s),
+// s = max|v| / 32639, |X_i| <= 32639 = 0x7F7F, written as two signed base-256
+// digits X = d1 256 + d0, each in [-128, 127] (kPlanes; three planes give
+// 24-bit fixed point).  A packed int4 weight byte holds two unsigned nibbles
+// n = q + 8 (section 06 format), so one row's dot product is
 //     sum_i q_i v_i = s * sum_p 256^p (sum_i n_i d_{p,i} - 8 sum_i d_{p,i}),
 // with every inner sum exact in int32 (dp4a: four unsigned nibble bytes times
 // four signed digit bytes).  Only the final plane combination and the scale
 // are floating point.  The representation error of v is at most
-// max|v| * 2^-24 per element, the same order as one float32 rounding.
+// max|v| * 2^-16 per element (measured against the double oracle: 1.1e-4
+// worst relative error on the GLM layer, 5e-4 after 40 chained layers).
 //
 // Digits in shared memory: for chunk c (elements 32c..32c+31, one 16-byte
-// weight load) and q = 2p + lh, the uint4 at [q * C + c] holds, in word m,
+// weight load) and q = 2p + lh (q < kQ), the uint4 at [q * C + c] holds, in word m,
 // the plane-p digits of elements 8m+{0,2,4,6} (lh = 0: the low nibbles of
 // word m) or 8m+{1,3,5,7} (lh = 1: the high nibbles), one per byte.
 //
@@ -62,7 +63,11 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kDnRows = 4;          // output rows per down unit
 constexpr int kSmemBudget = 64 * 1024;
 constexpr unsigned long long kWaitNs = 500ull * 1000 * 1000;   // every wait gives up after 0.5 s
-constexpr float kQMax = 8355711.0f;         // 0x7F7F7F
+constexpr int kPlanes = 2;                  // activation digits (bytes of fixed point) per value
+constexpr int kQ = 2 * kPlanes;             // digit words (uint4) per 32-value chunk
+constexpr int kQMaxInt = kPlanes == 2 ? 0x7F7F : 0x7F7F7F;   // largest |X| with balanced digits
+constexpr unsigned kBias = kPlanes == 2 ? 0x8080u : 0x808080u;
+constexpr float kQMax = (float)kQMaxInt;
 constexpr int kSwWords = (kMaxSlots + 3) / 4 * 4;   // s_w padded to 16 bytes
 static_assert(kMaxSlots * 16 % 16 == 0 && kSwWords >= kMaxSlots, "shared-memory carving");
 
@@ -85,30 +90,32 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int m) {
     return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
 }
 
-__device__ __forceinline__ float planes_lh_to_float(const int (&lo)[3], const int (&hi)[3]) {
-    const int a0 = lo[0] + (hi[0] >> 4), a1 = lo[1] + (hi[1] >> 4), a2 = lo[2] + (hi[2] >> 4);
-    return fmaf(__int2float_rn(a2), 65536.0f, fmaf(__int2float_rn(a1), 256.0f, __int2float_rn(a0)));
+__device__ __forceinline__ float planes_lh_to_float(const int (&lo)[kPlanes], const int (&hi)[kPlanes]) {
+    float r = 0.0f;
+#pragma unroll
+    for (int p = kPlanes - 1; p >= 0; p--) r = fmaf(r, 256.0f, __int2float_rn(lo[p] + (hi[p] >> 4)));
+    return r;
 }
 
 // Digits of the 32 values of one chunk (natural order) scaled by inv = 1/s;
-// dsum[p] = sum of the plane-p digits.  With U = X + 0x808080 (>= 0), byte p
-// of U minus 128 is the balanced digit d_p, i.e. byte p of U xor 0x80 read
-// as a signed byte; bytes are gathered into words with byte permutes.
-__device__ __forceinline__ void quant_chunk(const float (&v)[32], float inv, uint4 (&dig)[6], int (&dsum)[3]) {
+// dsum[p] = sum of the plane-p digits.  With U = X + kBias (>= 0), byte p of U
+// minus 128 is the balanced digit d_p, i.e. byte p of U xor 0x80 read as a
+// signed byte; bytes are gathered into words with byte permutes.
+__device__ __forceinline__ void quant_chunk(const float (&v)[32], float inv, uint4 (&dig)[kQ], int (&dsum)[kPlanes]) {
     uint32_t U[32];
 #pragma unroll
     for (int i = 0; i < 32; i++) {
-        const int X = min(max(__float2int_rn(v[i] * inv), -8355711), 8355711);
-        U[i] = (uint32_t)(X + 0x808080);
+        const int X = min(max(__float2int_rn(v[i] * inv), -kQMaxInt), kQMaxInt);
+        U[i] = (uint32_t)(X + (int)kBias);
     }
-    uint32_t w[6][4];
+    uint32_t w[kQ][4];
 #pragma unroll
     for (int m = 0; m < 4; m++) {
 #pragma unroll
         for (int lh = 0; lh < 2; lh++) {
             const int e0 = 8 * m + lh;       // elements e0, e0 + 2, e0 + 4, e0 + 6
 #pragma unroll
-            for (int p = 0; p < 3; p++) {
+            for (int p = 0; p < kPlanes; p++) {
                 const uint32_t sel = (uint32_t)p | ((uint32_t)(4 + p) << 4);
                 const uint32_t a = __byte_perm(U[e0], U[e0 + 2], sel);
                 const uint32_t b = __byte_perm(U[e0 + 4], U[e0 + 6], sel);
@@ -117,9 +124,9 @@ __device__ __forceinline__ void quant_chunk(const float (&v)[32], float inv, uin
         }
     }
 #pragma unroll
-    for (int q = 0; q < 6; q++) dig[q] = make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]);
+    for (int q = 0; q < kQ; q++) dig[q] = make_uint4(w[q][0], w[q][1], w[q][2], w[q][3]);
 #pragma unroll
-    for (int p = 0; p < 3; p++) {
+    for (int p = 0; p < kPlanes; p++) {
         int t = 0;
 #pragma unroll
         for (int m = 0; m < 4; m++) {
@@ -133,8 +140,8 @@ __device__ __forceinline__ void quant_chunk(const float (&v)[32], float inv, uin
 // lo[rr][p] += low-nibble sums, hi[rr][p] += 16 x high-nibble sums for NR
 // rows of one chunk, issued so that consecutive dp4a go to different rows.
 template <int NR>
-__device__ __forceinline__ void dot_rows(const uint4 (&w)[NR], const uint4 (&dig)[6], int (&lo)[NR][3],
-                                         int (&hi)[NR][3]) {
+__device__ __forceinline__ void dot_rows(const uint4 (&w)[NR], const uint4 (&dig)[kQ], int (&lo)[NR][kPlanes],
+                                         int (&hi)[NR][kPlanes]) {
 #pragma unroll
     for (int m = 0; m < 4; m++) {
         uint32_t l[NR], h[NR];
@@ -145,7 +152,7 @@ __device__ __forceinline__ void dot_rows(const uint4 (&w)[NR], const uint4 (&dig
             h[rr] = word & 0xF0F0F0F0u;
         }
 #pragma unroll
-        for (int p = 0; p < 3; p++) {
+        for (int p = 0; p < kPlanes; p++) {
             const uint32_t dl = word_of(dig[2 * p], m), dh = word_of(dig[2 * p + 1], m);
 #pragma unroll
             for (int rr = 0; rr < NR; rr++) dp4a_us(lo[rr][p], l[rr], dl);
@@ -251,7 +258,7 @@ __host__ __device__ inline FusedShape fused_shape(const Dims &d) {
     s.drowbytes = d.I / 2;
     s.J = d.K + d.n_shared;
     s.RB = d.H / kDnRows;
-    s.dig_bytes = 7 * 16 * (s.C > 2 * s.Cd ? s.C : 2 * s.Cd);
+    s.dig_bytes = (kQ + 1) * 16 * (s.C > 2 * s.Cd ? s.C : 2 * s.Cd);
     // digits | red[64] | slab[33] | scale[33] | w[36] | flags[4] | score keys[E] | sel[32]
     s.smem = (size_t)s.dig_bytes + 64 * 4 + kMaxSlots * 16 + kSwWords * 4 + 16 + (size_t)(d.E + 3) / 4 * 16 + 32 * 4;
     return s;
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
                                                                    unsigned gen, int want_counts) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint4 *xdig = reinterpret_cast<uint4 *>(smem);
-    int4 *xdsum = reinterpret_cast<int4 *>(xdig + 6 * sh.C);
+    int4 *xdsum = reinterpret_cast<int4 *>(xdig + kQ * sh.C);
     float *red = reinterpret_cast<float *>(smem + sh.dig_bytes);
     const uint8_t **s_slab = reinterpret_cast<const uint8_t **>(red + 64);
     const float **s_scale = reinterpret_cast<const float **>(s_slab + kMaxSlots);
@@ -462,12 +469,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         float v[32];
 #pragma unroll
         for (int i = 0; i < 32; i++) v[i] = xv[i] * r;
-        uint4 dig[6];
-        int ds[3];
+        uint4 dig[kQ];
+        int ds[kPlanes];
         quant_chunk(v, inv, dig, ds);
 #pragma unroll
-        for (int q = 0; q < 6; q++) xdig[q * C + tid] = dig[q];
-        xdsum[tid] = make_int4(ds[0], ds[1], ds[2], 0);
+        for (int q = 0; q < kQ; q++) xdig[q * C + tid] = dig[q];
+        xdsum[tid] = make_int4(ds[0], ds[1], kPlanes > 2 ? ds[kPlanes - 1] : 0, 0);
     }
 
     // ---- barrier 1 and routing: warp 0 waits for every block's scores and picks the top K
@@ -567,29 +574,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
 
     // ---- phase 1: gate/up + SwiGLU ------------------------------------------------------
     mark(2);
-    int corr[3] = {0, 0, 0};
+    int corr[kPlanes] = {};
 #pragma unroll
     for (int k = 0; k < CPLH; k++) {
         if (fullH || lane + 32 * k < C) {
             const int4 t = xdsum[lane + 32 * k];
-            corr[0] -= 8 * t.x; corr[1] -= 8 * t.y; corr[2] -= 8 * t.z;
+            const int tv[3] = {t.x, t.y, t.z};
+#pragma unroll
+            for (int q = 0; q < kPlanes; q++) corr[q] -= 8 * tv[q];
         }
     }
     const uint32_t xdig_a = smem_u32(xdig) + (uint32_t)(lane * 16);
     auto gu_compute = [&](Unit u, const uint4 (&w2)[2 * CPLH], float sg, float su) {
         const int slot = u.pos < 0 ? K : u.pos, o = u.o;
-        int lo[2][3], hi[2][3];
+        int lo[2][kPlanes], hi[2][kPlanes];
 #pragma unroll
-        for (int rr = 0; rr < 2; rr++) {
-            lo[rr][0] = corr[0]; lo[rr][1] = corr[1]; lo[rr][2] = corr[2];
-            hi[rr][0] = 0; hi[rr][1] = 0; hi[rr][2] = 0;
-        }
+        for (int rr = 0; rr < 2; rr++)
+#pragma unroll
+            for (int q = 0; q < kPlanes; q++) { lo[rr][q] = corr[q]; hi[rr][q] = 0; }
 #pragma unroll
         for (int k = 0; k < CPLH; k++) {
             if (fullH || lane + 32 * k < C) {
-                uint4 dig[6];
+                uint4 dig[kQ];
 #pragma unroll
-                for (int q = 0; q < 6; q++) dig[q] = lds128(xdig_a + (uint32_t)(q * C * 16 + 512 * k));
+                for (int q = 0; q < kQ; q++) dig[q] = lds128(xdig_a + (uint32_t)(q * C * 16 + 512 * k));
                 const uint4 w[2] = {w2[k], w2[CPLH + k]};
                 dot_rows<2>(w, dig, lo, hi);
             }
@@ -686,39 +694,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     const float hs = hmax / kQMax;                    // NaN propagates
     const float hinv = (hs > 0.0f && isfinite(hs)) ? 1.0f / hs : 0.0f;
     const float coef_j = s_w[j] * hs;
-    uint4 *hd = xdig + (size_t)hb * 7 * Cd;
+    uint4 *hd = xdig + (size_t)hb * (kQ + 1) * Cd;
     if (hchunk) {
-        uint4 dig[6];
-        int ds[3];
+        uint4 dig[kQ];
+        int ds[kPlanes];
         quant_chunk(hv, hinv, dig, ds);
 #pragma unroll
-        for (int q = 0; q < 6; q++) hd[q * Cd + ht] = dig[q];
-        hd[6 * Cd + ht] = make_uint4((unsigned)ds[0], (unsigned)ds[1], (unsigned)ds[2], 0u);
+        for (int q = 0; q < kQ; q++) hd[q * Cd + ht] = dig[q];
+        hd[kQ * Cd + ht] = make_uint4((unsigned)ds[0], (unsigned)ds[1], kPlanes > 2 ? (unsigned)ds[kPlanes - 1] : 0u, 0u);
     }
     named_barrier(1 + hb, 128);
     mark(4);
-    uint4 hdig[CPLI][6];
-    int dcorr[3] = {0, 0, 0};
+    uint4 hdig[CPLI][kQ];
+    int dcorr[kPlanes] = {};
 #pragma unroll
     for (int k = 0; k < CPLI; k++) {
         const int c = lane + 32 * k;
         if (fullI || c < Cd) {
 #pragma unroll
-            for (int q = 0; q < 6; q++) hdig[k][q] = hd[q * Cd + c];
-            const uint4 t = hd[6 * Cd + c];
-            dcorr[0] -= 8 * (int)t.x; dcorr[1] -= 8 * (int)t.y; dcorr[2] -= 8 * (int)t.z;
+            for (int q = 0; q < kQ; q++) hdig[k][q] = hd[q * Cd + c];
+            const uint4 t = hd[kQ * Cd + c];
+            const int tv[3] = {(int)t.x, (int)t.y, (int)t.z};
+#pragma unroll
+            for (int q = 0; q < kPlanes; q++) dcorr[q] -= 8 * tv[q];
         } else {
 #pragma unroll
-            for (int q = 0; q < 6; q++) hdig[k][q] = make_uint4(0u, 0u, 0u, 0u);
+            for (int q = 0; q < kQ; q++) hdig[k][q] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
     auto dn_compute = [&](int rb, const uint4 (&w2)[kDnRows * CPLI], float sc) {
-        int lo[kDnRows][3], hi[kDnRows][3];
+        int lo[kDnRows][kPlanes], hi[kDnRows][kPlanes];
 #pragma unroll
-        for (int rr = 0; rr < kDnRows; rr++) {
-            lo[rr][0] = dcorr[0]; lo[rr][1] = dcorr[1]; lo[rr][2] = dcorr[2];
-            hi[rr][0] = 0; hi[rr][1] = 0; hi[rr][2] = 0;
-        }
+        for (int rr = 0; rr < kDnRows; rr++)
+#pragma unroll
+            for (int q = 0; q < kPlanes; q++) { lo[rr][q] = dcorr[q]; hi[rr][q] = 0; }
 #pragma unroll
         for (int k = 0; k < CPLI; k++) {
             if (fullI || lane + 32 * k < Cd) {

@@ -151,10 +151,12 @@ def test_batched_is_deterministic_and_token_independent(moe):
     a = layer.forward(xd).clone()
     b = layer.forward(xd).clone()
     assert torch.equal(a, b)
-    # a token's output does not depend on the rest of the batch beyond rounding
+    # a token's output does not depend on the rest of the batch: alone (T = 1) it runs the
+    # decode kernel, whose 16-bit fixed-point activations differ from the batched path's
+    # exact fp32 arithmetic by at most ~2^-16 of each vector's largest element per element
     c = layer.forward(xd[5:6].contiguous())
     torch.cuda.synchronize()
-    assert rel_err(c.cpu().numpy()[0].astype(np.float64), a[5].cpu().numpy().astype(np.float64)) < 1e-5
+    assert rel_err(c.cpu().numpy()[0].astype(np.float64), a[5].cpu().numpy().astype(np.float64)) < 5e-4
 
 
 # --- 40-layer stack (x <- x + moe(rmsnorm(x))) -------------------------------------
