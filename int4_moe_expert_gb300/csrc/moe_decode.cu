@@ -33,7 +33,7 @@
 // with every inner sum exact in int32 (dp4a: four unsigned nibble bytes times
 // four signed digit bytes).  Only the final plane combination and the scale
 // are floating point.  The representation error of v is at most
-// max|v| * 2^-16 per element (measured against the double oracle: 1.1e-4
+// max|v| * 2^-16 per element (measured against a double-precision evaluation: 1.1e-4
 // worst relative error on the GLM layer, 5e-4 after 40 chained layers).
 //
 // Digits in shared memory: for chunk c (elements 32c..32c+31, one 16-byte
@@ -69,7 +69,10 @@ constexpr int kQMaxInt = kPlanes == 2 ? 0x7F7F : 0x7F7F7F;   // largest |X| with
 constexpr unsigned kBias = kPlanes == 2 ? 0x8080u : 0x808080u;
 constexpr float kQMax = (float)kQMaxInt;
 constexpr int kSwWords = (kMaxSlots + 3) / 4 * 4;   // s_w padded to 16 bytes
+constexpr int kPtab = 4;       // expert pointers each thread stages: E <= kPtab * kThreads
+constexpr int kKeyBatch = 8;   // score loads a routing lane has in flight at once
 static_assert(kMaxSlots * 16 % 16 == 0 && kSwWords >= kMaxSlots, "shared-memory carving");
+static_assert(kPtab * kThreads >= 1024, "pointer staging covers the largest expert count");
 
 enum : unsigned { kErrGrid = 8u };
 
@@ -259,8 +262,10 @@ __host__ __device__ inline FusedShape fused_shape(const Dims &d) {
     s.J = d.K + d.n_shared;
     s.RB = d.H / kDnRows;
     s.dig_bytes = (kQ + 1) * 16 * (s.C > 2 * s.Cd ? s.C : 2 * s.Cd);
-    // digits | red[64] | slab[33] | scale[33] | w[36] | flags[4] | score keys[E] | sel[32]
-    s.smem = (size_t)s.dig_bytes + 64 * 4 + kMaxSlots * 16 + kSwWords * 4 + 16 + (size_t)(d.E + 3) / 4 * 16 + 32 * 4;
+    // digits | red[64] | slab[33] | scale[33] | w[36] | flags[4] | score keys[E] | sel[32] | sigmoids[E]
+    // | expert slab pointers[E] | expert scale pointers[E]   (E padded to 4 entries)
+    const size_t e4 = (size_t)(d.E + 3) / 4 * 4;
+    s.smem = (size_t)s.dig_bytes + 64 * 4 + kMaxSlots * 16 + kSwWords * 4 + 16 + e4 * 4 + 32 * 4 + e4 * 4 + e4 * 16;
     return s;
 }
 
@@ -286,6 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     volatile int *s_flags = reinterpret_cast<volatile int *>(s_w + kSwWords);   // [0] ok [1] abort
     unsigned *s_key = reinterpret_cast<unsigned *>(const_cast<int *>(s_flags + 4));   // [E] (+pad)
     int *s_sel = reinterpret_cast<int *>(s_key + (p.d.E + 3) / 4 * 4);                // [32]
+    float *s_sig = reinterpret_cast<float *>(s_sel + 32);                               // [E] (+pad)
+    const uint8_t **s_pslab = reinterpret_cast<const uint8_t **>(s_sig + (p.d.E + 3) / 4 * 4);   // [E] (+pad)
+    const float **s_pscale = reinterpret_cast<const float **>(s_pslab + (p.d.E + 3) / 4 * 4);    // [E] (+pad)
 
     const Dims &d = p.d;
     const int H = d.H, E = d.E, K = d.K, J = sh.J, C = sh.C, Cd = sh.Cd;
@@ -374,6 +382,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             u1[k] = has1 ? __ldg(w1 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
+    // every expert's slab and scale pointers, for the slot tables after routing (E <= 4 x kThreads)
+    const uint8_t *pt_slab[kPtab];
+    const float *pt_scale[kPtab];
+#pragma unroll
+    for (int i = 0; i < kPtab; i++) {
+        const int e = tid + i * kThreads;
+        pt_slab[i] = e < E ? p.slabs[e] : nullptr;
+        pt_scale[i] = e < E ? p.scales[e] : nullptr;
+    }
     // the first unit's loads go out now if it is the shared expert's (routing not needed)
     if (u_first.pos < 0) {
         load_gu(u_first, wa, sga, sua);
@@ -461,6 +478,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         }
     }
 
+#pragma unroll
+    for (int i = 0; i < kPtab; i++) {
+        const int e = tid + i * kThreads;
+        if (e < E) {
+            s_pslab[e] = pt_slab[i];
+            s_pscale[e] = pt_scale[i];
+        }
+    }
+
     // x digits (pre-normed when asked), from the registers already loaded
     const float m = amax * r;
     const float s_x = bad ? __int_as_float(0x7fc00000) : m / kQMax;
@@ -498,12 +524,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         if (trace && lane == 0) tr[7] = now_ns();
         // top K by (score desc, index asc): K rounds of a warp-wide max over each
         // lane's best remaining expert (lane l holds experts l + 32 i)
+        // (the scores of up to kKeyBatch x 32 experts are requested together: one round trip)
         unsigned best = 0u;
         int bidx = 0x7fffffff;
-        for (int e = lane; e < E; e += 32) {
-            const unsigned k = order_key(__ldcg(p.ws.dscore + E + e));
-            s_key[e] = k;
-            if (k > best) { best = k; bidx = e; }
+        for (int e0 = lane; e0 < E; e0 += 32 * kKeyBatch) {
+            float c[kKeyBatch], sgv[kKeyBatch];
+#pragma unroll
+            for (int i = 0; i < kKeyBatch; i++) {
+                const int e = e0 + 32 * i;
+                c[i] = e < E ? __ldcg(p.ws.dscore + E + e) : 0.0f;
+                sgv[i] = e < E ? __ldcg(p.ws.dscore + e) : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < kKeyBatch; i++) {
+                const int e = e0 + 32 * i;
+                if (e < E) {
+                    const unsigned k = order_key(c[i]);
+                    s_key[e] = k;
+                    s_sig[e] = sgv[i];
+                    if (k > best) { best = k; bidx = e; }
+                }
+            }
         }
         for (int r = 0; r < K; r++) {
             const unsigned mx = __reduce_max_sync(kFull, best);
@@ -521,14 +562,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         }
         __syncwarp();
         const int me = lane < K ? s_sel[lane] : 0;   // written by lane 0 of this warp
-        const float sg = lane < K ? __ldcg(p.ws.dscore + me) : 0.0f;
+        const float sg = lane < K ? s_sig[me] : 0.0f;
         float sum = sg;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
         const float mw = d.norm_topk ? d.scale * sg / (sum + 1e-20f) : d.scale * sg;
         if (lane < K) {
-            s_slab[lane] = p.slabs[me];
-            s_scale[lane] = p.scales[me];
+            s_slab[lane] = s_pslab[me];
+            s_scale[lane] = s_pscale[me];
             s_w[lane] = mw;
         } else if (lane == K && d.n_shared) {
             s_slab[lane] = p.sh_slab;
