@@ -84,6 +84,7 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
     d->eps = c->rms_eps;
     d->max_tokens = max_tokens;
     d->fast_decode = moe::decode_fast_supported(*d) ? 1 : 0;
+    d->mma = moe::mma_supported(*d) ? 1 : 0;
     d->trace = (c->flags & MOE_FLAG_TRACE) ? 1 : 0;
     return MOE_OK;
 }

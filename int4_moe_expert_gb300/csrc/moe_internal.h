@@ -19,6 +19,7 @@ struct Dims {
     float eps;          // rms_eps
     int max_tokens;
     int fast_decode;    // T == 1 runs the streaming kernels (moe_decode.cu)
+    int mma;            // T > 1 runs the tensor-core expert kernels (H, I, I_sh multiples of 128)
     int trace;          // MOE_FLAG_TRACE: the decode kernel records its timeline
 };
 
@@ -39,6 +40,11 @@ struct Workspace {
     int *slot_expert;    // [E] active experts, ascending id
     int *n_slots;        // [1]
     float *dbuf;         // [(maxT*K + maxT), H] unweighted down outputs (T > 1)
+    // T > 1 tensor-core path: f16 activations in mma order (mma_pos in moe_kernels.cu)
+    uint16_t *x16;       // [maxT, H] pre-normed x
+    uint16_t *h16;       // [(maxT*K + maxT), I_max] SwiGLU activations, rows as h
+    int *items;          // [2 * max_items] (slot, first token) of every kItemTokens-token work item
+    int *n_items;        // [1]
     // decode (T == 1) streaming path
     unsigned *claims;    // [kClaimWords] work counters: [0] gate/up units, [1 + j] down rows of
                          // slot j; each call's last barrier is followed by their reset to 0
@@ -50,6 +56,12 @@ struct Workspace {
 };
 
 constexpr int kMaxSlots = 33;   // K <= 32 routed + 1 shared
+constexpr int kItemTokens = 32;  // tokens of one tensor-core work item (4 n8 tiles)
+inline int max_items(int T, int K, int E, int n_shared) {   // work items of one T-token call, at most
+    const int P = T * K;
+    return P / kItemTokens + (E < P ? E : P) + (n_shared ? (T + kItemTokens - 1) / kItemTokens : 0) + 1;
+}
+bool mma_supported(const Dims &d);
 constexpr int kClaimWords = 64;  // >= 1 + kMaxSlots
 constexpr int kTraceBlocks = 1024;   // decode blocks the trace buffer holds
 

@@ -12,6 +12,7 @@
 // "chunk-permuted" order so that one 16-byte weight load (32 int4 values)
 // meets its 32 activations as eight float4 loads that are contiguous across
 // the lanes of a warp; see perm_pos.
+#include <cuda_fp16.h>
 #include <math.h>
 #include <stdint.h>
 
@@ -44,6 +45,17 @@ __host__ __device__ __forceinline__ int perm_pos(int i, int L) {
     const int k = 2 * m + (e & 1), r = e >> 1;
     return ((k * C + c) << 2) + r;
 }
+
+// Position of element i of a vector in the f16 "mma order" of the T > 1
+// tensor-core kernels: within each group of 8 consecutive elements the order
+// is 0 4 1 5 2 6 3 7, so that one 32-bit word of packed int4 weights (8
+// values) and the matching 16 bytes of activations split into the same four
+// (element, element + 4) pairs; see mma_expert_kernel.
+__host__ __device__ __forceinline__ int mma_pos(int i) {
+    return (i & ~7) | ((i & 3) << 1) | ((i >> 2) & 1);
+}
+
+__device__ __forceinline__ uint16_t f2h_bits(float v) { return __half_as_ushort(__float2half_rn(v)); }
 
 // 16-byte streaming load of weights: read-only path, no L1 allocation.
 __device__ __forceinline__ uint4 ld_stream(const void *ptr) {
@@ -189,32 +201,54 @@ __device__ void bucket_phase(const Params &p, int T, int *ismem) {
     __syncthreads();
     if (warp == 0) {
         // exclusive scans of counts and of "active" flags, E <= 1024
+        // (and of work items for the tensor-core kernels: kItemTokens tokens of one slot each)
         const int per = (E + 31) / 32;
         const int b = lane * per;
-        int s = 0, a = 0;
+        const bool items = p.d.mma && T > 1;
+        int s = 0, a = 0, c = 0;
         for (int i = 0; i < per; i++) {
             const int e = b + i;
-            if (e < E) { s += cnt[e]; a += cnt[e] > 0; }
+            if (e < E) { s += cnt[e]; a += cnt[e] > 0; c += (cnt[e] + kItemTokens - 1) / kItemTokens; }
         }
-        int ps = s, pa = a;
+        int ps = s, pa = a, pc = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int vs = __shfl_up_sync(0xffffffffu, ps, o);
             const int va = __shfl_up_sync(0xffffffffu, pa, o);
-            if (lane >= o) { ps += vs; pa += va; }
+            const int vc = __shfl_up_sync(0xffffffffu, pc, o);
+            if (lane >= o) { ps += vs; pa += va; pc += vc; }
         }
-        int off = ps - s, act = pa - a;
+        int off = ps - s, act = pa - a, it = pc - c;
         for (int i = 0; i < per; i++) {
             const int e = b + i;
             if (e < E) {
                 p.ws.cnt[e] = cnt[e];
                 p.ws.off[e] = off;
                 run[e] = off;
-                if (cnt[e] > 0) p.ws.slot_expert[act++] = e;
+                if (cnt[e] > 0) {
+                    if (items)
+                        for (int n0 = 0; n0 < cnt[e]; n0 += kItemTokens, it++) {
+                            p.ws.items[2 * it] = act;
+                            p.ws.items[2 * it + 1] = n0;
+                        }
+                    p.ws.slot_expert[act++] = e;
+                }
                 off += cnt[e];
             }
         }
-        if (lane == 31) { p.ws.off[E] = ps; *p.ws.n_slots = pa; }
+        if (lane == 31) {
+            p.ws.off[E] = ps;
+            *p.ws.n_slots = pa;
+            if (items) {                 // the shared expert: slot n_slots, all T tokens
+                int n = pc;
+                if (p.d.n_shared)
+                    for (int n0 = 0; n0 < T; n0 += kItemTokens, n++) {
+                        p.ws.items[2 * n] = pa;
+                        p.ws.items[2 * n + 1] = n0;
+                    }
+                *p.ws.n_items = n;
+            }
+        }
     }
     __syncthreads();
     const unsigned lt_mask = (1u << lane) - 1u;
@@ -289,7 +323,9 @@ __global__ void __launch_bounds__(kThreads) router_gemv_kernel(Params p, const f
     __syncthreads();
     for (int i = blockIdx.x * kThreads + threadIdx.x; i < T * H; i += gridDim.x * kThreads) {
         const int t = i / H, c = i - t * H;
-        p.ws.xperm[(size_t)t * H + perm_pos(c, H)] = x[i] * s_r[t];
+        const float v = x[i] * s_r[t];
+        p.ws.xperm[(size_t)t * H + perm_pos(c, H)] = v;
+        if (p.d.mma && T > 1) p.ws.x16[(size_t)t * H + mma_pos(c)] = f2h_bits(v);
     }
     const int e = blockIdx.x * kWarps + warp;
     if (e < E) {
@@ -490,8 +526,11 @@ __global__ void __launch_bounds__(kThreads) router_tiled_kernel(Params p, const 
         for (int tl = warp; tl < 32 && t0 + tl < T; tl += kWarps) {
             const int t = t0 + tl;
             if (lane == 0) p.ws.rnorm[t] = s_r[tl];
-            for (int i = lane; i < H; i += 32)
-                p.ws.xperm[(size_t)t * H + perm_pos(i, H)] = x[(size_t)t * H + i] * s_r[tl];
+            for (int i = lane; i < H; i += 32) {
+                const float v = x[(size_t)t * H + i] * s_r[tl];
+                p.ws.xperm[(size_t)t * H + perm_pos(i, H)] = v;
+                if (p.d.mma) p.ws.x16[(size_t)t * H + mma_pos(i)] = f2h_bits(v);
+            }
         }
     }
     router_tail(p, T, buckets, gridDim.x * gridDim.y, smem);
@@ -788,6 +827,185 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Params p, const float
     }
 }
 
+// ---------------------------------------------------------------------------
+// Batched (T > 1) on the tensor cores: mma.sync m16n8k16, f16 x f16 -> f32.
+//
+// A = int4 weight rows (exact in f16), B = f16 activations of up to
+// kItemTokens tokens (one work item: a slot and a run of its tokens), C in
+// f32 registers.  Each thread streams, per 128-element block of the reduction,
+// the 16 bytes at offset 16 q (q = lane % 4) of each of its weight rows: four
+// 32-bit words of 8 int4 values.  One word w splits with two masks and two
+// shifts into the f16 pairs (e0, e4), (e1, e5), (e2, e6), (e3, e7) (1024 + n
+// or 1024 + 16 n in the f16 bit pattern, then one subtract or fma), and the
+// mma order of the activations (mma_pos) stores each 8-element group as
+// 0 4 1 5 2 6 3 7, so the same pairs are adjacent f16 values there.  Word w
+// of thread q covers two k-steps: pairs (e0,e4) / (e1,e5) are the fragment's
+// columns (2q, 2q+1) / (2q+8, 2q+9) of the first, (e2,e6) / (e3,e7) of the
+// second.  A dot product does not depend on the order of its terms, so A and B
+// only have to agree on it, which they do.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t h2_sub(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t h2_fma(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+// 8 packed int4 values (q + 8, element 2b in the low nibble of byte b) -> the
+// f16x2 pairs (e0,e4), (e1,e5), (e2,e6), (e3,e7), exact.
+__device__ __forceinline__ void int4x8_to_f16x2(uint32_t w, uint32_t (&h)[4]) {
+    constexpr uint32_t kMagic = 0x64006400u;   // f16 1024 in both halves
+    constexpr uint32_t kSubLo = 0x64086408u;   // 1032 = 1024 + 8
+    constexpr uint32_t kMulHi = 0x2C002C00u;   // 1/16
+    constexpr uint32_t kAddHi = 0xD480D480u;   // -72 = -(1024/16 + 8)
+    h[0] = h2_sub((w & 0x000F000Fu) | kMagic, kSubLo);
+    h[1] = h2_fma((w & 0x00F000F0u) | kMagic, kMulHi, kAddHi);
+    h[2] = h2_sub(((w >> 8) & 0x000F000Fu) | kMagic, kSubLo);
+    h[3] = h2_fma(((w >> 8) & 0x00F000F0u) | kMagic, kMulHi, kAddHi);
+}
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                        uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t u4w(const uint4 &v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+
+constexpr int kMmaNT = kItemTokens / 8;     // n8 tiles per work item
+
+// One work item times one tile of output rows.  GU (gate/up + SwiGLU): warp w
+// owns output rows o0 + 16 w + {0..15}, as two m16 tiles: those gate rows and
+// the same up rows; 128 rows per block; writes h16.  Down: warp w owns rows
+// o0 + 32 w + {0..31} (two m16 tiles), 256 rows per block; writes dbuf.
+template <bool GU>
+__global__ void __launch_bounds__(kThreads) mma_expert_kernel(Params p, int T) {
+    __shared__ int s_brow[kItemTokens], s_orow[kItemTokens];
+    const int item = blockIdx.y;
+    if (item >= *p.ws.n_items) return;
+    const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
+    const SlotInfo s = slot_info(p, T, slot);
+    if (!s.valid) return;
+    const int H = p.d.H, Is = s.Is;
+    const int o0 = blockIdx.x * (GU ? 128 : 256);
+    if (o0 >= (GU ? Is : H)) return;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
+    const int nt = min(kItemTokens, s.n - n0);
+    if (tid < kItemTokens) {
+        int tok = 0, row = -1;
+        if (tid < nt) slot_token(p, s, T, n0 + tid, &tok, &row);
+        s_brow[tid] = GU ? tok : row;          // activation row the tensor cores read
+        s_orow[tid] = row;                     // output row (h16 / dbuf)
+    }
+    __syncthreads();
+    const int ob = o0 + (GU ? 16 : 32) * warp;          // the warp's first output row
+    if (ob >= (GU ? Is : H)) return;                     // (rows are multiples of 128: all or none)
+    const int Kd = GU ? H : Is;                          // reduction length
+    const size_t arb = (size_t)(Kd >> 1);                // weight row bytes
+    const uint8_t *abase = GU ? s.slab : s.slab + (size_t)2 * Is * (size_t)(H >> 1);
+    int ar[4];                                           // tile 0 rows g, g+8; tile 1 rows g, g+8
+    if (GU) { ar[0] = ob + g; ar[1] = ob + g + 8; ar[2] = Is + ob + g; ar[3] = Is + ob + g + 8; }
+    else { ar[0] = ob + g; ar[1] = ob + g + 8; ar[2] = ob + 16 + g; ar[3] = ob + 24 + g; }
+    const uint4 *ap[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) ap[i] = reinterpret_cast<const uint4 *>(abase + (size_t)ar[i] * arb) + q;
+    const uint16_t *act = GU ? p.ws.x16 : p.ws.h16;
+    const size_t ald = GU ? (size_t)H : (size_t)p.d.I_max;     // activation row stride (f16)
+    const uint4 *bp[kMmaNT];
+#pragma unroll
+    for (int j = 0; j < kMmaNT; j++) {
+        const int n = 8 * j + g;
+        bp[j] = reinterpret_cast<const uint4 *>(act + (size_t)s_brow[n < nt ? n : 0] * ald) + 4 * q;
+    }
+    const int ntiles = (nt + 7) >> 3;
+    float acc[2][kMmaNT][4];
+#pragma unroll
+    for (int t = 0; t < 2; t++)
+#pragma unroll
+        for (int j = 0; j < kMmaNT; j++)
+#pragma unroll
+            for (int c = 0; c < 4; c++) acc[t][j][c] = 0.0f;
+    const int nkb = Kd >> 7;
+    uint4 an[4];
+#pragma unroll
+    for (int i = 0; i < 4; i++) an[i] = ld_stream(ap[i]);
+#pragma unroll 1
+    for (int kb = 0; kb < nkb; kb++) {
+        uint4 a[4];
+#pragma unroll
+        for (int i = 0; i < 4; i++) a[i] = an[i];
+        if (kb + 1 < nkb) {
+#pragma unroll
+            for (int i = 0; i < 4; i++) an[i] = ld_stream(ap[i] + 4 * (kb + 1));
+        }
+        uint4 b[kMmaNT][4];
+#pragma unroll
+        for (int j = 0; j < kMmaNT; j++)
+            if (j < ntiles) {
+#pragma unroll
+                for (int w = 0; w < 4; w++) b[j][w] = __ldg(bp[j] + 16 * kb + w);
+            }
+#pragma unroll
+        for (int w = 0; w < 4; w++) {            // word w: k-steps 2w (pairs 0, 1) and 2w + 1 (pairs 2, 3)
+            uint32_t h[4][4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) int4x8_to_f16x2(u4w(a[i], w), h[i]);
+#pragma unroll
+            for (int ss = 0; ss < 2; ss++) {
+                const int lo = 2 * ss, hi = 2 * ss + 1;
+#pragma unroll
+                for (int j = 0; j < kMmaNT; j++)
+                    if (j < ntiles) {
+                        const uint32_t b0 = u4w(b[j][w], lo), b1 = u4w(b[j][w], hi);
+                        mma_f16(acc[0][j], h[0][lo], h[1][lo], h[0][hi], h[1][hi], b0, b1);
+                        mma_f16(acc[1][j], h[2][lo], h[3][lo], h[2][hi], h[3][hi], b0, b1);
+                    }
+            }
+        }
+    }
+    // accumulator (tile t, n-tile j, c): row g + 8 (c >> 1) of the tile, token 8 j + 2 q + (c & 1)
+    if (GU) {
+#pragma unroll
+        for (int rh = 0; rh < 2; rh++) {
+            const int o = ob + g + 8 * rh;
+            const float sg = s.sc[o], su = s.sc[Is + o];
+            const int pos = mma_pos(o);
+#pragma unroll
+            for (int j = 0; j < kMmaNT; j++)
+#pragma unroll
+                for (int c = 0; c < 2; c++) {
+                    const int n = 8 * j + 2 * q + c;
+                    if (j < ntiles && n < nt) {
+                        const float hv = silu_mul(sg * acc[0][j][2 * rh + c], su * acc[1][j][2 * rh + c]);
+                        p.ws.h16[(size_t)s_orow[n] * p.d.I_max + pos] = f2h_bits(hv);
+                    }
+                }
+        }
+    } else {
+        const float *sd = s.sc + 2 * Is;
+#pragma unroll
+        for (int t = 0; t < 2; t++)
+#pragma unroll
+            for (int rh = 0; rh < 2; rh++) {
+                const int o = ob + 16 * t + g + 8 * rh;
+                const float sc = sd[o];
+#pragma unroll
+                for (int j = 0; j < kMmaNT; j++)
+#pragma unroll
+                    for (int c = 0; c < 2; c++) {
+                        const int n = 8 * j + 2 * q + c;
+                        if (j < ntiles && n < nt) p.ws.dbuf[(size_t)s_orow[n] * H + o] = sc * acc[t][j][2 * rh + c];
+                    }
+            }
+    }
+}
+
 size_t router_smem_bytes(const Dims &d) {
     const size_t topk = (size_t)kWarps * 2 * d.E * sizeof(float);
     const size_t bucket = (size_t)(2 + kWarps) * d.E * sizeof(int);
@@ -833,12 +1051,22 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
     ws->trace = reinterpret_cast<unsigned long long *>(
         take(d.trace ? (size_t)kTraceBlocks * MOE_TRACE_SLOTS * sizeof(unsigned long long) : 0));
     ws->dbuf = reinterpret_cast<float *>(take((P + T) * d.H * sizeof(float)));
+    const bool mma = d.mma != 0 && T > 1;
+    ws->x16 = reinterpret_cast<uint16_t *>(take(mma ? T * d.H * sizeof(uint16_t) : 0));
+    ws->h16 = reinterpret_cast<uint16_t *>(take(mma ? (P + T) * d.I_max * sizeof(uint16_t) : 0));
+    ws->items = reinterpret_cast<int *>(
+        take(mma ? 2 * (size_t)max_items((int)T, d.K, d.E, d.n_shared) * sizeof(int) : 0));
+    ws->n_items = reinterpret_cast<int *>(take(sizeof(int)));
     ws->total_bytes = o;
 }
 
 // ---------------------------------------------------------------------------
 // Launch
 // ---------------------------------------------------------------------------
+
+bool mma_supported(const Dims &d) {
+    return d.max_tokens > 1 && d.H % 128 == 0 && d.I % 128 == 0 && (!d.n_shared || d.I_sh % 128 == 0);
+}
 
 cudaError_t prepare_kernels(const Dims &d) {
     const int smem = (int)router_smem_bytes(d);
@@ -884,6 +1112,21 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
         down_decode_kernel<RPW_D><<<g2, kThreads, 0, st>>>(p, x, y);
         check();
         mark(3);
+        mark(4);
+        return e;
+    }
+    if (d.mma) {
+        const int ni = max_items(T, d.K, d.E, d.n_shared);
+        const dim3 g1(d.I_max / 128, ni);
+        mma_expert_kernel<true><<<g1, kThreads, 0, st>>>(p, T);
+        check();
+        mark(2);
+        const dim3 g2((d.H + 255) / 256, ni);
+        mma_expert_kernel<false><<<g2, kThreads, 0, st>>>(p, T);
+        check();
+        mark(3);
+        combine_kernel<<<T, kThreads, 0, st>>>(p, x, y, T);
+        check();
         mark(4);
         return e;
     }

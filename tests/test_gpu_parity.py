@@ -215,6 +215,11 @@ def small_workload(**kw):
     dict(I_shared=32, K=8, E=64),          # streaming decode: small rows, lanes idle
     dict(I_shared=32, n_shared=0, E=40, K=32, H=96),   # streaming decode: 32 slots, H = 96
     dict(I_shared=32, n_layers=2, H=1056, I=160),      # streaming decode, odd chunk counts
+    # T > 1 on the tensor cores (H, I, I_shared multiples of 128)
+    dict(H=384, I=128, I_shared=256, E=40, K=8),       # 256-row down tiles half used; I_sh != I
+    dict(H=256, I=256, n_shared=0, I_shared=0, E=8, K=8),   # E == K: 37 tokens on every expert
+    dict(H=128, I=128, I_shared=128, E=300, K=32),     # K at its limit
+    dict(H=256, I=128, I_shared=128, E=2, K=2, n_layers=2),  # two work items per expert, pre-norm
 ])
 def test_edge_configs(moe, kw):
     wl = small_workload(**kw)
