@@ -45,6 +45,7 @@ struct Workspace {
     uint16_t *h16;       // [(maxT*K + maxT), I_max] SwiGLU activations, rows as h
     int *items;          // [2 * max_items] (slot, first token) of every kItemTokens-token work item
     int *n_items;        // [1]
+    unsigned *gcount;    // [ceil(maxT / 32)] tiled router: blocks done per 32-token group
     // decode (T == 1) streaming path
     unsigned *claims;    // [kClaimWords] work counters: [0] gate/up units, [1 + j] down rows of
                          // slot j; each call's last barrier is followed by their reset to 0

@@ -125,15 +125,15 @@ __device__ __forceinline__ bool ranks_before(float v, int e, float bv, int be) {
     return v > bv || (v == bv && e < be);
 }
 
-// Top-K for tokens [0, T): one warp per token.  Scores live in shared memory
+// Top-K for tokens [t_begin, t_end): one warp per token.  Scores live in shared memory
 // (sig and choice, E floats per warp).  NaN scores rank last, so an index in
 // [0, E) is always produced.
-__device__ void topk_phase(const Params &p, int T, float *smem) {
+__device__ void topk_phase(const Params &p, int t_begin, int t_end, float *smem) {
     const int E = p.d.E, K = p.d.K;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float *sig = smem + warp * 2 * E;
     float *choice = sig + E;
-    for (int t = warp; t < T; t += kWarps) {
+    for (int t = t_begin + warp; t < t_end; t += kWarps) {
         for (int base = 0; base < E; base += 256) {     // loads issued 8 at a time
             float lv[8], bv8[8];
 #pragma unroll
@@ -197,7 +197,7 @@ __device__ void bucket_phase(const Params &p, int T, int *ismem) {
     for (int e = tid; e < E; e += kThreads) cnt[e] = 0;
     for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
     __syncthreads();
-    for (int q = tid; q < P; q += kThreads) atomicAdd(&cnt[p.ws.topk_idx[q]], 1);
+    for (int q = tid; q < P; q += kThreads) atomicAdd(&cnt[__ldcg(p.ws.topk_idx + q)], 1);
     __syncthreads();
     if (warp == 0) {
         // exclusive scans of counts and of "active" flags, E <= 1024
@@ -254,7 +254,7 @@ __device__ void bucket_phase(const Params &p, int T, int *ismem) {
     const unsigned lt_mask = (1u << lane) - 1u;
     for (int base = 0; base < P; base += kThreads) {
         const int q = base + tid;
-        const int e = q < P ? p.ws.topk_idx[q] : -1;
+        const int e = q < P ? __ldcg(p.ws.topk_idx + q) : -1;
         const unsigned same = __match_any_sync(0xffffffffu, e);
         const int lrank = __popc(same & lt_mask);
         if (e >= 0 && lrank == 0) wcnt[warp * E + e] = __popc(same);
@@ -289,7 +289,7 @@ __device__ void router_tail(const Params &p, int T, int buckets, unsigned nblock
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    topk_phase(p, T, smem);
+    topk_phase(p, 0, T, smem);
     __syncthreads();
     if (buckets) bucket_phase(p, T, reinterpret_cast<int *>(smem));
     if (threadIdx.x == 0) *p.ws.counters = 0u;     // ready for the next call
@@ -533,7 +533,27 @@ __global__ void __launch_bounds__(kThreads) router_tiled_kernel(Params p, const 
             }
         }
     }
-    router_tail(p, T, buckets, gridDim.x * gridDim.y, smem);
+    // two-level tail: the last block of this 32-token group picks the group's top K; the
+    // last group to finish builds the buckets
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = atomicAdd(p.ws.gcount + blockIdx.y, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    topk_phase(p, t0, min(T, t0 + 32), smem);
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+        p.ws.gcount[blockIdx.y] = 0u;              // ready for the next call
+        s_last = atomicAdd(p.ws.counters, 1u) == gridDim.y - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (buckets) bucket_phase(p, T, reinterpret_cast<int *>(smem));
+    if (tid == 0) *p.ws.counters = 0u;
 }
 
 // ---------------------------------------------------------------------------
@@ -879,13 +899,39 @@ __device__ __forceinline__ uint32_t u4w(const uint4 &v, int i) {
 }
 
 constexpr int kMmaNT = kItemTokens / 8;     // n8 tiles per work item
+constexpr int kMmaStages = 4;               // k-blocks (128 elements) in the shared-memory ring
+constexpr int kMmaARows = 256;              // weight rows per block (GU: 128 gate + 128 up)
+constexpr int kMmaABytes = kMmaARows * 64;  // one k-block of them (int4)
+constexpr int kMmaBLd = 136;                // f16 per staged activation row (128 + 8: no bank conflicts)
+constexpr int kMmaBBytes = kItemTokens * kMmaBLd * 2;
+constexpr int kMmaStageBytes = kMmaABytes + kMmaBBytes;
+constexpr size_t kMmaSmem = (size_t)kMmaStages * kMmaStageBytes;
+
+__device__ __forceinline__ uint32_t smem_u32(const void *ptr) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ uint4 lds128_u(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
 
 // One work item times one tile of output rows.  GU (gate/up + SwiGLU): warp w
 // owns output rows o0 + 16 w + {0..15}, as two m16 tiles: those gate rows and
 // the same up rows; 128 rows per block; writes h16.  Down: warp w owns rows
 // o0 + 32 w + {0..31} (two m16 tiles), 256 rows per block; writes dbuf.
+// Weights (256 rows x 64 bytes per k-block) and the item's activations
+// (kItemTokens rows x 256 bytes) move through a kMmaStages-deep ring in shared
+// memory with cp.async; every k-block is one __syncthreads.
 template <bool GU>
-__global__ void __launch_bounds__(kThreads) mma_expert_kernel(Params p, int T) {
+__global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T) {
+    extern __shared__ __align__(128) unsigned char mma_smem[];
     __shared__ int s_brow[kItemTokens], s_orow[kItemTokens];
     const int item = blockIdx.y;
     if (item >= *p.ws.n_items) return;
@@ -893,8 +939,9 @@ __global__ void __launch_bounds__(kThreads) mma_expert_kernel(Params p, int T) {
     const SlotInfo s = slot_info(p, T, slot);
     if (!s.valid) return;
     const int H = p.d.H, Is = s.Is;
+    const int rows = GU ? Is : H;                       // output rows of the slot
     const int o0 = blockIdx.x * (GU ? 128 : 256);
-    if (o0 >= (GU ? Is : H)) return;
+    if (o0 >= rows) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
     const int nt = min(kItemTokens, s.n - n0);
     if (tid < kItemTokens) {
@@ -904,25 +951,56 @@ __global__ void __launch_bounds__(kThreads) mma_expert_kernel(Params p, int T) {
         s_orow[tid] = row;                     // output row (h16 / dbuf)
     }
     __syncthreads();
-    const int ob = o0 + (GU ? 16 : 32) * warp;          // the warp's first output row
-    if (ob >= (GU ? Is : H)) return;                     // (rows are multiples of 128: all or none)
     const int Kd = GU ? H : Is;                          // reduction length
     const size_t arb = (size_t)(Kd >> 1);                // weight row bytes
     const uint8_t *abase = GU ? s.slab : s.slab + (size_t)2 * Is * (size_t)(H >> 1);
-    int ar[4];                                           // tile 0 rows g, g+8; tile 1 rows g, g+8
-    if (GU) { ar[0] = ob + g; ar[1] = ob + g + 8; ar[2] = Is + ob + g; ar[3] = Is + ob + g + 8; }
-    else { ar[0] = ob + g; ar[1] = ob + g + 8; ar[2] = ob + 16 + g; ar[3] = ob + 24 + g; }
-    const uint4 *ap[4];
-#pragma unroll
-    for (int i = 0; i < 4; i++) ap[i] = reinterpret_cast<const uint4 *>(abase + (size_t)ar[i] * arb) + q;
     const uint16_t *act = GU ? p.ws.x16 : p.ws.h16;
     const size_t ald = GU ? (size_t)H : (size_t)p.d.I_max;     // activation row stride (f16)
-    const uint4 *bp[kMmaNT];
+    // this thread's cp.async pieces of one k-block: weights 4 x 16 B, activations 2 x 16 B
+    const uint8_t *asrc[4];
+    uint32_t adst[4];
+    bool aok[4];
 #pragma unroll
-    for (int j = 0; j < kMmaNT; j++) {
-        const int n = 8 * j + g;
-        bp[j] = reinterpret_cast<const uint4 *>(act + (size_t)s_brow[n < nt ? n : 0] * ald) + 4 * q;
+    for (int i = 0; i < 4; i++) {
+        const int c = tid + i * kThreads, lr = c >> 2, piece = c & 3;
+        const int gr = GU ? (lr < 128 ? o0 + lr : Is + o0 + lr - 128) : o0 + lr;
+        aok[i] = GU || gr < H;
+        asrc[i] = abase + (size_t)(aok[i] ? gr : 0) * arb + piece * 16;
+        adst[i] = (uint32_t)(lr * 64 + piece * 16);
     }
+    const uint16_t *bsrc[2];
+    uint32_t bdst[2];
+#pragma unroll
+    for (int i = 0; i < 2; i++) {
+        const int c = tid + i * kThreads, n = c >> 4, piece = c & 15;
+        bsrc[i] = act + (size_t)s_brow[n < nt ? n : 0] * ald + piece * 8;
+        bdst[i] = (uint32_t)(kMmaABytes + (n * kMmaBLd + piece * 8) * 2);
+    }
+    const uint32_t sbase = smem_u32(mma_smem);
+    const int nkb = Kd >> 7;
+    auto issue = [&](int kb) {
+        const uint32_t st = sbase + (uint32_t)((kb % kMmaStages) * kMmaStageBytes);
+#pragma unroll
+        for (int i = 0; i < 4; i++)
+            if (aok[i]) cp_async16(st + adst[i], asrc[i] + (size_t)kb * 64);
+#pragma unroll
+        for (int i = 0; i < 2; i++) cp_async16(st + bdst[i], bsrc[i] + (size_t)kb * 128);
+    };
+    const int ob = o0 + (GU ? 16 : 32) * warp;            // the warp's first output row
+    const bool active = ob < rows;                         // (rows are multiples of 128)
+    // shared-memory offsets of the warp's four weight rows (tile 0 rows g, g+8; tile 1 rows g, g+8)
+    uint32_t aoff[4];
+    {
+        const int l0 = GU ? 16 * warp + g : 32 * warp + g;
+        const int l1 = GU ? 128 + 16 * warp + g : 32 * warp + 16 + g;
+        aoff[0] = (uint32_t)(l0 * 64 + q * 16);
+        aoff[1] = aoff[0] + 8 * 64;
+        aoff[2] = (uint32_t)(l1 * 64 + q * 16);
+        aoff[3] = aoff[2] + 8 * 64;
+    }
+    uint32_t boff[kMmaNT];
+#pragma unroll
+    for (int j = 0; j < kMmaNT; j++) boff[j] = (uint32_t)(kMmaABytes + ((8 * j + g) * kMmaBLd + 32 * q) * 2);
     const int ntiles = (nt + 7) >> 3;
     float acc[2][kMmaNT][4];
 #pragma unroll
@@ -931,44 +1009,43 @@ __global__ void __launch_bounds__(kThreads) mma_expert_kernel(Params p, int T) {
         for (int j = 0; j < kMmaNT; j++)
 #pragma unroll
             for (int c = 0; c < 4; c++) acc[t][j][c] = 0.0f;
-    const int nkb = Kd >> 7;
-    uint4 an[4];
 #pragma unroll
-    for (int i = 0; i < 4; i++) an[i] = ld_stream(ap[i]);
+    for (int k = 0; k < kMmaStages - 1; k++) {
+        if (k < nkb) issue(k);
+        cp_async_commit();
+    }
 #pragma unroll 1
     for (int kb = 0; kb < nkb; kb++) {
+        cp_async_wait<kMmaStages - 2>();     // this thread's pieces of k-block kb have landed
+        __syncthreads();                     // everyone's have; everyone is done with kb - 1
+        if (kb + kMmaStages - 1 < nkb) issue(kb + kMmaStages - 1);
+        cp_async_commit();
+        if (!active) continue;
+        const uint32_t st = sbase + (uint32_t)((kb % kMmaStages) * kMmaStageBytes);
         uint4 a[4];
 #pragma unroll
-        for (int i = 0; i < 4; i++) a[i] = an[i];
-        if (kb + 1 < nkb) {
-#pragma unroll
-            for (int i = 0; i < 4; i++) an[i] = ld_stream(ap[i] + 4 * (kb + 1));
-        }
-        uint4 b[kMmaNT][4];
-#pragma unroll
-        for (int j = 0; j < kMmaNT; j++)
-            if (j < ntiles) {
-#pragma unroll
-                for (int w = 0; w < 4; w++) b[j][w] = __ldg(bp[j] + 16 * kb + w);
-            }
+        for (int i = 0; i < 4; i++) a[i] = lds128_u(st + aoff[i]);
 #pragma unroll
         for (int w = 0; w < 4; w++) {            // word w: k-steps 2w (pairs 0, 1) and 2w + 1 (pairs 2, 3)
             uint32_t h[4][4];
 #pragma unroll
             for (int i = 0; i < 4; i++) int4x8_to_f16x2(u4w(a[i], w), h[i]);
 #pragma unroll
-            for (int ss = 0; ss < 2; ss++) {
-                const int lo = 2 * ss, hi = 2 * ss + 1;
+            for (int j = 0; j < kMmaNT; j++)
+                if (j < ntiles) {
+                    const uint4 b = lds128_u(st + boff[j] + 16 * w);
 #pragma unroll
-                for (int j = 0; j < kMmaNT; j++)
-                    if (j < ntiles) {
-                        const uint32_t b0 = u4w(b[j][w], lo), b1 = u4w(b[j][w], hi);
+                    for (int ss = 0; ss < 2; ss++) {
+                        const int lo = 2 * ss, hi = 2 * ss + 1;
+                        const uint32_t b0 = u4w(b, lo), b1 = u4w(b, hi);
                         mma_f16(acc[0][j], h[0][lo], h[1][lo], h[0][hi], h[1][hi], b0, b1);
                         mma_f16(acc[1][j], h[2][lo], h[3][lo], h[2][hi], h[3][hi], b0, b1);
                     }
-            }
+                }
         }
     }
+    cp_async_wait<0>();
+    if (!active) return;
     // accumulator (tile t, n-tile j, c): row g + 8 (c >> 1) of the tile, token 8 j + 2 q + (c & 1)
     if (GU) {
 #pragma unroll
@@ -1057,6 +1134,7 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
     ws->items = reinterpret_cast<int *>(
         take(mma ? 2 * (size_t)max_items((int)T, d.K, d.E, d.n_shared) * sizeof(int) : 0));
     ws->n_items = reinterpret_cast<int *>(take(sizeof(int)));
+    ws->gcount = reinterpret_cast<unsigned *>(take((T + 31) / 32 * sizeof(unsigned)));
     ws->total_bytes = o;
 }
 
@@ -1075,6 +1153,10 @@ cudaError_t prepare_kernels(const Dims &d) {
         e = cudaFuncSetAttribute(router_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(router_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess && d.mma)
+        e = cudaFuncSetAttribute(mma_expert_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmaSmem);
+    if (e == cudaSuccess && d.mma)
+        e = cudaFuncSetAttribute(mma_expert_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmaSmem);
     if (e == cudaSuccess && d.fast_decode) e = prepare_decode_fast(d);
     return e;
 }
@@ -1118,11 +1200,11 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
     if (d.mma) {
         const int ni = max_items(T, d.K, d.E, d.n_shared);
         const dim3 g1(d.I_max / 128, ni);
-        mma_expert_kernel<true><<<g1, kThreads, 0, st>>>(p, T);
+        mma_expert_kernel<true><<<g1, kThreads, kMmaSmem, st>>>(p, T);
         check();
         mark(2);
         const dim3 g2((d.H + 255) / 256, ni);
-        mma_expert_kernel<false><<<g2, kThreads, 0, st>>>(p, T);
+        mma_expert_kernel<false><<<g2, kThreads, kMmaSmem, st>>>(p, T);
         check();
         mark(3);
         combine_kernel<<<T, kThreads, 0, st>>>(p, x, y, T);
