@@ -154,6 +154,13 @@ moe_status moe_device_error(moe_handle *h, uint32_t *flags);
  * I <= 2048, H <= 8192, E <= 1024, K + n_shared <= 32). */
 int32_t moe_uses_streaming_decode(const moe_handle *h);
 
+/* 1 if T > 1 calls on this handle run the experts on the tensor cores
+ * (mma.sync m16n8k16: exact int4 weights times f16 activations, f32
+ * accumulation), 0 if they use the CUDA-core batched kernels (exact f32
+ * arithmetic; shapes where H, I or I_shared is not a multiple of 128, or
+ * max_tokens == 1).  NULL -> 0. */
+int32_t moe_uses_tensor_cores(const moe_handle *h);
+
 /*
  * Timeline of the last T == 1 call on a handle created with MOE_FLAG_TRACE
  * (decode kernel only; a diagnostic of this library, not a step of the

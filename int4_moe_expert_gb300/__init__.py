@@ -18,7 +18,7 @@ __all__ = [
     "lib", "library_path", "moe_init", "moe_forward", "moe_forward_debug", "moe_forward_host",
     "moe_destroy", "moe_last_error", "moe_workspace_bytes", "moe_abi_version",
     "moe_profile_start", "moe_profile_read", "moe_route_noalloc", "moe_device_error",
-    "moe_uses_streaming_decode",
+    "moe_uses_streaming_decode", "moe_uses_tensor_cores",
 ]
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_CUDA, MOE_ERR_NOMEM, MOE_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
@@ -87,6 +87,8 @@ def lib():
         L.moe_device_error.restype = C.c_int
         L.moe_uses_streaming_decode.argtypes = [vp]
         L.moe_uses_streaming_decode.restype = i32
+        L.moe_uses_tensor_cores.argtypes = [vp]
+        L.moe_uses_tensor_cores.restype = i32
         L.moe_route_noalloc.argtypes = [C.POINTER(MoeConfig), vp, vp, vp, i32, vp, vp, vp]
         L.moe_route_noalloc.restype = C.c_int
         L.moe_trace_read.argtypes = [vp, vp, i32, C.POINTER(i32)]
@@ -191,6 +193,10 @@ def moe_device_error(handle: int) -> int:
 
 def moe_uses_streaming_decode(handle: int) -> bool:
     return bool(lib().moe_uses_streaming_decode(handle))
+
+
+def moe_uses_tensor_cores(handle: int) -> bool:
+    return bool(lib().moe_uses_tensor_cores(handle))
 
 
 def moe_destroy(handle: int) -> None:

@@ -340,6 +340,8 @@ moe_status moe_device_error(moe_handle *h, uint32_t *flags) {
 
 int32_t moe_uses_streaming_decode(const moe_handle *h) { return h ? h->p.d.fast_decode : 0; }
 
+int32_t moe_uses_tensor_cores(const moe_handle *h) { return h ? h->p.d.mma : 0; }
+
 moe_status moe_trace_read(moe_handle *h, uint64_t *out, int32_t capacity_blocks, int32_t *n_blocks) {
     if (!h || !out || !n_blocks || capacity_blocks < 0) return fail(MOE_ERR_INVALID, "NULL argument or negative capacity");
     if (!h->p.d.trace || !h->p.d.fast_decode)

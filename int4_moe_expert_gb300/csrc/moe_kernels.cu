@@ -477,8 +477,11 @@ __global__ void __launch_bounds__(kThreads) router_decode_kernel(Params p, const
 __global__ void __launch_bounds__(kThreads) router_tiled_kernel(Params p, const float *__restrict__ x,
                                                                 int T, int buckets) {
     extern __shared__ float smem[];
-    __shared__ float Ws[32][33];
-    __shared__ float Xs[32][33];
+    // k-tiles of 32, transposed in shared memory ([k][row], rows padded to 34 floats so the
+    // 8-byte reads are aligned), double-buffered: the next tile's global loads are in
+    // flight while this one is used
+    __shared__ __align__(16) float Wt[2][32][34];
+    __shared__ __align__(16) float Xt[2][32][34];
     __shared__ float s_r[32];
     const int H = p.d.H, E = p.d.E;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -486,27 +489,44 @@ __global__ void __launch_bounds__(kThreads) router_tiled_kernel(Params p, const 
     const int ty = tid >> 4, tx = tid & 15;
     float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
     float ss[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int k0 = 0; k0 < H; k0 += 32) {
+    float wv[4], xv[4];
+    auto load = [&](int k0) {
 #pragma unroll
         for (int i = 0; i < 4; i++) {
             const int row = warp + 8 * i;      // tile row handled by this warp
             const int e = e0 + row, t = t0 + row;
-            Ws[row][lane] = e < E ? __ldg(p.router_w + (size_t)e * H + k0 + lane) : 0.0f;
-            const float xv = t < T ? __ldg(x + (size_t)t * H + k0 + lane) : 0.0f;
-            Xs[row][lane] = xv;
-            ss[i] = fmaf(xv, xv, ss[i]);
+            wv[i] = e < E ? __ldg(p.router_w + (size_t)e * H + k0 + lane) : 0.0f;
+            xv[i] = t < T ? __ldg(x + (size_t)t * H + k0 + lane) : 0.0f;
         }
-        __syncthreads();
+    };
+    auto store = [&](int buf) {
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const int row = warp + 8 * i;
+            Wt[buf][lane][row] = wv[i];
+            Xt[buf][lane][row] = xv[i];
+            ss[i] = fmaf(xv[i], xv[i], ss[i]);
+        }
+    };
+    load(0);
+    store(0);
+    __syncthreads();
+    int cur = 0;
+    for (int k0 = 0; k0 < H; k0 += 32) {
+        const bool more = k0 + 32 < H;
+        if (more) load(k0 + 32);
 #pragma unroll 8
         for (int kk = 0; kk < 32; kk++) {
-            const float a0 = Ws[ty * 2][kk], a1 = Ws[ty * 2 + 1][kk];
-            const float b0 = Xs[tx * 2][kk], b1 = Xs[tx * 2 + 1][kk];
-            acc[0][0] = fmaf(a0, b0, acc[0][0]);
-            acc[0][1] = fmaf(a0, b1, acc[0][1]);
-            acc[1][0] = fmaf(a1, b0, acc[1][0]);
-            acc[1][1] = fmaf(a1, b1, acc[1][1]);
+            const float2 a = *reinterpret_cast<const float2 *>(&Wt[cur][kk][ty * 2]);
+            const float2 b = *reinterpret_cast<const float2 *>(&Xt[cur][kk][tx * 2]);
+            acc[0][0] = fmaf(a.x, b.x, acc[0][0]);
+            acc[0][1] = fmaf(a.x, b.y, acc[0][1]);
+            acc[1][0] = fmaf(a.y, b.x, acc[1][0]);
+            acc[1][1] = fmaf(a.y, b.y, acc[1][1]);
         }
+        if (more) store(cur ^ 1);
         __syncthreads();
+        cur ^= 1;
     }
 #pragma unroll
     for (int i = 0; i < 4; i++) {

@@ -111,6 +111,22 @@ def test_batched_small_configs_ragged(moe, name, T):
     run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=100 + T), f"{name} T={T}")
 
 
+def test_tensor_core_path_selection(moe):
+    """T > 1 runs on the tensor cores exactly when H, I and I_shared are multiples of 128."""
+    for name, want in (("tiny", True), ("olmoe", True)):
+        wl, li, layer = layer_for(moe, name, 64)
+        assert moe.moe_uses_tensor_cores(layer.handle) == want, name
+    wl = small_workload()                      # H = 64: the CUDA-core batched kernels
+    li = synth.layer_inputs(wl)
+    layer = upload(moe, wl, li, 4)
+    assert not moe.moe_uses_tensor_cores(layer.handle)
+    layer.close()
+    wl, li, _ = layer_for(moe, "tiny", 64)
+    single = upload(moe, wl, li, 1)            # max_tokens == 1: no T > 1 calls possible
+    assert not moe.moe_uses_tensor_cores(single.handle)
+    single.close()
+
+
 def test_batched_glm_512_sampled(moe):
     """Full-size batched layer: all 512 routing decisions, outputs on a sample."""
     wl, li, layer = layer_for(moe, "glm_batched", 512)
