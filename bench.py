@@ -270,7 +270,9 @@ def run_ours(args, rank, world, local_rank, dist_on):
     # One cooperative launch per step on the decode path (the step events
     # bracket exactly that kernel); otherwise router, gate/up, down (+ combine).
     fused = T == 1 and moe.moe_uses_streaming_decode(layer.handle)
-    kernels_per_step = 1 if fused else (3 if T == 1 else 4)
+    # launches per step: the fused kernel; or router, gate/up, down; or router (+ activation
+    # conversion when T > 8), gate/up, down, combine
+    kernels_per_step = 1 if fused else (3 if T == 1 else (4 if T <= 8 else 5))
     stage_ms, n_calls, event_ms = None, 0, 0.0
     if not fused:
         # Per-kernel times: the same steps again with the library recording an

@@ -27,6 +27,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kGemvMaxT = 8;       // router GEMV handles up to this many tokens
+constexpr int kRouterBlocks = 456;  // tiled router: aim for ~3 blocks per SM (split-K over H)
 
 // ---------------------------------------------------------------------------
 // Layout helpers
@@ -508,12 +509,15 @@ __global__ void __launch_bounds__(kThreads) router_tiled_kernel(Params p, const 
             ss[i] = fmaf(xv[i], xv[i], ss[i]);
         }
     };
-    load(0);
+    // this block's share of the reduction (split-K over gridDim.z, whole k-tiles)
+    const int nk = H / 32, z = blockIdx.z, S = gridDim.z;
+    const int kbeg = (int)((long)z * nk / S) * 32, kend = (int)((long)(z + 1) * nk / S) * 32;
+    load(kbeg);
     store(0);
     __syncthreads();
     int cur = 0;
-    for (int k0 = 0; k0 < H; k0 += 32) {
-        const bool more = k0 + 32 < H;
+    for (int k0 = kbeg; k0 < kend; k0 += 32) {
+        const bool more = k0 + 32 < kend;
         if (more) load(k0 + 32);
 #pragma unroll 8
         for (int kk = 0; kk < 32; kk++) {
@@ -528,40 +532,52 @@ __global__ void __launch_bounds__(kThreads) router_tiled_kernel(Params p, const 
         __syncthreads();
         cur ^= 1;
     }
+    // partial sums of this k-range: logits [z][t][e] and sums of squares [z][t]
 #pragma unroll
     for (int i = 0; i < 4; i++) {
-        const float s = warp_sum(ss[i]);
-        if (lane == 0)
-            s_r[warp + 8 * i] = p.d.prenorm ? 1.0f / sqrtf(s / (float)H + p.d.eps) : 1.0f;
+        const float sq = warp_sum(ss[i]);
+        const int t = t0 + warp + 8 * i;
+        if (lane == 0 && blockIdx.x == 0 && t < T) p.ws.sspart[(size_t)z * T + t] = sq;
     }
-    __syncthreads();
 #pragma unroll
     for (int a = 0; a < 2; a++)
 #pragma unroll
         for (int b = 0; b < 2; b++) {
-            const int e = e0 + ty * 2 + a, tl = tx * 2 + b, t = t0 + tl;
-            if (e < E && t < T) p.ws.logits[(size_t)t * E + e] = acc[a][b] * s_r[tl];
+            const int e = e0 + ty * 2 + a, t = t0 + tx * 2 + b;
+            if (e < E && t < T) p.ws.lpart[((size_t)z * T + t) * E + e] = acc[a][b];
         }
-    if (blockIdx.x == 0) {
-        for (int tl = warp; tl < 32 && t0 + tl < T; tl += kWarps) {
-            const int t = t0 + tl;
-            if (lane == 0) p.ws.rnorm[t] = s_r[tl];
-            for (int i = lane; i < H; i += 32) {
-                const float v = x[(size_t)t * H + i] * s_r[tl];
-                p.ws.xperm[(size_t)t * H + perm_pos(i, H)] = v;
-                if (p.d.mma) p.ws.x16[(size_t)t * H + mma_pos(i)] = f2h_bits(v);
-            }
-        }
-    }
-    // two-level tail: the last block of this 32-token group picks the group's top K; the
-    // last group to finish builds the buckets
+    // two-level tail: the last block of this 32-token group adds the partials (z ascending),
+    // scales by 1/rms, and picks the group's top K; the last group builds the buckets
     __shared__ int s_last;
     __threadfence();
     __syncthreads();
-    if (tid == 0) s_last = atomicAdd(p.ws.gcount + blockIdx.y, 1u) == gridDim.x - 1;
+    if (tid == 0) s_last = atomicAdd(p.ws.gcount + blockIdx.y, 1u) == gridDim.x * gridDim.z - 1;
     __syncthreads();
     if (!s_last) return;
     __threadfence();
+    if (tid < 32 && t0 + tid < T) {
+        float sq = 0.0f;
+        for (int k = 0; k < S; k++) sq += __ldcg(p.ws.sspart + (size_t)k * T + t0 + tid);
+        const float r = p.d.prenorm ? 1.0f / sqrtf(sq / (float)H + p.d.eps) : 1.0f;
+        s_r[tid] = r;
+        p.ws.rnorm[t0 + tid] = r;
+    }
+    __syncthreads();
+    for (int i = tid; i < 32 * E; i += kThreads) {
+        const int tl = i / E, e = i - tl * E, t = t0 + tl;
+        if (t < T) {
+            float pv[kRouterMaxSplit];
+#pragma unroll
+            for (int k = 0; k < kRouterMaxSplit; k++)
+                pv[k] = k < S ? __ldcg(p.ws.lpart + ((size_t)k * T + t) * E + e) : 0.0f;
+            float v = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kRouterMaxSplit; k++)
+                if (k < S) v += pv[k];
+            p.ws.logits[(size_t)t * E + e] = v * s_r[tl];
+        }
+    }
+    __syncthreads();
     topk_phase(p, t0, min(T, t0 + 32), smem);
     __threadfence();
     __syncthreads();
@@ -574,6 +590,31 @@ __global__ void __launch_bounds__(kThreads) router_tiled_kernel(Params p, const 
     __threadfence();
     if (buckets) bucket_phase(p, T, reinterpret_cast<int *>(smem));
     if (tid == 0) *p.ws.counters = 0u;
+}
+
+// Activations of a T > kGemvMaxT call for the expert kernels, x_t / rms_t: f16 in mma order
+// (tensor-core path) or f32 chunk-permuted (CUDA-core path); 8 elements per thread.
+__global__ void __launch_bounds__(kThreads) act_convert_kernel(Params p, const float *__restrict__ x, int T) {
+    const int H = p.d.H;
+    const size_t n8 = (size_t)T * H / 8;
+    for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < n8; i += (size_t)gridDim.x * kThreads) {
+        const int t = (int)(i * 8 / H), c = (int)(i * 8 - (size_t)t * H);
+        const float r = p.ws.rnorm[t];
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + c));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + c) + 1);
+        const float v[8] = {a.x * r, a.y * r, a.z * r, a.w * r, b.x * r, b.y * r, b.z * r, b.w * r};
+        if (p.d.mma) {       // group order 0 4 1 5 2 6 3 7
+            uint4 o;
+            o.x = (uint32_t)f2h_bits(v[0]) | ((uint32_t)f2h_bits(v[4]) << 16);
+            o.y = (uint32_t)f2h_bits(v[1]) | ((uint32_t)f2h_bits(v[5]) << 16);
+            o.z = (uint32_t)f2h_bits(v[2]) | ((uint32_t)f2h_bits(v[6]) << 16);
+            o.w = (uint32_t)f2h_bits(v[3]) | ((uint32_t)f2h_bits(v[7]) << 16);
+            *reinterpret_cast<uint4 *>(p.ws.x16 + (size_t)t * H + c) = o;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; j++) p.ws.xperm[(size_t)t * H + perm_pos(c + j, H)] = v[j];
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1155,6 +1196,9 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
         take(mma ? 2 * (size_t)max_items((int)T, d.K, d.E, d.n_shared) * sizeof(int) : 0));
     ws->n_items = reinterpret_cast<int *>(take(sizeof(int)));
     ws->gcount = reinterpret_cast<unsigned *>(take((T + 31) / 32 * sizeof(unsigned)));
+    const bool tiled = T > (size_t)kGemvMaxT;
+    ws->lpart = reinterpret_cast<float *>(take(tiled ? kRouterMaxSplit * T * d.E * sizeof(float) : 0));
+    ws->sspart = reinterpret_cast<float *>(take(tiled ? kRouterMaxSplit * T * sizeof(float) : 0));
     ws->total_bytes = o;
 }
 
@@ -1199,8 +1243,16 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
         const int grid = (d.E + kWarps - 1) / kWarps;
         router_gemv_kernel<<<grid, kThreads, smem, st>>>(p, x, T, buckets);
     } else {
-        const dim3 grid((d.E + 31) / 32, (T + 31) / 32);
+        const int bxy = ((d.E + 31) / 32) * ((T + 31) / 32);
+        int S = (kRouterBlocks + bxy - 1) / bxy;
+        S = S < 1 ? 1 : (S > kRouterMaxSplit ? kRouterMaxSplit : S);
+        S = S > d.H / 32 ? d.H / 32 : S;
+        const dim3 grid((d.E + 31) / 32, (T + 31) / 32, S);
         router_tiled_kernel<<<grid, kThreads, smem, st>>>(p, x, T, buckets);
+        check();
+        const size_t n8 = (size_t)T * d.H / 8;
+        const int cb = (int)((n8 + kThreads - 1) / kThreads < 4096 ? (n8 + kThreads - 1) / kThreads : 4096);
+        act_convert_kernel<<<cb, kThreads, 0, st>>>(p, x, T);
     }
     check();
     mark(1);
