@@ -36,7 +36,11 @@ class Cfg(C.Structure):
     _fields_ = [("H", C.c_int), ("E", C.c_int), ("K", C.c_int), ("I", C.c_int),
                 ("n_shared", C.c_int), ("I_shared", C.c_int), ("n_group", C.c_int),
                 ("norm_topk", C.c_int), ("prenorm_residual", C.c_int),
-                ("routed_scale", C.c_double), ("rms_eps", C.c_double)]
+                ("routed_scale", C.c_double), ("rms_eps", C.c_double),
+                ("topk_group", C.c_int), ("score_func", C.c_int)]
+
+
+SCORE_SIGMOID, SCORE_SOFTMAX = 0, 1
 
 
 class Layer(C.Structure):
@@ -75,14 +79,16 @@ def _p(a: np.ndarray | None):
 
 
 def make_cfg(H, E, K, I, n_shared=0, I_shared=0, routed_scale=1.0, norm_topk=1,
-             prenorm_residual=0, rms_eps=1e-5, n_group=1) -> Cfg:
+             prenorm_residual=0, rms_eps=1e-5, n_group=1, topk_group=1,
+             score_func=SCORE_SIGMOID) -> Cfg:
     return Cfg(H, E, K, I, n_shared, I_shared, n_group, norm_topk, prenorm_residual,
-               float(routed_scale), float(rms_eps))
+               float(routed_scale), float(rms_eps), topk_group, score_func)
 
 
 def cfg_from_workload(wl) -> Cfg:
     return make_cfg(wl.H, wl.E, wl.K, wl.I, wl.n_shared, wl.I_shared, wl.routed_scale,
-                    wl.norm_topk, int(wl.prenorm_residual), wl.rms_eps)
+                    wl.norm_topk, int(wl.prenorm_residual), wl.rms_eps, wl.n_group,
+                    wl.topk_group, wl.score_func)
 
 
 def unpack_int4(row: np.ndarray, n: int) -> np.ndarray:

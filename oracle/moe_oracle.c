@@ -117,10 +117,21 @@ static int by_score_desc(const void *a, const void *b) {
 }
 
 static int cfg_ok(const oracle_cfg *c) {
-    return c && c->H > 0 && c->E > 0 && c->K > 0 && c->K <= c->E && c->I > 0 &&
-           c->n_group == 1 && (c->n_shared == 0 || (c->n_shared == 1 && c->I_shared > 0));
+    if (!c || c->H <= 0 || c->E <= 0 || c->K <= 0 || c->K > c->E || c->I <= 0) return 0;
+    if (!(c->n_shared == 0 || (c->n_shared == 1 && c->I_shared > 0))) return 0;
+    if (c->score_func != ORACLE_SCORE_SIGMOID && c->score_func != ORACLE_SCORE_SOFTMAX) return 0;
+    if (c->n_group < 1 || c->E % c->n_group != 0) return 0;
+    if (c->n_group > 1) {
+        if (c->score_func != ORACLE_SCORE_SIGMOID) return 0;
+        if (c->topk_group < 1 || c->topk_group > c->n_group) return 0;
+        if (c->K > c->topk_group * (c->E / c->n_group)) return 0;
+    }
+    return 1;
 }
 
+/* Per-expert scores.  Sigmoid family: sig = sigmoid(logit), selection score
+ * sig + bias.  Softmax family: sig = softmax(logits) (shifted by the largest
+ * logit), selection score sig; the bias is not used. */
 static void router_scores(const oracle_cfg *c, const float *W, const float *b,
                           const double *x, double *logit, double *sig, double *choice) {
 #pragma omp parallel for schedule(static)
@@ -129,15 +140,58 @@ static void router_scores(const oracle_cfg *c, const float *W, const float *b,
         double acc = 0.0;
         for (int h = 0; h < c->H; h++) acc += (double)wr[h] * x[h];
         logit[e] = acc;
-        sig[e] = 1.0 / (1.0 + exp(-acc));
-        choice[e] = sig[e] + (double)b[e];
+    }
+    if (c->score_func == ORACLE_SCORE_SOFTMAX) {
+        double m = -INFINITY, z = 0.0;
+        for (int e = 0; e < c->E; e++) m = logit[e] > m ? logit[e] : m;
+        for (int e = 0; e < c->E; e++) z += exp(logit[e] - m);
+        for (int e = 0; e < c->E; e++) {
+            sig[e] = exp(logit[e] - m) / z;
+            choice[e] = sig[e];
+        }
+    } else {
+        for (int e = 0; e < c->E; e++) {
+            sig[e] = 1.0 / (1.0 + exp(-logit[e]));
+            choice[e] = sig[e] + (double)b[e];
+        }
     }
 }
 
+/* Group-limited selection (n_group > 1): group g holds experts
+ * [g E/n_group, (g+1) E/n_group); its score is the sum of its two best
+ * selection scores (one when a group has one expert).  The topk_group best
+ * groups are kept (ties: lower group first) and every expert of the other
+ * groups gets -inf.  Returns gs_(topk_group) - gs_(topk_group+1), +inf when
+ * every group is kept. */
+static double mask_groups(const oracle_cfg *c, double *choice) {
+    const int G = c->n_group, m = c->E / c->n_group;
+    if (G <= 1) return INFINITY;
+    scored *gs = (scored *)malloc(sizeof(scored) * G);
+    for (int g = 0; g < G; g++) {
+        double b1 = -INFINITY, b2 = -INFINITY;
+        for (int i = 0; i < m; i++) {
+            const double v = choice[g * m + i];
+            if (v > b1) { b2 = b1; b1 = v; }
+            else if (v > b2) b2 = v;
+        }
+        gs[g].c = m > 1 ? b1 + b2 : b1;
+        gs[g].e = g;
+    }
+    qsort(gs, G, sizeof(scored), by_score_desc);
+    for (int r = c->topk_group; r < G; r++)
+        for (int i = 0; i < m; i++) choice[gs[r].e * m + i] = -INFINITY;
+    const double gm = c->topk_group < G ? gs[c->topk_group - 1].c - gs[c->topk_group].c : INFINITY;
+    free(gs);
+    return gm;
+}
+
+/* Weights of the selection idx[K]: w_k = s * sig_k / (sum_S sig + 1e-20) for the
+ * sigmoid family, s * g_k / sum_S g for the softmax family (norm_topk); s * sig_k
+ * (s * g_k) without renormalisation. */
 static void weights_of(const oracle_cfg *c, const double *sig, const int *idx, double *w) {
     double den = 0.0;
     for (int k = 0; k < c->K; k++) den += sig[idx[k]];
-    den += 1e-20;
+    if (c->score_func == ORACLE_SCORE_SIGMOID) den += 1e-20;
     for (int k = 0; k < c->K; k++)
         w[k] = c->norm_topk ? c->routed_scale * sig[idx[k]] / den
                             : c->routed_scale * sig[idx[k]];
@@ -150,11 +204,15 @@ int oracle_route(const oracle_cfg *c, const float *router_w, const float *router
     double *logit = (double *)malloc(sizeof(double) * 3 * E);
     double *sig = logit + E, *choice = logit + 2 * E;
     router_scores(c, router_w, router_b, x, logit, sig, choice);
+    const double gmargin = mask_groups(c, choice);
     scored *s = (scored *)malloc(sizeof(scored) * E);
     for (int e = 0; e < E; e++) { s[e].c = choice[e]; s[e].e = e; }
     qsort(s, E, sizeof(scored), by_score_desc);
     for (int k = 0; k < K; k++) idx[k] = s[k].e;
-    if (margin) *margin = (K < E) ? s[K - 1].c - s[K].c : INFINITY;
+    if (margin) {
+        double mg = (K < E && s[K].c > -INFINITY) ? s[K - 1].c - s[K].c : INFINITY;
+        *margin = gmargin < mg ? gmargin : mg;
+    }
     if (w) weights_of(c, sig, idx, w);
     if (scores) memcpy(scores, logit, sizeof(double) * 3 * E);
     free(s);
@@ -165,17 +223,15 @@ int oracle_route(const oracle_cfg *c, const float *router_w, const float *router
 int oracle_weights_for(const oracle_cfg *c, const float *router_w, const double *x,
                        const int *idx, double *w) {
     if (!cfg_ok(c)) return -1;
-    double *sig = (double *)malloc(sizeof(double) * c->E);
-    for (int e = 0; e < c->E; e++) {
-        const float *wr = router_w + (int64_t)e * c->H;
-        double acc = 0.0;
-        for (int h = 0; h < c->H; h++) acc += (double)wr[h] * x[h];
-        sig[e] = 1.0 / (1.0 + exp(-acc));
-    }
+    double *logit = (double *)malloc(sizeof(double) * 3 * c->E);
+    double *sig = logit + c->E, *choice = logit + 2 * c->E;
+    float *zero_b = (float *)calloc(c->E, sizeof(float));   /* the bias does not enter weights */
+    router_scores(c, router_w, zero_b, x, logit, sig, choice);
+    free(zero_b);
     for (int k = 0; k < c->K; k++)
-        if (idx[k] < 0 || idx[k] >= c->E) { free(sig); return -1; }
+        if (idx[k] < 0 || idx[k] >= c->E) { free(logit); return -1; }
     weights_of(c, sig, idx, w);
-    free(sig);
+    free(logit);
     return 0;
 }
 

@@ -17,7 +17,13 @@
  *    bytes, pad nibble 8; one float32 scale per output row (".qs").
  *  - same page, section 04 "手写的基础数学": RMSNorm and SiLU.
  *  - Edge0 article (magicnetworld.com), section 七 "路由数学": renormalised
- *    sigmoid weights w_i = s * sigma_i / (sum_{j in S} sigma_j + 1e-20).
+ *    sigmoid weights w_i = s * sigma_i / (sum_{j in S} sigma_j + 1e-20); the
+ *    softmax-top-k family (g = softmax(logits), top-K of g, w_i = g_i / sum_S g)
+ *    and group-limited selection for the sigmoid family (groups ranked by the
+ *    sum of their two best selection scores, the best topk_group kept, the
+ *    rest masked to -inf, then top-K among the survivors).
+ *  - reader.mx page, section 03 (the OLMoE engine's moe()): softmax over the E
+ *    logits, greedy top-K by strict '>', weight = the probability itself.
  *  - GLM-5.2 operator breakdown (devpress.csdn.net), section 2.3 and stage
  *    "Step 6 (MoE)" 6a-6d: output = sum of routed outputs + shared expert.
  *
@@ -41,12 +47,17 @@ typedef struct {
     int I;            /* routed expert intermediate size */
     int n_shared;     /* 0 or 1 */
     int I_shared;     /* shared expert intermediate size */
-    int n_group;      /* expert groups; only 1 is defined here */
-    int norm_topk;    /* 1: renormalise the selected sigmoid weights */
+    int n_group;      /* expert groups (E % n_group == 0); > 1 only with the sigmoid score */
+    int norm_topk;    /* 1: renormalise the selected weights */
     int prenorm_residual; /* 1: y = x + moe(rmsnorm(x)) */
     double routed_scale;
     double rms_eps;
+    int topk_group;   /* groups kept when n_group > 1 (1..n_group) */
+    int score_func;   /* ORACLE_SCORE_SIGMOID or ORACLE_SCORE_SOFTMAX */
 } oracle_cfg;
+
+#define ORACLE_SCORE_SIGMOID 0   /* sigma = sigmoid(logit); selection by sigma + bias */
+#define ORACLE_SCORE_SOFTMAX 1   /* g = softmax(logits); selection by g; bias unused */
 
 typedef struct {
     const float *router_w;            /* [E, H] */
@@ -74,8 +85,10 @@ void oracle_expert(int H, int I, const uint8_t *slab, const float *scale,
 
 /* Router for one token.  Returns 0, or -1 on an invalid config.
  * idx[K] in descending selection-score order, w[K] routing weights,
- * *margin = c_(K) - c_(K+1) (+inf when K == E), scores (nullable) [3*E]:
- * logits | sigmoid | sigmoid + bias. */
+ * *margin = c_(K) - c_(K+1) (+inf when none is left), and with groups the
+ * smaller of that and gs_(topk_group) - gs_(topk_group+1) over the group
+ * scores; scores (nullable) [3*E]: logits | sigmoid (softmax probability) |
+ * selection score (-inf outside the kept groups). */
 int oracle_route(const oracle_cfg *c, const float *router_w, const float *router_b,
                  const double *x, int *idx, double *w, double *margin, double *scores);
 

@@ -161,6 +161,9 @@ class Workload:
     scale_hi: float = 0.02
     norm_topk: int = 1
     rms_eps: float = 1e-5
+    n_group: int = 1        # > 1: group-limited selection (sigmoid family)
+    topk_group: int = 1     # groups kept when n_group > 1
+    score_func: int = 0     # 0 sigmoid (+ bias for selection), 1 softmax
 
     @property
     def slab_bytes(self) -> int:
@@ -202,6 +205,17 @@ WORKLOADS = {
     "glm_batched": Workload("glm_batched", T=512, H=6144, E=256, K=8, I=2048, n_shared=1,
                             I_shared=2048, routed_scale=2.5, seed=4,
                             bias_dist=("normal", 0.0, 0.5)),
+    # routing variants (the router-math section of the Edge0 article; the OLMoE engine of the
+    # reader.mx page): group-limited sigmoid with the 8B tier's routing constants (8 groups,
+    # 4 kept, top-8, scale 2.5) on OLMoE-sized experts plus a shared one
+    "group8": Workload("group8", T=1, H=2048, E=64, K=8, I=1024, n_shared=1, I_shared=1024,
+                       routed_scale=2.5, seed=5, n_group=8, topk_group=4),
+    # softmax top-k renormalised to sum 1 (Qwen family), no shared expert
+    "softmax_renorm": Workload("softmax_renorm", T=1, H=2048, E=128, K=8, I=768, n_shared=0,
+                               I_shared=0, routed_scale=1.0, seed=6, score_func=1),
+    # OLMoE engine: softmax over the E logits, top-8, the probability itself as weight
+    "olmoe_softmax": Workload("olmoe_softmax", T=1, H=2048, E=64, K=8, I=1024, n_shared=0,
+                              I_shared=0, routed_scale=1.0, seed=7, score_func=1, norm_topk=0),
 }
 
 

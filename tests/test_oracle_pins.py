@@ -239,9 +239,112 @@ def test_zero_bias_is_topk_of_logits_and_weights_use_unbiased_sigmoid():
 
 
 def test_invalid_group_config_rejected():
-    cfg = oracle.make_cfg(4, 4, 2, 8, n_group=2)
-    with pytest.raises(ValueError):
-        oracle.route(cfg, np.zeros((4, 4), np.float32), np.zeros(4, np.float32), np.ones(4))
+    W, b, x = np.zeros((8, 4), np.float32), np.zeros(8, np.float32), np.ones(4)
+    for kw in (dict(n_group=3),                          # E not a multiple of n_group
+               dict(n_group=4, topk_group=0),
+               dict(n_group=4, topk_group=5),
+               dict(n_group=4, topk_group=1, K=3),      # K > topk_group * E / n_group
+               dict(n_group=2, topk_group=1, score_func=oracle.SCORE_SOFTMAX),
+               dict(score_func=2)):
+        args = dict(K=2)
+        args.update(kw)
+        K = args.pop("K")
+        cfg = oracle.make_cfg(4, 8, K, 8, **args)
+        with pytest.raises(ValueError):
+            oracle.route(cfg, W, b, x)
+
+
+# --- routing variants (Edge0 section 七; reader.mx section 03, the OLMoE engine) -------
+
+def _route_grouped(bias, K, n_group, topk_group):
+    E, H = len(bias), 4
+    cfg = oracle.make_cfg(H, E, K, 8, routed_scale=1.0, n_group=n_group, topk_group=topk_group)
+    return oracle.route(cfg, np.zeros((E, H), np.float32), np.asarray(bias, np.float32), np.ones(H))
+
+
+def test_group_limited_hand_cases():
+    g = _golden("route_group_limited.txt")
+    w = np.array([float(v) for v in g["w"]])
+    for case in ("a", "b"):
+        bias = [float(v) for v in g[case + "_bias"]]
+        idx, wt, margin, sc = _route_grouped(bias, 3, 4, 2)
+        assert idx.tolist() == [int(v) for v in g[case + "_idx"]], case
+        np.testing.assert_allclose(wt, w, rtol=1e-12)
+        assert margin == pytest.approx(float(g[case + "_margin"][0]), abs=1e-6), case
+        # experts of the dropped groups carry -inf
+        kept = {e // 2 for e in idx.tolist()}
+        assert all((sc[2][e] == -np.inf) == (e // 2 not in kept) for e in range(8)) or case == "b"
+    idx, _, _, _ = _route_grouped([float(v) for v in g["a_bias"]], 3, 1, 1)
+    assert idx.tolist() == [int(v) for v in g["a_idx_ungrouped"]]
+
+
+def test_group_ties_keep_lower_groups():
+    idx, _, margin, _ = _route_grouped([0.1] * 8, 3, 4, 2)
+    assert idx.tolist() == [0, 1, 2] and margin == 0.0
+
+
+def test_grouping_that_keeps_everything_is_plain_topk():
+    rng = np.random.default_rng(21)
+    for _ in range(30):
+        bias = rng.uniform(-0.3, 0.3, 16)
+        ref, wref, _, _ = _route_grouped(bias, 5, 1, 1)
+        for n_group, topk_group in ((4, 4), (16, 16), (16, 5), (16, 7)):
+            # all groups kept; or groups of one expert with at least K kept: the top-K survive
+            idx, w, _, _ = _route_grouped(bias, 5, n_group, topk_group)
+            assert idx.tolist() == ref.tolist() and np.array_equal(w, wref)
+
+
+def _softmax_case(seed, E=24, H=40, K=5):
+    rng = np.random.default_rng(seed)
+    W = rng.normal(0, 0.4, (E, H)).astype(np.float32)
+    x = rng.standard_normal(H)
+    b = rng.uniform(-0.5, 0.5, E).astype(np.float32)
+    return W, b, x, W.astype(np.float64) @ x
+
+
+@pytest.mark.parametrize("norm_topk", [1, 0])
+def test_softmax_topk_matches_scipy_softmax(norm_topk):
+    from scipy.special import softmax
+    for seed in range(10):
+        W, b, x, logits = _softmax_case(seed)
+        E, H, K, s = W.shape[0], W.shape[1], 5, 1.75
+        cfg = oracle.make_cfg(H, E, K, 8, routed_scale=s, norm_topk=norm_topk,
+                              score_func=oracle.SCORE_SOFTMAX)
+        idx, w, margin, sc = oracle.route(cfg, W, b, x)
+        g = softmax(logits)
+        assert margin > 1e-9
+        assert idx.tolist() == np.argsort(-g, kind="stable")[:K].tolist()
+        np.testing.assert_allclose(sc[1], g, rtol=1e-12)
+        want = s * g[idx] / g[idx].sum() if norm_topk else s * g[idx]
+        np.testing.assert_allclose(w, want, rtol=1e-12)
+        # the bias plays no part in the softmax family
+        idx0, w0, _, _ = oracle.route(cfg, W, np.zeros_like(b), x)
+        assert idx0.tolist() == idx.tolist() and np.array_equal(w0, w)
+
+
+def test_softmax_all_selected_weights_sum_to_scale():
+    W, b, x, logits = _softmax_case(3, E=6, K=6)
+    for norm in (1, 0):
+        cfg = oracle.make_cfg(W.shape[1], 6, 6, 8, routed_scale=2.0, norm_topk=norm,
+                              score_func=oracle.SCORE_SOFTMAX)
+        _, w, margin, _ = oracle.route(cfg, W, b, x)
+        assert w.sum() == pytest.approx(2.0, rel=1e-13) and margin == math.inf
+
+
+def test_softmax_is_shift_invariant():
+    # a constant added to every logit (here: a column of W against x_h = 1) changes nothing
+    W, b, x, _ = _softmax_case(5, E=12, H=16, K=3)
+    x = x.copy()
+    x[0] = 1.0
+    W = W.copy()
+    W[:, 0] = 0.0               # so that the shifted column is exact in float32
+    W2 = W.copy()
+    W2[:, 0] = 0.375
+    cfg = oracle.make_cfg(16, 12, 3, 8, routed_scale=1.0, score_func=oracle.SCORE_SOFTMAX)
+    i1, w1, _, _ = oracle.route(cfg, W, b, x)
+    i2, w2, _, _ = oracle.route(cfg, W2, b, x)
+    assert i1.tolist() == i2.tolist()
+    np.testing.assert_allclose(w1, w2, rtol=1e-12)
 
 
 # --- whole layer ---------------------------------------------------------------
