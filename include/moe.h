@@ -17,6 +17,14 @@
  *    score order.
  *  - Renormalisation (Edge0 article, magicnetworld.com, section 七 "路由数学",
  *    sigmoid family): w = s * sigma / (sum_{selected} sigma + 1e-20).
+ *  - Routing variants (same section): group-limited selection for the sigmoid
+ *    family (n_group > 1: groups ranked by the sum of their two best selection
+ *    scores, the best topk_group kept, every expert of the other groups masked
+ *    to -inf before the top-K; a group tie is won by the lower group index);
+ *    the softmax family (score_func = MOE_SCORE_SOFTMAX: g = softmax(logits),
+ *    top-K of g, the bias unused, w = s * g / sum_{selected} g, or s * g
+ *    without renormalisation as in the OLMoE engine of the reader.mx page,
+ *    section 03).
  *  - Expert format (reader.mx page, section 06 "从 FP8 到 int4"): each row of a
  *    matrix [O, n] is ceil(n/2) bytes, element 2j in the low nibble of byte j
  *    and 2j+1 in the high nibble, stored as q+8 with q in [-8, 7]; one float32
@@ -42,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 /* y = x + moe(rmsnorm(x)) instead of y = moe(x). */
 #define MOE_FLAG_PRENORM_RESIDUAL 1u
@@ -65,12 +73,18 @@ typedef struct moe_config {
     int32_t moe_inter;     /* I: multiple of 32, 32..16384 */
     int32_t n_shared;      /* 0 or 1 */
     int32_t shared_inter;  /* I_sh: multiple of 32 when n_shared == 1 */
-    int32_t n_group;       /* must be 1 (group-limited routing is not implemented) */
+    int32_t n_group;       /* expert groups: 1..32, divides n_experts; > 1 only with the sigmoid score */
     int32_t norm_topk;     /* 1: renormalise the selected weights (see above); 0: w = s * sigma */
     float routed_scale;    /* s, routed_scaling_factor */
     float rms_eps;         /* used with MOE_FLAG_PRENORM_RESIDUAL */
     uint32_t flags;        /* MOE_FLAG_* */
+    int32_t topk_group;    /* groups kept when n_group > 1: 1..n_group, with
+                              top_k <= topk_group * n_experts / n_group; ignored when n_group == 1 */
+    int32_t score_func;    /* MOE_SCORE_SIGMOID (0) or MOE_SCORE_SOFTMAX (1) */
 } moe_config;
+
+#define MOE_SCORE_SIGMOID 0   /* sigma = sigmoid(logit), selection by sigma + bias */
+#define MOE_SCORE_SOFTMAX 1   /* g = softmax(logits), selection by g, bias unused */
 
 /*
  * Weights are BORROWED device pointers: the caller allocates them, keeps them
@@ -151,7 +165,8 @@ moe_status moe_device_error(moe_handle *h, uint32_t *flags);
  * (a cooperative launch; weights streamed from HBM into registers;
  * fixed-point activations and dp4a), 0 if they use the generic kernels
  * (shapes outside its limits: H, I multiples of 32, I == I_shared,
- * I <= 2048, H <= 8192, E <= 1024, K + n_shared <= 32). */
+ * I <= 2048, H <= 8192, E <= 1024, K + n_shared <= 32; and the routing
+ * variants: n_group > 1 or the softmax score). */
 int32_t moe_uses_streaming_decode(const moe_handle *h);
 
 /* 1 if T > 1 calls on this handle run the experts on the tensor cores

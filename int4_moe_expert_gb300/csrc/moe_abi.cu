@@ -60,8 +60,18 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
         (c->shared_inter < 32 || c->shared_inter > 16384 || c->shared_inter % 32))
         return fail(MOE_ERR_UNSUPPORTED, "shared_inter=%d: need a multiple of 32 in [32, 16384]",
                     c->shared_inter);
-    if (c->n_group != 1)
-        return fail(MOE_ERR_UNSUPPORTED, "n_group=%d: only n_group == 1 is implemented", c->n_group);
+    if (c->score_func != MOE_SCORE_SIGMOID && c->score_func != MOE_SCORE_SOFTMAX)
+        return fail(MOE_ERR_INVALID, "score_func=%d: need MOE_SCORE_SIGMOID or MOE_SCORE_SOFTMAX", c->score_func);
+    if (c->n_group < 1 || c->n_group > 32 || c->n_experts % c->n_group)
+        return fail(MOE_ERR_INVALID, "n_group=%d: need 1..32 dividing n_experts", c->n_group);
+    if (c->n_group > 1) {
+        if (c->score_func != MOE_SCORE_SIGMOID)
+            return fail(MOE_ERR_INVALID, "n_group > 1 needs the sigmoid score");
+        if (c->topk_group < 1 || c->topk_group > c->n_group)
+            return fail(MOE_ERR_INVALID, "topk_group=%d: need 1..n_group", c->topk_group);
+        if (c->top_k > c->topk_group * (c->n_experts / c->n_group))
+            return fail(MOE_ERR_INVALID, "top_k=%d exceeds the experts of the kept groups", c->top_k);
+    }
     if (c->norm_topk != 0 && c->norm_topk != 1)
         return fail(MOE_ERR_INVALID, "norm_topk=%d: need 0 or 1", c->norm_topk);
     if (!isfinite(c->routed_scale)) return fail(MOE_ERR_INVALID, "routed_scale is not finite");
@@ -79,6 +89,9 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
     d->I_sh = c->n_shared ? c->shared_inter : 0;
     d->I_max = d->I > d->I_sh ? d->I : d->I_sh;
     d->norm_topk = c->norm_topk;
+    d->n_group = c->n_group;
+    d->topk_group = c->n_group > 1 ? c->topk_group : 1;
+    d->score_func = c->score_func;
     d->prenorm = (c->flags & MOE_FLAG_PRENORM_RESIDUAL) ? 1 : 0;
     d->scale = c->routed_scale;
     d->eps = c->rms_eps;

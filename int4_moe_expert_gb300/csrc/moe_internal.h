@@ -14,6 +14,8 @@ struct Dims {
     int H, E, K, I, n_shared, I_sh;
     int I_max;          // max(I, I_sh)
     int norm_topk;
+    int n_group, topk_group;   // group-limited selection when n_group > 1
+    int score_func;     // MOE_SCORE_SIGMOID / MOE_SCORE_SOFTMAX
     int prenorm;        // MOE_FLAG_PRENORM_RESIDUAL
     float scale;        // routed_scale
     float eps;          // rms_eps

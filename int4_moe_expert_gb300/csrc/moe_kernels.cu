@@ -128,34 +128,93 @@ __device__ __forceinline__ bool ranks_before(float v, int e, float bv, int be) {
 
 // Top-K for tokens [t_begin, t_end): one warp per token.  Scores live in shared memory
 // (sig and choice, E floats per warp).  NaN scores rank last, so an index in
-// [0, E) is always produced.
+// [0, E) is always produced.  Sigmoid family: sig = sigmoid(logit), choice =
+// sig + bias, then (n_group > 1) the experts of all but the topk_group best
+// groups are masked to -inf, a group's score being the sum of its two best
+// choices.  Softmax family: sig = choice = softmax(logits).
 __device__ void topk_phase(const Params &p, int t_begin, int t_end, float *smem) {
     const int E = p.d.E, K = p.d.K;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool softmax = p.d.score_func == MOE_SCORE_SOFTMAX;
     float *sig = smem + warp * 2 * E;
     float *choice = sig + E;
     for (int t = t_begin + warp; t < t_end; t += kWarps) {
+        float lmax = -INFINITY;
         for (int base = 0; base < E; base += 256) {     // loads issued 8 at a time
             float lv[8], bv8[8];
 #pragma unroll
             for (int i = 0; i < 8; i++) {
                 const int e = base + lane + 32 * i;
                 lv[i] = e < E ? __ldcg(p.ws.logits + (size_t)t * E + e) : 0.0f;
-                bv8[i] = e < E ? p.router_b[e] : 0.0f;
+                bv8[i] = e < E && !softmax ? p.router_b[e] : 0.0f;
             }
 #pragma unroll
             for (int i = 0; i < 8; i++) {
                 const int e = base + lane + 32 * i;
                 if (e < E) {
-                    const float s = 1.0f / (1.0f + expf(-lv[i]));
-                    float c = s + bv8[i];
-                    if (isnan(c)) c = -INFINITY;
-                    sig[e] = s;
-                    choice[e] = c;
+                    if (softmax) {
+                        sig[e] = lv[i];
+                        lmax = fmaxf(lmax, lv[i]);
+                    } else {
+                        const float s = 1.0f / (1.0f + expf(-lv[i]));
+                        float c = s + bv8[i];
+                        if (isnan(c)) c = -INFINITY;
+                        sig[e] = s;
+                        choice[e] = c;
+                    }
                 }
             }
         }
+        if (softmax) {     // g = exp(l - max) / sum exp(l - max)
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, o));
+            float z = 0.0f;
+            for (int e = lane; e < E; e += 32) {
+                const float v = expf(sig[e] - lmax);
+                sig[e] = v;
+                z += v;
+            }
+            z = warp_sum(z);
+            for (int e = lane; e < E; e += 32) {
+                const float g = sig[e] / z;
+                sig[e] = g;
+                choice[e] = isnan(g) ? -INFINITY : g;
+            }
+        }
         __syncwarp();
+        if (p.d.n_group > 1) {
+            // group `lane` (lane < n_group): the sum of its two best choices
+            const int G = p.d.n_group, m = E / G;
+            float gsc = -INFINITY;
+            if (lane < G) {
+                float b1 = -INFINITY, b2 = -INFINITY;
+                for (int i = 0; i < m; i++) {
+                    const float v = choice[lane * m + i];
+                    if (v > b1) { b2 = b1; b1 = v; }
+                    else if (v > b2) b2 = v;
+                }
+                gsc = m > 1 ? b1 + b2 : b1;
+            }
+            // keep the topk_group best groups (a tie goes to the lower group)
+            uint32_t keep = 0u;
+            bool taken = false;
+            for (int r = 0; r < p.d.topk_group; r++) {
+                float bv = taken ? -INFINITY : gsc;
+                int be = (lane < G && !taken) ? lane : 0x7fffffff;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                    const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                    if (ranks_before(ov, oe, bv, be)) { bv = ov; be = oe; }
+                }
+                keep |= 1u << be;
+                if (lane == be) taken = true;
+            }
+            __syncwarp();
+            for (int e = lane; e < E; e += 32)
+                if (!((keep >> (e / m)) & 1u)) choice[e] = -INFINITY;
+            __syncwarp();
+        }
         uint32_t taken = 0;       // bit i: expert lane + 32 i already chosen
         float sum_sig = 0.0f, my_sig = 0.0f;
         int my_e = 0;
@@ -181,7 +240,7 @@ __device__ void topk_phase(const Params &p, int t_begin, int t_end, float *smem)
         }
         // lane kk holds choice kk (K <= 32)
         if (lane < K) {
-            const float den = sum_sig + 1e-20f;
+            const float den = softmax ? sum_sig : sum_sig + 1e-20f;
             p.ws.topk_idx[(size_t)t * K + lane] = my_e;
             p.ws.topk_w[(size_t)t * K + lane] = p.d.norm_topk ? p.d.scale * my_sig / den : p.d.scale * my_sig;
         }
@@ -363,114 +422,6 @@ __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
     acc = fmaf(a.y, b.y, acc);
     acc = fmaf(a.z, b.z, acc);
     return fmaf(a.w, b.w, acc);
-}
-
-// Top-K for one token from per-expert (sigmoid, selection score) pairs in
-// ws.dscore, by one warp: every lane loads its experts e = lane + 32 i at once
-// and the K argmax rounds run on registers.  Lane k then writes choice k.
-__device__ void topk_decode_warp(const Params &p, int lane) {
-    const int E = p.d.E, K = p.d.K;
-    constexpr int kPer = 32;                       // E <= 1024
-    float c[kPer], sg[kPer];
-#pragma unroll
-    for (int i = 0; i < kPer; i++) {
-        const int e = lane + 32 * i;
-        sg[i] = e < E ? __ldcg(p.ws.dscore + e) : 0.0f;
-        c[i] = e < E ? __ldcg(p.ws.dscore + E + e) : -INFINITY;
-    }
-    uint32_t taken = 0;
-    float sum_sig = 0.0f, my_sig = 0.0f;
-    int my_e = 0;
-    for (int kk = 0; kk < K; kk++) {
-        float bv = -INFINITY, bs = 0.0f;
-        int be = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < kPer; i++) {
-            const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u) && ranks_before(c[i], e, bv, be)) { bv = c[i]; be = e; bs = sg[i]; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-            const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-            if (ranks_before(ov, oe, bv, be)) { bv = ov; be = oe; bs = os; }
-        }
-        if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        sum_sig += bs;
-        if (lane == kk) { my_e = be; my_sig = bs; }
-    }
-    if (lane < K) {
-        const float den = sum_sig + 1e-20f;
-        p.ws.topk_idx[lane] = my_e;
-        p.ws.topk_w[lane] = p.d.norm_topk ? p.d.scale * my_sig / den : p.d.scale * my_sig;
-    }
-}
-
-// Router for one token on the streaming decode path: two expert rows per
-// block, each row split over all threads, so ~E/2 blocks keep enough loads
-// in flight.  Each block turns its logits into (sigmoid, sigmoid + bias); the
-// last block to finish picks the top K.  It lets the dependent gate/up grid
-// launch at once; that grid waits for this one before it reads the routing.
-__global__ void __launch_bounds__(kThreads) router_decode_kernel(Params p, const float *__restrict__ x,
-                                                                 int buckets) {
-    extern __shared__ float smem[];
-    __shared__ float s_part[kWarps][3];
-    __shared__ int s_last;
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int H = p.d.H, E = p.d.E, H4 = H / 4;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int e0 = blockIdx.x * 2;
-    const bool has1 = e0 + 1 < E;
-    const float4 *x4 = reinterpret_cast<const float4 *>(x);
-    const float4 *w0 = reinterpret_cast<const float4 *>(p.router_w + (size_t)e0 * H);
-    const float4 *w1 = reinterpret_cast<const float4 *>(p.router_w + (size_t)(has1 ? e0 + 1 : e0) * H);
-    const float b0 = p.router_b[e0], b1 = p.router_b[has1 ? e0 + 1 : e0];
-    float a0 = 0.0f, a1 = 0.0f, ss = 0.0f;
-#pragma unroll 8
-    for (int i = tid; i < H4; i += kThreads) {
-        const float4 xv = __ldg(x4 + i);
-        a0 = dot4(__ldg(w0 + i), xv, a0);
-        a1 = dot4(__ldg(w1 + i), xv, a1);
-        ss = dot4(xv, xv, ss);
-    }
-    a0 = warp_sum(a0);
-    a1 = warp_sum(a1);
-    ss = warp_sum(ss);
-    if (lane == 0) {
-        s_part[warp][0] = a0;
-        s_part[warp][1] = a1;
-        s_part[warp][2] = ss;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        float A0 = 0.0f, A1 = 0.0f, S = 0.0f;
-        for (int w = 0; w < kWarps; w++) { A0 += s_part[w][0]; A1 += s_part[w][1]; S += s_part[w][2]; }
-        const float r = p.d.prenorm ? 1.0f / sqrtf(S / (float)H + p.d.eps) : 1.0f;
-        const float l0 = A0 * r, l1 = A1 * r;
-        const float s0 = 1.0f / (1.0f + expf(-l0)), s1 = 1.0f / (1.0f + expf(-l1));
-        float c0 = s0 + b0, c1 = s1 + b1;
-        if (isnan(c0)) c0 = -INFINITY;
-        if (isnan(c1)) c1 = -INFINITY;
-        p.ws.logits[e0] = l0;
-        p.ws.dscore[e0] = s0;
-        p.ws.dscore[E + e0] = c0;
-        if (has1) {
-            p.ws.logits[e0 + 1] = l1;
-            p.ws.dscore[e0 + 1] = s1;
-            p.ws.dscore[E + e0 + 1] = c1;
-        }
-        if (blockIdx.x == 0) p.ws.rnorm[0] = r;
-        __threadfence();
-        s_last = (atomicAdd(p.ws.counters, 1u) == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (warp == 0) topk_decode_warp(p, lane);
-    __syncthreads();
-    if (buckets) bucket_phase(p, 1, reinterpret_cast<int *>(smem));
-    if (tid == 0) *p.ws.counters = 0u;
 }
 
 // Router for larger T: a 32 (experts) x 32 (tokens) tile per block, k-loop
@@ -1215,8 +1166,6 @@ cudaError_t prepare_kernels(const Dims &d) {
     cudaError_t e = cudaFuncSetAttribute(router_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(router_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(router_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess && d.mma)
         e = cudaFuncSetAttribute(mma_expert_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmaSmem);
     if (e == cudaSuccess && d.mma)
@@ -1392,7 +1341,12 @@ extern "C" moe_status moe_route_noalloc(const moe_config *cfg, const float *rout
     if (cfg->hidden < 32 || cfg->hidden > 16384 || cfg->hidden % 32) return MOE_ERR_UNSUPPORTED;
     if (cfg->n_experts < 1 || cfg->n_experts > MOE_ROUTE_NOALLOC_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED;
     if (cfg->top_k < 1 || cfg->top_k > cfg->n_experts || cfg->top_k > 32) return MOE_ERR_INVALID;
-    if (cfg->n_group != 1) return MOE_ERR_UNSUPPORTED;
+    if (cfg->score_func != MOE_SCORE_SIGMOID && cfg->score_func != MOE_SCORE_SOFTMAX) return MOE_ERR_INVALID;
+    if (cfg->n_group < 1 || cfg->n_group > 32 || cfg->n_experts % cfg->n_group) return MOE_ERR_INVALID;
+    if (cfg->n_group > 1 && (cfg->score_func != MOE_SCORE_SIGMOID || cfg->topk_group < 1 ||
+                             cfg->topk_group > cfg->n_group ||
+                             cfg->top_k > cfg->topk_group * (cfg->n_experts / cfg->n_group)))
+        return MOE_ERR_INVALID;
     if (cfg->norm_topk != 0 && cfg->norm_topk != 1) return MOE_ERR_INVALID;
     if (T < 0 || T > MOE_ROUTE_NOALLOC_MAX_TOKENS) return MOE_ERR_INVALID;
     if ((reinterpret_cast<uintptr_t>(router_w) | reinterpret_cast<uintptr_t>(x)) & 15u) return MOE_ERR_INVALID;
@@ -1404,6 +1358,9 @@ extern "C" moe_status moe_route_noalloc(const moe_config *cfg, const float *rout
     d.E = cfg->n_experts;
     d.K = cfg->top_k;
     d.norm_topk = cfg->norm_topk;
+    d.n_group = cfg->n_group;
+    d.topk_group = cfg->n_group > 1 ? cfg->topk_group : 1;
+    d.score_func = cfg->score_func;
     d.prenorm = (cfg->flags & MOE_FLAG_PRENORM_RESIDUAL) ? 1 : 0;
     d.scale = cfg->routed_scale;
     d.eps = cfg->rms_eps;

@@ -37,8 +37,8 @@ def test_library_exports_every_declared_symbol(moe):
 
 
 def test_config_struct_layout_matches_header(moe):
-    # eleven 4-byte fields, no padding
-    assert C.sizeof(moe.MoeConfig) == 44
+    # thirteen 4-byte fields, no padding
+    assert C.sizeof(moe.MoeConfig) == 52
     assert C.sizeof(moe.MoeWeights) == 6 * C.sizeof(C.c_void_p)
 
 
@@ -54,7 +54,14 @@ def test_workspace_bytes_validates_config(moe):
         moe.make_config(6144, 256, 8, 2000, 1, 2048),        # I not a multiple of 32
         moe.make_config(6144, 256, 8, 2048, 1, 100),         # I_shared not a multiple of 32
         moe.make_config(6144, 256, 8, 2048, 2, 2048),        # two shared experts
-        moe.make_config(6144, 256, 8, 2048, 1, 2048, n_group=8),
+        moe.make_config(6144, 256, 8, 2048, 1, 2048, n_group=3),           # E % n_group != 0
+        moe.make_config(6144, 256, 8, 2048, 1, 2048, n_group=64, topk_group=4),   # n_group > 32
+        moe.make_config(6144, 256, 8, 2048, 1, 2048, n_group=8, topk_group=0),
+        moe.make_config(6144, 256, 8, 2048, 1, 2048, n_group=8, topk_group=9),
+        moe.make_config(256, 16, 3, 128, 1, 128, n_group=8, topk_group=1),      # K > 1 group of 2
+        moe.make_config(6144, 256, 8, 2048, 1, 2048, n_group=8, topk_group=4,
+                        score_func=moe.MOE_SCORE_SOFTMAX),                    # groups need sigmoid
+        moe.make_config(6144, 256, 8, 2048, 1, 2048, score_func=2),
         moe.make_config(6144, 2048, 8, 2048, 1, 2048),       # E > 1024
         moe.make_config(6144, 256, 8, 2048, 1, 2048, routed_scale=float("inf")),
     ]
@@ -63,6 +70,10 @@ def test_workspace_bytes_validates_config(moe):
     bad.append(unknown_flag)
     for cfg in bad:
         assert moe.moe_workspace_bytes(cfg, 1) == 0
+    for cfg in (moe.make_config(6144, 256, 8, 2048, 1, 2048, 2.5, n_group=8, topk_group=4),
+                moe.make_config(2048, 64, 8, 1024, score_func=moe.MOE_SCORE_SOFTMAX),
+                moe.make_config(2048, 64, 8, 1024, norm_topk=0, score_func=moe.MOE_SCORE_SOFTMAX)):
+        assert moe.moe_workspace_bytes(cfg, 4) > 0
     # the trace flag is accepted and adds the trace buffer (1024 blocks x 64 x 8 B)
     traced = moe.make_config(6144, 256, 8, 2048, 1, 2048, 2.5, trace=True)
     assert moe.moe_workspace_bytes(traced, 1) >= moe.moe_workspace_bytes(good, 1) + 1024 * 64 * 8
@@ -81,15 +92,15 @@ def test_null_arguments_are_errors_not_crashes(moe):
     assert L.moe_forward(None, None, 1, None, None) == moe.MOE_ERR_INVALID
     assert L.moe_forward_host(None, None, 1, None, None) == moe.MOE_ERR_INVALID
     assert L.moe_destroy(None) == moe.MOE_OK
-    cfg_bad = moe.make_config(256, 16, 2, 128, 1, 128, n_group=4)
-    assert L.moe_init(C.byref(cfg_bad), None, 1, C.byref(h)) == moe.MOE_ERR_UNSUPPORTED
+    cfg_bad = moe.make_config(256, 16, 2, 128, 1, 128, n_group=3)
+    assert L.moe_init(C.byref(cfg_bad), None, 1, C.byref(h)) == moe.MOE_ERR_INVALID
     assert "n_group" in moe.moe_last_error()
     with pytest.raises(moe.MoeError):
         moe.moe_forward(0, None, 1, None, stream=0)
 
 
 def test_abi_version(moe):
-    assert moe.moe_abi_version() == 1
+    assert moe.moe_abi_version() == 2
 
 
 def test_product_path_does_not_reference_the_oracle():

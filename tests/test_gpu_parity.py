@@ -7,6 +7,8 @@ K-th score and the output is checked against the oracle re-run with that
 set); per token max|y - y_ref| / max|y_ref| <= 2e-3; routing weights within
 1e-4 relative per expert id.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -175,6 +177,32 @@ def test_batched_is_deterministic_and_token_independent(moe):
     assert rel_err(c.cpu().numpy()[0].astype(np.float64), a[5].cpu().numpy().astype(np.float64)) < 5e-4
 
 
+# --- routing variants (group-limited sigmoid, softmax top-k) --------------------------
+
+@pytest.mark.parametrize("name", ["group8", "softmax_renorm", "olmoe_softmax"])
+def test_routing_variants(moe, name):
+    wl, li, layer = layer_for(moe, name, 64)
+    assert not moe.moe_uses_streaming_decode(layer.handle)     # the generic T == 1 kernels
+    assert moe.moe_uses_tensor_cores(layer.handle)
+    for T in (1, 5, 40):
+        run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=200 + T), f"{name} T={T}")
+
+
+def test_routing_variant_selection_differs_from_plain(moe):
+    """The group mask and the softmax really change what is selected (not a no-op)."""
+    wl, li, layer = layer_for(moe, "group8", 64)
+    x = torch.from_numpy(synth.tokens(wl, T=40, stream=9)).cuda()
+    _, idx, _ = layer.forward_debug(x)
+    idx = idx.cpu().numpy()
+    m = wl.E // wl.n_group
+    assert all(len({e // m for e in row}) <= wl.topk_group for row in idx)
+    plain = dataclasses.replace(wl, n_group=1, topk_group=1)
+    layer2 = upload(moe, plain, li, 64)
+    _, idx2, _ = layer2.forward_debug(x)
+    layer2.close()
+    assert (np.sort(idx, 1) != np.sort(idx2.cpu().numpy(), 1)).any()
+
+
 # --- 40-layer stack (x <- x + moe(rmsnorm(x))) -------------------------------------
 
 def test_stack_35b_40_layers(moe):
@@ -231,6 +259,9 @@ def small_workload(**kw):
     dict(I_shared=32, K=8, E=64),          # streaming decode: small rows, lanes idle
     dict(I_shared=32, n_shared=0, E=40, K=32, H=96),   # streaming decode: 32 slots, H = 96
     dict(I_shared=32, n_layers=2, H=1056, I=160),      # streaming decode, odd chunk counts
+    dict(n_group=4, topk_group=2),                     # group-limited, CUDA-core batched kernels
+    dict(score_func=1),                                # softmax top-k, renormalised
+    dict(score_func=1, norm_topk=0, n_shared=0, I_shared=0),   # softmax, probability as weight
     # T > 1 on the tensor cores (H, I, I_shared multiples of 128)
     dict(H=384, I=128, I_shared=256, E=40, K=8),       # 256-row down tiles half used; I_sh != I
     dict(H=256, I=256, n_shared=0, I_shared=0, E=8, K=8),   # E == K: 37 tokens on every expert
