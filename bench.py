@@ -67,9 +67,12 @@ def step_bytes(wl, T: int, touched: int) -> int:
 
 
 def workload_desc(wl) -> str:
+    route = ("softmax top-k" if wl.score_func == 1 else
+             f"sigmoid+bias noaux_tc n_group={wl.n_group}" + (f" topk_group={wl.topk_group}" if wl.n_group > 1 else ""))
     s = (f"{wl.name}: T={wl.T}, H={wl.H}, E={wl.E} routed, top-{wl.K}, moe_inter={wl.I}, "
-         f"{wl.n_shared} shared (inter {wl.I_shared}), sigmoid+bias noaux_tc n_group=1, "
-         f"norm_topk, routed_scale={wl.routed_scale}, int4 per-row weights, seed {wl.seed}")
+         f"{wl.n_shared} shared (inter {wl.I_shared}), {route}, "
+         f"{'norm_topk' if wl.norm_topk else 'no renorm'}, routed_scale={wl.routed_scale}, "
+         f"int4 per-row weights, seed {wl.seed}")
     if wl.n_layers > 1:
         s += f", {wl.n_layers} chained layers x <- x + moe(rmsnorm(x))"
     return s
@@ -208,12 +211,17 @@ def run_ours(args, rank, world, local_rank, dist_on):
         # profiling captures: same per-launch expert work, fewer experts resident
         import dataclasses
         wl = dataclasses.replace(wl, E=args.resident_experts, name=wl.name + f"_e{args.resident_experts}")
+    if args.tokens:
+        # a small decode batch (e.g. a speculative-verify batch) of the same layer
+        import dataclasses
+        wl = dataclasses.replace(wl, T=args.tokens, name=wl.name + f"_t{args.tokens}")
     T = wl.T
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     li = synth.layer_inputs(wl, experts=[0] if args.alias_experts else None)
     cfg = moe.make_config(wl.H, wl.E, wl.K, wl.I, wl.n_shared, wl.I_shared, wl.routed_scale,
-                          wl.norm_topk, False, wl.rms_eps)
+                          wl.norm_topk, False, wl.rms_eps, n_group=wl.n_group, topk_group=wl.topk_group,
+                          score_func=wl.score_func, cuda_cores=args.cuda_cores)
     slabs, scales = li.slabs, li.scales
     if args.alias_experts:
         # profiling only: every expert pointer aliases expert 0's slab
@@ -526,6 +534,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--alias-experts", action="store_true",
                     help="profiling only: all routed experts share one slab (router captures)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="tokens per step instead of the workload's T (small decode batches)")
+    ap.add_argument("--cuda-cores", action="store_true",
+                    help="T > 1 on the CUDA-core kernels instead of the tensor cores (comparison)")
     ap.add_argument("--resident-experts", type=int, default=0,
                     help="profiling only: keep this many routed experts resident instead of E")
     args = ap.parse_args()

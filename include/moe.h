@@ -57,6 +57,9 @@ extern "C" {
 /* Record the timeline of every T == 1 call on the single-kernel decode path
  * (see moe_trace_read); results are identical with and without it. */
 #define MOE_FLAG_TRACE 2u
+/* T > 1 calls use the CUDA-core batched kernels (exact f32 arithmetic) even
+ * where the tensor-core kernels apply (for comparisons at small T). */
+#define MOE_FLAG_CUDA_CORES 4u
 
 typedef enum {
     MOE_OK = 0,

@@ -75,7 +75,7 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
     if (c->norm_topk != 0 && c->norm_topk != 1)
         return fail(MOE_ERR_INVALID, "norm_topk=%d: need 0 or 1", c->norm_topk);
     if (!isfinite(c->routed_scale)) return fail(MOE_ERR_INVALID, "routed_scale is not finite");
-    if (c->flags & ~(MOE_FLAG_PRENORM_RESIDUAL | MOE_FLAG_TRACE))
+    if (c->flags & ~(MOE_FLAG_PRENORM_RESIDUAL | MOE_FLAG_TRACE | MOE_FLAG_CUDA_CORES))
         return fail(MOE_ERR_INVALID, "unknown flags 0x%x", c->flags);
     if ((c->flags & MOE_FLAG_PRENORM_RESIDUAL) && !(c->rms_eps >= 0.0f && isfinite(c->rms_eps)))
         return fail(MOE_ERR_INVALID, "rms_eps must be finite and >= 0");
@@ -97,7 +97,7 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
     d->eps = c->rms_eps;
     d->max_tokens = max_tokens;
     d->fast_decode = moe::decode_fast_supported(*d) ? 1 : 0;
-    d->mma = moe::mma_supported(*d) ? 1 : 0;
+    d->mma = (moe::mma_supported(*d) && !(c->flags & MOE_FLAG_CUDA_CORES)) ? 1 : 0;
     d->trace = (c->flags & MOE_FLAG_TRACE) ? 1 : 0;
     return MOE_OK;
 }

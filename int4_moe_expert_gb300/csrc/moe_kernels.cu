@@ -355,13 +355,56 @@ __device__ void router_tail(const Params &p, int T, int buckets, unsigned nblock
     if (threadIdx.x == 0) *p.ws.counters = 0u;     // ready for the next call
 }
 
-// Router for T <= kGemvMaxT tokens: one warp per expert row.  Also writes
+// Router logits of experts 2 blockIdx.x and 2 blockIdx.x + 1 for T <= kGemvMaxT tokens,
+// scaled by s_r[t]: warps 4 r .. 4 r + 3 share expert row r, each a quarter of H; the
+// quarters' sums are added in order.  Every thread of the block calls it.
+__device__ void gemv_logits(const Params &p, const float *__restrict__ x, int T, const float *s_r) {
+    __shared__ float s_part[kWarps][kGemvMaxT];
+    const int H = p.d.H, E = p.d.E, H4 = H / 4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 2 + (warp >> 2), part = warp & 3;
+    const int per = (H4 + 3) / 4, i0 = part * per, i1 = min(H4, i0 + per);
+    float acc[kGemvMaxT];
+#pragma unroll
+    for (int t = 0; t < kGemvMaxT; t++) acc[t] = 0.0f;
+    if (e < E) {
+        const float4 *w4 = reinterpret_cast<const float4 *>(p.router_w + (size_t)e * H);
+        for (int i = i0 + lane; i < i1; i += 32) {
+            const float4 wv = __ldg(w4 + i);
+#pragma unroll
+            for (int t = 0; t < kGemvMaxT; t++) {
+                if (t < T) {
+                    const float4 xv = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H) + i);
+                    acc[t] = fmaf(wv.x, xv.x, acc[t]);
+                    acc[t] = fmaf(wv.y, xv.y, acc[t]);
+                    acc[t] = fmaf(wv.z, xv.z, acc[t]);
+                    acc[t] = fmaf(wv.w, xv.w, acc[t]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < kGemvMaxT; t++) {
+        const float v = warp_sum(acc[t]);
+        if (lane == 0) s_part[warp][t] = v;
+    }
+    __syncthreads();
+    if (threadIdx.x < 2 * kGemvMaxT) {
+        const int r = threadIdx.x / kGemvMaxT, t = threadIdx.x % kGemvMaxT, er = blockIdx.x * 2 + r;
+        if (er < E && t < T) {
+            const float v = s_part[4 * r][t] + s_part[4 * r + 1][t] + s_part[4 * r + 2][t] + s_part[4 * r + 3][t];
+            p.ws.logits[(size_t)t * E + er] = v * s_r[t];
+        }
+    }
+}
+
+// Router for T <= kGemvMaxT tokens: four warps per expert row (gemv_logits).  Also writes
 // rnorm and the permuted (and pre-normed) activations used by gate/up.
 __global__ void __launch_bounds__(kThreads) router_gemv_kernel(Params p, const float *__restrict__ x,
                                                                int T, int buckets) {
     extern __shared__ float smem[];
     __shared__ float s_r[kGemvMaxT];
-    const int H = p.d.H, E = p.d.E;
+    const int H = p.d.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp < T) {
         float ss = 0.0f;
@@ -387,42 +430,10 @@ __global__ void __launch_bounds__(kThreads) router_gemv_kernel(Params p, const f
         p.ws.xperm[(size_t)t * H + perm_pos(c, H)] = v;
         if (p.d.mma && T > 1) p.ws.x16[(size_t)t * H + mma_pos(c)] = f2h_bits(v);
     }
-    const int e = blockIdx.x * kWarps + warp;
-    if (e < E) {
-        float acc[kGemvMaxT];
-#pragma unroll
-        for (int t = 0; t < kGemvMaxT; t++) acc[t] = 0.0f;
-        const float4 *w4 = reinterpret_cast<const float4 *>(p.router_w + (size_t)e * H);
-        for (int i = lane; i < H / 4; i += 32) {
-            const float4 wv = __ldg(w4 + i);
-#pragma unroll
-            for (int t = 0; t < kGemvMaxT; t++) {
-                if (t < T) {
-                    const float4 xv = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H) + i);
-                    acc[t] = fmaf(wv.x, xv.x, acc[t]);
-                    acc[t] = fmaf(wv.y, xv.y, acc[t]);
-                    acc[t] = fmaf(wv.z, xv.z, acc[t]);
-                    acc[t] = fmaf(wv.w, xv.w, acc[t]);
-                }
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < kGemvMaxT; t++) {
-            if (t < T) {
-                const float v = warp_sum(acc[t]);
-                if (lane == 0) p.ws.logits[(size_t)t * E + e] = v * s_r[t];
-            }
-        }
-    }
+    gemv_logits(p, x, T, s_r);
     router_tail(p, T, buckets, gridDim.x, smem);
 }
 
-__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
-    acc = fmaf(a.x, b.x, acc);
-    acc = fmaf(a.y, b.y, acc);
-    acc = fmaf(a.z, b.z, acc);
-    return fmaf(a.w, b.w, acc);
-}
 
 // Router for larger T: a 32 (experts) x 32 (tokens) tile per block, k-loop
 // over H in steps of 32 through shared memory.
@@ -844,19 +855,31 @@ __global__ void __launch_bounds__(kThreads) down_batched_kernel(Params p, int T)
 }
 
 // y[t] = sum_k w[t,k] d[(t,k)] (k ascending) + d_shared[t] (+ x[t] with pre-norm residual)
+// Grid (T, ceil(H / (4 kThreads))): four consecutive outputs per thread.
 __global__ void __launch_bounds__(kThreads) combine_kernel(Params p, const float *__restrict__ x,
                                                            float *__restrict__ y, int T) {
     const int t = blockIdx.x, H = p.d.H, K = p.d.K;
-    for (int o = threadIdx.x; o < H; o += kThreads) {
-        float v = 0.0f;
-        for (int k = 0; k < K; k++) {
-            const int q = t * K + k;
-            v = fmaf(p.ws.topk_w[q], p.ws.dbuf[(size_t)p.ws.inv[q] * H + o], v);
-        }
-        if (p.d.n_shared) v += p.ws.dbuf[(size_t)(T * K + t) * H + o];
-        if (p.d.prenorm) v += x[(size_t)t * H + o];
-        y[(size_t)t * H + o] = v;
+    const int o = (blockIdx.y * kThreads + threadIdx.x) * 4;
+    if (o >= H) return;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < K; k++) {
+        const int q = t * K + k;
+        const float w = p.ws.topk_w[q];
+        const float4 d = __ldg(reinterpret_cast<const float4 *>(p.ws.dbuf + (size_t)p.ws.inv[q] * H + o));
+        v.x = fmaf(w, d.x, v.x);
+        v.y = fmaf(w, d.y, v.y);
+        v.z = fmaf(w, d.z, v.z);
+        v.w = fmaf(w, d.w, v.w);
     }
+    if (p.d.n_shared) {
+        const float4 d = __ldg(reinterpret_cast<const float4 *>(p.ws.dbuf + (size_t)(T * K + t) * H + o));
+        v.x += d.x; v.y += d.y; v.z += d.z; v.w += d.w;
+    }
+    if (p.d.prenorm) {
+        const float4 r = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + o));
+        v.x += r.x; v.y += r.y; v.z += r.z; v.w += r.w;
+    }
+    *reinterpret_cast<float4 *>(y + (size_t)t * H + o) = v;
 }
 
 // ---------------------------------------------------------------------------
@@ -945,14 +968,14 @@ template <bool GU>
 __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T) {
     extern __shared__ __align__(128) unsigned char mma_smem[];
     __shared__ int s_brow[kItemTokens], s_orow[kItemTokens];
-    const int item = blockIdx.y;
+    const int item = blockIdx.x;
     if (item >= *p.ws.n_items) return;
     const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
     const SlotInfo s = slot_info(p, T, slot);
     if (!s.valid) return;
     const int H = p.d.H, Is = s.Is;
     const int rows = GU ? Is : H;                       // output rows of the slot
-    const int o0 = blockIdx.x * (GU ? 128 : 256);
+    const int o0 = blockIdx.y * (GU ? 128 : 256);
     if (o0 >= rows) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
     const int nt = min(kItemTokens, s.n - n0);
@@ -982,9 +1005,11 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
     }
     const uint16_t *bsrc[2];
     uint32_t bdst[2];
+    bool bok[2];                                   // rows of n8 tiles that are computed
 #pragma unroll
     for (int i = 0; i < 2; i++) {
         const int c = tid + i * kThreads, n = c >> 4, piece = c & 15;
+        bok[i] = n < ((nt + 7) & ~7);
         bsrc[i] = act + (size_t)s_brow[n < nt ? n : 0] * ald + piece * 8;
         bdst[i] = (uint32_t)(kMmaABytes + (n * kMmaBLd + piece * 8) * 2);
     }
@@ -996,7 +1021,8 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
         for (int i = 0; i < 4; i++)
             if (aok[i]) cp_async16(st + adst[i], asrc[i] + (size_t)kb * 64);
 #pragma unroll
-        for (int i = 0; i < 2; i++) cp_async16(st + bdst[i], bsrc[i] + (size_t)kb * 128);
+        for (int i = 0; i < 2; i++)
+            if (bok[i]) cp_async16(st + bdst[i], bsrc[i] + (size_t)kb * 128);
     };
     const int ob = o0 + (GU ? 16 : 32) * warp;            // the warp's first output row
     const bool active = ob < rows;                         // (rows are multiples of 128)
@@ -1189,7 +1215,7 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
     };
     mark(0);
     if (T <= kGemvMaxT) {
-        const int grid = (d.E + kWarps - 1) / kWarps;
+        const int grid = (d.E + 1) / 2;
         router_gemv_kernel<<<grid, kThreads, smem, st>>>(p, x, T, buckets);
     } else {
         const int bxy = ((d.E + 31) / 32) * ((T + 31) / 32);
@@ -1220,15 +1246,15 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
     }
     if (d.mma) {
         const int ni = max_items(T, d.K, d.E, d.n_shared);
-        const dim3 g1(d.I_max / 128, ni);
+        const dim3 g1(ni, d.I_max / 128);
         mma_expert_kernel<true><<<g1, kThreads, kMmaSmem, st>>>(p, T);
         check();
         mark(2);
-        const dim3 g2((d.H + 255) / 256, ni);
+        const dim3 g2(ni, (d.H + 255) / 256);
         mma_expert_kernel<false><<<g2, kThreads, kMmaSmem, st>>>(p, T);
         check();
         mark(3);
-        combine_kernel<<<T, kThreads, 0, st>>>(p, x, y, T);
+        combine_kernel<<<dim3(T, (d.H + 4 * kThreads - 1) / (4 * kThreads)), kThreads, 0, st>>>(p, x, y, T);
         check();
         mark(4);
         return e;
@@ -1243,7 +1269,7 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
     down_batched_kernel<RPW_D, NT><<<g2, kThreads, 0, st>>>(p, T);
     check();
     mark(3);
-    combine_kernel<<<T, kThreads, 0, st>>>(p, x, y, T);
+    combine_kernel<<<dim3(T, (d.H + 4 * kThreads - 1) / (4 * kThreads)), kThreads, 0, st>>>(p, x, y, T);
     check();
     mark(4);
     return e;
@@ -1277,7 +1303,7 @@ __global__ void __launch_bounds__(kThreads) router_noalloc_kernel(Params p, cons
                                                                   int T) {
     extern __shared__ float smem[];
     __shared__ float s_r[kGemvMaxT];
-    const int H = p.d.H, E = p.d.E;
+    const int H = p.d.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (warp < T) {
         float ss = 0.0f;
@@ -1293,33 +1319,7 @@ __global__ void __launch_bounds__(kThreads) router_noalloc_kernel(Params p, cons
         if (lane == 0) s_r[warp] = p.d.prenorm ? 1.0f / sqrtf(ss / (float)H + p.d.eps) : 1.0f;
     }
     __syncthreads();
-    const int e = blockIdx.x * kWarps + warp;
-    if (e < E) {
-        float acc[kGemvMaxT];
-#pragma unroll
-        for (int t = 0; t < kGemvMaxT; t++) acc[t] = 0.0f;
-        const float4 *w4 = reinterpret_cast<const float4 *>(p.router_w + (size_t)e * H);
-        for (int i = lane; i < H / 4; i += 32) {
-            const float4 wv = __ldg(w4 + i);
-#pragma unroll
-            for (int t = 0; t < kGemvMaxT; t++) {
-                if (t < T) {
-                    const float4 xv = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H) + i);
-                    acc[t] = fmaf(wv.x, xv.x, acc[t]);
-                    acc[t] = fmaf(wv.y, xv.y, acc[t]);
-                    acc[t] = fmaf(wv.z, xv.z, acc[t]);
-                    acc[t] = fmaf(wv.w, xv.w, acc[t]);
-                }
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < kGemvMaxT; t++) {
-            if (t < T) {
-                const float v = warp_sum(acc[t]);
-                if (lane == 0) p.ws.logits[(size_t)t * E + e] = v * s_r[t];
-            }
-        }
-    }
+    gemv_logits(p, x, T, s_r);
     router_tail(p, T, 0, gridDim.x, smem);
 }
 
@@ -1390,7 +1390,7 @@ extern "C" moe_status moe_route_noalloc(const moe_config *cfg, const float *rout
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The ticket must start at zero; logits are fully rewritten by every call.
     if (cudaMemsetAsync(p.ws.counters, 0, sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
-    const int grid = (d.E + kWarps - 1) / kWarps;
+    const int grid = (d.E + 1) / 2;
     router_noalloc_kernel<<<grid, kThreads, smem, st>>>(p, x, T);
     return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

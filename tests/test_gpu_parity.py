@@ -127,6 +127,18 @@ def test_tensor_core_path_selection(moe):
     single = upload(moe, wl, li, 1)            # max_tokens == 1: no T > 1 calls possible
     assert not moe.moe_uses_tensor_cores(single.handle)
     single.close()
+    forced = moe.MoeLayer(moe.make_config(wl.H, wl.E, wl.K, wl.I, wl.n_shared, wl.I_shared,
+                                          wl.routed_scale, cuda_cores=True),
+                          li.router_w, li.router_b, li.slabs, li.scales, li.sh_slab, li.sh_scale,
+                          max_tokens=64)
+    assert not moe.moe_uses_tensor_cores(forced.handle)
+    # both T > 1 paths agree within the f16 rounding of the activations
+    x = torch.from_numpy(synth.tokens(wl, T=20, stream=4)).cuda()
+    a = forced.forward(x).cpu().numpy().astype(np.float64)
+    b = layer_for(moe, "tiny", 64)[2].forward(x).cpu().numpy().astype(np.float64)
+    forced.close()
+    for t in range(20):
+        assert rel_err(b[t], a[t]) < 2e-3
 
 
 def test_batched_glm_512_sampled(moe):
