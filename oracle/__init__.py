@@ -37,10 +37,12 @@ class Cfg(C.Structure):
                 ("n_shared", C.c_int), ("I_shared", C.c_int), ("n_group", C.c_int),
                 ("norm_topk", C.c_int), ("prenorm_residual", C.c_int),
                 ("routed_scale", C.c_double), ("rms_eps", C.c_double),
-                ("topk_group", C.c_int), ("score_func", C.c_int)]
+                ("topk_group", C.c_int), ("score_func", C.c_int),
+                ("expert_format", C.c_int), ("shared_format", C.c_int)]
 
 
 SCORE_SIGMOID, SCORE_SOFTMAX = 0, 1
+FORMAT_INT4, FORMAT_INT8 = 0, 1
 
 
 class Layer(C.Structure):
@@ -61,6 +63,8 @@ def lib():
         L.oracle_silu.restype = C.c_double
         L.oracle_rmsnorm.argtypes = [vp, ip, C.c_double, vp]
         L.oracle_expert.argtypes = [ip, ip, vp, vp, vp, vp, vp]
+        L.oracle_expert_fmt.argtypes = [ip, ip, ip, vp, vp, vp, vp, vp]
+        L.oracle_quantize_int8.argtypes = [vp, ip, ip, vp, vp]
         L.oracle_route.argtypes = [C.POINTER(Cfg), vp, vp, vp, vp, vp, vp, vp]
         L.oracle_route.restype = ip
         L.oracle_weights_for.argtypes = [C.POINTER(Cfg), vp, vp, vp, vp]
@@ -80,15 +84,17 @@ def _p(a: np.ndarray | None):
 
 def make_cfg(H, E, K, I, n_shared=0, I_shared=0, routed_scale=1.0, norm_topk=1,
              prenorm_residual=0, rms_eps=1e-5, n_group=1, topk_group=1,
-             score_func=SCORE_SIGMOID) -> Cfg:
+             score_func=SCORE_SIGMOID, expert_format=FORMAT_INT4,
+             shared_format=FORMAT_INT4) -> Cfg:
     return Cfg(H, E, K, I, n_shared, I_shared, n_group, norm_topk, prenorm_residual,
-               float(routed_scale), float(rms_eps), topk_group, score_func)
+               float(routed_scale), float(rms_eps), topk_group, score_func, expert_format,
+               shared_format)
 
 
 def cfg_from_workload(wl) -> Cfg:
     return make_cfg(wl.H, wl.E, wl.K, wl.I, wl.n_shared, wl.I_shared, wl.routed_scale,
                     wl.norm_topk, int(wl.prenorm_residual), wl.rms_eps, wl.n_group,
-                    wl.topk_group, wl.score_func)
+                    wl.topk_group, wl.score_func, wl.expert_format, wl.shared_format)
 
 
 def unpack_int4(row: np.ndarray, n: int) -> np.ndarray:
@@ -107,6 +113,15 @@ def quantize_int4(w: np.ndarray):
     return q4, s
 
 
+def quantize_int8(w: np.ndarray):
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    O, I = w.shape
+    q = np.zeros((O, I), dtype=np.int8)
+    s = np.zeros(O, dtype=np.float32)
+    lib().oracle_quantize_int8(_p(w), O, I, _p(q), _p(s))
+    return q, s
+
+
 def silu(v: float) -> float:
     return lib().oracle_silu(float(v))
 
@@ -118,13 +133,14 @@ def rmsnorm(x: np.ndarray, eps: float) -> np.ndarray:
     return out
 
 
-def expert(H: int, I: int, slab: np.ndarray, scale: np.ndarray, x: np.ndarray):
+def expert(H: int, I: int, slab: np.ndarray, scale: np.ndarray, x: np.ndarray,
+           fmt: int = FORMAT_INT4):
     slab = np.ascontiguousarray(slab, dtype=np.uint8)
     scale = np.ascontiguousarray(scale, dtype=np.float32)
     x = np.ascontiguousarray(x, dtype=np.float64)
     d = np.zeros(H, dtype=np.float64)
     h = np.zeros(I, dtype=np.float64)
-    lib().oracle_expert(H, I, _p(slab), _p(scale), _p(x), _p(d), _p(h))
+    lib().oracle_expert_fmt(H, I, int(fmt), _p(slab), _p(scale), _p(x), _p(d), _p(h))
     return d, h
 
 

@@ -86,6 +86,61 @@ static void int4_matvec(const uint8_t *q4, const float *scale, int O, int n,
     }
 }
 
+/* out[o] = scale[o] * sum_i q[o,i] * v[i] over one int8 [O, n] matrix (row stride n bytes). */
+static void int8_matvec(const uint8_t *q8, const float *scale, int O, int n,
+                        const double *v, double *out) {
+#pragma omp parallel for schedule(static)
+    for (int o = 0; o < O; o++) {
+        const int8_t *row = (const int8_t *)(q8 + (int64_t)o * n);
+        double acc = 0.0;
+        for (int i = 0; i < n; i++) acc += (double)row[i] * v[i];
+        out[o] = (double)scale[o] * acc;
+    }
+}
+
+/* The reader.mx page's OLMoE-engine quantiser (section 03, quantize_rows with
+ * bits = 8), in its float32 arithmetic: per row s = max(amax / 127, 1e-8),
+ * q = clip(rint(w / s), -128, 127). */
+void oracle_quantize_int8(const float *w, int O, int I, int8_t *q, float *scale) {
+    const int qmax = 127;
+    for (int o = 0; o < O; o++) {
+        const float *wr = w + (int64_t)o * I;
+        float amax = 0.f;
+        for (int i = 0; i < I; i++) { float a = fabsf(wr[i]); if (a > amax) amax = a; }
+        float s = amax / qmax;
+        if (s < 1e-8f) s = 1e-8f;
+        scale[o] = s;
+        for (int i = 0; i < I; i++) {
+            int v = (int)lrintf(wr[i] / s);
+            if (v > qmax) v = qmax;
+            if (v < -qmax - 1) v = -qmax - 1;
+            q[(int64_t)o * I + i] = (int8_t)v;
+        }
+    }
+}
+
+/* Section 11 expert in either weight format: g = W_g x, u = W_u x,
+ * h = silu(g) * u, d = W_d h.  int8 slab: gate [I, H] | up [I, H] | down [H, I]
+ * bytes, signed, one float32 scale per output row as for int4. */
+void oracle_expert_fmt(int H, int I, int format, const uint8_t *slab, const float *scale,
+                       const double *x, double *d_out, double *h_out) {
+    if (format != ORACLE_FORMAT_INT8) {
+        oracle_expert(H, I, slab, scale, x, d_out, h_out);
+        return;
+    }
+    const uint8_t *qg = slab, *qu = slab + (int64_t)I * H, *qd = slab + 2 * (int64_t)I * H;
+    const float *sg = scale, *su = scale + I, *sd = scale + 2 * I;
+    double *g = (double *)malloc(sizeof(double) * I);
+    double *u = (double *)malloc(sizeof(double) * I);
+    double *h = (double *)malloc(sizeof(double) * I);
+    int8_matvec(qg, sg, I, H, x, g);
+    int8_matvec(qu, su, I, H, x, u);
+    for (int i = 0; i < I; i++) h[i] = oracle_silu(g[i]) * u[i];
+    int8_matvec(qd, sd, H, I, h, d_out);
+    if (h_out) memcpy(h_out, h, sizeof(double) * I);
+    free(g); free(u); free(h);
+}
+
 /* Section 11 expert: g = W_g x, u = W_u x, h = silu(g) * u, d = W_d h. */
 void oracle_expert(int H, int I, const uint8_t *slab, const float *scale,
                    const double *x, double *d_out, double *h_out) {
@@ -120,6 +175,8 @@ static int cfg_ok(const oracle_cfg *c) {
     if (!c || c->H <= 0 || c->E <= 0 || c->K <= 0 || c->K > c->E || c->I <= 0) return 0;
     if (!(c->n_shared == 0 || (c->n_shared == 1 && c->I_shared > 0))) return 0;
     if (c->score_func != ORACLE_SCORE_SIGMOID && c->score_func != ORACLE_SCORE_SOFTMAX) return 0;
+    if ((c->expert_format != ORACLE_FORMAT_INT4 && c->expert_format != ORACLE_FORMAT_INT8) ||
+        (c->shared_format != ORACLE_FORMAT_INT4 && c->shared_format != ORACLE_FORMAT_INT8)) return 0;
     if (c->n_group < 1 || c->E % c->n_group != 0) return 0;
     if (c->n_group > 1) {
         if (c->score_func != ORACLE_SCORE_SIGMOID) return 0;
@@ -263,11 +320,11 @@ int oracle_moe_token(const oracle_cfg *c, const oracle_layer *L, const double *x
             const uint8_t *slab = L->slab[idx[k]];
             const float *scale = L->scale[idx[k]];
             if (!slab || !scale) { rc = -2; break; }
-            oracle_expert(H, c->I, slab, scale, xin, d, NULL);
+            oracle_expert_fmt(H, c->I, c->expert_format, slab, scale, xin, d, NULL);
             for (int h = 0; h < H; h++) acc[h] += w[k] * d[h];
         }
         if (rc == 0 && c->n_shared) {
-            oracle_expert(H, c->I_shared, L->sh_slab, L->sh_scale, xin, d, NULL);
+            oracle_expert_fmt(H, c->I_shared, c->shared_format, L->sh_slab, L->sh_scale, xin, d, NULL);
             for (int h = 0; h < H; h++) acc[h] += d[h];
         }
         if (rc == 0) {

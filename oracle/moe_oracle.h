@@ -16,6 +16,8 @@
  *    2j in the low nibble, 2j+1 in the high nibble; row stride ceil(I/2)
  *    bytes, pad nibble 8; one float32 scale per output row (".qs").
  *  - same page, section 04 "手写的基础数学": RMSNorm and SiLU.
+ *  - same page, section 03 (the OLMoE engine): int8 expert weights, one signed
+ *    byte per value and one float32 scale per row (quantize_rows, bits = 8).
  *  - Edge0 article (magicnetworld.com), section 七 "路由数学": renormalised
  *    sigmoid weights w_i = s * sigma_i / (sum_{j in S} sigma_j + 1e-20); the
  *    softmax-top-k family (g = softmax(logits), top-K of g, w_i = g_i / sum_S g)
@@ -54,7 +56,12 @@ typedef struct {
     double rms_eps;
     int topk_group;   /* groups kept when n_group > 1 (1..n_group) */
     int score_func;   /* ORACLE_SCORE_SIGMOID or ORACLE_SCORE_SOFTMAX */
+    int expert_format;   /* routed experts: ORACLE_FORMAT_INT4 or ORACLE_FORMAT_INT8 */
+    int shared_format;   /* shared expert: the same choice */
 } oracle_cfg;
+
+#define ORACLE_FORMAT_INT4 0     /* section 06: two values per byte, q + 8, low nibble first */
+#define ORACLE_FORMAT_INT8 1     /* section 03 (OLMoE engine): one signed byte per value */
 
 #define ORACLE_SCORE_SIGMOID 0   /* sigma = sigmoid(logit); selection by sigma + bias */
 #define ORACLE_SCORE_SOFTMAX 1   /* g = softmax(logits); selection by g; bias unused */
@@ -73,6 +80,15 @@ void oracle_unpack_int4(const uint8_t *row, int n, int *q);
 
 /* Offline quantiser of section 06 (float32 arithmetic, as printed). */
 void oracle_quantize_int4(const float *w, int O, int I, uint8_t *q4, float *scale);
+
+/* The OLMoE engine's per-row int8 quantiser (section 03, bits = 8), float32
+ * arithmetic as printed. */
+void oracle_quantize_int8(const float *w, int O, int I, int8_t *q, float *scale);
+
+/* oracle_expert for either weight format (ORACLE_FORMAT_*); the int8 slab is
+ * gate [I, H] | up [I, H] | down [H, I] signed bytes with the same scales. */
+void oracle_expert_fmt(int H, int I, int format, const uint8_t *slab, const float *scale,
+                       const double *x, double *d_out, double *h_out);
 
 double oracle_silu(double v);
 

@@ -164,22 +164,27 @@ class Workload:
     n_group: int = 1        # > 1: group-limited selection (sigmoid family)
     topk_group: int = 1     # groups kept when n_group > 1
     score_func: int = 0     # 0 sigmoid (+ bias for selection), 1 softmax
+    expert_format: int = 0  # routed experts: 0 int4 (two per byte), 1 int8 (one signed byte)
+    shared_format: int = 0  # shared expert: same choice
 
     @property
     def slab_bytes(self) -> int:
-        return slab_bytes(self.H, self.I)
+        return slab_bytes(self.H, self.I, self.expert_format)
 
     @property
     def shared_slab_bytes(self) -> int:
-        return slab_bytes(self.H, self.I_shared) if self.n_shared else 0
+        return slab_bytes(self.H, self.I_shared, self.shared_format) if self.n_shared else 0
 
     @property
     def prenorm_residual(self) -> bool:
         return self.n_layers > 1
 
 
-def slab_bytes(H: int, I: int) -> int:
-    """Packed bytes of one expert: gate and up [I, ceil(H/2)], down [H, ceil(I/2)]."""
+def slab_bytes(H: int, I: int, fmt: int = 0) -> int:
+    """Bytes of one expert.  int4 (fmt 0): gate and up [I, ceil(H/2)], down [H, ceil(I/2)];
+    int8 (fmt 1): gate and up [I, H], down [H, I], one signed byte per value."""
+    if fmt == 1:
+        return 3 * I * H
     return 2 * I * ((H + 1) // 2) + H * ((I + 1) // 2)
 
 
@@ -216,6 +221,13 @@ WORKLOADS = {
     # OLMoE engine: softmax over the E logits, top-8, the probability itself as weight
     "olmoe_softmax": Workload("olmoe_softmax", T=1, H=2048, E=64, K=8, I=1024, n_shared=0,
                               I_shared=0, routed_scale=1.0, seed=7, score_func=1, norm_topk=0),
+    # weight formats (reader.mx page): the OLMoE engine of section 03 (int8 per-row experts,
+    # softmax top-8, the probability as weight); GLM decode with the shared expert in int8 as
+    # the GLM engine keeps it (section 06)
+    "olmoe_int8": Workload("olmoe_int8", T=1, H=2048, E=64, K=8, I=1024, n_shared=0, I_shared=0,
+                           routed_scale=1.0, seed=8, score_func=1, norm_topk=0, expert_format=1),
+    "glm_int8_shared": Workload("glm_int8_shared", T=1, H=6144, E=256, K=8, I=2048, n_shared=1,
+                                I_shared=2048, routed_scale=2.5, seed=9, shared_format=1),
 }
 
 

@@ -163,6 +163,77 @@ def test_expert_equals_dense_swiglu(H, I):
     np.testing.assert_allclose(d, _dense_swiglu(H, I, slab, scale, x), rtol=1e-10, atol=1e-12)
 
 
+# --- int8 per-row experts (reader.mx section 03, the OLMoE engine) -------------------
+
+def test_int8_quantize_roundtrip_exact_on_integer_rows():
+    rng = np.random.default_rng(41)
+    O, I = 6, 40
+    k = rng.integers(-127, 128, (O, I))
+    k[:, 0] = 127                                  # amax / 127 is the power-of-two scale
+    s = 2.0 ** rng.integers(-12, -4, O)
+    q, sc = oracle.quantize_int8((k * s[:, None]).astype(np.float32))
+    assert np.array_equal(q, k.astype(np.int8))
+    np.testing.assert_array_equal(sc, s.astype(np.float32))
+    q0, s0 = oracle.quantize_int8(np.zeros((2, 8), np.float32))   # zero rows: scale floor 1e-8
+    assert not q0.any() and np.all(s0 == np.float32(1e-8))
+
+
+def _int8_slab(rng, H, I):
+    return rng.integers(-128, 128, 3 * I * H).astype(np.int8).view(np.uint8)
+
+
+@pytest.mark.parametrize("H,I", [(64, 32), (7, 5)])
+def test_int8_expert_equals_dense_swiglu(H, I):
+    rng = np.random.default_rng(H + 7 * I)
+    slab = _int8_slab(rng, H, I)
+    scale = rng.uniform(0.005, 0.02, 2 * I + H).astype(np.float32)
+    x = rng.standard_normal(H)
+    q = slab.view(np.int8).astype(np.float64)
+    Wg = q[:I * H].reshape(I, H) * scale[:I, None]
+    Wu = q[I * H:2 * I * H].reshape(I, H) * scale[I:2 * I, None]
+    Wd = q[2 * I * H:].reshape(H, I) * scale[2 * I:, None]
+    g = Wg @ x
+    want = Wd @ (g * expit(g) * (Wu @ x))
+    d, _ = oracle.expert(H, I, slab, scale, x, fmt=oracle.FORMAT_INT8)
+    np.testing.assert_allclose(d, want, rtol=1e-10, atol=1e-12)
+
+
+def test_int8_and_int4_agree_on_int4_values():
+    # the same integer weights in [-8, 7] stored in both formats give the same expert exactly
+    rng = np.random.default_rng(5)
+    H, I = 16, 8
+    vals = [rng.integers(-8, 8, (I, H)), rng.integers(-8, 8, (I, H)), rng.integers(-8, 8, (H, I))]
+    def pack4(m):
+        m = m + 8
+        return (m[:, 0::2] | (m[:, 1::2] << 4)).astype(np.uint8).ravel()
+    slab4 = np.concatenate([pack4(v) for v in vals])
+    slab8 = np.concatenate([v.astype(np.int8).ravel() for v in vals]).view(np.uint8)
+    scale = rng.uniform(0.005, 0.02, 2 * I + H).astype(np.float32)
+    x = rng.standard_normal(H)
+    d4, h4 = oracle.expert(H, I, slab4, scale, x)
+    d8, h8 = oracle.expert(H, I, slab8, scale, x, fmt=oracle.FORMAT_INT8)
+    assert np.array_equal(d4, d8) and np.array_equal(h4, h8)
+
+
+def test_int8_layer_single_expert_and_shared_format():
+    rng = np.random.default_rng(9)
+    H, I = 24, 16
+    slab = _int8_slab(rng, H, I)
+    scale = rng.uniform(0.005, 0.02, 2 * I + H).astype(np.float32)
+    sh = _int8_slab(rng, H, I)
+    shs = rng.uniform(0.005, 0.02, 2 * I + H).astype(np.float32)
+    x = rng.standard_normal(H)
+    W = rng.normal(0, 0.1, (1, H)).astype(np.float32)
+    cfg = oracle.make_cfg(H, 1, 1, I, 1, I, routed_scale=2.5, expert_format=oracle.FORMAT_INT8,
+                          shared_format=oracle.FORMAT_INT8)
+    ref = oracle.LayerRef(cfg, W, np.zeros(1, np.float32), [slab], [scale], sh, shs)
+    y, idx, w, _ = ref.token(x)
+    d, _ = oracle.expert(H, I, slab, scale, x, fmt=oracle.FORMAT_INT8)
+    ds, _ = oracle.expert(H, I, sh, shs, x, fmt=oracle.FORMAT_INT8)
+    np.testing.assert_allclose(y, w[0] * d + ds, rtol=1e-12, atol=1e-14)
+    assert w[0] == pytest.approx(2.5, rel=1e-15)
+
+
 # --- router (section 11; Edge0 section 七) ------------------------------------
 
 def _route_scores(c_values, K, x=None):
