@@ -46,23 +46,23 @@ TRAFFIC_FILES = {
 
 # --------------------------------------------------------------------------- helpers
 
-def expert_bytes(H: int, I: int) -> int:
-    """Packed int4 gate/up/down bytes + float32 per-row scales of one expert."""
-    return synth.slab_bytes(H, I) + 4 * synth.scale_count(H, I)
+def expert_bytes(H: int, I: int, fmt: int = 0) -> int:
+    """Gate/up/down weight bytes (int4 packed or int8) + float32 per-row scales of one expert."""
+    return synth.slab_bytes(H, I, fmt) + 4 * synth.scale_count(H, I)
 
 
-def gateup_bytes(H: int, I: int) -> int:
-    """Bytes the gate/up kernel must read for one expert: two [I, H/2] int4
-    matrices and their 2I float32 scales."""
-    return 2 * I * ((H + 1) // 2) + 8 * I
+def gateup_bytes(H: int, I: int, fmt: int = 0) -> int:
+    """Bytes the gate/up kernel must read for one expert: two [I, H] weight
+    matrices (H/2 bytes per int4 row, H per int8 row) and their 2I float32 scales."""
+    return 2 * I * (H if fmt == 1 else (H + 1) // 2) + 8 * I
 
 
 def step_bytes(wl, T: int, touched: int) -> int:
     """Algorithmic HBM bytes of one step: router weight and bias, every routed
     expert the batch touches (each read once), the shared expert, x and y."""
-    b = wl.E * wl.H * 4 + wl.E * 4 + touched * expert_bytes(wl.H, wl.I)
+    b = wl.E * wl.H * 4 + wl.E * 4 + touched * expert_bytes(wl.H, wl.I, wl.expert_format)
     if wl.n_shared:
-        b += expert_bytes(wl.H, wl.I_shared)
+        b += expert_bytes(wl.H, wl.I_shared, wl.shared_format)
     return b + 2 * T * wl.H * 4
 
 
@@ -72,7 +72,9 @@ def workload_desc(wl) -> str:
     s = (f"{wl.name}: T={wl.T}, H={wl.H}, E={wl.E} routed, top-{wl.K}, moe_inter={wl.I}, "
          f"{wl.n_shared} shared (inter {wl.I_shared}), {route}, "
          f"{'norm_topk' if wl.norm_topk else 'no renorm'}, routed_scale={wl.routed_scale}, "
-         f"int4 per-row weights, seed {wl.seed}")
+         f"{'int8' if wl.expert_format == 1 else 'int4'} per-row routed weights"
+         + (f", {'int8' if wl.shared_format == 1 else 'int4'} shared" if wl.n_shared else "")
+         + f", seed {wl.seed}")
     if wl.n_layers > 1:
         s += f", {wl.n_layers} chained layers x <- x + moe(rmsnorm(x))"
     return s
@@ -221,7 +223,8 @@ def run_ours(args, rank, world, local_rank, dist_on):
     li = synth.layer_inputs(wl, experts=[0] if args.alias_experts else None)
     cfg = moe.make_config(wl.H, wl.E, wl.K, wl.I, wl.n_shared, wl.I_shared, wl.routed_scale,
                           wl.norm_topk, False, wl.rms_eps, n_group=wl.n_group, topk_group=wl.topk_group,
-                          score_func=wl.score_func, cuda_cores=args.cuda_cores)
+                          score_func=wl.score_func, cuda_cores=args.cuda_cores,
+                          expert_format=wl.expert_format, shared_format=wl.shared_format)
     slabs, scales = li.slabs, li.scales
     if args.alias_experts:
         # profiling only: every expert pointer aliases expert 0's slab
@@ -280,7 +283,9 @@ def run_ours(args, rank, world, local_rank, dist_on):
     fused = T == 1 and moe.moe_uses_streaming_decode(layer.handle)
     # launches per step: the fused kernel; or router, gate/up, down; or router (+ activation
     # conversion when T > 8), gate/up, down, combine
-    kernels_per_step = 1 if fused else (3 if T == 1 else (4 if T <= 8 else 5))
+    # (T == 1 with an int8 expert runs the tensor-core flow: router, gate/up, down, combine)
+    t1_tensor = T == 1 and (wl.expert_format == 1 or (wl.n_shared and wl.shared_format == 1))
+    kernels_per_step = 1 if fused else ((4 if t1_tensor else 3) if T == 1 else (4 if T <= 8 else 5))
     stage_ms, n_calls, event_ms = None, 0, 0.0
     if not fused:
         # Per-kernel times: the same steps again with the library recording an
@@ -340,7 +345,8 @@ def run_ours(args, rank, world, local_rank, dist_on):
         dom_name = "gate/up + SwiGLU (int4 GEMV/GEMM), T=%d" % T
         n_r = mean_touched if T > 1 else wl.K
         units = n_r + wl.n_shared
-        dom_bytes = n_r * gateup_bytes(wl.H, wl.I) + (gateup_bytes(wl.H, wl.I_shared) if wl.n_shared else 0)
+        dom_bytes = (n_r * gateup_bytes(wl.H, wl.I, wl.expert_format) +
+                     (gateup_bytes(wl.H, wl.I_shared, wl.shared_format) if wl.n_shared else 0))
         dom_ms = stage_ms["gate_up"] - event_ms
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     tensor = T > 1 and moe.moe_uses_tensor_cores(layer.handle)
@@ -371,7 +377,7 @@ def run_ours(args, rank, world, local_rank, dist_on):
             "config": {
                 "workload": workload_desc(wl),
                 "tokens_per_step": T,
-                "experts_resident_GB": round(wl.E * expert_bytes(wl.H, wl.I) / 1e9, 3),
+                "experts_resident_GB": round(wl.E * expert_bytes(wl.H, wl.I, wl.expert_format) / 1e9, 3),
                 "l2": "flushed before every step (256 MiB write + 256 MiB read), outside the events",
                 "x_rotation": N_X,
                 "parallelism": f"{world} independent replicas (no collective on the data path)",

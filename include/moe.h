@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 /* y = x + moe(rmsnorm(x)) instead of y = moe(x). */
 #define MOE_FLAG_PRENORM_RESIDUAL 1u
@@ -84,7 +84,18 @@ typedef struct moe_config {
     int32_t topk_group;    /* groups kept when n_group > 1: 1..n_group, with
                               top_k <= topk_group * n_experts / n_group; ignored when n_group == 1 */
     int32_t score_func;    /* MOE_SCORE_SIGMOID (0) or MOE_SCORE_SOFTMAX (1) */
+    int32_t expert_format; /* routed experts: MOE_FORMAT_INT4 (0) or MOE_FORMAT_INT8 (1) */
+    int32_t shared_format; /* shared expert: MOE_FORMAT_INT4 (0) or MOE_FORMAT_INT8 (1) */
 } moe_config;
+
+/* Weight formats of an expert slab (both with one float32 scale per output row):
+ * INT4: gate [I, H/2] | up [I, H/2] | down [H, I/2] bytes, two values per byte;
+ * INT8: gate [I, H] | up [I, H] | down [H, I] bytes, one signed value per byte
+ *       (the OLMoE engine of the reader.mx page, section 03).  A config with an
+ *       int8 expert runs every call on the tensor-core expert kernels and needs
+ *       H, I and I_shared to be multiples of 128 (else MOE_ERR_UNSUPPORTED). */
+#define MOE_FORMAT_INT4 0
+#define MOE_FORMAT_INT8 1
 
 #define MOE_SCORE_SIGMOID 0   /* sigma = sigmoid(logit), selection by sigma + bias */
 #define MOE_SCORE_SOFTMAX 1   /* g = softmax(logits), selection by g, bias unused */
@@ -95,7 +106,8 @@ typedef struct moe_config {
  * per-expert pointer arrays themselves are HOST arrays of E entries; they are
  * copied at moe_init and not referenced afterwards.
  *
- * Expert slab (one per routed expert, and one for the shared expert):
+ * Expert slab (one per routed expert, and one for the shared expert), in the
+ * expert's format (MOE_FORMAT_*, below); int4:
  *     gate q4 [I, H/2] | up q4 [I, H/2] | down q4 [H, I/2]     uint8, row-major
  * Expert scales:
  *     gate s [I] | up s [I] | down s [H]                        float32

@@ -14,7 +14,7 @@ import numpy as np
 
 __all__ = [
     "MOE_OK", "MOE_ERR_INVALID", "MOE_ERR_CUDA", "MOE_ERR_NOMEM", "MOE_ERR_UNSUPPORTED",
-    "MOE_FLAG_PRENORM_RESIDUAL", "MOE_FLAG_TRACE", "MOE_FLAG_CUDA_CORES", "MOE_SCORE_SIGMOID", "MOE_SCORE_SOFTMAX", "MOE_TRACE_SLOTS", "moe_trace_read", "MoeError", "MoeConfig", "MoeWeights", "MoeLayer",
+    "MOE_FLAG_PRENORM_RESIDUAL", "MOE_FLAG_TRACE", "MOE_FLAG_CUDA_CORES", "MOE_SCORE_SIGMOID", "MOE_SCORE_SOFTMAX", "MOE_FORMAT_INT4", "MOE_FORMAT_INT8", "MOE_TRACE_SLOTS", "moe_trace_read", "MoeError", "MoeConfig", "MoeWeights", "MoeLayer",
     "lib", "library_path", "moe_init", "moe_forward", "moe_forward_debug", "moe_forward_host",
     "moe_destroy", "moe_last_error", "moe_workspace_bytes", "moe_abi_version",
     "moe_profile_start", "moe_profile_read", "moe_route_noalloc", "moe_device_error",
@@ -27,6 +27,7 @@ MOE_FLAG_TRACE = 2
 MOE_FLAG_CUDA_CORES = 4
 MOE_TRACE_SLOTS = 64
 MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
+MOE_FORMAT_INT4, MOE_FORMAT_INT8 = 0, 1
 _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CUDA", 3: "MOE_ERR_NOMEM",
            4: "MOE_ERR_UNSUPPORTED"}
 
@@ -46,7 +47,7 @@ class MoeConfig(C.Structure):
                 ("moe_inter", C.c_int32), ("n_shared", C.c_int32), ("shared_inter", C.c_int32),
                 ("n_group", C.c_int32), ("norm_topk", C.c_int32), ("routed_scale", C.c_float),
                 ("rms_eps", C.c_float), ("flags", C.c_uint32), ("topk_group", C.c_int32),
-                ("score_func", C.c_int32)]
+                ("score_func", C.c_int32), ("expert_format", C.c_int32), ("shared_format", C.c_int32)]
 
 
 class MoeWeights(C.Structure):
@@ -208,11 +209,12 @@ def moe_destroy(handle: int) -> None:
 
 def make_config(H, E, K, I, n_shared=0, I_shared=0, routed_scale=1.0, norm_topk=1,
                 prenorm_residual=False, rms_eps=1e-5, n_group=1, trace=False, topk_group=1,
-                score_func=0, cuda_cores=False) -> MoeConfig:
+                score_func=0, cuda_cores=False, expert_format=0, shared_format=0) -> MoeConfig:
     flags = ((MOE_FLAG_PRENORM_RESIDUAL if prenorm_residual else 0) | (MOE_FLAG_TRACE if trace else 0) |
              (MOE_FLAG_CUDA_CORES if cuda_cores else 0))
     return MoeConfig(H, E, K, I, n_shared, I_shared if n_shared else 0, n_group, norm_topk,
-                     float(routed_scale), float(rms_eps), flags, topk_group, score_func)
+                     float(routed_scale), float(rms_eps), flags, topk_group, score_func,
+                     expert_format, shared_format)
 
 
 def moe_trace_read(handle: int, capacity_blocks: int = 1024):

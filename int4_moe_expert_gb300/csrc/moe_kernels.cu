@@ -264,7 +264,7 @@ __device__ void bucket_phase(const Params &p, int T, int *ismem) {
         // (and of work items for the tensor-core kernels: kItemTokens tokens of one slot each)
         const int per = (E + 31) / 32;
         const int b = lane * per;
-        const bool items = p.d.mma && T > 1;
+        const bool items = p.d.mma && (T > 1 || p.d.int8_any);
         int s = 0, a = 0, c = 0;
         for (int i = 0; i < per; i++) {
             const int e = b + i;
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kThreads) router_gemv_kernel(Params p, const f
         const int t = i / H, c = i - t * H;
         const float v = x[i] * s_r[t];
         p.ws.xperm[(size_t)t * H + perm_pos(c, H)] = v;
-        if (p.d.mma && T > 1) p.ws.x16[(size_t)t * H + mma_pos(c)] = f2h_bits(v);
+        if (p.d.mma && (T > 1 || p.d.int8_any)) p.ws.x16[(size_t)t * H + mma_pos(c)] = f2h_bits(v);
     }
     gemv_logits(p, x, T, s_r);
     router_tail(p, T, buckets, gridDim.x, smem);
@@ -934,10 +934,14 @@ __device__ __forceinline__ uint32_t u4w(const uint4 &v, int i) {
 }
 
 constexpr int kMmaNT = kItemTokens / 8;     // n8 tiles per work item
-constexpr int kMmaStages = 4;               // k-blocks (128 elements) in the shared-memory ring
+constexpr int kMmaKB = 128;                 // reduction elements per ring stage (a multiple of 128)
+constexpr int kMmaSub = kMmaKB / 128;       // 128-element sub-blocks per stage
+constexpr int kMmaStages = 4;               // stages in the shared-memory ring
 constexpr int kMmaARows = 256;              // weight rows per block (GU: 128 gate + 128 up)
-constexpr int kMmaABytes = kMmaARows * 64;  // one k-block of them (int4)
-constexpr int kMmaBLd = 136;                // f16 per staged activation row (128 + 8: no bank conflicts)
+constexpr int kMmaARowB = kMmaKB / 2;       // bytes of one weight row per stage (int4)
+constexpr int kMmaABytes = kMmaARows * kMmaARowB;
+constexpr int kMmaBLd = kMmaKB + 8;         // f16 per staged activation row (+ 8: no bank conflicts)
+constexpr int kMmaBPieces = kMmaKB / 8;     // 16-byte copies per activation row per stage
 constexpr int kMmaBBytes = kItemTokens * kMmaBLd * 2;
 constexpr int kMmaStageBytes = kMmaABytes + kMmaBBytes;
 constexpr size_t kMmaSmem = (size_t)kMmaStages * kMmaStageBytes;
@@ -957,72 +961,90 @@ __device__ __forceinline__ uint4 lds128_u(uint32_t addr) {
     return v;
 }
 
-// One work item times one tile of output rows.  GU (gate/up + SwiGLU): warp w
-// owns output rows o0 + 16 w + {0..15}, as two m16 tiles: those gate rows and
-// the same up rows; 128 rows per block; writes h16.  Down: warp w owns rows
-// o0 + 32 w + {0..31} (two m16 tiles), 256 rows per block; writes dbuf.
-// Weights (256 rows x 64 bytes per k-block) and the item's activations
-// (kItemTokens rows x 256 bytes) move through a kMmaStages-deep ring in shared
-// memory with cp.async; every k-block is one __syncthreads.
-template <bool GU>
-__global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T) {
-    extern __shared__ __align__(128) unsigned char mma_smem[];
-    __shared__ int s_brow[kItemTokens], s_orow[kItemTokens];
-    const int item = blockIdx.x;
-    if (item >= *p.ws.n_items) return;
-    const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
-    const SlotInfo s = slot_info(p, T, slot);
-    if (!s.valid) return;
+// 8 signed int8 weights e0..e7 (bytes of lo = e0..e3, hi = e4..e7) -> the f16x2 pairs
+// (e0,e4), (e1,e5), (e2,e6), (e3,e7), exact: the byte with its sign bit flipped is
+// e + 128 in [0, 255], so 0x6400 | (e + 128) is the f16 1024 + e + 128; subtract 1152.
+__device__ __forceinline__ void int8x8_to_f16x2(uint32_t lo, uint32_t hi, uint32_t (&h)[4]) {
+    constexpr uint32_t kMagic = 0x64006400u;   // f16 1024 in both halves
+    constexpr uint32_t kSub = 0x64806480u;     // 1152 = 1024 + 128
+    lo ^= 0x80808080u;
+    hi ^= 0x80808080u;
+    h[0] = h2_sub((__byte_perm(lo, hi, 0x0400) & 0x00FF00FFu) | kMagic, kSub);
+    h[1] = h2_sub((__byte_perm(lo, hi, 0x0501) & 0x00FF00FFu) | kMagic, kSub);
+    h[2] = h2_sub((__byte_perm(lo, hi, 0x0602) & 0x00FF00FFu) | kMagic, kSub);
+    h[3] = h2_sub((__byte_perm(lo, hi, 0x0703) & 0x00FF00FFu) | kMagic, kSub);
+}
+
+// Per-format layout of the weight half of a ring stage.  int4: a row's stage segment is
+// kMmaKB / 2 bytes, stored unpadded (16-byte reads of rows 64 bytes apart are
+// conflict-free); int8: kMmaKB bytes, rows padded by 16 bytes (a 128-byte stride would put
+// a warp's eight rows on the same banks); two stages only, so both fit one allocation.
+template <int FMT>
+struct MmaFmt {
+    static constexpr int kRowB = FMT == MOE_FORMAT_INT8 ? kMmaKB : kMmaKB / 2;   // global bytes per row
+    static constexpr int kSRow = FMT == MOE_FORMAT_INT8 ? kRowB + 16 : kRowB;     // shared stride
+    static constexpr int kPcs = kRowB / 16;                                      // 16-byte pieces per row
+    static constexpr int kABytes = kMmaARows * kSRow;
+    static constexpr int kStage = kABytes + kMmaBBytes;
+    static constexpr int kStages = FMT == MOE_FORMAT_INT8 ? 2 : kMmaStages;
+    static constexpr int kThrB = FMT == MOE_FORMAT_INT8 ? 32 : 16;               // a thread's bytes per row per sub-block
+};
+static_assert((size_t)MmaFmt<MOE_FORMAT_INT8>::kStages * MmaFmt<MOE_FORMAT_INT8>::kStage <= kMmaSmem,
+              "the int8 ring fits the int4 ring's shared memory");
+
+// One work item times one tile of output rows (see mma_expert_kernel), weights in format FMT.
+template <bool GU, int FMT>
+__device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo &s, int nt, int o0,
+                                         unsigned char *mma_smem, const int *s_brow, const int *s_orow) {
+    using F = MmaFmt<FMT>;
     const int H = p.d.H, Is = s.Is;
     const int rows = GU ? Is : H;                       // output rows of the slot
-    const int o0 = blockIdx.y * (GU ? 128 : 256);
-    if (o0 >= rows) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
-    const int nt = min(kItemTokens, s.n - n0);
-    if (tid < kItemTokens) {
-        int tok = 0, row = -1;
-        if (tid < nt) slot_token(p, s, T, n0 + tid, &tok, &row);
-        s_brow[tid] = GU ? tok : row;          // activation row the tensor cores read
-        s_orow[tid] = row;                     // output row (h16 / dbuf)
-    }
-    __syncthreads();
     const int Kd = GU ? H : Is;                          // reduction length
-    const size_t arb = (size_t)(Kd >> 1);                // weight row bytes
-    const uint8_t *abase = GU ? s.slab : s.slab + (size_t)2 * Is * (size_t)(H >> 1);
+    const size_t arb = FMT == MOE_FORMAT_INT8 ? (size_t)Kd : (size_t)(Kd >> 1);   // weight row bytes
+    const uint8_t *abase = GU ? s.slab : s.slab + 2 * (size_t)Is * (FMT == MOE_FORMAT_INT8 ? H : H >> 1);
     const uint16_t *act = GU ? p.ws.x16 : p.ws.h16;
     const size_t ald = GU ? (size_t)H : (size_t)p.d.I_max;     // activation row stride (f16)
-    // this thread's cp.async pieces of one k-block: weights 4 x 16 B, activations 2 x 16 B
-    const uint8_t *asrc[4];
-    uint32_t adst[4];
-    bool aok[4];
+    // this thread's cp.async pieces of one stage
+    constexpr int kAP = F::kPcs, kBP = kItemTokens * kMmaBPieces / kThreads;   // copies per thread
+    const uint8_t *asrc[kAP];
+    uint32_t adst[kAP];
+    int apiece[kAP];
+    bool aok[kAP];
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const int c = tid + i * kThreads, lr = c >> 2, piece = c & 3;
+    for (int i = 0; i < kAP; i++) {
+        const int c = tid + i * kThreads, lr = c / F::kPcs, piece = c % F::kPcs;
         const int gr = GU ? (lr < 128 ? o0 + lr : Is + o0 + lr - 128) : o0 + lr;
         aok[i] = GU || gr < H;
+        apiece[i] = piece;
         asrc[i] = abase + (size_t)(aok[i] ? gr : 0) * arb + piece * 16;
-        adst[i] = (uint32_t)(lr * 64 + piece * 16);
+        adst[i] = (uint32_t)(lr * F::kSRow + piece * 16);
     }
-    const uint16_t *bsrc[2];
-    uint32_t bdst[2];
-    bool bok[2];                                   // rows of n8 tiles that are computed
+    const uint16_t *bsrc[kBP];
+    uint32_t bdst[kBP];
+    int bpiece[kBP];
+    bool bok[kBP];                                 // rows of n8 tiles that are computed
 #pragma unroll
-    for (int i = 0; i < 2; i++) {
-        const int c = tid + i * kThreads, n = c >> 4, piece = c & 15;
+    for (int i = 0; i < kBP; i++) {
+        const int c = tid + i * kThreads, n = c / kMmaBPieces, piece = c % kMmaBPieces;
         bok[i] = n < ((nt + 7) & ~7);
+        bpiece[i] = piece;
         bsrc[i] = act + (size_t)s_brow[n < nt ? n : 0] * ald + piece * 8;
-        bdst[i] = (uint32_t)(kMmaABytes + (n * kMmaBLd + piece * 8) * 2);
+        bdst[i] = (uint32_t)(F::kABytes + (n * kMmaBLd + piece * 8) * 2);
     }
     const uint32_t sbase = smem_u32(mma_smem);
-    const int nkb = Kd >> 7;
+    const int nkb = (Kd + kMmaKB - 1) / kMmaKB;     // the last stage may hold fewer sub-blocks
     auto issue = [&](int kb) {
-        const uint32_t st = sbase + (uint32_t)((kb % kMmaStages) * kMmaStageBytes);
+        const uint32_t st = sbase + (uint32_t)((kb % F::kStages) * F::kStage);
+        const int valid = min(kMmaKB, Kd - kb * kMmaKB);   // elements of this stage
+        constexpr int kElemPerPiece = FMT == MOE_FORMAT_INT8 ? 16 : 32;
 #pragma unroll
-        for (int i = 0; i < 4; i++)
-            if (aok[i]) cp_async16(st + adst[i], asrc[i] + (size_t)kb * 64);
+        for (int i = 0; i < kAP; i++)
+            if (aok[i] && apiece[i] * kElemPerPiece < valid)
+                cp_async16(st + adst[i], asrc[i] + (size_t)kb * F::kRowB);
 #pragma unroll
-        for (int i = 0; i < 2; i++)
-            if (bok[i]) cp_async16(st + bdst[i], bsrc[i] + (size_t)kb * 128);
+        for (int i = 0; i < kBP; i++)
+            if (bok[i] && bpiece[i] * 8 < valid) cp_async16(st + bdst[i], bsrc[i] + (size_t)kb * kMmaKB);
     };
     const int ob = o0 + (GU ? 16 : 32) * warp;            // the warp's first output row
     const bool active = ob < rows;                         // (rows are multiples of 128)
@@ -1031,14 +1053,14 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
     {
         const int l0 = GU ? 16 * warp + g : 32 * warp + g;
         const int l1 = GU ? 128 + 16 * warp + g : 32 * warp + 16 + g;
-        aoff[0] = (uint32_t)(l0 * 64 + q * 16);
-        aoff[1] = aoff[0] + 8 * 64;
-        aoff[2] = (uint32_t)(l1 * 64 + q * 16);
-        aoff[3] = aoff[2] + 8 * 64;
+        aoff[0] = (uint32_t)(l0 * F::kSRow + q * F::kThrB);
+        aoff[1] = aoff[0] + 8 * F::kSRow;
+        aoff[2] = (uint32_t)(l1 * F::kSRow + q * F::kThrB);
+        aoff[3] = aoff[2] + 8 * F::kSRow;
     }
     uint32_t boff[kMmaNT];
 #pragma unroll
-    for (int j = 0; j < kMmaNT; j++) boff[j] = (uint32_t)(kMmaABytes + ((8 * j + g) * kMmaBLd + 32 * q) * 2);
+    for (int j = 0; j < kMmaNT; j++) boff[j] = (uint32_t)(F::kABytes + ((8 * j + g) * kMmaBLd + 32 * q) * 2);
     const int ntiles = (nt + 7) >> 3;
     float acc[2][kMmaNT][4];
 #pragma unroll
@@ -1048,38 +1070,53 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
 #pragma unroll
             for (int c = 0; c < 4; c++) acc[t][j][c] = 0.0f;
 #pragma unroll
-    for (int k = 0; k < kMmaStages - 1; k++) {
+    for (int k = 0; k < F::kStages - 1; k++) {
         if (k < nkb) issue(k);
         cp_async_commit();
     }
 #pragma unroll 1
     for (int kb = 0; kb < nkb; kb++) {
-        cp_async_wait<kMmaStages - 2>();     // this thread's pieces of k-block kb have landed
+        cp_async_wait<F::kStages - 2>();     // this thread's pieces of stage kb have landed
         __syncthreads();                     // everyone's have; everyone is done with kb - 1
-        if (kb + kMmaStages - 1 < nkb) issue(kb + kMmaStages - 1);
+        if (kb + F::kStages - 1 < nkb) issue(kb + F::kStages - 1);
         cp_async_commit();
         if (!active) continue;
-        const uint32_t st = sbase + (uint32_t)((kb % kMmaStages) * kMmaStageBytes);
-        uint4 a[4];
+        const uint32_t st = sbase + (uint32_t)((kb % F::kStages) * F::kStage);
+        const int nsub = min(kMmaSub, (Kd - kb * kMmaKB) >> 7);
 #pragma unroll
-        for (int i = 0; i < 4; i++) a[i] = lds128_u(st + aoff[i]);
+        for (int sb = 0; sb < kMmaSub; sb++) {       // 128-element sub-blocks of the stage
+            if (sb >= nsub) break;
+            constexpr int kW = FMT == MOE_FORMAT_INT8 ? 2 : 1;     // 16-byte reads per row
+            uint4 a[4][kW];
 #pragma unroll
-        for (int w = 0; w < 4; w++) {            // word w: k-steps 2w (pairs 0, 1) and 2w + 1 (pairs 2, 3)
-            uint32_t h[4][4];
+            for (int i = 0; i < 4; i++)
 #pragma unroll
-            for (int i = 0; i < 4; i++) int4x8_to_f16x2(u4w(a[i], w), h[i]);
+                for (int r = 0; r < kW; r++) a[i][r] = lds128_u(st + aoff[i] + F::kThrB * 4 * sb + 16 * r);
 #pragma unroll
-            for (int j = 0; j < kMmaNT; j++)
-                if (j < ntiles) {
-                    const uint4 b = lds128_u(st + boff[j] + 16 * w);
+            for (int w = 0; w < 4; w++) {        // group w: k-steps 2w (pairs 0, 1) and 2w + 1 (pairs 2, 3)
+                uint32_t h[4][4];
 #pragma unroll
-                    for (int ss = 0; ss < 2; ss++) {
-                        const int lo = 2 * ss, hi = 2 * ss + 1;
-                        const uint32_t b0 = u4w(b, lo), b1 = u4w(b, hi);
-                        mma_f16(acc[0][j], h[0][lo], h[1][lo], h[0][hi], h[1][hi], b0, b1);
-                        mma_f16(acc[1][j], h[2][lo], h[3][lo], h[2][hi], h[3][hi], b0, b1);
+                for (int i = 0; i < 4; i++) {
+                    if constexpr (FMT == MOE_FORMAT_INT8) {   // words 2w, 2w + 1 of the 32 bytes
+                        const uint4 &v = a[i][w >> 1];
+                        int8x8_to_f16x2(u4w(v, (2 * w) & 3), u4w(v, (2 * w + 1) & 3), h[i]);
+                    } else {
+                        int4x8_to_f16x2(u4w(a[i][0], w), h[i]);
                     }
                 }
+#pragma unroll
+                for (int j = 0; j < kMmaNT; j++)
+                    if (j < ntiles) {
+                        const uint4 b = lds128_u(st + boff[j] + 256 * sb + 16 * w);
+#pragma unroll
+                        for (int ss = 0; ss < 2; ss++) {
+                            const int lo = 2 * ss, hi = 2 * ss + 1;
+                            const uint32_t b0 = u4w(b, lo), b1 = u4w(b, hi);
+                            mma_f16(acc[0][j], h[0][lo], h[1][lo], h[0][hi], h[1][hi], b0, b1);
+                            mma_f16(acc[1][j], h[2][lo], h[3][lo], h[2][hi], h[3][hi], b0, b1);
+                        }
+                    }
+            }
         }
     }
     cp_async_wait<0>();
@@ -1119,6 +1156,40 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
                     }
             }
     }
+}
+
+// One work item times one tile of output rows.  GU (gate/up + SwiGLU): warp w
+// owns output rows o0 + 16 w + {0..15}, as two m16 tiles: those gate rows and
+// the same up rows; 128 rows per block; writes h16.  Down: warp w owns rows
+// o0 + 32 w + {0..31} (two m16 tiles), 256 rows per block; writes dbuf.
+// Weights (256 rows per stage) and the item's activations (kItemTokens rows)
+// move through a ring in shared memory with cp.async; every stage is one
+// __syncthreads.  The slot's weight format (int4 or int8) picks the body.
+template <bool GU>
+__global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T) {
+    extern __shared__ __align__(128) unsigned char mma_smem[];
+    __shared__ int s_brow[kItemTokens], s_orow[kItemTokens];
+    const int item = blockIdx.x;
+    if (item >= *p.ws.n_items) return;
+    const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
+    const SlotInfo s = slot_info(p, T, slot);
+    if (!s.valid) return;
+    const int o0 = blockIdx.y * (GU ? 128 : 256);
+    if (o0 >= (GU ? s.Is : p.d.H)) return;
+    const int tid = threadIdx.x;
+    const int nt = min(kItemTokens, s.n - n0);
+    if (tid < kItemTokens) {
+        int tok = 0, row = -1;
+        if (tid < nt) slot_token(p, s, T, n0 + tid, &tok, &row);
+        s_brow[tid] = GU ? tok : row;          // activation row the tensor cores read
+        s_orow[tid] = row;                     // output row (h16 / dbuf)
+    }
+    __syncthreads();
+    const int fmt = s.base < 0 ? p.d.shared_fmt : p.d.expert_fmt;
+    if (fmt == MOE_FORMAT_INT8)
+        mma_body<GU, MOE_FORMAT_INT8>(p, T, s, nt, o0, mma_smem, s_brow, s_orow);
+    else
+        mma_body<GU, MOE_FORMAT_INT4>(p, T, s, nt, o0, mma_smem, s_brow, s_orow);
 }
 
 size_t router_smem_bytes(const Dims &d) {
@@ -1166,7 +1237,7 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
     ws->trace = reinterpret_cast<unsigned long long *>(
         take(d.trace ? (size_t)kTraceBlocks * MOE_TRACE_SLOTS * sizeof(unsigned long long) : 0));
     ws->dbuf = reinterpret_cast<float *>(take((P + T) * d.H * sizeof(float)));
-    const bool mma = d.mma != 0 && T > 1;
+    const bool mma = d.mma != 0 && (T > 1 || d.int8_any);
     ws->x16 = reinterpret_cast<uint16_t *>(take(mma ? T * d.H * sizeof(uint16_t) : 0));
     ws->h16 = reinterpret_cast<uint16_t *>(take(mma ? (P + T) * d.I_max * sizeof(uint16_t) : 0));
     ws->items = reinterpret_cast<int *>(
@@ -1184,7 +1255,8 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
 // ---------------------------------------------------------------------------
 
 bool mma_supported(const Dims &d) {
-    return d.max_tokens > 1 && d.H % 128 == 0 && d.I % 128 == 0 && (!d.n_shared || d.I_sh % 128 == 0);
+    return (d.max_tokens > 1 || d.int8_any) && d.H % 128 == 0 && d.I % 128 == 0 &&
+           (!d.n_shared || d.I_sh % 128 == 0);
 }
 
 cudaError_t prepare_kernels(const Dims &d) {
@@ -1205,7 +1277,8 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
     const Dims &d = p.d;
     if (T == 1 && d.fast_decode) return launch_decode_fast(p, x, y, st, ev, want_buckets);
     const size_t smem = router_smem_bytes(d);
-    const int buckets = (T > 1 || want_buckets) ? 1 : 0;
+    const bool mma_all = d.mma && (T > 1 || d.int8_any);   // the tensor-core expert kernels
+    const int buckets = (T > 1 || want_buckets || mma_all) ? 1 : 0;
     cudaError_t e = cudaSuccess;
     auto mark = [&](int i) {
         if (ev && e == cudaSuccess) e = cudaEventRecord(ev[i], st);
@@ -1231,7 +1304,7 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
     }
     check();
     mark(1);
-    if (T == 1) {
+    if (T == 1 && !mma_all) {
         constexpr int RPW_GU = 2, RPW_D = 4;
         const dim3 g1((d.I_max + kWarps * RPW_GU - 1) / (kWarps * RPW_GU), d.K + d.n_shared);
         gateup_decode_kernel<RPW_GU><<<g1, kThreads, 0, st>>>(p);
@@ -1244,7 +1317,7 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
         mark(4);
         return e;
     }
-    if (d.mma) {
+    if (mma_all) {
         const int ni = max_items(T, d.K, d.E, d.n_shared);
         const dim3 g1(ni, d.I_max / 128);
         mma_expert_kernel<true><<<g1, kThreads, kMmaSmem, st>>>(p, T);

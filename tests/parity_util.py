@@ -15,7 +15,8 @@ W_RTOL = 1e-4      # routing weights, per expert id (float32 sigmoid vs double)
 def gpu_config(moe, wl):
     return moe.make_config(wl.H, wl.E, wl.K, wl.I, wl.n_shared, wl.I_shared, wl.routed_scale,
                            wl.norm_topk, wl.prenorm_residual, wl.rms_eps, n_group=wl.n_group,
-                           topk_group=wl.topk_group, score_func=wl.score_func)
+                           topk_group=wl.topk_group, score_func=wl.score_func,
+                           expert_format=wl.expert_format, shared_format=wl.shared_format)
 
 
 def upload(moe, wl, li, max_tokens):

@@ -37,8 +37,8 @@ def test_library_exports_every_declared_symbol(moe):
 
 
 def test_config_struct_layout_matches_header(moe):
-    # thirteen 4-byte fields, no padding
-    assert C.sizeof(moe.MoeConfig) == 52
+    # fifteen 4-byte fields, no padding
+    assert C.sizeof(moe.MoeConfig) == 60
     assert C.sizeof(moe.MoeWeights) == 6 * C.sizeof(C.c_void_p)
 
 
@@ -62,6 +62,10 @@ def test_workspace_bytes_validates_config(moe):
         moe.make_config(6144, 256, 8, 2048, 1, 2048, n_group=8, topk_group=4,
                         score_func=moe.MOE_SCORE_SOFTMAX),                    # groups need sigmoid
         moe.make_config(6144, 256, 8, 2048, 1, 2048, score_func=2),
+        moe.make_config(6144, 256, 8, 2048, 1, 2048, expert_format=2),
+        moe.make_config(6144, 256, 8, 2048, 1, 2048, shared_format=2),
+        moe.make_config(2048, 64, 8, 1056, expert_format=1),                  # int8: I % 128 != 0
+        moe.make_config(2048, 64, 8, 1024, expert_format=1, cuda_cores=True),  # int8: tensor cores only
         moe.make_config(6144, 2048, 8, 2048, 1, 2048),       # E > 1024
         moe.make_config(6144, 256, 8, 2048, 1, 2048, routed_scale=float("inf")),
     ]
@@ -72,7 +76,9 @@ def test_workspace_bytes_validates_config(moe):
         assert moe.moe_workspace_bytes(cfg, 1) == 0
     for cfg in (moe.make_config(6144, 256, 8, 2048, 1, 2048, 2.5, n_group=8, topk_group=4),
                 moe.make_config(2048, 64, 8, 1024, score_func=moe.MOE_SCORE_SOFTMAX),
-                moe.make_config(2048, 64, 8, 1024, norm_topk=0, score_func=moe.MOE_SCORE_SOFTMAX)):
+                moe.make_config(2048, 64, 8, 1024, norm_topk=0, score_func=moe.MOE_SCORE_SOFTMAX),
+                moe.make_config(2048, 64, 8, 1024, expert_format=moe.MOE_FORMAT_INT8),
+                moe.make_config(6144, 256, 8, 2048, 1, 2048, shared_format=moe.MOE_FORMAT_INT8)):
         assert moe.moe_workspace_bytes(cfg, 4) > 0
     # the trace flag is accepted and adds the trace buffer (1024 blocks x 64 x 8 B)
     traced = moe.make_config(6144, 256, 8, 2048, 1, 2048, 2.5, trace=True)
@@ -100,7 +106,7 @@ def test_null_arguments_are_errors_not_crashes(moe):
 
 
 def test_abi_version(moe):
-    assert moe.moe_abi_version() == 2
+    assert moe.moe_abi_version() == 3
 
 
 def test_product_path_does_not_reference_the_oracle():

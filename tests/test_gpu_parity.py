@@ -215,6 +215,40 @@ def test_routing_variant_selection_differs_from_plain(moe):
     assert (np.sort(idx, 1) != np.sort(idx2.cpu().numpy(), 1)).any()
 
 
+# --- weight formats (int8 per-row experts) -----------------------------------------
+
+def test_int8_experts_olmoe_engine(moe):
+    """All routed experts int8, softmax top-8, probability as weight (the OLMoE engine)."""
+    wl, li, layer = layer_for(moe, "olmoe_int8", 64)
+    assert moe.moe_uses_tensor_cores(layer.handle) and not moe.moe_uses_streaming_decode(layer.handle)
+    for T in (1, 5, 40):
+        run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=300 + T), f"olmoe_int8 T={T}")
+
+
+def test_int8_shared_expert_glm(moe):
+    """GLM-5.2 layer with int4 routed experts and an int8 shared expert, full size."""
+    wl = synth.WORKLOADS["glm_int8_shared"]
+    li = synth.layer_inputs(wl)
+    layer = upload(moe, wl, li, 4)
+    for T in (1, 3):
+        run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=310 + T), f"glm_int8_shared T={T}")
+    layer.close()
+
+
+@pytest.mark.parametrize("kw", [
+    dict(H=128, I=128, I_shared=256, E=8, K=2, expert_format=1, shared_format=1),
+    dict(H=256, I=128, I_shared=128, E=8, K=2, shared_format=1),            # int4 routed, int8 shared
+    dict(H=384, I=256, n_shared=0, I_shared=0, E=6, K=6, expert_format=1),  # E == K, half-used down tiles
+])
+def test_int8_edge_configs(moe, kw):
+    wl = small_workload(**kw)
+    li = synth.layer_inputs(wl)
+    layer = upload(moe, wl, li, 40)
+    for T in (1, 2, 37):
+        run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=T), f"{kw} T={T}")
+    layer.close()
+
+
 # --- 40-layer stack (x <- x + moe(rmsnorm(x))) -------------------------------------
 
 def test_stack_35b_40_layers(moe):
