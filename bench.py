@@ -48,13 +48,13 @@ TRAFFIC_FILES = {
 
 def expert_bytes(H: int, I: int, fmt: int = 0) -> int:
     """Gate/up/down weight bytes (int4 packed or int8) + float32 per-row scales of one expert."""
-    return synth.slab_bytes(H, I, fmt) + 4 * synth.scale_count(H, I)
+    return synth.slab_bytes(H, I, fmt) + 4 * synth.scale_count(H, I, fmt)
 
 
 def gateup_bytes(H: int, I: int, fmt: int = 0) -> int:
     """Bytes the gate/up kernel must read for one expert: two [I, H] weight
     matrices (H/2 bytes per int4 row, H per int8 row) and their 2I float32 scales."""
-    return 2 * I * (H if fmt == 1 else (H + 1) // 2) + 8 * I
+    return 2 * I * (H if fmt == 1 else (H + 1) // 2) + (2 * I * H // 64 * 4 if fmt == 2 else 8 * I)
 
 
 def step_bytes(wl, T: int, touched: int) -> int:

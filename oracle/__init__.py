@@ -42,7 +42,7 @@ class Cfg(C.Structure):
 
 
 SCORE_SIGMOID, SCORE_SOFTMAX = 0, 1
-FORMAT_INT4, FORMAT_INT8 = 0, 1
+FORMAT_INT4, FORMAT_INT8, FORMAT_G64 = 0, 1, 2
 
 
 class Layer(C.Structure):

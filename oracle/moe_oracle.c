@@ -119,11 +119,52 @@ void oracle_quantize_int8(const float *w, int O, int I, int8_t *q, float *scale)
     }
 }
 
+/* IEEE binary16 bit pattern -> double (exact). */
+static double half_to_double(uint16_t h) {
+    const int sgn = h >> 15, ex = (h >> 10) & 31, man = h & 1023;
+    double v;
+    if (ex == 0) v = ldexp((double)man, -24);                      /* zero, subnormal */
+    else if (ex == 31) v = man ? NAN : INFINITY;
+    else v = ldexp((double)(man + 1024), ex - 25);
+    return sgn ? -v : v;
+}
+
+/* out[o] = sum_i (s_{o,i/64} u[o,i] + b_{o,i/64}) v[i] over one affine-int4 [O, n]
+ * matrix: packed rows of n/2 bytes, (s, b) float16 pairs [O][n/64]. */
+static void g64_matvec(const uint8_t *q4, const uint16_t *sb, int O, int n, const double *v, double *out) {
+    const int rb = n / 2, ng = n / 64;
+#pragma omp parallel for schedule(static)
+    for (int o = 0; o < O; o++) {
+        const uint8_t *row = q4 + (int64_t)o * rb;
+        double acc = 0.0;
+        for (int i = 0; i < n; i++) {
+            const int u = (i & 1) ? (row[i >> 1] >> 4) : (row[i >> 1] & 15);
+            const uint16_t *p = sb + 2 * ((int64_t)o * ng + i / 64);
+            acc += (half_to_double(p[0]) * u + half_to_double(p[1])) * v[i];
+        }
+        out[o] = acc;
+    }
+}
+
 /* Section 11 expert in either weight format: g = W_g x, u = W_u x,
  * h = silu(g) * u, d = W_d h.  int8 slab: gate [I, H] | up [I, H] | down [H, I]
  * bytes, signed, one float32 scale per output row as for int4. */
 void oracle_expert_fmt(int H, int I, int format, const uint8_t *slab, const float *scale,
                        const double *x, double *d_out, double *h_out) {
+    if (format == ORACLE_FORMAT_G64) {
+        const int64_t rbH = H / 2;
+        const uint16_t *sb = (const uint16_t *)scale;
+        double *g = (double *)malloc(sizeof(double) * I);
+        double *u = (double *)malloc(sizeof(double) * I);
+        double *h = (double *)malloc(sizeof(double) * I);
+        g64_matvec(slab, sb, I, H, x, g);
+        g64_matvec(slab + (int64_t)I * rbH, sb + 2 * (int64_t)I * (H / 64), I, H, x, u);
+        for (int i = 0; i < I; i++) h[i] = oracle_silu(g[i]) * u[i];
+        g64_matvec(slab + 2 * (int64_t)I * rbH, sb + 4 * (int64_t)I * (H / 64), H, I, h, d_out);
+        if (h_out) memcpy(h_out, h, sizeof(double) * I);
+        free(g); free(u); free(h);
+        return;
+    }
     if (format != ORACLE_FORMAT_INT8) {
         oracle_expert(H, I, slab, scale, x, d_out, h_out);
         return;
@@ -175,8 +216,10 @@ static int cfg_ok(const oracle_cfg *c) {
     if (!c || c->H <= 0 || c->E <= 0 || c->K <= 0 || c->K > c->E || c->I <= 0) return 0;
     if (!(c->n_shared == 0 || (c->n_shared == 1 && c->I_shared > 0))) return 0;
     if (c->score_func != ORACLE_SCORE_SIGMOID && c->score_func != ORACLE_SCORE_SOFTMAX) return 0;
-    if ((c->expert_format != ORACLE_FORMAT_INT4 && c->expert_format != ORACLE_FORMAT_INT8) ||
-        (c->shared_format != ORACLE_FORMAT_INT4 && c->shared_format != ORACLE_FORMAT_INT8)) return 0;
+    if (c->expert_format < ORACLE_FORMAT_INT4 || c->expert_format > ORACLE_FORMAT_G64 ||
+        c->shared_format < ORACLE_FORMAT_INT4 || c->shared_format > ORACLE_FORMAT_G64) return 0;
+    if ((c->expert_format == ORACLE_FORMAT_G64 || (c->n_shared && c->shared_format == ORACLE_FORMAT_G64)) &&
+        (c->H % 64 || c->I % 64 || (c->n_shared && c->I_shared % 64))) return 0;
     if (c->n_group < 1 || c->E % c->n_group != 0) return 0;
     if (c->n_group > 1) {
         if (c->score_func != ORACLE_SCORE_SIGMOID) return 0;

@@ -18,6 +18,8 @@
  *  - same page, section 04 "手写的基础数学": RMSNorm and SiLU.
  *  - same page, section 03 (the OLMoE engine): int8 expert weights, one signed
  *    byte per value and one float32 scale per row (quantize_rows, bits = 8).
+ *  - Edge0 article, section 三: int4 affine with group size 64 (1.77 MB per
+ *    expert of the 35B-class model, group scales included).
  *  - Edge0 article (magicnetworld.com), section 七 "路由数学": renormalised
  *    sigmoid weights w_i = s * sigma_i / (sum_{j in S} sigma_j + 1e-20); the
  *    softmax-top-k family (g = softmax(logits), top-K of g, w_i = g_i / sum_S g)
@@ -62,6 +64,7 @@ typedef struct {
 
 #define ORACLE_FORMAT_INT4 0     /* section 06: two values per byte, q + 8, low nibble first */
 #define ORACLE_FORMAT_INT8 1     /* section 03 (OLMoE engine): one signed byte per value */
+#define ORACLE_FORMAT_G64 2      /* Edge0 article section 三: int4 affine, group size 64 */
 
 #define ORACLE_SCORE_SIGMOID 0   /* sigma = sigmoid(logit); selection by sigma + bias */
 #define ORACLE_SCORE_SOFTMAX 1   /* g = softmax(logits); selection by g; bias unused */
@@ -85,8 +88,13 @@ void oracle_quantize_int4(const float *w, int O, int I, uint8_t *q4, float *scal
  * arithmetic as printed. */
 void oracle_quantize_int8(const float *w, int O, int I, int8_t *q, float *scale);
 
-/* oracle_expert for either weight format (ORACLE_FORMAT_*); the int8 slab is
- * gate [I, H] | up [I, H] | down [H, I] signed bytes with the same scales. */
+/* oracle_expert for any weight format (ORACLE_FORMAT_*); the int8 slab is
+ * gate [I, H] | up [I, H] | down [H, I] signed bytes with the same scales.
+ * ORACLE_FORMAT_G64: the int4 slab layout with unsigned nibbles u in [0, 15]
+ * (element 2j low), and `scale` is not float32 but float16 pairs (s, b), one
+ * per 64 consecutive inputs of a row: gate [I][H/64] | up [I][H/64] |
+ * down [H][I/64], W[o,i] = s * u + b of the row's group i / 64 (H, I multiples
+ * of 64).  Read as uint16 bit patterns and widened exactly. */
 void oracle_expert_fmt(int H, int I, int format, const uint8_t *slab, const float *scale,
                        const double *x, double *d_out, double *h_out);
 

@@ -164,7 +164,8 @@ class Workload:
     n_group: int = 1        # > 1: group-limited selection (sigmoid family)
     topk_group: int = 1     # groups kept when n_group > 1
     score_func: int = 0     # 0 sigmoid (+ bias for selection), 1 softmax
-    expert_format: int = 0  # routed experts: 0 int4 (two per byte), 1 int8 (one signed byte)
+    expert_format: int = 0  # routed experts: 0 int4 (two per byte), 1 int8 (one signed byte),
+                            # 2 int4 affine group-64 (unsigned nibbles, float16 (scale, bias) per 64)
     shared_format: int = 0  # shared expert: same choice
 
     @property
@@ -188,8 +189,23 @@ def slab_bytes(H: int, I: int, fmt: int = 0) -> int:
     return 2 * I * ((H + 1) // 2) + H * ((I + 1) // 2)
 
 
-def scale_count(H: int, I: int) -> int:
+def scale_count(H: int, I: int, fmt: int = 0) -> int:
+    """4-byte words of one expert's scale buffer: float32 per output row (int4, int8), or
+    one float16 (scale, bias) pair per 64 inputs of every row (int4 affine group-64)."""
+    if fmt == 2:
+        return 3 * I * H // 64
     return 2 * I + H
+
+
+def _scales(key: int, H: int, I: int, fmt: int, lo: float, hi: float) -> np.ndarray:
+    if fmt != 2:
+        return uniform(key, scale_count(H, I), lo, hi)
+    n = scale_count(H, I, 2)
+    s = uniform(key, n, lo, hi).astype(np.float16)
+    # bias near -8 s, so that a group's weights s*u + b (u in 0..15) centre on zero
+    b = (-s.astype(np.float32) * (8.0 + uniform(key ^ 0x5bd1e995, n, -0.5, 0.5))).astype(np.float16)
+    pairs = s.view(np.uint16).astype(np.uint32) | (b.view(np.uint16).astype(np.uint32) << 16)
+    return pairs.view(np.float32)
 
 
 WORKLOADS = {
@@ -226,6 +242,11 @@ WORKLOADS = {
     # the GLM engine keeps it (section 06)
     "olmoe_int8": Workload("olmoe_int8", T=1, H=2048, E=64, K=8, I=1024, n_shared=0, I_shared=0,
                            routed_scale=1.0, seed=8, score_func=1, norm_topk=0, expert_format=1),
+    # the 35B-class layer of the Edge0 article with its int4 affine group-64 experts (1.77 MB
+    # each, scales included); routed and shared alike, one layer
+    "g64_35b": Workload("g64_35b", T=1, H=2048, E=256, K=4, I=512, n_shared=1, I_shared=512,
+                        routed_scale=1.0, seed=10, bias_dist=("normal", 0.0, 1.0), expert_format=2,
+                        shared_format=2),
     "glm_int8_shared": Workload("glm_int8_shared", T=1, H=6144, E=256, K=8, I=2048, n_shared=1,
                                 I_shared=2048, routed_scale=2.5, seed=9, shared_format=1),
 }
@@ -255,7 +276,7 @@ def expert_slab(wl: Workload, e: int, layer: int = 0) -> np.ndarray:
 
 
 def expert_scale(wl: Workload, e: int, layer: int = 0) -> np.ndarray:
-    return uniform(derive_key(wl.seed, layer, T_SCALE, e), scale_count(wl.H, wl.I),
+    return _scales(derive_key(wl.seed, layer, T_SCALE, e), wl.H, wl.I, wl.expert_format,
                    wl.scale_lo, wl.scale_hi)
 
 
@@ -264,7 +285,7 @@ def shared_slab(wl: Workload, layer: int = 0) -> np.ndarray:
 
 
 def shared_scale(wl: Workload, layer: int = 0) -> np.ndarray:
-    return uniform(derive_key(wl.seed, layer, T_SH_SCALE), scale_count(wl.H, wl.I_shared),
+    return _scales(derive_key(wl.seed, layer, T_SH_SCALE), wl.H, wl.I_shared, wl.shared_format,
                    wl.scale_lo, wl.scale_hi)
 
 
@@ -285,7 +306,7 @@ def layer_inputs(wl: Workload, layer: int = 0, experts=None) -> LayerInputs:
     (others are left zero), which is what the oracle needs at full size."""
     ids = range(wl.E) if experts is None else sorted(set(int(e) for e in experts))
     slabs = np.zeros((wl.E, wl.slab_bytes), dtype=np.uint8)
-    scales = np.zeros((wl.E, scale_count(wl.H, wl.I)), dtype=np.float32)
+    scales = np.zeros((wl.E, scale_count(wl.H, wl.I, wl.expert_format)), dtype=np.float32)
     for e in ids:
         slabs[e] = expert_slab(wl, e, layer)
         scales[e] = expert_scale(wl, e, layer)

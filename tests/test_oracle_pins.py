@@ -234,6 +234,64 @@ def test_int8_layer_single_expert_and_shared_format():
     assert w[0] == pytest.approx(2.5, rel=1e-15)
 
 
+# --- int4 affine group-64 (Edge0 article, section 三) -----------------------------------
+
+def test_g64_expert_bytes_match_the_pages_1_77MB_figure():
+    # 35B-class expert (H 2048, I 512): int4 payload plus one float16 (scale, bias) per 64
+    b = synth.slab_bytes(2048, 512, 2) + 4 * synth.scale_count(2048, 512, 2)
+    assert b == 1_572_864 + 196_608 == 1_769_472
+    assert round(b / 1e6, 2) == 1.77
+
+
+def _g64_pairs(s, b):
+    s16, b16 = np.asarray(s, np.float16), np.asarray(b, np.float16)
+    return (s16.view(np.uint16).astype(np.uint32) | (b16.view(np.uint16).astype(np.uint32) << 16)).view(np.float32)
+
+
+def _g64_dense(slab, pairs, O, n):
+    q = np.zeros((O, n))
+    q[:, 0::2] = (slab.reshape(O, n // 2) & 15)
+    q[:, 1::2] = (slab.reshape(O, n // 2) >> 4)
+    u = pairs.view(np.uint32)
+    s = (u & 0xFFFF).astype(np.uint16).view(np.float16).astype(np.float64).reshape(O, n // 64)
+    b = (u >> 16).astype(np.uint16).view(np.float16).astype(np.float64).reshape(O, n // 64)
+    return q * np.repeat(s, 64, 1) + np.repeat(b, 64, 1)
+
+
+def test_g64_expert_equals_dense_swiglu():
+    rng = np.random.default_rng(17)
+    H, I = 128, 64
+    slab = rng.integers(0, 256, synth.slab_bytes(H, I, 2), dtype=np.uint8)
+    ng = [I * H // 64, I * H // 64, H * I // 64]
+    s = rng.uniform(0.005, 0.02, sum(ng))
+    pairs = _g64_pairs(s, -s * rng.uniform(7.5, 8.5, sum(ng)))
+    x = rng.standard_normal(H)
+    o1, o2 = I * H // 2, 2 * I * H // 2
+    Wg = _g64_dense(slab[:o1], pairs[:ng[0]], I, H)
+    Wu = _g64_dense(slab[o1:o2], pairs[ng[0]:ng[0] + ng[1]], I, H)
+    Wd = _g64_dense(slab[o2:], pairs[ng[0] + ng[1]:], H, I)
+    g = Wg @ x
+    want = Wd @ (g * expit(g) * (Wu @ x))
+    d, _ = oracle.expert(H, I, slab, pairs, x, fmt=oracle.FORMAT_G64)
+    np.testing.assert_allclose(d, want, rtol=1e-10, atol=1e-12)
+
+
+def test_g64_with_bias_minus_8s_is_the_symmetric_int4_expert():
+    # u - 8 = q: with b = -8 s in every group of a row, affine = symmetric int4 with scale s
+    rng = np.random.default_rng(23)
+    H, I = 128, 64
+    slab = rng.integers(0, 256, synth.slab_bytes(H, I), dtype=np.uint8)
+    row_s = np.float16(rng.uniform(0.005, 0.02, 2 * I + H)).astype(np.float32)   # f16-exact scales
+    per_row = np.concatenate([np.repeat(row_s[:I], H // 64), np.repeat(row_s[I:2 * I], H // 64),
+                              np.repeat(row_s[2 * I:], I // 64)])
+    pairs = _g64_pairs(per_row, -8 * per_row)
+    x = rng.standard_normal(H)
+    d4, h4 = oracle.expert(H, I, slab, row_s, x)
+    dg, hg = oracle.expert(H, I, slab, pairs, x, fmt=oracle.FORMAT_G64)
+    np.testing.assert_allclose(hg, h4, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(dg, d4, rtol=1e-12, atol=1e-14)
+
+
 # --- router (section 11; Edge0 section 七) ------------------------------------
 
 def _route_scores(c_values, K, x=None):
