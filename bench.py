@@ -66,14 +66,17 @@ def step_bytes(wl, T: int, touched: int) -> int:
     return b + 2 * T * wl.H * 4
 
 
+FORMAT_NAMES = {0: "int4 per-row", 1: "int8 per-row", 2: "int4 affine group-64"}
+
+
 def workload_desc(wl) -> str:
     route = ("softmax top-k" if wl.score_func == 1 else
              f"sigmoid+bias noaux_tc n_group={wl.n_group}" + (f" topk_group={wl.topk_group}" if wl.n_group > 1 else ""))
     s = (f"{wl.name}: T={wl.T}, H={wl.H}, E={wl.E} routed, top-{wl.K}, moe_inter={wl.I}, "
          f"{wl.n_shared} shared (inter {wl.I_shared}), {route}, "
          f"{'norm_topk' if wl.norm_topk else 'no renorm'}, routed_scale={wl.routed_scale}, "
-         f"{'int8' if wl.expert_format == 1 else 'int4'} per-row routed weights"
-         + (f", {'int8' if wl.shared_format == 1 else 'int4'} shared" if wl.n_shared else "")
+         f"{FORMAT_NAMES[wl.expert_format]} routed weights"
+         + (f", {FORMAT_NAMES[wl.shared_format]} shared" if wl.n_shared else "")
          + f", seed {wl.seed}")
     if wl.n_layers > 1:
         s += f", {wl.n_layers} chained layers x <- x + moe(rmsnorm(x))"
@@ -284,7 +287,7 @@ def run_ours(args, rank, world, local_rank, dist_on):
     # launches per step: the fused kernel; or router, gate/up, down; or router (+ activation
     # conversion when T > 8), gate/up, down, combine
     # (T == 1 with an int8 expert runs the tensor-core flow: router, gate/up, down, combine)
-    t1_tensor = T == 1 and (wl.expert_format == 1 or (wl.n_shared and wl.shared_format == 1))
+    t1_tensor = T == 1 and (wl.expert_format != 0 or (wl.n_shared and wl.shared_format != 0))
     kernels_per_step = 1 if fused else ((4 if t1_tensor else 3) if T == 1 else (4 if T <= 8 else 5))
     stage_ms, n_calls, event_ms = None, 0, 0.0
     if not fused:

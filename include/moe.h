@@ -88,14 +88,23 @@ typedef struct moe_config {
     int32_t shared_format; /* shared expert: MOE_FORMAT_INT4 (0) or MOE_FORMAT_INT8 (1) */
 } moe_config;
 
-/* Weight formats of an expert slab (both with one float32 scale per output row):
- * INT4: gate [I, H/2] | up [I, H/2] | down [H, I/2] bytes, two values per byte;
+/* Weight formats of an expert slab:
+ * INT4: gate [I, H/2] | up [I, H/2] | down [H, I/2] bytes, two values per byte
+ *       (q + 8, low nibble first); scale buffer: one float32 per output row,
+ *       sg [I] | su [I] | sd [H].
  * INT8: gate [I, H] | up [I, H] | down [H, I] bytes, one signed value per byte
- *       (the OLMoE engine of the reader.mx page, section 03).  A config with an
- *       int8 expert runs every call on the tensor-core expert kernels and needs
- *       H, I and I_shared to be multiples of 128 (else MOE_ERR_UNSUPPORTED). */
+ *       (the OLMoE engine of the reader.mx page, section 03); scales as INT4.
+ * G64:  int4 affine, group size 64 (Edge0 article, section 三): the INT4 slab
+ *       layout holding unsigned nibbles u in [0, 15]; the scale buffer holds one
+ *       float16 pair (s, b) (s in the low half of each 4-byte word) per 64
+ *       consecutive inputs of every row, gate [I][H/64] | up [I][H/64] |
+ *       down [H][I/64], and W = s * u + b.
+ * A config with an INT8 or G64 expert runs every call on the tensor-core expert
+ * kernels and needs H, I and I_shared to be multiples of 128 (else
+ * MOE_ERR_UNSUPPORTED); G64 weights are formed in f16 there (one rounding). */
 #define MOE_FORMAT_INT4 0
 #define MOE_FORMAT_INT8 1
+#define MOE_FORMAT_G64 2
 
 #define MOE_SCORE_SIGMOID 0   /* sigma = sigmoid(logit), selection by sigma + bias */
 #define MOE_SCORE_SOFTMAX 1   /* g = softmax(logits), selection by g, bias unused */

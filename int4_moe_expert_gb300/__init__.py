@@ -14,7 +14,7 @@ import numpy as np
 
 __all__ = [
     "MOE_OK", "MOE_ERR_INVALID", "MOE_ERR_CUDA", "MOE_ERR_NOMEM", "MOE_ERR_UNSUPPORTED",
-    "MOE_FLAG_PRENORM_RESIDUAL", "MOE_FLAG_TRACE", "MOE_FLAG_CUDA_CORES", "MOE_SCORE_SIGMOID", "MOE_SCORE_SOFTMAX", "MOE_FORMAT_INT4", "MOE_FORMAT_INT8", "MOE_TRACE_SLOTS", "moe_trace_read", "MoeError", "MoeConfig", "MoeWeights", "MoeLayer",
+    "MOE_FLAG_PRENORM_RESIDUAL", "MOE_FLAG_TRACE", "MOE_FLAG_CUDA_CORES", "MOE_SCORE_SIGMOID", "MOE_SCORE_SOFTMAX", "MOE_FORMAT_INT4", "MOE_FORMAT_INT8", "MOE_FORMAT_G64", "MOE_TRACE_SLOTS", "moe_trace_read", "MoeError", "MoeConfig", "MoeWeights", "MoeLayer",
     "lib", "library_path", "moe_init", "moe_forward", "moe_forward_debug", "moe_forward_host",
     "moe_destroy", "moe_last_error", "moe_workspace_bytes", "moe_abi_version",
     "moe_profile_start", "moe_profile_read", "moe_route_noalloc", "moe_device_error",
@@ -27,7 +27,7 @@ MOE_FLAG_TRACE = 2
 MOE_FLAG_CUDA_CORES = 4
 MOE_TRACE_SLOTS = 64
 MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
-MOE_FORMAT_INT4, MOE_FORMAT_INT8 = 0, 1
+MOE_FORMAT_INT4, MOE_FORMAT_INT8, MOE_FORMAT_G64 = 0, 1, 2
 _STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CUDA", 3: "MOE_ERR_NOMEM",
            4: "MOE_ERR_UNSUPPORTED"}
 

@@ -60,14 +60,14 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
         (c->shared_inter < 32 || c->shared_inter > 16384 || c->shared_inter % 32))
         return fail(MOE_ERR_UNSUPPORTED, "shared_inter=%d: need a multiple of 32 in [32, 16384]",
                     c->shared_inter);
-    if ((c->expert_format != MOE_FORMAT_INT4 && c->expert_format != MOE_FORMAT_INT8) ||
-        (c->shared_format != MOE_FORMAT_INT4 && c->shared_format != MOE_FORMAT_INT8))
-        return fail(MOE_ERR_INVALID, "expert_format / shared_format: need MOE_FORMAT_INT4 or MOE_FORMAT_INT8");
-    if (c->expert_format == MOE_FORMAT_INT8 || (c->n_shared && c->shared_format == MOE_FORMAT_INT8)) {
+    if (c->expert_format < MOE_FORMAT_INT4 || c->expert_format > MOE_FORMAT_G64 ||
+        c->shared_format < MOE_FORMAT_INT4 || c->shared_format > MOE_FORMAT_G64)
+        return fail(MOE_ERR_INVALID, "expert_format / shared_format: need a MOE_FORMAT_* value");
+    if (c->expert_format != MOE_FORMAT_INT4 || (c->n_shared && c->shared_format != MOE_FORMAT_INT4)) {
         if (c->hidden % 128 || c->moe_inter % 128 || (c->n_shared && c->shared_inter % 128))
-            return fail(MOE_ERR_UNSUPPORTED, "int8 experts need H, I and I_shared multiples of 128");
+            return fail(MOE_ERR_UNSUPPORTED, "int8 / group-64 experts need H, I and I_shared multiples of 128");
         if (c->flags & MOE_FLAG_CUDA_CORES)
-            return fail(MOE_ERR_UNSUPPORTED, "int8 experts run on the tensor-core kernels only");
+            return fail(MOE_ERR_UNSUPPORTED, "int8 / group-64 experts run on the tensor-core kernels only");
     }
     if (c->score_func != MOE_SCORE_SIGMOID && c->score_func != MOE_SCORE_SOFTMAX)
         return fail(MOE_ERR_INVALID, "score_func=%d: need MOE_SCORE_SIGMOID or MOE_SCORE_SOFTMAX", c->score_func);
@@ -103,7 +103,7 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
     d->score_func = c->score_func;
     d->expert_fmt = c->expert_format;
     d->shared_fmt = c->n_shared ? c->shared_format : MOE_FORMAT_INT4;
-    d->int8_any = (d->expert_fmt == MOE_FORMAT_INT8 || d->shared_fmt == MOE_FORMAT_INT8) ? 1 : 0;
+    d->mma_fmt = (d->expert_fmt != MOE_FORMAT_INT4 || d->shared_fmt != MOE_FORMAT_INT4) ? 1 : 0;
     d->prenorm = (c->flags & MOE_FLAG_PRENORM_RESIDUAL) ? 1 : 0;
     d->scale = c->routed_scale;
     d->eps = c->rms_eps;

@@ -858,7 +858,7 @@ int decode_grid_blocks() { return g_blocks; }
 
 bool decode_fast_supported(const Dims &d) {
     if (d.n_group != 1 || d.score_func != MOE_SCORE_SIGMOID) return false;   // routing variants: generic path
-    if (d.int8_any) return false;                                             // int8 experts: tensor-core kernels
+    if (d.mma_fmt) return false;                                             // int8 experts: tensor-core kernels
     if (d.H % kDnRows != 0 || d.H % 32 != 0 || d.I % 32 != 0) return false;
     if (d.n_shared && d.I_sh != d.I) return false;
     if (d.K + d.n_shared > kMaxSlots || d.K + d.n_shared > 32 || d.E > 1024) return false;

@@ -17,7 +17,7 @@ struct Dims {
     int n_group, topk_group;   // group-limited selection when n_group > 1
     int score_func;     // MOE_SCORE_SIGMOID / MOE_SCORE_SOFTMAX
     int expert_fmt, shared_fmt;   // MOE_FORMAT_INT4 / MOE_FORMAT_INT8
-    int int8_any;       // an int8 expert: every T runs the tensor-core expert kernels
+    int mma_fmt;        // an int8 or group-64 expert: every T runs the tensor-core expert kernels
     int prenorm;        // MOE_FLAG_PRENORM_RESIDUAL
     float scale;        // routed_scale
     float eps;          // rms_eps

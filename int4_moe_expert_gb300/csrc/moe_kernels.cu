@@ -264,7 +264,7 @@ __device__ void bucket_phase(const Params &p, int T, int *ismem) {
         // (and of work items for the tensor-core kernels: kItemTokens tokens of one slot each)
         const int per = (E + 31) / 32;
         const int b = lane * per;
-        const bool items = p.d.mma && (T > 1 || p.d.int8_any);
+        const bool items = p.d.mma && (T > 1 || p.d.mma_fmt);
         int s = 0, a = 0, c = 0;
         for (int i = 0; i < per; i++) {
             const int e = b + i;
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kThreads) router_gemv_kernel(Params p, const f
         const int t = i / H, c = i - t * H;
         const float v = x[i] * s_r[t];
         p.ws.xperm[(size_t)t * H + perm_pos(c, H)] = v;
-        if (p.d.mma && (T > 1 || p.d.int8_any)) p.ws.x16[(size_t)t * H + mma_pos(c)] = f2h_bits(v);
+        if (p.d.mma && (T > 1 || p.d.mma_fmt)) p.ws.x16[(size_t)t * H + mma_pos(c)] = f2h_bits(v);
     }
     gemv_logits(p, x, T, s_r);
     router_tail(p, T, buckets, gridDim.x, smem);
@@ -955,6 +955,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ uint32_t lds32_u(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
 __device__ __forceinline__ uint4 lds128_u(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
@@ -979,18 +984,41 @@ __device__ __forceinline__ void int8x8_to_f16x2(uint32_t lo, uint32_t hi, uint32
 // kMmaKB / 2 bytes, stored unpadded (16-byte reads of rows 64 bytes apart are
 // conflict-free); int8: kMmaKB bytes, rows padded by 16 bytes (a 128-byte stride would put
 // a warp's eight rows on the same banks); two stages only, so both fit one allocation.
+// Affine group-64 (G64): the int4 layout plus each row's float16 (scale, bias) pairs of the
+// stage's groups (8 bytes per row per 128 elements) after the activations; three stages.
 template <int FMT>
 struct MmaFmt {
     static constexpr int kRowB = FMT == MOE_FORMAT_INT8 ? kMmaKB : kMmaKB / 2;   // global bytes per row
     static constexpr int kSRow = FMT == MOE_FORMAT_INT8 ? kRowB + 16 : kRowB;     // shared stride
     static constexpr int kPcs = kRowB / 16;                                      // 16-byte pieces per row
     static constexpr int kABytes = kMmaARows * kSRow;
-    static constexpr int kStage = kABytes + kMmaBBytes;
-    static constexpr int kStages = FMT == MOE_FORMAT_INT8 ? 2 : kMmaStages;
+    static constexpr int kSBRow = FMT == MOE_FORMAT_G64 ? kMmaKB / 64 * 4 : 0;  // group pairs per row
+    static constexpr int kSBOff = kABytes + kMmaBBytes;
+    static constexpr int kStage = kSBOff + kMmaARows * kSBRow;
+    static constexpr int kStages = FMT == MOE_FORMAT_INT8 ? 2 : (FMT == MOE_FORMAT_G64 ? 3 : kMmaStages);
     static constexpr int kThrB = FMT == MOE_FORMAT_INT8 ? 32 : 16;               // a thread's bytes per row per sub-block
 };
 static_assert((size_t)MmaFmt<MOE_FORMAT_INT8>::kStages * MmaFmt<MOE_FORMAT_INT8>::kStage <= kMmaSmem,
               "the int8 ring fits the int4 ring's shared memory");
+static_assert((size_t)MmaFmt<MOE_FORMAT_G64>::kStages * MmaFmt<MOE_FORMAT_G64>::kStage <= kMmaSmem,
+              "the group-64 ring fits the int4 ring's shared memory");
+static_assert(kMmaKB == 128, "the group-64 pairs of a stage are staged as one 8-byte copy per row");
+
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// 8 packed unsigned nibbles (element 2j in the low nibble) -> f16x2 pairs of u in [0, 15],
+// (e0,e4), (e1,e5), (e2,e6), (e3,e7), exact; then w = s u + b, one f16 rounding.
+__device__ __forceinline__ void g64x8_to_f16x2(uint32_t w, uint32_t s2, uint32_t b2, uint32_t (&h)[4]) {
+    constexpr uint32_t kMagic = 0x64006400u;   // f16 1024
+    constexpr uint32_t kMulHi = 0x2C002C00u;   // 1/16
+    constexpr uint32_t kAddHi = 0xD400D400u;   // -64 = -1024/16
+    h[0] = h2_fma(h2_sub((w & 0x000F000Fu) | kMagic, kMagic), s2, b2);
+    h[1] = h2_fma(h2_fma((w & 0x00F000F0u) | kMagic, kMulHi, kAddHi), s2, b2);
+    h[2] = h2_fma(h2_sub(((w >> 8) & 0x000F000Fu) | kMagic, kMagic), s2, b2);
+    h[3] = h2_fma(h2_fma(((w >> 8) & 0x00F000F0u) | kMagic, kMulHi, kAddHi), s2, b2);
+}
 
 // One work item times one tile of output rows (see mma_expert_kernel), weights in format FMT.
 template <bool GU, int FMT>
@@ -1032,6 +1060,16 @@ __device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo 
         bsrc[i] = act + (size_t)s_brow[n < nt ? n : 0] * ald + piece * 8;
         bdst[i] = (uint32_t)(F::kABytes + (n * kMmaBLd + piece * 8) * 2);
     }
+    // G64: this thread copies the stage's (scale, bias) pairs of weight row `tid`
+    const uint32_t *pbsrc = nullptr;
+    bool pbok = false;
+    if constexpr (FMT == MOE_FORMAT_G64) {
+        const int lr = tid, gr = GU ? (lr < 128 ? o0 + lr : Is + o0 + lr - 128) : o0 + lr;
+        pbok = GU || gr < H;
+        const uint32_t *pairs = reinterpret_cast<const uint32_t *>(s.sc);
+        pbsrc = GU ? pairs + (size_t)(pbok ? gr : 0) * (Kd / 64)
+                   : pairs + 2 * (size_t)Is * (H / 64) + (size_t)(pbok ? gr : 0) * (Is / 64);
+    }
     const uint32_t sbase = smem_u32(mma_smem);
     const int nkb = (Kd + kMmaKB - 1) / kMmaKB;     // the last stage may hold fewer sub-blocks
     auto issue = [&](int kb) {
@@ -1045,6 +1083,9 @@ __device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo 
 #pragma unroll
         for (int i = 0; i < kBP; i++)
             if (bok[i] && bpiece[i] * 8 < valid) cp_async16(st + bdst[i], bsrc[i] + (size_t)kb * kMmaKB);
+        if constexpr (FMT == MOE_FORMAT_G64) {
+            if (pbok) cp_async8(st + F::kSBOff + tid * 8, pbsrc + (size_t)kb * (kMmaKB / 64));
+        }
     };
     const int ob = o0 + (GU ? 16 : 32) * warp;            // the warp's first output row
     const bool active = ob < rows;                         // (rows are multiples of 128)
@@ -1057,6 +1098,15 @@ __device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo 
         aoff[1] = aoff[0] + 8 * F::kSRow;
         aoff[2] = (uint32_t)(l1 * F::kSRow + q * F::kThrB);
         aoff[3] = aoff[2] + 8 * F::kSRow;
+    }
+    uint32_t sboff[4] = {0u, 0u, 0u, 0u};     // G64: the row's pair of the thread's group (q / 2)
+    if constexpr (FMT == MOE_FORMAT_G64) {
+        const int l0 = GU ? 16 * warp + g : 32 * warp + g;
+        const int l1 = GU ? 128 + 16 * warp + g : 32 * warp + 16 + g;
+        sboff[0] = (uint32_t)(F::kSBOff + l0 * 8 + (q >> 1) * 4);
+        sboff[1] = sboff[0] + 8 * 8;
+        sboff[2] = (uint32_t)(F::kSBOff + l1 * 8 + (q >> 1) * 4);
+        sboff[3] = sboff[2] + 8 * 8;
     }
     uint32_t boff[kMmaNT];
 #pragma unroll
@@ -1092,6 +1142,15 @@ __device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo 
             for (int i = 0; i < 4; i++)
 #pragma unroll
                 for (int r = 0; r < kW; r++) a[i][r] = lds128_u(st + aoff[i] + F::kThrB * 4 * sb + 16 * r);
+            uint32_t s2[4] = {0u, 0u, 0u, 0u}, b2[4] = {0u, 0u, 0u, 0u};   // G64: (s, s) and (b, b)
+            if constexpr (FMT == MOE_FORMAT_G64) {
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const uint32_t pr = lds32_u(st + sboff[i]);
+                    s2[i] = __byte_perm(pr, pr, 0x1010);
+                    b2[i] = __byte_perm(pr, pr, 0x3232);
+                }
+            }
 #pragma unroll
             for (int w = 0; w < 4; w++) {        // group w: k-steps 2w (pairs 0, 1) and 2w + 1 (pairs 2, 3)
                 uint32_t h[4][4];
@@ -1100,6 +1159,8 @@ __device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo 
                     if constexpr (FMT == MOE_FORMAT_INT8) {   // words 2w, 2w + 1 of the 32 bytes
                         const uint4 &v = a[i][w >> 1];
                         int8x8_to_f16x2(u4w(v, (2 * w) & 3), u4w(v, (2 * w + 1) & 3), h[i]);
+                    } else if constexpr (FMT == MOE_FORMAT_G64) {
+                        g64x8_to_f16x2(u4w(a[i][0], w), s2[i], b2[i], h[i]);
                     } else {
                         int4x8_to_f16x2(u4w(a[i][0], w), h[i]);
                     }
@@ -1126,7 +1187,8 @@ __device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo 
 #pragma unroll
         for (int rh = 0; rh < 2; rh++) {
             const int o = ob + g + 8 * rh;
-            const float sg = s.sc[o], su = s.sc[Is + o];
+            const float sg = FMT == MOE_FORMAT_G64 ? 1.0f : s.sc[o];     // G64: scales already applied
+            const float su = FMT == MOE_FORMAT_G64 ? 1.0f : s.sc[Is + o];
             const int pos = mma_pos(o);
 #pragma unroll
             for (int j = 0; j < kMmaNT; j++)
@@ -1146,7 +1208,7 @@ __device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo 
 #pragma unroll
             for (int rh = 0; rh < 2; rh++) {
                 const int o = ob + 16 * t + g + 8 * rh;
-                const float sc = sd[o];
+                const float sc = FMT == MOE_FORMAT_G64 ? 1.0f : sd[o];
 #pragma unroll
                 for (int j = 0; j < kMmaNT; j++)
 #pragma unroll
@@ -1164,8 +1226,10 @@ __device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo 
 // o0 + 32 w + {0..31} (two m16 tiles), 256 rows per block; writes dbuf.
 // Weights (256 rows per stage) and the item's activations (kItemTokens rows)
 // move through a ring in shared memory with cp.async; every stage is one
-// __syncthreads.  The slot's weight format (int4 or int8) picks the body.
-template <bool GU>
+// __syncthreads.  One instantiation per weight format: a launch serves the items
+// whose slot has format FMT (the routed experts share one format, the shared
+// expert may have another; the others return at once).
+template <bool GU, int FMT>
 __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T) {
     extern __shared__ __align__(128) unsigned char mma_smem[];
     __shared__ int s_brow[kItemTokens], s_orow[kItemTokens];
@@ -1174,6 +1238,7 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
     const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
     const SlotInfo s = slot_info(p, T, slot);
     if (!s.valid) return;
+    if ((s.base < 0 ? p.d.shared_fmt : p.d.expert_fmt) != FMT) return;
     const int o0 = blockIdx.y * (GU ? 128 : 256);
     if (o0 >= (GU ? s.Is : p.d.H)) return;
     const int tid = threadIdx.x;
@@ -1185,11 +1250,20 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
         s_orow[tid] = row;                     // output row (h16 / dbuf)
     }
     __syncthreads();
-    const int fmt = s.base < 0 ? p.d.shared_fmt : p.d.expert_fmt;
-    if (fmt == MOE_FORMAT_INT8)
-        mma_body<GU, MOE_FORMAT_INT8>(p, T, s, nt, o0, mma_smem, s_brow, s_orow);
-    else
-        mma_body<GU, MOE_FORMAT_INT4>(p, T, s, nt, o0, mma_smem, s_brow, s_orow);
+    mma_body<GU, FMT>(p, T, s, nt, o0, mma_smem, s_brow, s_orow);
+}
+
+// Launch the tensor-core kernels of one phase (gate/up or down) for every weight format
+// in use.
+template <bool GU>
+void launch_mma_phase(const Params &p, int T, dim3 grid, cudaStream_t st) {
+    const Dims &d = p.d;
+    for (int f = MOE_FORMAT_INT4; f <= MOE_FORMAT_G64; f++) {
+        if (f != d.expert_fmt && !(d.n_shared && f == d.shared_fmt)) continue;
+        if (f == MOE_FORMAT_INT8) mma_expert_kernel<GU, MOE_FORMAT_INT8><<<grid, kThreads, kMmaSmem, st>>>(p, T);
+        else if (f == MOE_FORMAT_G64) mma_expert_kernel<GU, MOE_FORMAT_G64><<<grid, kThreads, kMmaSmem, st>>>(p, T);
+        else mma_expert_kernel<GU, MOE_FORMAT_INT4><<<grid, kThreads, kMmaSmem, st>>>(p, T);
+    }
 }
 
 size_t router_smem_bytes(const Dims &d) {
@@ -1237,7 +1311,7 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
     ws->trace = reinterpret_cast<unsigned long long *>(
         take(d.trace ? (size_t)kTraceBlocks * MOE_TRACE_SLOTS * sizeof(unsigned long long) : 0));
     ws->dbuf = reinterpret_cast<float *>(take((P + T) * d.H * sizeof(float)));
-    const bool mma = d.mma != 0 && (T > 1 || d.int8_any);
+    const bool mma = d.mma != 0 && (T > 1 || d.mma_fmt);
     ws->x16 = reinterpret_cast<uint16_t *>(take(mma ? T * d.H * sizeof(uint16_t) : 0));
     ws->h16 = reinterpret_cast<uint16_t *>(take(mma ? (P + T) * d.I_max * sizeof(uint16_t) : 0));
     ws->items = reinterpret_cast<int *>(
@@ -1255,7 +1329,7 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
 // ---------------------------------------------------------------------------
 
 bool mma_supported(const Dims &d) {
-    return (d.max_tokens > 1 || d.int8_any) && d.H % 128 == 0 && d.I % 128 == 0 &&
+    return (d.max_tokens > 1 || d.mma_fmt) && d.H % 128 == 0 && d.I % 128 == 0 &&
            (!d.n_shared || d.I_sh % 128 == 0);
 }
 
@@ -1264,10 +1338,14 @@ cudaError_t prepare_kernels(const Dims &d) {
     cudaError_t e = cudaFuncSetAttribute(router_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(router_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e == cudaSuccess && d.mma)
-        e = cudaFuncSetAttribute(mma_expert_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmaSmem);
-    if (e == cudaSuccess && d.mma)
-        e = cudaFuncSetAttribute(mma_expert_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmaSmem);
+    if (d.mma) {
+        const void *ks[] = {
+            (const void *)mma_expert_kernel<true, MOE_FORMAT_INT4>, (const void *)mma_expert_kernel<false, MOE_FORMAT_INT4>,
+            (const void *)mma_expert_kernel<true, MOE_FORMAT_INT8>, (const void *)mma_expert_kernel<false, MOE_FORMAT_INT8>,
+            (const void *)mma_expert_kernel<true, MOE_FORMAT_G64>, (const void *)mma_expert_kernel<false, MOE_FORMAT_G64>};
+        for (const void *k : ks)
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmaSmem);
+    }
     if (e == cudaSuccess && d.fast_decode) e = prepare_decode_fast(d);
     return e;
 }
@@ -1277,7 +1355,7 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
     const Dims &d = p.d;
     if (T == 1 && d.fast_decode) return launch_decode_fast(p, x, y, st, ev, want_buckets);
     const size_t smem = router_smem_bytes(d);
-    const bool mma_all = d.mma && (T > 1 || d.int8_any);   // the tensor-core expert kernels
+    const bool mma_all = d.mma && (T > 1 || d.mma_fmt);   // the tensor-core expert kernels
     const int buckets = (T > 1 || want_buckets || mma_all) ? 1 : 0;
     cudaError_t e = cudaSuccess;
     auto mark = [&](int i) {
@@ -1320,11 +1398,11 @@ cudaError_t launch_forward(const Params &p, const float *x, int T, float *y, cud
     if (mma_all) {
         const int ni = max_items(T, d.K, d.E, d.n_shared);
         const dim3 g1(ni, d.I_max / 128);
-        mma_expert_kernel<true><<<g1, kThreads, kMmaSmem, st>>>(p, T);
+        launch_mma_phase<true>(p, T, g1, st);
         check();
         mark(2);
         const dim3 g2(ni, (d.H + 255) / 256);
-        mma_expert_kernel<false><<<g2, kThreads, kMmaSmem, st>>>(p, T);
+        launch_mma_phase<false>(p, T, g2, st);
         check();
         mark(3);
         combine_kernel<<<dim3(T, (d.H + 4 * kThreads - 1) / (4 * kThreads)), kThreads, 0, st>>>(p, x, y, T);

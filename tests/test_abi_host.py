@@ -62,10 +62,12 @@ def test_workspace_bytes_validates_config(moe):
         moe.make_config(6144, 256, 8, 2048, 1, 2048, n_group=8, topk_group=4,
                         score_func=moe.MOE_SCORE_SOFTMAX),                    # groups need sigmoid
         moe.make_config(6144, 256, 8, 2048, 1, 2048, score_func=2),
-        moe.make_config(6144, 256, 8, 2048, 1, 2048, expert_format=2),
-        moe.make_config(6144, 256, 8, 2048, 1, 2048, shared_format=2),
+        moe.make_config(6144, 256, 8, 2048, 1, 2048, expert_format=-1),
+        moe.make_config(6144, 256, 8, 2048, 1, 2048, shared_format=3),
         moe.make_config(2048, 64, 8, 1056, expert_format=1),                  # int8: I % 128 != 0
         moe.make_config(2048, 64, 8, 1024, expert_format=1, cuda_cores=True),  # int8: tensor cores only
+        moe.make_config(2048, 64, 8, 1056, expert_format=2),                  # group-64: I % 128 != 0
+        moe.make_config(2048, 64, 8, 1024, expert_format=3),
         moe.make_config(6144, 2048, 8, 2048, 1, 2048),       # E > 1024
         moe.make_config(6144, 256, 8, 2048, 1, 2048, routed_scale=float("inf")),
     ]
@@ -78,7 +80,9 @@ def test_workspace_bytes_validates_config(moe):
                 moe.make_config(2048, 64, 8, 1024, score_func=moe.MOE_SCORE_SOFTMAX),
                 moe.make_config(2048, 64, 8, 1024, norm_topk=0, score_func=moe.MOE_SCORE_SOFTMAX),
                 moe.make_config(2048, 64, 8, 1024, expert_format=moe.MOE_FORMAT_INT8),
-                moe.make_config(6144, 256, 8, 2048, 1, 2048, shared_format=moe.MOE_FORMAT_INT8)):
+                moe.make_config(6144, 256, 8, 2048, 1, 2048, shared_format=moe.MOE_FORMAT_INT8),
+                moe.make_config(2048, 256, 4, 512, 1, 512, expert_format=moe.MOE_FORMAT_G64,
+                                shared_format=moe.MOE_FORMAT_G64)):
         assert moe.moe_workspace_bytes(cfg, 4) > 0
     # the trace flag is accepted and adds the trace buffer (1024 blocks x 64 x 8 B)
     traced = moe.make_config(6144, 256, 8, 2048, 1, 2048, 2.5, trace=True)

@@ -235,7 +235,17 @@ def test_int8_shared_expert_glm(moe):
     layer.close()
 
 
+def test_g64_experts_35b_layer(moe):
+    """The 35B-class layer with int4 affine group-64 experts (routed and shared)."""
+    wl, li, layer = layer_for(moe, "g64_35b", 64)
+    assert moe.moe_uses_tensor_cores(layer.handle) and not moe.moe_uses_streaming_decode(layer.handle)
+    for T in (1, 5, 40):
+        run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=320 + T), f"g64_35b T={T}")
+
+
 @pytest.mark.parametrize("kw", [
+    dict(H=128, I=128, I_shared=256, E=8, K=2, expert_format=2, shared_format=1),   # group-64 + int8
+    dict(H=256, I=128, I_shared=128, E=8, K=2, shared_format=2),            # int4 routed, group-64 shared
     dict(H=128, I=128, I_shared=256, E=8, K=2, expert_format=1, shared_format=1),
     dict(H=256, I=128, I_shared=128, E=8, K=2, shared_format=1),            # int4 routed, int8 shared
     dict(H=384, I=256, n_shared=0, I_shared=0, E=6, K=6, expert_format=1),  # E == K, half-used down tiles
