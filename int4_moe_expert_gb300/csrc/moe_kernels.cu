@@ -1226,10 +1226,10 @@ __device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo 
 // o0 + 32 w + {0..31} (two m16 tiles), 256 rows per block; writes dbuf.
 // Weights (256 rows per stage) and the item's activations (kItemTokens rows)
 // move through a ring in shared memory with cp.async; every stage is one
-// __syncthreads.  One instantiation per weight format: a launch serves the items
-// whose slot has format FMT (the routed experts share one format, the shared
-// expert may have another; the others return at once).
-template <bool GU, int FMT>
+// __syncthreads.  FR / FS: weight formats of the routed experts / the shared
+// expert; each instantiation carries only the bodies it needs, so a config with
+// one format gets the lean kernel and a mixed one still runs in one launch.
+template <bool GU, int FR, int FS>
 __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T) {
     extern __shared__ __align__(128) unsigned char mma_smem[];
     __shared__ int s_brow[kItemTokens], s_orow[kItemTokens];
@@ -1238,7 +1238,6 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
     const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
     const SlotInfo s = slot_info(p, T, slot);
     if (!s.valid) return;
-    if ((s.base < 0 ? p.d.shared_fmt : p.d.expert_fmt) != FMT) return;
     const int o0 = blockIdx.y * (GU ? 128 : 256);
     if (o0 >= (GU ? s.Is : p.d.H)) return;
     const int tid = threadIdx.x;
@@ -1250,19 +1249,31 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
         s_orow[tid] = row;                     // output row (h16 / dbuf)
     }
     __syncthreads();
-    mma_body<GU, FMT>(p, T, s, nt, o0, mma_smem, s_brow, s_orow);
+    if (FR == FS || s.base >= 0)
+        mma_body<GU, FR>(p, T, s, nt, o0, mma_smem, s_brow, s_orow);
+    else
+        mma_body<GU, FS>(p, T, s, nt, o0, mma_smem, s_brow, s_orow);
 }
 
-// Launch the tensor-core kernels of one phase (gate/up or down) for every weight format
-// in use.
+template <bool GU, int FR, int FS>
+cudaError_t mma_attr() {
+    return cudaFuncSetAttribute(mma_expert_kernel<GU, FR, FS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kMmaSmem);
+}
+
+// The (routed, shared) format pair of a config as one switch value.
+inline int fmt_pair(const Dims &d) { return d.expert_fmt * 3 + (d.n_shared ? d.shared_fmt : d.expert_fmt); }
+
+#define MOE_FMT_PAIRS(X) X(0, 0) X(0, 1) X(0, 2) X(1, 0) X(1, 1) X(1, 2) X(2, 0) X(2, 1) X(2, 2)
+
+// Launch the tensor-core kernel of one phase (gate/up or down) for the config's formats.
 template <bool GU>
 void launch_mma_phase(const Params &p, int T, dim3 grid, cudaStream_t st) {
-    const Dims &d = p.d;
-    for (int f = MOE_FORMAT_INT4; f <= MOE_FORMAT_G64; f++) {
-        if (f != d.expert_fmt && !(d.n_shared && f == d.shared_fmt)) continue;
-        if (f == MOE_FORMAT_INT8) mma_expert_kernel<GU, MOE_FORMAT_INT8><<<grid, kThreads, kMmaSmem, st>>>(p, T);
-        else if (f == MOE_FORMAT_G64) mma_expert_kernel<GU, MOE_FORMAT_G64><<<grid, kThreads, kMmaSmem, st>>>(p, T);
-        else mma_expert_kernel<GU, MOE_FORMAT_INT4><<<grid, kThreads, kMmaSmem, st>>>(p, T);
+    switch (fmt_pair(p.d)) {
+#define MOE_LAUNCH(R, S) \
+    case R * 3 + S: mma_expert_kernel<GU, R, S><<<grid, kThreads, kMmaSmem, st>>>(p, T); break;
+        MOE_FMT_PAIRS(MOE_LAUNCH)
+#undef MOE_LAUNCH
     }
 }
 
@@ -1338,13 +1349,13 @@ cudaError_t prepare_kernels(const Dims &d) {
     cudaError_t e = cudaFuncSetAttribute(router_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(router_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (d.mma) {
-        const void *ks[] = {
-            (const void *)mma_expert_kernel<true, MOE_FORMAT_INT4>, (const void *)mma_expert_kernel<false, MOE_FORMAT_INT4>,
-            (const void *)mma_expert_kernel<true, MOE_FORMAT_INT8>, (const void *)mma_expert_kernel<false, MOE_FORMAT_INT8>,
-            (const void *)mma_expert_kernel<true, MOE_FORMAT_G64>, (const void *)mma_expert_kernel<false, MOE_FORMAT_G64>};
-        for (const void *k : ks)
-            if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmaSmem);
+    if (e == cudaSuccess && d.mma) {
+        switch (fmt_pair(d)) {
+#define MOE_ATTR(R, S) \
+    case R * 3 + S: e = mma_attr<true, R, S>(); if (e == cudaSuccess) e = mma_attr<false, R, S>(); break;
+            MOE_FMT_PAIRS(MOE_ATTR)
+#undef MOE_ATTR
+        }
     }
     if (e == cudaSuccess && d.fast_decode) e = prepare_decode_fast(d);
     return e;
