@@ -104,6 +104,7 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
     d->expert_fmt = c->expert_format;
     d->shared_fmt = c->n_shared ? c->shared_format : MOE_FORMAT_INT4;
     d->mma_fmt = (d->expert_fmt != MOE_FORMAT_INT4 || d->shared_fmt != MOE_FORMAT_INT4) ? 1 : 0;
+    d->tc = moe::tc_supported(*d) ? 1 : 0;
     d->prenorm = (c->flags & MOE_FLAG_PRENORM_RESIDUAL) ? 1 : 0;
     d->scale = c->routed_scale;
     d->eps = c->rms_eps;

@@ -18,6 +18,7 @@ struct Dims {
     int score_func;     // MOE_SCORE_SIGMOID / MOE_SCORE_SOFTMAX
     int expert_fmt, shared_fmt;   // MOE_FORMAT_INT4 / MOE_FORMAT_INT8
     int mma_fmt;        // an int8 or group-64 expert: every T runs the tensor-core expert kernels
+    int tc;             // int4 experts: calls with T >= kTcMinT run them on tcgen05
     int prenorm;        // MOE_FLAG_PRENORM_RESIDUAL
     float scale;        // routed_scale
     float eps;          // rms_eps
@@ -65,11 +66,12 @@ struct Workspace {
 constexpr int kMaxSlots = 33;   // K <= 32 routed + 1 shared
 constexpr int kRouterMaxSplit = 8;   // tiled router: k-ranges (split-K) at most
 constexpr int kItemTokens = 32;  // tokens of one tensor-core work item (4 n8 tiles)
-inline int max_items(int T, int K, int E, int n_shared) {   // work items of one T-token call, at most
+inline int max_items(int T, int K, int E, int n_shared, int item = kItemTokens) {   // work items, at most
     const int P = T * K;
-    return P / kItemTokens + (E < P ? E : P) + (n_shared ? (T + kItemTokens - 1) / kItemTokens : 0) + 1;
+    return P / item + (E < P ? E : P) + (n_shared ? (T + item - 1) / item : 0) + 1;
 }
 bool mma_supported(const Dims &d);
+bool tc_supported(const Dims &d);   // int4 experts on the tensor-core path: tcgen05 for large T
 constexpr int kClaimWords = 64;  // >= 1 + kMaxSlots
 constexpr int kTraceBlocks = 1024;   // decode blocks the trace buffer holds
 
@@ -84,6 +86,7 @@ struct Params {
     const float *sh_scale;
     Workspace ws;
     unsigned gen;                   // call number on this handle (grid barrier targets)
+    int item_tok;                   // this call: tokens per tensor-core work item
 };
 
 size_t workspace_bytes(const Dims &d);

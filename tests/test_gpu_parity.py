@@ -189,6 +189,20 @@ def test_batched_is_deterministic_and_token_independent(moe):
     assert rel_err(c.cpu().numpy()[0].astype(np.float64), a[5].cpu().numpy().astype(np.float64)) < 5e-4
 
 
+@pytest.mark.parametrize("kw", [
+    dict(H=384, I=128, I_shared=256, E=8, K=2),                   # half-used down tiles, I_sh != I
+    dict(H=256, I=256, n_shared=0, I_shared=0, E=2, K=2),         # every expert 2-3 items of 128
+])
+def test_tcgen05_path_large_batches(moe, kw):
+    """T >= 256 int4 calls run the experts on tcgen05 (128-token items, TMEM accumulators)."""
+    wl = small_workload(**kw)
+    li = synth.layer_inputs(wl)
+    layer = upload(moe, wl, li, 300)
+    for T in (256, 300):
+        run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=T), f"{kw} T={T}")
+    layer.close()
+
+
 # --- routing variants (group-limited sigmoid, softmax top-k) --------------------------
 
 @pytest.mark.parametrize("name", ["group8", "softmax_renorm", "olmoe_softmax"])
