@@ -1259,16 +1259,16 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
 // Batched (T > 1) int4 experts on the 5th-generation tensor cores (tcgen05.mma,
 // accumulators in tensor memory).
 //
-// One block = one work item (a slot and up to kTcTok of its tokens) x two
-// 128-row weight tiles (gate/up: the gate rows and the up rows of 128 outputs;
-// down: 256 output rows).  Measured on this GPU, one tcgen05.mma of M 128, K 16
+// One block = one work item (a slot and up to kTcTok of its tokens) x kTcTiles
+// 128-row weight tiles, one f32 accumulator each in tensor memory (gate/up: the
+// gate rows and the up rows of 256 outputs; down: 512 output rows).  Measured on this GPU, one tcgen05.mma of M 128, K 16
 // occupies the SM's tensor core ~36 ns for any N up to 128, so the items are 128
 // tokens wide (N 128 reaches the dense f16 peak; N 32 only a quarter of it).
 // The reduction runs in stages of kTcKB elements through a kTcS-slot ring in
 // shared memory: the threads dequantise the int4 rows (loaded into registers
 // kTcKAhead stages ahead) into f16 operand tiles of the slot, the activations
-// arrive by cp.async kTcS - 2 stages ahead straight in the layout the tensor core
-// reads, and one thread issues 2 x (kTcKB / 16) MMAs and commits them to the
+// arrive by cp.async kTcS - kTcLag stages ahead straight in the layout the tensor core
+// reads, and one thread issues kTcTiles x (kTcKB / 16) MMAs and commits them to the
 // slot's mbarrier, which frees the slot.  Operands are K-major without swizzle:
 // core matrices of 8 rows x 16 bytes, 128 bytes apart along K and
 // kTcKB / 8 * 128 bytes apart per 8 rows.  The K order inside every 8-element
@@ -1278,21 +1278,24 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
 // ---------------------------------------------------------------------------
 
 constexpr int kTcTok = 128;                        // tokens of a work item on this path (MMA N)
-constexpr int kTcKB = 64;                          // reduction elements per stage
+constexpr int kTcTiles = 4;                        // 128-row weight tiles per block (one accumulator each)
+constexpr int kTcRows = 128 * kTcTiles;            // weight rows per block (gate/up: half gate, half up)
+constexpr int kTcKB = 32;                          // reduction elements per stage
 constexpr int kTcS = 4;                            // ring slots
+constexpr int kTcLag = 2;                          // stage kb waits for the MMAs of stage kb - kTcLag
 constexpr int kTcKAhead = 4;                       // stages of int4 rows in registers ahead
 constexpr int kTcSBO = kTcKB / 8 * 128;            // bytes between 8-row groups of an operand
 constexpr int kTcATile = 128 * kTcKB * 2;          // one 128-row f16 weight tile of a stage
 constexpr int kTcBTile = kTcTok * kTcKB * 2;       // the item's f16 activations of a stage
-constexpr int kTcSlot = 2 * kTcATile + kTcBTile;
+constexpr int kTcSlot = kTcTiles * kTcATile + kTcBTile;
 constexpr size_t kTcSmem = (size_t)kTcS * kTcSlot + 1024;
-constexpr int kTcCols = 2 * kTcTok;                // tensor-memory columns: two f32 accumulators
+constexpr int kTcCols = kTcTiles * kTcTok;         // tensor-memory columns: one f32 accumulator per tile
 constexpr unsigned kErrTc = 32u;
 // kind::f16: D f32 (bits 4-5 = 1), A and B f16 (0), both K-major (0), N >> 3 at bit 17, M >> 4 at bit 24
 constexpr uint32_t kTcIdesc = (1u << 4) | ((uint32_t)(kTcTok >> 3) << 17) | ((128u >> 4) << 24);
 constexpr unsigned long long kTcWaitNs = 500ull * 1000 * 1000;
 static_assert(kTcSmem <= 227 * 1024, "the ring fits one block's shared memory");
-static_assert(kTcS >= 3, "activations are fetched kTcS - 2 stages ahead");
+static_assert(kTcS >= kTcLag + 1 && kTcLag >= 1, "activations are fetched kTcS - kTcLag stages ahead");
 
 __device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {   // no-swizzle K-major operand
     return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) |
@@ -1363,7 +1366,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
     if (!s.valid) return;
     const int H = p.d.H, Is = s.Is;
     const int rows = GU ? Is : H;
-    const int o0 = blockIdx.y * (GU ? 128 : 256);
+    const int o0 = blockIdx.y * (GU ? kTcRows / 2 : kTcRows);
     if (o0 >= rows) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nt = min(kTcTok, s.n - n0);
@@ -1396,7 +1399,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
     const size_t ald = GU ? (size_t)H : (size_t)p.d.I_max;
     const uint32_t sbase = (smem_u32(tc_smem) + 1023u) & ~1023u;
     // weights: thread piece i covers 16 bytes (four words, k-groups 4 piece .. + 3) of row lr
-    constexpr int kAP = 2 * 128 * (kTcKB / 2) / 16 / kThreads;     // 16-byte pieces per thread per stage
+    constexpr int kAP = kTcRows * (kTcKB / 2) / 16 / kThreads;    // 16-byte pieces per thread per stage
     constexpr int kRowPcs = kTcKB / 2 / 16;                        // 16-byte pieces per row per stage
     const uint4 *asrc[kAP];
     uint32_t adst[kAP];
@@ -1404,11 +1407,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
 #pragma unroll
     for (int i = 0; i < kAP; i++) {
         const int c = tid + i * kThreads, lr = c / kRowPcs, piece = c % kRowPcs;
-        const int gr = GU ? (lr < 128 ? o0 + lr : Is + o0 + lr - 128) : o0 + lr;
-        aok[i] = GU || gr < H;
+        // gate/up: rows [0, kTcRows / 2) are gate rows o0 + lr, the rest the matching up rows
+        const int ol = GU ? (lr < kTcRows / 2 ? lr : lr - kTcRows / 2) : lr;
+        const int gr = GU ? (lr < kTcRows / 2 ? o0 + ol : Is + o0 + ol) : o0 + lr;
+        aok[i] = o0 + ol < rows;
         asrc[i] = reinterpret_cast<const uint4 *>(abase + (size_t)(aok[i] ? gr : 0) * arb) + piece;
         const int t = lr >> 7, r = lr & 127;
         adst[i] = (uint32_t)(t * kTcATile + ((r >> 3) * (kTcKB / 8) + piece * 4) * 128 + (r & 7) * 16);
+        static_assert(kTcKB / 2 / 16 * 4 <= kTcKB / 8, "a piece's four k-groups lie inside the stage");
     }
     // activations: thread piece i covers 8 f16 (k-group j) of token n
     constexpr int kBP = kTcTok * (kTcKB / 8) / kThreads;
@@ -1420,7 +1426,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
         const int c = tid + i * kThreads, n = c / (kTcKB / 8), j = c % (kTcKB / 8);
         bok[i] = n < ((nt + 7) & ~7);
         bsrc[i] = act + (size_t)s_brow[n < nt ? n : 0] * ald + j * 8;
-        bdst[i] = (uint32_t)(2 * kTcATile + ((n >> 3) * (kTcKB / 8) + j) * 128 + (n & 7) * 16);
+        bdst[i] = (uint32_t)(kTcTiles * kTcATile + ((n >> 3) * (kTcKB / 8) + j) * 128 + (n & 7) * 16);
     }
     auto slot_addr = [&](int kb) { return sbase + (uint32_t)((kb % kTcS) * kTcSlot); };
     auto issue_b = [&](int kb) {
@@ -1443,13 +1449,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
 #pragma unroll
     for (int k = 0; k < kTcKAhead; k++) load_a(ar[k], k);
 #pragma unroll
-    for (int k = 0; k < kTcS - 2; k++) issue_b(k);
-    // stage kb: wait for the MMAs of stage kb - 2 (their slot takes the activations of stage
-    // kb + kTcS - 2; completion in order also frees this stage's slot, last used by kb - kTcS),
+    for (int k = 0; k < kTcS - kTcLag; k++) issue_b(k);
+    // stage kb: wait for the MMAs of stage kb - kTcLag (their slot takes the activations of
+    // stage kb + kTcS - kTcLag; completion in order also frees this stage's slot, last used by
+    // kb - kTcS),
     // dequantise the weights of stage kb into its slot, then one thread issues the MMAs
     auto step = [&](int kb, uint4 (&r)[kAP]) -> bool {   // true: give up (block-uniform)
         const uint32_t st = slot_addr(kb);
-        if (kb >= 2 && !mbar_wait(smem_u32(&s_bar[(kb - 2) % kTcS]), (uint32_t)((kb - 2) / kTcS) & 1u)) s_fail = 1;
+        if (kb >= kTcLag &&
+            !mbar_wait(smem_u32(&s_bar[(kb - kTcLag) % kTcS]), (uint32_t)((kb - kTcLag) / kTcS) & 1u))
+            s_fail = 1;
 #pragma unroll
         for (int i = 0; i < kAP; i++) {
             const uint32_t w4[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
@@ -1460,9 +1469,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
                 sts128(st + adst[i] + 128 * m, h[0], h[1], h[2], h[3]);
             }
         }
-        issue_b(kb + kTcS - 2);
+        issue_b(kb + kTcS - kTcLag);
         load_a(r, kb + kTcKAhead);
-        cp_async_wait<kTcS - 2>();                 // activations of stage kb have landed
+        cp_async_wait<kTcS - kTcLag>();            // activations of stage kb have landed
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncthreads();
         const bool fail = s_fail != 0;             // the same in every thread until the next barrier
@@ -1470,10 +1479,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
             for (int ks = 0; ks < kTcKB / 16; ks++) {     // K 16 per MMA: two core matrices
-                const uint64_t bd = tc_desc(st + 2 * kTcATile + 256 * ks);
+                const uint64_t bd = tc_desc(st + kTcTiles * kTcATile + 256 * ks);
                 const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-                tc_mma(taddr, tc_desc(st + 256 * ks), bd, acc);
-                tc_mma(taddr + kTcTok, tc_desc(st + kTcATile + 256 * ks), bd, acc);
+#pragma unroll
+                for (int t = 0; t < kTcTiles; t++)
+                    tc_mma(taddr + kTcTok * t, tc_desc(st + t * kTcATile + 256 * ks), bd, acc);
             }
             tc_commit(smem_u32(&s_bar[kb % kTcS]));
         }
@@ -1497,37 +1507,45 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
     } else {
         // TMEM lane = row of a tile; warp w reads lanes 32 (w % 4) ..; accumulator t at column
         // kTcTok t, token n at + n
+        // warp w: lane quarter q4 of the tiles hw, hw + 2, ... (gate/up: gate tile hw with up
+        // tile hw + kTcTiles / 2)
         const int q4 = warp & 3, hw = warp >> 2;
         const uint32_t trow = taddr + ((uint32_t)(32 * q4) << 16);
         if (GU) {
-            const int o = o0 + 32 * q4 + lane;              // gate row o and up row o
-            const float sg = s.sc[o], su = s.sc[Is + o];
-            const int pos = mma_pos(o);
 #pragma unroll 1
-            for (int c = 0; c < kTcTok / 2 / 16; c++) {     // this warp's half of the tokens
-                const int nb = kTcTok / 2 * hw + 16 * c;
-                float g[16], u[16];
-                tc_ld16(trow + nb, g);
-                tc_ld16(trow + kTcTok + nb, u);
-#pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    const int n = nb + i;
-                    if (n < nt)
-                        p.ws.h16[(size_t)s_orow[n] * p.d.I_max + pos] = f2h_bits(silu_mul(sg * g[i], su * u[i]));
-                }
-            }
-        } else {
-            const int o = o0 + 128 * hw + 32 * q4 + lane;    // row of tile hw
-            const float sd = o < H ? s.sc[2 * Is + o] : 0.0f;
+            for (int t = hw; t < kTcTiles / 2; t += 2) {
+                const int o = o0 + 128 * t + 32 * q4 + lane;     // gate row o and up row o
+                const bool ok = o < Is;
+                const float sg = ok ? s.sc[o] : 0.0f, su = ok ? s.sc[Is + o] : 0.0f;
+                const int pos = mma_pos(o);
 #pragma unroll 1
-            for (int c = 0; c < kTcTok / 16; c++) {
-                float v[16];
-                tc_ld16(trow + kTcTok * hw + 16 * c, v);
-                if (o < H) {
+                for (int c = 0; c < kTcTok / 16; c++) {
+                    float g[16], u[16];
+                    tc_ld16(trow + kTcTok * t + 16 * c, g);
+                    tc_ld16(trow + kTcTok * (t + kTcTiles / 2) + 16 * c, u);
 #pragma unroll
                     for (int i = 0; i < 16; i++) {
                         const int n = 16 * c + i;
-                        if (n < nt) p.ws.dbuf[(size_t)s_orow[n] * H + o] = sd * v[i];
+                        if (ok && n < nt)
+                            p.ws.h16[(size_t)s_orow[n] * p.d.I_max + pos] = f2h_bits(silu_mul(sg * g[i], su * u[i]));
+                    }
+                }
+            }
+        } else {
+#pragma unroll 1
+            for (int t = hw; t < kTcTiles; t += 2) {
+                const int o = o0 + 128 * t + 32 * q4 + lane;     // row of tile t
+                const float sd = o < H ? s.sc[2 * Is + o] : 0.0f;
+#pragma unroll 1
+                for (int c = 0; c < kTcTok / 16; c++) {
+                    float v[16];
+                    tc_ld16(trow + kTcTok * t + 16 * c, v);
+                    if (o < H) {
+#pragma unroll
+                        for (int i = 0; i < 16; i++) {
+                            const int n = 16 * c + i;
+                            if (n < nt) p.ws.dbuf[(size_t)s_orow[n] * H + o] = sd * v[i];
+                        }
                     }
                 }
             }
@@ -1559,7 +1577,8 @@ constexpr int kTcMinT = 256;
 template <bool GU>
 void launch_mma_phase(const Params &p, int T, dim3 grid, cudaStream_t st) {
     if (p.item_tok == kTcTok) {
-        tc_expert_kernel<GU><<<grid, kThreads, kTcSmem, st>>>(p, T);
+        const dim3 g(grid.x, GU ? (p.d.I_max + kTcRows / 2 - 1) / (kTcRows / 2) : (p.d.H + kTcRows - 1) / kTcRows);
+        tc_expert_kernel<GU><<<g, kThreads, kTcSmem, st>>>(p, T);
         return;
     }
     switch (fmt_pair(p.d)) {
