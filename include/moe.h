@@ -143,7 +143,12 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, int32_t max_tok
  * overlap, and y is overwritten.  0 <= T <= max_tokens (T == 0 does nothing).
  * Launches on `stream` (a cudaStream_t; NULL = legacy default stream) and
  * returns without waiting.  Calls on one handle must not overlap on the GPU:
- * they share the handle's workspace. */
+ * they share the handle's workspace.  The call may be captured in a CUDA
+ * graph (stream capture): it keeps no per-call state on the host (the
+ * single-kernel decode path counts its calls in device memory), so every
+ * replay of a captured call computes the step on the x buffer's contents at
+ * that time.  Not for capture: moe_forward_host (it synchronises) and calls
+ * while moe_profile_start is recording. */
 moe_status moe_forward(moe_handle *h, const float *x, int32_t T, float *y, void *stream);
 
 /* As moe_forward, and also writes the router's choice: topk_idx[T,K] int32
@@ -194,8 +199,9 @@ moe_status moe_device_error(moe_handle *h, uint32_t *flags);
 int32_t moe_uses_streaming_decode(const moe_handle *h);
 
 /* 1 if T > 1 calls on this handle run the experts on the tensor cores
- * (mma.sync m16n8k16: exact int4 weights times f16 activations, f32
- * accumulation), 0 if they use the CUDA-core batched kernels (exact f32
+ * (exact int4 weights times f16 activations, f32 accumulation: tcgen05.mma
+ * with tensor-memory accumulators for T >= 256 with int4 experts, mma.sync
+ * m16n8k16 otherwise), 0 if they use the CUDA-core batched kernels (exact f32
  * arithmetic; shapes where H, I or I_shared is not a multiple of 128, or
  * max_tokens == 1).  NULL -> 0. */
 int32_t moe_uses_tensor_cores(const moe_handle *h);

@@ -194,7 +194,6 @@ moe_status run(moe_handle *h, const float *x, int32_t T, float *y, int32_t *topk
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaEvent_t *ev = nullptr;
     if (h->prof_ev && h->prof_n < h->prof_max) ev = h->prof_ev + (size_t)(h->prof_n++) * (moe::kStages + 1);
-    if (T == 1 && h->p.d.fast_decode) h->p.gen++;
     e = moe::launch_forward(h->p, x, T, y, st, counts != nullptr, ev);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     if (debug) {
@@ -356,7 +355,6 @@ moe_status moe_device_error(moe_handle *h, uint32_t *flags) {
         if (e == cudaSuccess) e = cudaMemset(h->p.ws.counters, 0, 16 * sizeof(unsigned));
         if (e == cudaSuccess) e = cudaMemset(h->p.ws.claims, 0, moe::kClaimWords * sizeof(unsigned));
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
-        h->p.gen = 0;
     }
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
     *flags = v;

@@ -280,7 +280,7 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {   // weights: read
 template <int CPLH, int CPLI>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, const float *__restrict__ x,
                                                                    float *__restrict__ y, FusedShape sh,
-                                                                   unsigned gen, int want_counts) {
+                                                                   int want_counts) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint4 *xdig = reinterpret_cast<uint4 *>(smem);
     int4 *xdsum = reinterpret_cast<int4 *>(xdig + kQ * sh.C);
@@ -299,9 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     const int H = d.H, E = d.E, K = d.K, J = sh.J, C = sh.C, Cd = sh.Cd;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int G = gridDim.x, nw = G * kWarps, gw = blockIdx.x * kWarps + warp;
-    const unsigned target = gen * (unsigned)G;
     const unsigned kFull = 0xffffffffu;
     unsigned *bar1 = p.ws.counters + 4, *bar2 = p.ws.counters + 5, *bar3 = p.ws.counters + 6;
+    // this call's number on the handle: the previous call's + 1, kept in device memory (so a
+    // captured graph replays correctly); block 0 advances it once every block is past
+    // barrier 2, i.e. after every block has read it.  Only thread 0 uses it.
+    unsigned *epoch = p.ws.counters + 7;
+    const unsigned gen = tid == 0 ? *reinterpret_cast<volatile unsigned *>(epoch) + 1u : 0u;
+    const unsigned target = gen * (unsigned)G;
     const bool fullH = (C % 32) == 0, fullI = (Cd % 32) == 0;
     // timeline (MOE_FLAG_TRACE): block b's record of MOE_TRACE_SLOTS global-timer readings
     const bool trace = p.d.trace != 0 && blockIdx.x < kTraceBlocks;
@@ -699,6 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
 
     // ---- barrier 2: every SwiGLU activation is written ------------------------------------
     if (!grid_barrier(bar2, target, p.ws.err, s_flags + 1)) return;
+    if (blockIdx.x == 0 && tid == 0) *reinterpret_cast<volatile unsigned *>(epoch) = gen;
     mark(3);
 
     // ---- phase 2: the half-block loads slot j's h (thread t of the half: chunk t), takes
@@ -818,20 +824,20 @@ constexpr int kMaxCplI = 2;   // I up to 2048 (digits of more chunks do not fit 
 
 template <int A, int B>
 cudaError_t launch_t(cudaLaunchConfig_t &cfg, const Params &p, const float *x, float *y, const FusedShape &s,
-                     unsigned gen, int counts) {
-    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<A, B>, p, x, y, s, gen, counts);
+                     int counts) {
+    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<A, B>, p, x, y, s, counts);
 }
 
 template <int B>
 cudaError_t launch_h(int a, cudaLaunchConfig_t &cfg, const Params &p, const float *x, float *y,
-                     const FusedShape &s, unsigned gen, int counts) {
+                     const FusedShape &s, int counts) {
     switch (a) {
-        case 1: return launch_t<1, B>(cfg, p, x, y, s, gen, counts);
-        case 2: return launch_t<2, B>(cfg, p, x, y, s, gen, counts);
-        case 3: return launch_t<3, B>(cfg, p, x, y, s, gen, counts);
-        case 4: return launch_t<4, B>(cfg, p, x, y, s, gen, counts);
-        case 6: return launch_t<6, B>(cfg, p, x, y, s, gen, counts);
-        case 8: return launch_t<8, B>(cfg, p, x, y, s, gen, counts);
+        case 1: return launch_t<1, B>(cfg, p, x, y, s, counts);
+        case 2: return launch_t<2, B>(cfg, p, x, y, s, counts);
+        case 3: return launch_t<3, B>(cfg, p, x, y, s, counts);
+        case 4: return launch_t<4, B>(cfg, p, x, y, s, counts);
+        case 6: return launch_t<6, B>(cfg, p, x, y, s, counts);
+        case 8: return launch_t<8, B>(cfg, p, x, y, s, counts);
     }
     return cudaErrorInvalidValue;
 }
@@ -912,8 +918,8 @@ cudaError_t launch_decode_fast(const Params &p, const float *x, float *y, cudaSt
     if (e != cudaSuccess) return e;
     const int b = (p.d.I / 32 + 31) / 32;
     const int counts = want_counts ? 1 : 0;
-    e = b == 1 ? launch_h<1>(cpl_h(p.d), cfg, p, x, y, s, p.gen, counts)
-               : launch_h<2>(cpl_h(p.d), cfg, p, x, y, s, p.gen, counts);
+    e = b == 1 ? launch_h<1>(cpl_h(p.d), cfg, p, x, y, s, counts)
+               : launch_h<2>(cpl_h(p.d), cfg, p, x, y, s, counts);
     for (int i = 2; ev && e == cudaSuccess && i < 5; i++) e = cudaEventRecord(ev[i], st);
     return e;
 }

@@ -85,7 +85,6 @@ struct Params {
     const uint8_t *sh_slab;
     const float *sh_scale;
     Workspace ws;
-    unsigned gen;                   // call number on this handle (grid barrier targets)
     int item_tok;                   // this call: tokens per tensor-core work item
 };
 
@@ -99,7 +98,8 @@ constexpr int kStages = 4;   // router, gate/up, down, combine
 
 // Decode path (moe_decode.cu): T == 1 as one persistent cooperative kernel.
 // ws.counters[4..6] are its grid barriers: they only grow, by gridDim per
-// call; p.gen numbers the calls from 1.
+// call; ws.counters[7] counts the calls (read and advanced on the device, so
+// the launch has no per-call host state and can be captured in a graph).
 bool decode_fast_supported(const Dims &d);
 cudaError_t prepare_decode_fast(const Dims &d);
 int decode_grid_blocks();   // blocks of the decode launch (0 before prepare)

@@ -104,6 +104,37 @@ def test_host_entry_point_matches_device_call(moe):
     assert np.array_equal(out.numpy(), y_dev)
 
 
+@pytest.mark.parametrize("name,T,max_tokens", [("glm_decode", 1, 1), ("tiny", 1, 64), ("tiny", 6, 64),
+                                               ("olmoe", 3, 64)])
+def test_forward_replays_from_a_cuda_graph(moe, name, T, max_tokens):
+    """A moe_forward captured in a CUDA graph computes, at every replay, the step
+    on the input buffer's contents at that time, bit-identical to a direct call
+    (the decode kernel's call counter lives in device memory), with direct calls
+    on the same handle between the replays."""
+    wl, li, layer = layer_for(moe, name, max_tokens)
+    x_static = torch.from_numpy(synth.tokens(wl, T=T, stream=40)).cuda()
+    y_static = torch.empty_like(x_static)
+    layer.forward(x_static, y_static)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.moe_forward(layer.handle, x_static, T, y_static)
+    ref = oracle_layer(wl, li)
+    for i in range(3):
+        x = synth.tokens(wl, T=T, stream=41 + i)
+        x_static.copy_(torch.from_numpy(x))
+        g.replay()
+        y_graph = y_static.clone()
+        y_direct, idx, w = layer.forward_debug(x_static)
+        torch.cuda.synchronize()
+        assert moe.moe_device_error(layer.handle) == 0
+        assert torch.equal(y_graph, y_direct), f"{name} T={T} replay {i}"
+        y_np, idx, w = y_graph.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+        for t in range(T):
+            check_token(wl, ref, x[t], y_np[t], idx[t], w[t], where=f"{name} graph replay {i} t={t}")
+    g.reset()
+
+
 # --- batched (T > 1) --------------------------------------------------------------
 
 @pytest.mark.parametrize("name,T", [("tiny", 2), ("tiny", 7), ("tiny", 33), ("olmoe", 3),
