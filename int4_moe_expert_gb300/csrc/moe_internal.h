@@ -50,9 +50,8 @@ struct Workspace {
     uint16_t *h16;       // [(maxT*K + maxT), I_max] SwiGLU activations, rows as h
     int *items;          // [2 * max_items] (slot, first token) of every kItemTokens-token work item
     int *n_items;        // [1]
-    unsigned *gcount;    // [ceil(maxT / 32)] tiled router: blocks done per 32-token group
-    float *lpart;        // [kRouterMaxSplit, maxT, E] tiled router: logits of each k-range
-    float *sspart;       // [kRouterMaxSplit, maxT] tiled router: sums of squares of each k-range
+    float *lpart;        // [S, T, E] tiled router: logits of each of a call's S k-ranges
+    float *sspart;       // [S, T] tiled router: sums of squares of each k-range
     // decode (T == 1) streaming path
     unsigned *claims;    // [kClaimWords] work counters: [0] gate/up units, [1 + j] down rows of
                          // slot j; each call's last barrier is followed by their reset to 0
@@ -64,7 +63,7 @@ struct Workspace {
 };
 
 constexpr int kMaxSlots = 33;   // K <= 32 routed + 1 shared
-constexpr int kRouterMaxSplit = 8;   // tiled router: k-ranges (split-K) at most
+constexpr int kRouterMaxSplit = 32;  // tiled router: k-ranges (split-K) at most
 constexpr int kItemTokens = 32;  // tokens of one tensor-core work item (4 n8 tiles)
 inline int max_items(int T, int K, int E, int n_shared, int item = kItemTokens) {   // work items, at most
     const int P = T * K;

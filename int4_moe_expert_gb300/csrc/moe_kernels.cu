@@ -27,7 +27,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kGemvMaxT = 8;       // router GEMV handles up to this many tokens
-constexpr int kRouterBlocks = 456;  // tiled router: aim for ~3 blocks per SM (split-K over H)
+constexpr int kRouterBlocks = 456;  // tiled router: aim for 3 blocks per SM (split-K over H)
 
 // ---------------------------------------------------------------------------
 // Layout helpers
@@ -252,12 +252,24 @@ __device__ void bucket_phase(const Params &p, int T, int *ismem) {
     const int E = p.d.E, K = p.d.K, P = T * K;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     int *cnt = ismem;               // [E]
-    int *run = cnt + E;             // [E] next free position per expert
-    int *wcnt = run + E;            // [kWarps][E] per-warp counts in a chunk
-    for (int e = tid; e < E; e += kThreads) cnt[e] = 0;
+    int *run = cnt + E;             // [E] first position of each expert's pairs
+    int *wcnt = run + E;            // [kWarps][E] pairs of each warp's range per expert, then
+                                    // the warp's next position within the expert's pairs
+    // warp w owns the pairs [q0, q1): its counts, then every warp's prefix per expert
+    const int span = (P + kWarps - 1) / kWarps, q0 = min(P, warp * span), q1 = min(P, q0 + span);
     for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
     __syncthreads();
-    for (int q = tid; q < P; q += kThreads) atomicAdd(&cnt[__ldcg(p.ws.topk_idx + q)], 1);
+    for (int q = q0 + lane; q < q1; q += 32) atomicAdd(&wcnt[warp * E + __ldcg(p.ws.topk_idx + q)], 1);
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads) {
+        int s = 0;
+        for (int w = 0; w < kWarps; w++) {
+            const int c = wcnt[w * E + e];
+            wcnt[w * E + e] = s;
+            s += c;
+        }
+        cnt[e] = s;
+    }
     __syncthreads();
     if (warp == 0) {
         // exclusive scans of counts and of "active" flags, E <= 1024
@@ -311,28 +323,22 @@ __device__ void bucket_phase(const Params &p, int T, int *ismem) {
         }
     }
     __syncthreads();
+    // each warp places its own pairs in order (pairs of one expert: warp ranges in order,
+    // then q ascending within a range), 32 at a time
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int base = 0; base < P; base += kThreads) {
-        const int q = base + tid;
-        const int e = q < P ? __ldcg(p.ws.topk_idx + q) : -1;
+    for (int base = q0; base < q1; base += 32) {
+        const int q = base + lane;
+        const int e = q < q1 ? __ldcg(p.ws.topk_idx + q) : -1;
         const unsigned same = __match_any_sync(0xffffffffu, e);
         const int lrank = __popc(same & lt_mask);
-        if (e >= 0 && lrank == 0) wcnt[warp * E + e] = __popc(same);
-        __syncthreads();
         if (e >= 0) {
-            int pre = 0;
-            for (int w = 0; w < warp; w++) pre += wcnt[w * E + e];
-            const int pos = run[e] + pre + lrank;
+            const int pos = run[e] + wcnt[warp * E + e] + lrank;
             p.ws.perm[pos] = q;
             p.ws.inv[q] = pos;
         }
-        __syncthreads();
-        for (int e2 = tid; e2 < E; e2 += kThreads) {
-            int s = 0;
-            for (int w = 0; w < kWarps; w++) { s += wcnt[w * E + e2]; wcnt[w * E + e2] = 0; }
-            run[e2] += s;
-        }
-        __syncthreads();
+        __syncwarp();
+        if (e >= 0 && lrank == 0) wcnt[warp * E + e] += __popc(same);
+        __syncwarp();
     }
 }
 
@@ -435,148 +441,188 @@ __global__ void __launch_bounds__(kThreads) router_gemv_kernel(Params p, const f
 }
 
 
-// Router for larger T: a 32 (experts) x 32 (tokens) tile per block, k-loop
-// over H in steps of 32 through shared memory.
+// Router for T > kGemvMaxT tokens: the fp32 product logits[t][e] = sum_h x[t][h] W[e][h]
+// (router GEMV of section 11, as a small GEMM) over 64-token x 64-expert tiles, the
+// reduction split into gridDim.z k-ranges (whole 32-element stages).  Each stage of x
+// and W rows goes through a kRtStages-slot cp.async ring (rows padded to kRtLd floats);
+// thread (th, ty, tx) of warp 2 eq + th keeps a 4 x 4 block of sums, tokens
+// 32 th + ty + 8 j and experts 16 eq + tx + 4 i, and reads float4s along k, so each
+// shared-memory read serves 8 (tokens) or 4 (experts) lanes at once, conflict-free.
+// Every block writes its k-range's partial logits (and, for pre-norm, the tokens'
+// partial sums of squares); router_reduce_kernel adds them.  Deterministic: every sum
+// has a fixed order.
+constexpr int kRtTok = 64, kRtExp = 64, kRtK = 32, kRtStages = 4, kRtLd = kRtK + 4;
+constexpr int kRtCv = 4;                               // activation steps a thread loads at once
+constexpr size_t kRtSmem = (size_t)kRtStages * 2 * 64 * kRtLd * sizeof(float);
+
+__device__ __forceinline__ void rt_cp16(uint32_t dst, const void *src, uint32_t bytes) {   // bytes 0: zero fill
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void rt_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void rt_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 __global__ void __launch_bounds__(kThreads) router_tiled_kernel(Params p, const float *__restrict__ x,
-                                                                int T, int buckets) {
-    extern __shared__ float smem[];
-    // k-tiles of 32, transposed in shared memory ([k][row], rows padded to 34 floats so the
-    // 8-byte reads are aligned), double-buffered: the next tile's global loads are in
-    // flight while this one is used
-    __shared__ __align__(16) float Wt[2][32][34];
-    __shared__ __align__(16) float Xt[2][32][34];
-    __shared__ float s_r[32];
+                                                                int T) {
+    extern __shared__ __align__(16) float smem[];
     const int H = p.d.H, E = p.d.E;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int e0 = blockIdx.x * 32, t0 = blockIdx.y * 32;
-    const int ty = tid >> 4, tx = tid & 15;
-    float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-    float ss[4] = {0.f, 0.f, 0.f, 0.f};
-    float wv[4], xv[4];
-    auto load = [&](int k0) {
+    const int e0 = blockIdx.x * kRtExp, t0 = blockIdx.y * kRtTok;
+    const int th = warp & 1, eq = warp >> 1, ty = lane >> 2, tx = lane & 3;
+    const int nk = H / kRtK, z = blockIdx.z, S = gridDim.z;
+    const int kb0 = (int)((long)z * nk / S), nkb = (int)((long)(z + 1) * nk / S) - kb0;
+    const bool want_ss = p.d.prenorm && blockIdx.x == 0;    // block-uniform
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    // stage kb into its slot: 64 x rows then 64 W rows of 8 16-byte pieces, 4 pieces per thread
+    auto issue = [&](int kb) {
+        if (kb < nkb) {
+            const int slot = kb % kRtStages;
+            const int k0 = (kb0 + kb) * kRtK;
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const int row = warp + 8 * i;      // tile row handled by this warp
-            const int e = e0 + row, t = t0 + row;
-            wv[i] = e < E ? __ldg(p.router_w + (size_t)e * H + k0 + lane) : 0.0f;
-            xv[i] = t < T ? __ldg(x + (size_t)t * H + k0 + lane) : 0.0f;
+            for (int q = 0; q < 4; q++) {
+                const int c = tid + kThreads * (q & 1), row = c >> 3, piece = c & 7;
+                const bool isw = q >= 2;
+                const int g = (isw ? e0 : t0) + row;
+                const bool ok = g < (isw ? E : T);
+                const float *src = (isw ? p.router_w : x) + (size_t)(ok ? g : 0) * H + k0 + 4 * piece;
+                const uint32_t dst = sbase + (uint32_t)((((2 * slot + (isw ? 1 : 0)) * 64 + row) * kRtLd + 4 * piece) * 4);
+                rt_cp16(dst, src, ok ? 16u : 0u);
+            }
         }
+        rt_commit();
     };
-    auto store = [&](int buf) {
+    float acc[4][4], ss[4];
 #pragma unroll
-        for (int i = 0; i < 4; i++) {
-            const int row = warp + 8 * i;
-            Wt[buf][lane][row] = wv[i];
-            Xt[buf][lane][row] = xv[i];
-            ss[i] = fmaf(xv[i], xv[i], ss[i]);
-        }
-    };
-    // this block's share of the reduction (split-K over gridDim.z, whole k-tiles)
-    const int nk = H / 32, z = blockIdx.z, S = gridDim.z;
-    const int kbeg = (int)((long)z * nk / S) * 32, kend = (int)((long)(z + 1) * nk / S) * 32;
-    load(kbeg);
-    store(0);
-    __syncthreads();
-    int cur = 0;
-    for (int k0 = kbeg; k0 < kend; k0 += 32) {
-        const bool more = k0 + 32 < kend;
-        if (more) load(k0 + 32);
-#pragma unroll 8
-        for (int kk = 0; kk < 32; kk++) {
-            const float2 a = *reinterpret_cast<const float2 *>(&Wt[cur][kk][ty * 2]);
-            const float2 b = *reinterpret_cast<const float2 *>(&Xt[cur][kk][tx * 2]);
-            acc[0][0] = fmaf(a.x, b.x, acc[0][0]);
-            acc[0][1] = fmaf(a.x, b.y, acc[0][1]);
-            acc[1][0] = fmaf(a.y, b.x, acc[1][0]);
-            acc[1][1] = fmaf(a.y, b.y, acc[1][1]);
-        }
-        if (more) store(cur ^ 1);
-        __syncthreads();
-        cur ^= 1;
-    }
-    // partial sums of this k-range: logits [z][t][e] and sums of squares [z][t]
+    for (int j = 0; j < 4; j++) {
+        ss[j] = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; i++) {
-        const float sq = warp_sum(ss[i]);
-        const int t = t0 + warp + 8 * i;
-        if (lane == 0 && blockIdx.x == 0 && t < T) p.ws.sspart[(size_t)z * T + t] = sq;
+        for (int i = 0; i < 4; i++) acc[j][i] = 0.0f;
     }
 #pragma unroll
-    for (int a = 0; a < 2; a++)
+    for (int k = 0; k < kRtStages - 1; k++) issue(k);
+#pragma unroll 1
+    for (int kb = 0; kb < nkb; kb++) {
+        rt_wait<kRtStages - 2>();     // stage kb has landed (this thread's pieces)
+        __syncthreads();              // ... everyone's; and everyone is done with stage kb - 1
+        issue(kb + kRtStages - 1);    // into stage kb - 1's slot
+        const float *X = smem + (size_t)(2 * (kb % kRtStages)) * 64 * kRtLd;
+        const float *Wr = X + 64 * kRtLd;
 #pragma unroll
-        for (int b = 0; b < 2; b++) {
-            const int e = e0 + ty * 2 + a, t = t0 + tx * 2 + b;
-            if (e < E && t < T) p.ws.lpart[((size_t)z * T + t) * E + e] = acc[a][b];
+        for (int k4 = 0; k4 < kRtK / 4; k4++) {
+            float4 xa[4], wb[4];
+#pragma unroll
+            for (int j = 0; j < 4; j++) xa[j] = *reinterpret_cast<const float4 *>(X + (32 * th + ty + 8 * j) * kRtLd + 4 * k4);
+#pragma unroll
+            for (int i = 0; i < 4; i++) wb[i] = *reinterpret_cast<const float4 *>(Wr + (16 * eq + tx + 4 * i) * kRtLd + 4 * k4);
+#pragma unroll
+            for (int j = 0; j < 4; j++)
+#pragma unroll
+                for (int i = 0; i < 4; i++)
+                    acc[j][i] = fmaf(xa[j].w, wb[i].w, fmaf(xa[j].z, wb[i].z, fmaf(xa[j].y, wb[i].y, fmaf(xa[j].x, wb[i].x, acc[j][i]))));
+            if (want_ss) {
+#pragma unroll
+                for (int j = 0; j < 4; j++)
+                    ss[j] = fmaf(xa[j].w, xa[j].w, fmaf(xa[j].z, xa[j].z, fmaf(xa[j].y, xa[j].y, fmaf(xa[j].x, xa[j].x, ss[j]))));
+            }
         }
-    // two-level tail: the last block of this 32-token group adds the partials (z ascending),
-    // scales by 1/rms, and picks the group's top K; the last group builds the buckets
-    __shared__ int s_last;
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) s_last = atomicAdd(p.ws.gcount + blockIdx.y, 1u) == gridDim.x * gridDim.z - 1;
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-    if (tid < 32 && t0 + tid < T) {
-        float sq = 0.0f;
-        for (int k = 0; k < S; k++) sq += __ldcg(p.ws.sspart + (size_t)k * T + t0 + tid);
-        const float r = p.d.prenorm ? 1.0f / sqrtf(sq / (float)H + p.d.eps) : 1.0f;
-        s_r[tid] = r;
-        p.ws.rnorm[t0 + tid] = r;
     }
-    __syncthreads();
-    for (int i = tid; i < 32 * E; i += kThreads) {
-        const int tl = i / E, e = i - tl * E, t = t0 + tl;
+    rt_wait<0>();
+    // this k-range's partial logits [z][t][e] (and sums of squares [z][t])
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+        const int t = t0 + 32 * th + ty + 8 * j;
         if (t < T) {
-            float pv[kRouterMaxSplit];
 #pragma unroll
-            for (int k = 0; k < kRouterMaxSplit; k++)
-                pv[k] = k < S ? __ldcg(p.ws.lpart + ((size_t)k * T + t) * E + e) : 0.0f;
-            float v = 0.0f;
-#pragma unroll
-            for (int k = 0; k < kRouterMaxSplit; k++)
-                if (k < S) v += pv[k];
-            p.ws.logits[(size_t)t * E + e] = v * s_r[tl];
+            for (int i = 0; i < 4; i++) {
+                const int e = e0 + 16 * eq + tx + 4 * i;
+                if (e < E) p.ws.lpart[((size_t)z * T + t) * E + e] = acc[j][i];
+            }
+            if (want_ss && eq == 0 && tx == 0) p.ws.sspart[(size_t)z * T + t] = ss[j];
         }
     }
-    __syncthreads();
-    topk_phase(p, t0, min(T, t0 + 32), smem);
+}
+
+// Second router kernel of a T > kGemvMaxT call, one block per token: the token's 1/rms
+// (pre-norm), its logits = (sum of the k-range partials, in k-range order) / rms, its
+// activations for the expert kernels (x / rms: f16 in mma order for the tensor-core path,
+// f32 chunk-permuted for the CUDA-core path), then its top-K (warp 0); the last block to
+// finish builds the buckets.  One block per token keeps every SM's share of the partial
+// and activation traffic small.
+__global__ void __launch_bounds__(kThreads) router_reduce_kernel(Params p, const float *__restrict__ x, int T,
+                                                                 int S, int buckets) {
+    extern __shared__ __align__(16) float smem[];
+    __shared__ float s_red[kWarps];
+    __shared__ int s_last;
+    const int H = p.d.H, E = p.d.E;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t = blockIdx.x;
+    float r = 1.0f;
+    if (p.d.prenorm) {
+        float sq = 0.0f;
+        if (warp == 0) {
+            for (int k = lane; k < S; k += 32) sq += __ldcg(p.ws.sspart + (size_t)k * T + t);
+            // the k-range order of the sum is fixed by the butterfly
+            sq = warp_sum(sq);
+            if (lane == 0) s_red[0] = sq;
+        }
+        __syncthreads();
+        r = 1.0f / sqrtf(s_red[0] / (float)H + p.d.eps);
+    }
+    if (tid == 0) p.ws.rnorm[t] = r;
+    for (int e = tid; e < E; e += kThreads) {
+        float v = 0.0f;
+        for (int k0 = 0; k0 < S; k0 += 16) {      // 16 partials in flight, added in k-range order
+            float pv[16];
+#pragma unroll
+            for (int k = 0; k < 16; k++)
+                pv[k] = k0 + k < S ? __ldcg(p.ws.lpart + ((size_t)(k0 + k) * T + t) * E + e) : 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; k++)
+                if (k0 + k < S) v += pv[k];
+        }
+        p.ws.logits[(size_t)t * E + e] = v * r;
+    }
+    // activations, 8 elements per thread per step, kRtCv steps' loads in flight at once
+    for (int c0 = 8 * tid; c0 < H; c0 += 8 * kThreads * kRtCv) {
+        float4 va[kRtCv], vb[kRtCv];
+#pragma unroll
+        for (int u = 0; u < kRtCv; u++) {
+            const int c = c0 + 8 * kThreads * u;
+            if (c < H) {
+                va[u] = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + c));
+                vb[u] = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + c) + 1);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kRtCv; u++) {
+            const int c = c0 + 8 * kThreads * u;
+            if (c < H) {
+                const float4 a = va[u], b = vb[u];
+                const float v[8] = {a.x * r, a.y * r, a.z * r, a.w * r, b.x * r, b.y * r, b.z * r, b.w * r};
+                if (p.d.mma) {       // group order 0 4 1 5 2 6 3 7
+                    uint4 o;
+                    o.x = (uint32_t)f2h_bits(v[0]) | ((uint32_t)f2h_bits(v[4]) << 16);
+                    o.y = (uint32_t)f2h_bits(v[1]) | ((uint32_t)f2h_bits(v[5]) << 16);
+                    o.z = (uint32_t)f2h_bits(v[2]) | ((uint32_t)f2h_bits(v[6]) << 16);
+                    o.w = (uint32_t)f2h_bits(v[3]) | ((uint32_t)f2h_bits(v[7]) << 16);
+                    *reinterpret_cast<uint4 *>(p.ws.x16 + (size_t)t * H + c) = o;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; j++) p.ws.xperm[(size_t)t * H + perm_pos(c + j, H)] = v[j];
+                }
+            }
+        }
+    }
+    __syncthreads();              // this token's logits are written
+    topk_phase(p, t, t + 1, smem);
     __threadfence();
     __syncthreads();
-    if (tid == 0) {
-        p.ws.gcount[blockIdx.y] = 0u;              // ready for the next call
-        s_last = atomicAdd(p.ws.counters, 1u) == gridDim.y - 1;
-    }
+    if (tid == 0) s_last = atomicAdd(p.ws.counters, 1u) == gridDim.x - 1;
     __syncthreads();
     if (!s_last) return;
     __threadfence();
     if (buckets) bucket_phase(p, T, reinterpret_cast<int *>(smem));
     if (tid == 0) *p.ws.counters = 0u;
-}
-
-// Activations of a T > kGemvMaxT call for the expert kernels, x_t / rms_t: f16 in mma order
-// (tensor-core path) or f32 chunk-permuted (CUDA-core path); 8 elements per thread.
-__global__ void __launch_bounds__(kThreads) act_convert_kernel(Params p, const float *__restrict__ x, int T) {
-    const int H = p.d.H;
-    const size_t n8 = (size_t)T * H / 8;
-    for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < n8; i += (size_t)gridDim.x * kThreads) {
-        const int t = (int)(i * 8 / H), c = (int)(i * 8 - (size_t)t * H);
-        const float r = p.ws.rnorm[t];
-        const float4 a = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + c));
-        const float4 b = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + c) + 1);
-        const float v[8] = {a.x * r, a.y * r, a.z * r, a.w * r, b.x * r, b.y * r, b.z * r, b.w * r};
-        if (p.d.mma) {       // group order 0 4 1 5 2 6 3 7
-            uint4 o;
-            o.x = (uint32_t)f2h_bits(v[0]) | ((uint32_t)f2h_bits(v[4]) << 16);
-            o.y = (uint32_t)f2h_bits(v[1]) | ((uint32_t)f2h_bits(v[5]) << 16);
-            o.z = (uint32_t)f2h_bits(v[2]) | ((uint32_t)f2h_bits(v[6]) << 16);
-            o.w = (uint32_t)f2h_bits(v[3]) | ((uint32_t)f2h_bits(v[7]) << 16);
-            *reinterpret_cast<uint4 *>(p.ws.x16 + (size_t)t * H + c) = o;
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; j++) p.ws.xperm[(size_t)t * H + perm_pos(c + j, H)] = v[j];
-        }
-    }
 }
 
 // ---------------------------------------------------------------------------
@@ -1595,6 +1641,25 @@ size_t router_smem_bytes(const Dims &d) {
     return topk > bucket ? topk : bucket;
 }
 
+// k-ranges of the tiled router for T tokens: about kRouterBlocks blocks in all
+int router_split(int T, int E, int H) {
+    const int tiles = ((E + kRtExp - 1) / kRtExp) * ((T + kRtTok - 1) / kRtTok);
+    int S = kRouterBlocks / tiles;
+    if (S > kRouterMaxSplit) S = kRouterMaxSplit;
+    if (S > H / kRtK) S = H / kRtK;
+    return S < 1 ? 1 : S;
+}
+
+// largest S * T of any tiled-router call up to maxT tokens (partial-logit rows)
+size_t router_part_rows(const Dims &d) {
+    size_t m = 0;
+    for (int T = kGemvMaxT + 1; T <= d.max_tokens; T++) {
+        const size_t v = (size_t)router_split(T, d.E, d.H) * (size_t)T;
+        if (v > m) m = v;
+    }
+    return m;
+}
+
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 }  // namespace
@@ -1640,10 +1705,10 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
     ws->items = reinterpret_cast<int *>(
         take(mma ? 2 * (size_t)max_items((int)T, d.K, d.E, d.n_shared) * sizeof(int) : 0));
     ws->n_items = reinterpret_cast<int *>(take(sizeof(int)));
-    ws->gcount = reinterpret_cast<unsigned *>(take((T + 31) / 32 * sizeof(unsigned)));
     const bool tiled = T > (size_t)kGemvMaxT;
-    ws->lpart = reinterpret_cast<float *>(take(tiled ? kRouterMaxSplit * T * d.E * sizeof(float) : 0));
-    ws->sspart = reinterpret_cast<float *>(take(tiled ? kRouterMaxSplit * T * sizeof(float) : 0));
+    const size_t prows = tiled ? router_part_rows(d) : 0;
+    ws->lpart = reinterpret_cast<float *>(take(prows * d.E * sizeof(float)));
+    ws->sspart = reinterpret_cast<float *>(take(prows * sizeof(float)));
     ws->total_bytes = o;
 }
 
@@ -1665,7 +1730,9 @@ cudaError_t prepare_kernels(const Dims &d) {
     const int smem = (int)router_smem_bytes(d);
     cudaError_t e = cudaFuncSetAttribute(router_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(router_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        e = cudaFuncSetAttribute(router_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRtSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(router_reduce_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess && d.mma && d.tc) {
         e = cudaFuncSetAttribute(tc_expert_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
         if (e == cudaSuccess)
@@ -1706,16 +1773,11 @@ cudaError_t launch_forward(const Params &p0, const float *x, int T, float *y, cu
         const int grid = (d.E + 1) / 2;
         router_gemv_kernel<<<grid, kThreads, smem, st>>>(p, x, T, buckets);
     } else {
-        const int bxy = ((d.E + 31) / 32) * ((T + 31) / 32);
-        int S = (kRouterBlocks + bxy - 1) / bxy;
-        S = S < 1 ? 1 : (S > kRouterMaxSplit ? kRouterMaxSplit : S);
-        S = S > d.H / 32 ? d.H / 32 : S;
-        const dim3 grid((d.E + 31) / 32, (T + 31) / 32, S);
-        router_tiled_kernel<<<grid, kThreads, smem, st>>>(p, x, T, buckets);
+        const int S = router_split(T, d.E, d.H);
+        const dim3 grid((d.E + kRtExp - 1) / kRtExp, (T + kRtTok - 1) / kRtTok, S);
+        router_tiled_kernel<<<grid, kThreads, kRtSmem, st>>>(p, x, T);
         check();
-        const size_t n8 = (size_t)T * d.H / 8;
-        const int cb = (int)((n8 + kThreads - 1) / kThreads < 4096 ? (n8 + kThreads - 1) / kThreads : 4096);
-        act_convert_kernel<<<cb, kThreads, 0, st>>>(p, x, T);
+        router_reduce_kernel<<<T, kThreads, smem, st>>>(p, x, T, S, buckets);
     }
     check();
     mark(1);
