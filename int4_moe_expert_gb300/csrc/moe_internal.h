@@ -64,7 +64,7 @@ struct Workspace {
 
 constexpr int kMaxSlots = 33;   // K <= 32 routed + 1 shared
 constexpr int kRouterMaxSplit = 32;  // tiled router: k-ranges (split-K) at most
-constexpr int kItemTokens = 32;  // tokens of one tensor-core work item (4 n8 tiles)
+constexpr int kItemTokens = 16;  // tokens of the smallest mma.sync work item (2 n8 tiles)
 inline int max_items(int T, int K, int E, int n_shared, int item = kItemTokens) {   // work items, at most
     const int P = T * K;
     return P / item + (E < P ? E : P) + (n_shared ? (T + item - 1) / item : 0) + 1;

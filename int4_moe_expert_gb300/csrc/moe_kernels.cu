@@ -273,7 +273,7 @@ __device__ void bucket_phase(const Params &p, int T, int *ismem) {
     __syncthreads();
     if (warp == 0) {
         // exclusive scans of counts and of "active" flags, E <= 1024
-        // (and of work items for the tensor-core kernels: kItemTokens tokens of one slot each)
+        // (and of work items for the tensor-core kernels: p.item_tok tokens of one slot each)
         const int per = (E + 31) / 32;
         const int b = lane * per;
         const bool items = p.d.mma && (T > 1 || p.d.mma_fmt);
@@ -932,7 +932,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Params p, const float
 // Batched (T > 1) on the tensor cores: mma.sync m16n8k16, f16 x f16 -> f32.
 //
 // A = int4 weight rows (exact in f16), B = f16 activations of up to
-// kItemTokens tokens (one work item: a slot and a run of its tokens), C in
+// 16 or 32 tokens (one work item: a slot and a run of its tokens), C in
 // f32 registers.  Each thread streams, per 128-element block of the reduction,
 // the 16 bytes at offset 16 q (q = lane % 4) of each of its weight rows: four
 // 32-bit words of 8 int4 values.  One word w splits with two masks and two
@@ -979,7 +979,7 @@ __device__ __forceinline__ uint32_t u4w(const uint4 &v, int i) {
     return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
 
-constexpr int kMmaNT = kItemTokens / 8;     // n8 tiles per work item
+constexpr int kMmaItemMax = 32;             // tokens of the largest mma.sync work item (4 n8 tiles)
 constexpr int kMmaKB = 128;                 // reduction elements per ring stage (a multiple of 128)
 constexpr int kMmaSub = kMmaKB / 128;       // 128-element sub-blocks per stage
 constexpr int kMmaStages = 4;               // stages in the shared-memory ring
@@ -988,7 +988,7 @@ constexpr int kMmaARowB = kMmaKB / 2;       // bytes of one weight row per stage
 constexpr int kMmaABytes = kMmaARows * kMmaARowB;
 constexpr int kMmaBLd = kMmaKB + 8;         // f16 per staged activation row (+ 8: no bank conflicts)
 constexpr int kMmaBPieces = kMmaKB / 8;     // 16-byte copies per activation row per stage
-constexpr int kMmaBBytes = kItemTokens * kMmaBLd * 2;
+constexpr int kMmaBBytes = kMmaItemMax * kMmaBLd * 2;
 constexpr int kMmaStageBytes = kMmaABytes + kMmaBBytes;
 constexpr size_t kMmaSmem = (size_t)kMmaStages * kMmaStageBytes;
 
@@ -1067,10 +1067,11 @@ __device__ __forceinline__ void g64x8_to_f16x2(uint32_t w, uint32_t s2, uint32_t
 }
 
 // One work item times one tile of output rows (see mma_expert_kernel), weights in format FMT.
-template <bool GU, int FMT>
+template <bool GU, int FMT, int NT>
 __device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo &s, int nt, int o0,
                                          unsigned char *mma_smem, const int *s_brow, const int *s_orow) {
     using F = MmaFmt<FMT>;
+    constexpr int kMmaNT = NT / 8;                     // n8 tiles of a work item
     const int H = p.d.H, Is = s.Is;
     const int rows = GU ? Is : H;                       // output rows of the slot
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
@@ -1080,7 +1081,7 @@ __device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo 
     const uint16_t *act = GU ? p.ws.x16 : p.ws.h16;
     const size_t ald = GU ? (size_t)H : (size_t)p.d.I_max;     // activation row stride (f16)
     // this thread's cp.async pieces of one stage
-    constexpr int kAP = F::kPcs, kBP = kItemTokens * kMmaBPieces / kThreads;   // copies per thread
+    constexpr int kAP = F::kPcs, kBP = NT * kMmaBPieces / kThreads;   // copies per thread
     const uint8_t *asrc[kAP];
     uint32_t adst[kAP];
     int apiece[kAP];
@@ -1270,15 +1271,15 @@ __device__ __forceinline__ void mma_body(const Params &p, int T, const SlotInfo 
 // owns output rows o0 + 16 w + {0..15}, as two m16 tiles: those gate rows and
 // the same up rows; 128 rows per block; writes h16.  Down: warp w owns rows
 // o0 + 32 w + {0..31} (two m16 tiles), 256 rows per block; writes dbuf.
-// Weights (256 rows per stage) and the item's activations (kItemTokens rows)
+// Weights (256 rows per stage) and the item's activations (NT rows)
 // move through a ring in shared memory with cp.async; every stage is one
 // __syncthreads.  FR / FS: weight formats of the routed experts / the shared
 // expert; each instantiation carries only the bodies it needs, so a config with
 // one format gets the lean kernel and a mixed one still runs in one launch.
-template <bool GU, int FR, int FS>
+template <bool GU, int FR, int FS, int NT>
 __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T) {
     extern __shared__ __align__(128) unsigned char mma_smem[];
-    __shared__ int s_brow[kItemTokens], s_orow[kItemTokens];
+    __shared__ int s_brow[NT], s_orow[NT];
     const int item = blockIdx.x;
     if (item >= *p.ws.n_items) return;
     const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
@@ -1287,8 +1288,8 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
     const int o0 = blockIdx.y * (GU ? 128 : 256);
     if (o0 >= (GU ? s.Is : p.d.H)) return;
     const int tid = threadIdx.x;
-    const int nt = min(kItemTokens, s.n - n0);
-    if (tid < kItemTokens) {
+    const int nt = min(NT, s.n - n0);
+    if (tid < NT) {
         int tok = 0, row = -1;
         if (tid < nt) slot_token(p, s, T, n0 + tid, &tok, &row);
         s_brow[tid] = GU ? tok : row;          // activation row the tensor cores read
@@ -1296,9 +1297,9 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
     }
     __syncthreads();
     if (FR == FS || s.base >= 0)
-        mma_body<GU, FR>(p, T, s, nt, o0, mma_smem, s_brow, s_orow);
+        mma_body<GU, FR, NT>(p, T, s, nt, o0, mma_smem, s_brow, s_orow);
     else
-        mma_body<GU, FS>(p, T, s, nt, o0, mma_smem, s_brow, s_orow);
+        mma_body<GU, FS, NT>(p, T, s, nt, o0, mma_smem, s_brow, s_orow);
 }
 
 // ---------------------------------------------------------------------------
@@ -1605,8 +1606,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
 
 template <bool GU, int FR, int FS>
 cudaError_t mma_attr() {
-    return cudaFuncSetAttribute(mma_expert_kernel<GU, FR, FS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kMmaSmem);
+    cudaError_t e = cudaFuncSetAttribute(mma_expert_kernel<GU, FR, FS, 16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMmaSmem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(mma_expert_kernel<GU, FR, FS, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kMmaSmem);
+    return e;
 }
 
 // The (routed, shared) format pair of a config as one switch value.
@@ -1619,6 +1624,16 @@ constexpr bool kUseTc = true;   // int4 experts on tcgen05 for large T (else alw
 // on the GLM layer: gate/up 0.68 vs 0.78 ms at T 512; at T <= 64 the mma.sync kernel is faster)
 constexpr int kTcMinT = 256;
 
+// Tokens of a tensor-core work item for a call of T tokens: 128 on tcgen05; on the
+// mma.sync kernel 16 while experts see few tokens each (measured on the GLM layer at
+// T 16 and 64: gate/up and down ~22 % faster than with 32-token items), 32 once the mean
+// routed expert gets 24 or more (OLMoE-shaped int8 layer at T 256: 32-token items 22 %
+// faster, each expert's weights read half as often).
+int mma_item_tokens(const Dims &d, int T) {
+    if (d.tc && T >= kTcMinT) return kTcTok;
+    return (long)T * d.K >= 24L * d.E ? kMmaItemMax : kItemTokens;
+}
+
 // Launch the tensor-core kernel of one phase (gate/up or down) for the config's formats.
 template <bool GU>
 void launch_mma_phase(const Params &p, int T, dim3 grid, cudaStream_t st) {
@@ -1628,8 +1643,11 @@ void launch_mma_phase(const Params &p, int T, dim3 grid, cudaStream_t st) {
         return;
     }
     switch (fmt_pair(p.d)) {
-#define MOE_LAUNCH(R, S) \
-    case R * 3 + S: mma_expert_kernel<GU, R, S><<<grid, kThreads, kMmaSmem, st>>>(p, T); break;
+#define MOE_LAUNCH(R, S)                                                                  \
+    case R * 3 + S:                                                                       \
+        if (p.item_tok == 32) mma_expert_kernel<GU, R, S, 32><<<grid, kThreads, kMmaSmem, st>>>(p, T); \
+        else mma_expert_kernel<GU, R, S, 16><<<grid, kThreads, kMmaSmem, st>>>(p, T);    \
+        break;
         MOE_FMT_PAIRS(MOE_LAUNCH)
 #undef MOE_LAUNCH
     }
@@ -1755,7 +1773,7 @@ cudaError_t launch_forward(const Params &p0, const float *x, int T, float *y, cu
     // this call's tensor-core work items: 128 tokens on the tcgen05 kernel (T >= kTcMinT),
     // else 32 on the mma.sync kernel
     Params p = p0;
-    p.item_tok = (p0.d.tc && T >= kTcMinT) ? kTcTok : kItemTokens;
+    p.item_tok = mma_item_tokens(p0.d, T);
     const Dims &d = p.d;
     if (T == 1 && d.fast_decode) return launch_decode_fast(p, x, y, st, ev, want_buckets);
     const size_t smem = router_smem_bytes(d);
