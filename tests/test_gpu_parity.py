@@ -172,21 +172,24 @@ def test_tensor_core_path_selection(moe):
         assert rel_err(b[t], a[t]) < 2e-3
 
 
-def test_batched_glm_512_sampled(moe):
-    """Full-size batched layer: all 512 routing decisions, outputs on a sample."""
+@pytest.mark.parametrize("T", [64, 512])
+def test_batched_glm_512_sampled(moe, T):
+    """Full-size batched layer: all T routing decisions, outputs on a sample (T=64: the
+    router's reduction split into 32 k-ranges, 16-token mma.sync items; T=512: 14 k-ranges,
+    tcgen05 experts)."""
     wl, li, layer = layer_for(moe, "glm_batched", 512)
-    x = synth.tokens(wl, T=512, stream=0)
+    x = synth.tokens(wl, T=T, stream=0)
     xd = torch.from_numpy(x).cuda()
     y, idx, w, cnt = layer.forward_debug(xd, counts=True)
     torch.cuda.synchronize()
     y, idx, w, cnt = y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy(), cnt.cpu().numpy()
     # bucketing: a histogram of the routing decisions
-    assert cnt.sum() == 512 * wl.K
+    assert cnt.sum() == T * wl.K
     assert np.array_equal(cnt, np.bincount(idx.ravel(), minlength=wl.E))
     ref = oracle_layer(wl, li)
     import oracle
     n_tie = 0
-    for t in range(512):
+    for t in range(T):
         ridx, _, margin, scores = oracle.route(ref.cfg, ref.router_w, ref.router_b,
                                                x[t].astype(np.float64))
         if margin > MARGIN:
@@ -197,12 +200,12 @@ def test_batched_glm_512_sampled(moe):
     # load is uneven, as the workload asks (bias ~ N(0, 0.5))
     assert cnt.max() >= 2 * cnt[cnt > 0].mean()
     rng = np.random.default_rng(0)
-    sample = sorted(set([0, 1, 255, 511] + rng.choice(512, 20, replace=False).tolist()))
+    sample = sorted(set([0, 1, T // 2, T - 1] + rng.choice(T, 20, replace=False).tolist()))
     worst = 0.0
     for t in sample:
-        err, _ = check_token(wl, ref, x[t], y[t], idx[t], w[t], where=f"glm512 t={t}")
+        err, _ = check_token(wl, ref, x[t], y[t], idx[t], w[t], where=f"glm T={T} t={t}")
         worst = max(worst, err)
-    print(f"glm batched: worst sampled rel err {worst:.3e}, near ties {n_tie}")
+    print(f"glm batched T={T}: worst sampled rel err {worst:.3e}, near ties {n_tie}")
 
 
 def test_batched_is_deterministic_and_token_independent(moe):
