@@ -27,6 +27,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kGemvMaxT = 8;       // router GEMV handles up to this many tokens
+constexpr int kGemvAhead = 4;      // router GEMV: row steps (32 lanes x 16 bytes) loaded at once
 constexpr int kRouterBlocks = 456;  // tiled router: aim for 3 blocks per SM (split-K over H)
 
 // ---------------------------------------------------------------------------
@@ -375,7 +376,31 @@ __device__ void gemv_logits(const Params &p, const float *__restrict__ x, int T,
     for (int t = 0; t < kGemvMaxT; t++) acc[t] = 0.0f;
     if (e < E) {
         const float4 *w4 = reinterpret_cast<const float4 *>(p.router_w + (size_t)e * H);
-        for (int i = i0 + lane; i < i1; i += 32) {
+        int i = i0 + lane;
+        // kGemvAhead steps of the row at once (their loads in flight together); the sums
+        // still run in step order
+        for (; i + 32 * (kGemvAhead - 1) < i1; i += 32 * kGemvAhead) {
+            float4 wv[kGemvAhead];
+#pragma unroll
+            for (int u = 0; u < kGemvAhead; u++) wv[u] = __ldg(w4 + i + 32 * u);
+#pragma unroll
+            for (int t = 0; t < kGemvMaxT; t++) {
+                if (t < T) {
+                    float4 xv[kGemvAhead];
+#pragma unroll
+                    for (int u = 0; u < kGemvAhead; u++)
+                        xv[u] = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H) + i + 32 * u);
+#pragma unroll
+                    for (int u = 0; u < kGemvAhead; u++) {
+                        acc[t] = fmaf(wv[u].x, xv[u].x, acc[t]);
+                        acc[t] = fmaf(wv[u].y, xv[u].y, acc[t]);
+                        acc[t] = fmaf(wv[u].z, xv[u].z, acc[t]);
+                        acc[t] = fmaf(wv[u].w, xv[u].w, acc[t]);
+                    }
+                }
+            }
+        }
+        for (; i < i1; i += 32) {
             const float4 wv = __ldg(w4 + i);
 #pragma unroll
             for (int t = 0; t < kGemvMaxT; t++) {
