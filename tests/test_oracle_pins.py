@@ -58,7 +58,7 @@ def test_expert_bytes_match_the_pages_19MB_figure():
     b = synth.slab_bytes(6144, 2048) + 4 * synth.scale_count(6144, 2048)
     assert b == 18_915_328
     assert abs(b / 1e6 - 19) < 0.2
-    # the survey's per-config figures for the other shapes
+    # per-expert bytes of the other layer shapes (b_exp = 2 I ceil(H/2) + H ceil(I/2) + 4 (2I + H))
     assert synth.slab_bytes(256, 128) + 4 * synth.scale_count(256, 128) == 51_200
     assert synth.slab_bytes(2048, 1024) + 4 * synth.scale_count(2048, 1024) == 3_162_112
     assert synth.slab_bytes(2048, 512) + 4 * synth.scale_count(2048, 512) == 1_585_152
