@@ -91,6 +91,17 @@ def test_workspace_bytes_validates_config(moe):
     assert moe.moe_workspace_bytes(good, 1 << 20) == 0
 
 
+def test_workspace_grows_linearly_in_max_tokens(moe):
+    """The workspace is per-token buffers (h, down outputs, f16 activations, routing) plus
+    the tiled router's partial logits, which are bounded in rows (split count x tokens):
+    about 0.4 MB per token on the GLM layer from 64 tokens up, never a quadratic term."""
+    glm = moe.make_config(6144, 256, 8, 2048, 1, 2048, 2.5)
+    sizes = {T: moe.moe_workspace_bytes(glm, T) for T in (64, 512, 4096, 16384)}
+    for T, b in sizes.items():
+        assert 0 < b / T < 420_000, (T, b)
+    assert sizes[512] < sizes[4096] < sizes[16384]
+
+
 def test_null_arguments_are_errors_not_crashes(moe):
     L = moe.lib()
     cfg = moe.make_config(256, 16, 2, 128, 1, 128, 2.5)
