@@ -1,0 +1,46 @@
+"""Host-side arithmetic of bench.py: the algorithmic byte counts behind the reported HBM
+figures and roofline fractions (no GPU needed)."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+import synth  # noqa: E402
+
+
+def test_glm_decode_step_bytes():
+    # 9 experts x 18,915,328 B + router 256 x 6144 x 4 + bias 256 x 4 + x and y (2 x 6144 x 4)
+    wl = synth.WORKLOADS["glm_decode"]
+    assert bench.expert_bytes(6144, 2048) == 18_915_328
+    assert bench.step_bytes(wl, 1, 8) == 9 * 18_915_328 + 6_291_456 + 1_024 + 2 * 24_576
+    assert bench.step_bytes(wl, 1, 8) == 176_579_584
+
+
+def test_gateup_bytes_are_two_thirds_of_an_expert_plus_their_scales():
+    # gate and up: 2 x 2048 rows of 3072 bytes, 2 x 2048 float32 scales
+    assert bench.gateup_bytes(6144, 2048) == 2 * 2048 * 3072 + 8 * 2048
+    # int8 rows: one byte per value
+    assert bench.gateup_bytes(6144, 2048, 1) == 2 * 2048 * 6144 + 8 * 2048
+
+
+def test_stack_bytes_per_token():
+    # 40 layers x (4 routed + 1 shared expert of 1,585,152 B + router 256 x 2048 x 4 + bias + x, y)
+    wl = synth.WORKLOADS["stack35b"]
+    per_layer = 5 * 1_585_152 + 256 * 2048 * 4 + 256 * 4 + 2 * 2048 * 4
+    assert bench.step_bytes(wl, 1, wl.K) == per_layer
+    assert wl.n_layers * per_layer == 401_612_800
+
+
+def test_batched_step_counts_each_touched_expert_once():
+    wl = synth.WORKLOADS["glm_batched"]
+    one = bench.step_bytes(wl, 512, 1)
+    two = bench.step_bytes(wl, 512, 2)
+    assert two - one == bench.expert_bytes(6144, 2048)
+
+
+def test_workload_description_names_the_shapes():
+    d = bench.workload_desc(synth.WORKLOADS["glm_decode"])
+    for part in ("T=1", "H=6144", "E=256", "top-8", "moe_inter=2048", "routed_scale=2.5"):
+        assert part in d, part
