@@ -48,7 +48,7 @@ struct Workspace {
     // T > 1 tensor-core path: f16 activations in mma order (mma_pos in moe_kernels.cu)
     uint16_t *x16;       // [maxT, H] pre-normed x
     uint16_t *h16;       // [(maxT*K + maxT), I_max] SwiGLU activations, rows as h
-    int *items;          // [2 * max_items] (slot, first token) of every kItemTokens-token work item
+    int *items;          // [2 * max_items] (slot, first token) of every work item (item_tok tokens)
     int *n_items;        // [1]
     float *lpart;        // [S, T, E] tiled router: logits of each of a call's S k-ranges
     float *sspart;       // [S, T] tiled router: sums of squares of each k-range
