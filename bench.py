@@ -183,6 +183,13 @@ def measured_tensor_peak():
     return 1900.0, "fallback (1.9 PFLOP/s bf16 burst)"
 
 
+def binding_roofline(hbm_frac: float, tensor_frac: float) -> str:
+    """The roof a tensor-core kernel is nearer to: 'tensor' when its fraction of the tensor
+    peak is at least its fraction of the copy bandwidth, else 'hbm' (small batches stream
+    weights far below the tensor peak)."""
+    return "tensor" if tensor_frac >= hbm_frac else "hbm"
+
+
 def recorded_traffic(kind: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary (already scaled to the bench workload), or None when the kernel
@@ -421,7 +428,11 @@ def run_ours(args, rank, world, local_rank, dist_on):
             "gpu_launches": world * K * kernels_per_step,
             "clocks": clk.summary(),
         }
-        if tensor:
+        if tensor and binding_roofline(achieved / peak, achieved_t / tpeak) == "hbm":
+            out["roofline"]["tensor_view"] = {"achieved_tflops": round(achieved_t, 1), "peak_tflops": tpeak,
+                                              "frac": round(achieved_t / tpeak, 4),
+                                              "flops_per_launch": int(dom_flops)}
+        elif tensor:
             out["roofline"] = {
                 "kernel": dom_name,
                 "bound": "tensor",

@@ -44,3 +44,10 @@ def test_workload_description_names_the_shapes():
     d = bench.workload_desc(synth.WORKLOADS["glm_decode"])
     for part in ("T=1", "H=6144", "E=256", "top-8", "moe_inter=2048", "routed_scale=2.5"):
         assert part in d, part
+
+
+def test_binding_roofline_is_the_nearer_roof():
+    # T=512 on tcgen05: 0.18 of the tensor peak, 0.10 of the copy bandwidth
+    assert bench.binding_roofline(0.10, 0.18) == "tensor"
+    # T=2 on mma.sync: weights streamed at 0.45 of the copy bandwidth, 0.007 of the tensor peak
+    assert bench.binding_roofline(0.45, 0.007) == "hbm"
