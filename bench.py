@@ -662,22 +662,34 @@ def run_stack(args, rank, world, local_rank, dist_on):
 
 def cpu_baseline(wl, li, xs_host, seconds):
     """The oracle, as it stands, on this host's cores over a bounded sample of
-    the same workload (whole tokens through the layer in double precision)."""
+    the same workload (whole tokens through the layer in double precision), and
+    the same on one core for a quarter of the time."""
     import oracle
     ref = oracle.LayerRef.from_inputs(oracle.cfg_from_workload(wl), li)
-    n_tok, t0 = 0, time.perf_counter()
-    i = 0
-    while True:
-        ref.forward(xs_host[i % len(xs_host)])
-        n_tok += xs_host[0].shape[0]
-        i += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or i >= 4096:
-            break
-    return {"value": round(n_tok / el, 4), "unit": "tokens/s", "cores": oracle.threads(),
+
+    def timed(budget):
+        n_tok, i, t0 = 0, 0, time.perf_counter()
+        while True:
+            ref.forward(xs_host[i % len(xs_host)])
+            n_tok += xs_host[0].shape[0]
+            i += 1
+            el = time.perf_counter() - t0
+            if el >= budget or i >= 4096:
+                return n_tok, i, el
+
+    cores = oracle.threads()
+    n_tok, i, el = timed(seconds)
+    oracle.set_threads(1)
+    try:
+        n1, i1, el1 = timed(seconds / 4)
+    finally:
+        oracle.set_threads(cores)
+    return {"value": round(n_tok / el, 4), "unit": "tokens/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{n_tok} tokens ({i} calls of T={xs_host[0].shape[0]}) of the same layer "
-                      f"through the double-precision C oracle, OpenMP over output rows, {el:.1f} s"}
+                      f"through the double-precision C oracle, OpenMP over output rows, {el:.1f} s",
+            "single_core": {"value": round(n1 / el1, 4), "unit": "tokens/s", "cores": 1,
+                            "sample": f"{n1} tokens ({i1} calls), one thread, {el1:.1f} s"}}
 
 
 # --------------------------------------------------------------------------- reference arm

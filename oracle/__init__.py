@@ -74,6 +74,8 @@ def lib():
         L.oracle_moe_forward.argtypes = [C.POINTER(Cfg), C.POINTER(Layer), vp, ip, vp, vp, vp, vp]
         L.oracle_moe_forward.restype = ip
         L.oracle_threads.restype = ip
+        L.oracle_set_threads.argtypes = [ip]
+        L.oracle_set_threads.restype = None
         _lib = L
     return _lib
 
@@ -219,3 +221,8 @@ class LayerRef:
 
 def threads() -> int:
     return lib().oracle_threads()
+
+
+def set_threads(n: int) -> None:
+    """OpenMP threads of the following oracle calls (timing on one core)."""
+    lib().oracle_set_threads(int(n))

@@ -21,6 +21,15 @@ int oracle_threads(void) {
 #endif
 }
 
+/* Threads of the following calls (n >= 1); used to time the oracle on one core. */
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Section 06: element 2j is the low nibble of byte j, 2j+1 the high nibble;
  * the stored nibble is q + 8. */
 static int nibble_at(const uint8_t *row, int i) {

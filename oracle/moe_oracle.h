@@ -131,6 +131,7 @@ int oracle_moe_forward(const oracle_cfg *c, const oracle_layer *L, const float *
 
 /* Threads an OpenMP build would use (1 without OpenMP). */
 int oracle_threads(void);
+void oracle_set_threads(int n);
 
 #ifdef __cplusplus
 }

@@ -51,3 +51,16 @@ def test_binding_roofline_is_the_nearer_roof():
     assert bench.binding_roofline(0.10, 0.18) == "tensor"
     # T=2 on mma.sync: weights streamed at 0.45 of the copy bandwidth, 0.007 of the tensor peak
     assert bench.binding_roofline(0.45, 0.007) == "hbm"
+
+
+def test_cpu_baseline_times_all_cores_and_one():
+    import oracle
+    oracle.build()
+    wl = synth.WORKLOADS["tiny"]
+    li = synth.layer_inputs(wl)
+    xs = [synth.tokens(wl, T=1, stream=s) for s in range(4)]
+    cores = oracle.threads()
+    out = bench.cpu_baseline(wl, li, xs, 0.4)
+    assert out["kind"] == "oracle" and out["cores"] == cores and out["value"] > 0
+    assert out["single_core"]["cores"] == 1 and out["single_core"]["value"] > 0
+    assert oracle.threads() == cores          # the thread count is restored
