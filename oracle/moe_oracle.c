@@ -42,32 +42,39 @@ void oracle_unpack_int4(const uint8_t *row, int n, int *q) {
     for (int i = 0; i < n; i++) q[i] = nibble_at(row, i);
 }
 
-/* Section 06 quantiser: per row amax, s = max(amax/7, 1e-8),
- * q = clip(rint(w/s), -8, 7), pad value 0 (stored 8).  float32 as printed. */
+/* Scale of one row for a symmetric signed code with largest code qmax, in
+ * float32 as the pages define it: the row's peak magnitude over qmax, floored
+ * at 1e-8 so that an all-zero row keeps a finite, non-zero scale. */
+static float sym_row_scale(const float *row, int n, int qmax) {
+    float peak = 0.f;
+    for (int i = 0; i < n; i++) peak = fmaxf(peak, fabsf(row[i]));
+    return fmaxf(peak / (float)qmax, 1e-8f);
+}
+
+/* The code of v under scale s: v / s rounded to the nearest integer (ties to
+ * even, rintf in the default rounding mode), held inside [lo, hi]; NaN -> lo. */
+static int sym_code(float v, float s, int lo, int hi) {
+    const float c = rintf(v / s);
+    if (!(c > (float)lo)) return lo;
+    if (c > (float)hi) return hi;
+    return (int)c;
+}
+
+/* int4 per-row quantiser of the reader.mx page, section 06 "从 FP8 到 int4":
+ * codes in [-8, 7] under sym_row_scale(row, 7), stored as code + 8 with element
+ * 2j in the low nibble of byte j; an odd row's last byte is padded with code 0. */
 void oracle_quantize_int4(const float *w, int O, int I, uint8_t *q4, float *scale) {
-    const int qmax = 7, rb = (I + 1) / 2;
+    const int stride = (I + 1) / 2;
+    memset(q4, 0x88, (size_t)O * (size_t)stride);   /* every nibble holds code 0 */
     for (int o = 0; o < O; o++) {
-        const float *wr = w + (int64_t)o * I;
-        float amax = 0.f;
-        for (int i = 0; i < I; i++) {
-            float a = fabsf(wr[i]);
-            if (a > amax) amax = a;
-        }
-        float s = amax / (float)qmax;
-        if (s < 1e-8f) s = 1e-8f;
+        const float *row = w + (int64_t)o * I;
+        uint8_t *dst = q4 + (int64_t)o * stride;
+        const float s = sym_row_scale(row, I, 7);
         scale[o] = s;
-        uint8_t *qr = q4 + (int64_t)o * rb;
-        for (int j = 0; j < rb; j++) {
-            int v[2] = {0, 0};
-            for (int h = 0; h < 2; h++) {
-                int i = 2 * j + h;
-                if (i >= I) break;
-                long r = lrintf(wr[i] / s);   /* round half to even */
-                if (r > qmax) r = qmax;
-                if (r < -8) r = -8;
-                v[h] = (int)r;
-            }
-            qr[j] = (uint8_t)((v[0] + 8) | ((v[1] + 8) << 4));
+        for (int i = 0; i < I; i++) {
+            const unsigned nib = (unsigned)(sym_code(row[i], s, -8, 7) + 8);
+            const unsigned shift = 4u * (unsigned)(i & 1);
+            dst[i >> 1] = (uint8_t)((dst[i >> 1] & ~(15u << shift)) | (nib << shift));
         }
     }
 }
@@ -107,24 +114,15 @@ static void int8_matvec(const uint8_t *q8, const float *scale, int O, int n,
     }
 }
 
-/* The reader.mx page's OLMoE-engine quantiser (section 03, quantize_rows with
- * bits = 8), in its float32 arithmetic: per row s = max(amax / 127, 1e-8),
- * q = clip(rint(w / s), -128, 127). */
+/* int8 per-row quantiser of the reader.mx page's OLMoE engine (section 03,
+ * 8-bit codes): codes in [-128, 127] under sym_row_scale(row, 127), one signed
+ * byte per value. */
 void oracle_quantize_int8(const float *w, int O, int I, int8_t *q, float *scale) {
-    const int qmax = 127;
     for (int o = 0; o < O; o++) {
-        const float *wr = w + (int64_t)o * I;
-        float amax = 0.f;
-        for (int i = 0; i < I; i++) { float a = fabsf(wr[i]); if (a > amax) amax = a; }
-        float s = amax / qmax;
-        if (s < 1e-8f) s = 1e-8f;
-        scale[o] = s;
-        for (int i = 0; i < I; i++) {
-            int v = (int)lrintf(wr[i] / s);
-            if (v > qmax) v = qmax;
-            if (v < -qmax - 1) v = -qmax - 1;
-            q[(int64_t)o * I + i] = (int8_t)v;
-        }
+        const float *row = w + (int64_t)o * I;
+        int8_t *dst = q + (int64_t)o * I;
+        scale[o] = sym_row_scale(row, I, 127);
+        for (int i = 0; i < I; i++) dst[i] = (int8_t)sym_code(row[i], scale[o], -128, 127);
     }
 }
 

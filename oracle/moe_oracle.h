@@ -81,11 +81,12 @@ typedef struct {
 /* int4 unpack of n values from one packed row: q[i] = nibble - 8. */
 void oracle_unpack_int4(const uint8_t *row, int n, int *q);
 
-/* Offline quantiser of section 06 (float32 arithmetic, as printed). */
+/* Per-row symmetric int4 codes of a float32 matrix [O, I] (section 06), computed
+ * in float32 because the stored bytes and scales are what the page defines. */
 void oracle_quantize_int4(const float *w, int O, int I, uint8_t *q4, float *scale);
 
-/* The OLMoE engine's per-row int8 quantiser (section 03, bits = 8), float32
- * arithmetic as printed. */
+/* Per-row symmetric int8 codes of a float32 matrix [O, I] (section 03, the
+ * OLMoE engine's 8-bit weights), computed in float32 like the int4 quantiser. */
 void oracle_quantize_int8(const float *w, int O, int I, int8_t *q, float *scale);
 
 /* oracle_expert for any weight format (ORACLE_FORMAT_*); the int8 slab is
