@@ -384,10 +384,11 @@ moe_status moe_destroy(moe_handle *h) {
     if (!h) return MOE_OK;
     int cur = -1;
     cudaGetDevice(&cur);
-    if (cur != h->device) cudaSetDevice(h->device);
+    const int dev = h->device;
+    if (cur != dev) cudaSetDevice(dev);
     const cudaError_t e = cudaDeviceSynchronize();
     free_handle(h);
-    if (cur >= 0 && cur != h->device) cudaSetDevice(cur);
+    if (cur >= 0 && cur != dev) cudaSetDevice(cur);
     if (e != cudaSuccess) return cuda_fail(e, "device synchronize before free");
     return MOE_OK;
 }
