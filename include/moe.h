@@ -84,8 +84,8 @@ typedef struct moe_config {
     int32_t topk_group;    /* groups kept when n_group > 1: 1..n_group, with
                               top_k <= topk_group * n_experts / n_group; ignored when n_group == 1 */
     int32_t score_func;    /* MOE_SCORE_SIGMOID (0) or MOE_SCORE_SOFTMAX (1) */
-    int32_t expert_format; /* routed experts: MOE_FORMAT_INT4 (0) or MOE_FORMAT_INT8 (1) */
-    int32_t shared_format; /* shared expert: MOE_FORMAT_INT4 (0) or MOE_FORMAT_INT8 (1) */
+    int32_t expert_format; /* routed experts: MOE_FORMAT_INT4 (0), MOE_FORMAT_INT8 (1) or MOE_FORMAT_G64 (2) */
+    int32_t shared_format; /* shared expert: MOE_FORMAT_INT4 (0), MOE_FORMAT_INT8 (1) or MOE_FORMAT_G64 (2) */
 } moe_config;
 
 /* Weight formats of an expert slab:
@@ -246,9 +246,13 @@ int32_t moe_abi_version(void);
  * (device float32), exactly what moe_forward_debug returns in topk_idx[T,K]
  * (int32, descending selection score) and topk_w[T,K] (float32): router
  * logits W_r x (with 1/rms(x) applied when cfg->flags has
- * MOE_FLAG_PRENORM_RESIDUAL), sigmoid + bias top-K, renormalised weights.
- * Only cfg's hidden, n_experts, top_k, n_group, norm_topk, routed_scale,
- * rms_eps and flags are read.
+ * MOE_FLAG_PRENORM_RESIDUAL), then the selection cfg describes: the sigmoid
+ * family (top-K of sigmoid + bias, group-limited when n_group > 1) or the
+ * softmax family (score_func = MOE_SCORE_SOFTMAX), each with or without
+ * renormalisation (norm_topk) and times routed_scale, as described at the
+ * top of this file.  The fields read are hidden, n_experts, top_k, n_group,
+ * topk_group, score_func, norm_topk, routed_scale, rms_eps and flags; the
+ * expert sizes and formats are ignored.
  *
  * Scratch: one fixed static device array in the library (logits of up to
  * MOE_ROUTE_NOALLOC_MAX_TOKENS x MOE_ROUTE_NOALLOC_MAX_EXPERTS floats plus a
@@ -263,11 +267,15 @@ int32_t moe_abi_version(void);
  * before its kernel; logits are rewritten in full every call.
  *
  * Errors: MOE_ERR_INVALID for NULL or misaligned pointers (router_w and x
- * 16-byte aligned), T outside 0..MOE_ROUTE_NOALLOC_MAX_TOKENS, bad top_k or
- * norm_topk; MOE_ERR_UNSUPPORTED for hidden not a multiple of 32 in
- * [32, 16384], n_experts outside 1..MOE_ROUTE_NOALLOC_MAX_EXPERTS, or
- * n_group != 1; MOE_ERR_CUDA if a CUDA call fails.  T == 0 does nothing.
- * This call does not set moe_last_error's message.
+ * 16-byte aligned), T outside 0..MOE_ROUTE_NOALLOC_MAX_TOKENS, and selection
+ * fields that moe_init would also reject: top_k outside 1..min(n_experts, 32),
+ * score_func not MOE_SCORE_SIGMOID or MOE_SCORE_SOFTMAX, n_group outside 1..32
+ * or not dividing n_experts, n_group > 1 with the softmax score, topk_group
+ * outside 1..n_group or top_k above topk_group * n_experts / n_group (when
+ * n_group > 1), norm_topk not 0 or 1.  MOE_ERR_UNSUPPORTED for hidden not a
+ * multiple of 32 in [32, 16384] or n_experts outside
+ * 1..MOE_ROUTE_NOALLOC_MAX_EXPERTS.  MOE_ERR_CUDA if a CUDA call fails.
+ * T == 0 does nothing.  This call does not set moe_last_error's message.
  */
 #define MOE_ROUTE_NOALLOC_MAX_TOKENS 8
 #define MOE_ROUTE_NOALLOC_MAX_EXPERTS 1024

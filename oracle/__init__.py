@@ -161,6 +161,19 @@ def route(cfg: Cfg, router_w: np.ndarray, router_b: np.ndarray, x: np.ndarray):
     return idx, w, float(m[0]), sc.reshape(3, cfg.E)
 
 
+def weights_for(cfg: Cfg, router_w: np.ndarray, x: np.ndarray, idx) -> np.ndarray:
+    """Routing weights the oracle gives a given selection idx[K] of token x (its
+    router input, already pre-normed where the layer asks for it)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    rw = np.ascontiguousarray(router_w, dtype=np.float32)
+    ii = np.ascontiguousarray(idx, dtype=np.int32)
+    w = np.zeros(cfg.K, dtype=np.float64)
+    rc = lib().oracle_weights_for(C.byref(cfg), _p(rw), _p(x), _p(ii), _p(w))
+    if rc != 0:
+        raise ValueError("oracle_weights_for: invalid config or selection")
+    return w
+
+
 class LayerRef:
     """Keeps the numpy arrays alive behind an oracle_layer struct."""
 

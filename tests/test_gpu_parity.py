@@ -69,11 +69,18 @@ def test_decode_small_configs(moe, name, streams):
 
 
 def test_decode_glm(moe):
+    """64 GLM-5.2 decode tokens, one call each (routing, slot tables and the
+    order in which blocks finish change with every token)."""
     wl, li, layer = layer_for(moe, "glm_decode", 1)
+    ref = oracle_layer(wl, li)
     worst = 0.0
-    for s in range(4):
-        err, _ = run_and_check(moe, wl, li, layer, synth.tokens(wl, T=1, stream=s), f"glm s={s}")
+    for s in range(64):
+        x = synth.tokens(wl, T=1, stream=s)
+        y, idx, w = layer.forward_debug(torch.from_numpy(x).cuda())
+        y, idx, w = y.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+        err, _ = check_token(wl, ref, x[0], y[0], idx[0], w[0], where=f"glm decode s={s}")
         worst = max(worst, err)
+    assert moe.moe_device_error(layer.handle) == 0
     print(f"glm decode worst rel err {worst:.3e}")
 
 
@@ -173,8 +180,8 @@ def test_tensor_core_path_selection(moe):
 
 
 @pytest.mark.parametrize("T", [64, 512])
-def test_batched_glm_512_sampled(moe, T):
-    """Full-size batched layer: all T routing decisions, outputs on a sample (T=64: the
+def test_batched_glm_full(moe, T):
+    """Full-size batched layer: every token's routing decision and output (T=64: the
     router's reduction split into 32 k-ranges, 16-token mma.sync items; T=512: 14 k-ranges,
     tcgen05 experts)."""
     wl, li, layer = layer_for(moe, "glm_batched", 512)
@@ -199,13 +206,11 @@ def test_batched_glm_512_sampled(moe, T):
             assert np.all(scores[2][idx[t]] >= scores[2][ridx[-1]] - MARGIN), t
     # load is uneven, as the workload asks (bias ~ N(0, 0.5))
     assert cnt.max() >= 2 * cnt[cnt > 0].mean()
-    rng = np.random.default_rng(0)
-    sample = sorted(set([0, 1, T // 2, T - 1] + rng.choice(T, 20, replace=False).tolist()))
     worst = 0.0
-    for t in sample:
+    for t in range(T):
         err, _ = check_token(wl, ref, x[t], y[t], idx[t], w[t], where=f"glm T={T} t={t}")
         worst = max(worst, err)
-    print(f"glm batched T={T}: worst sampled rel err {worst:.3e}, near ties {n_tie}")
+    print(f"glm batched T={T}: worst rel err {worst:.3e}, near ties {n_tie}")
 
 
 def test_batched_is_deterministic_and_token_independent(moe):
@@ -310,12 +315,17 @@ def test_int8_edge_configs(moe, kw):
 # --- 40-layer stack (x <- x + moe(rmsnorm(x))) -------------------------------------
 
 def test_stack_35b_40_layers(moe):
+    """The 40-layer stack: every layer teacher-forced (the oracle gets that layer's GPU
+    input), and the free-running oracle chain against the GPU chain at the end.  Where
+    the oracle's own chain meets a near-tie (margin <= 1e-5), it continues with the
+    GPU's selection at that layer, so the chained check always runs."""
+    import oracle
     wl = synth.WORKLOADS["stack35b"]
     x0 = synth.tokens(wl, T=1, stream=0)
     x_gpu = torch.from_numpy(x0).cuda()
     x_ref = x0[0].astype(np.float64)
-    chain_ok = True
     worst_tf = 0.0
+    n_forced = 0
     for l in range(wl.n_layers):
         li = synth.layer_inputs(wl, layer=l)
         layer = upload(moe, wl, li, 1)
@@ -324,22 +334,25 @@ def test_stack_35b_40_layers(moe):
         assert moe.moe_device_error(layer.handle) == 0
         assert moe.moe_uses_streaming_decode(layer.handle)
         ref = oracle_layer(wl, li)
+        idx_np = idx.cpu().numpy()[0]
         # teacher-forced: the oracle gets this layer's GPU input
-        err, tie = check_token(wl, ref, x_in[0], y.cpu().numpy()[0], idx.cpu().numpy()[0],
+        err, tie = check_token(wl, ref, x_in[0], y.cpu().numpy()[0], idx_np,
                                w.cpu().numpy()[0], where=f"stack layer {l}")
         worst_tf = max(worst_tf, err)
-        # free-running oracle chain
-        y_ref, _, _, margin = ref.token(x_ref)
-        chain_ok &= margin > MARGIN
-        x_ref = y_ref
+        # free-running oracle chain; a near-tie on its own input takes the GPU's selection
+        _, _, margin, _ = oracle.route(ref.cfg, ref.router_w, ref.router_b,
+                                       oracle.rmsnorm(x_ref, wl.rms_eps))
+        forced = idx_np.astype(np.int32) if margin <= MARGIN else None
+        n_forced += forced is not None
+        x_ref, _, _, _ = ref.token(x_ref, forced_idx=forced)
         x_gpu = y
         layer.close()
         del li
     final = x_gpu.cpu().numpy()[0].astype(np.float64)
     chain_err = rel_err(final, x_ref)
-    print(f"stack: worst teacher-forced layer err {worst_tf:.3e}, chained err {chain_err:.3e}")
-    if chain_ok:
-        assert chain_err <= REL_TOL
+    print(f"stack: worst teacher-forced layer err {worst_tf:.3e}, chained err {chain_err:.3e}, "
+          f"near-tie layers taken with the GPU's selection {n_forced}")
+    assert chain_err <= REL_TOL
 
 
 # --- edge cases -------------------------------------------------------------------

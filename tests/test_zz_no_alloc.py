@@ -5,14 +5,18 @@ memory belongs to another allocator, or their serving loop must never call
 cudaMalloc/cudaFree), so it cannot use a moe_handle.  Here it is called
 through the C ABI and its top-k indices and weights are compared with those
 moe_forward_debug returns for the same tokens, on two calls in a row (the
-static scratch keeps the previous call's contents).  This file sorts last so
-that a run stopping at the first failure has run every other test first.
+static scratch keeps the previous call's contents), and with the oracle's
+routing under the selection-margin rule, for the plain sigmoid router and
+the group-limited and softmax variants it also accepts.  This file sorts
+last so that a run stopping at the first failure has run every other test
+first.
 """
 import numpy as np
 import pytest
 
+import oracle
 import synth
-from parity_util import W_RTOL, upload
+from parity_util import W_RTOL, check_route, oracle_layer, upload
 
 torch = pytest.importorskip("torch")
 
@@ -36,6 +40,9 @@ CASES = [
                    routed_scale=2.5, seed=21),
     synth.Workload("prenorm", T=1, H=64, E=8, K=2, I=32, n_shared=1, I_shared=32,
                    routed_scale=1.0, seed=22, n_layers=2),
+    synth.WORKLOADS["group8"],
+    synth.WORKLOADS["softmax_renorm"],
+    synth.WORKLOADS["olmoe_softmax"],
 ]
 
 
@@ -52,6 +59,14 @@ def test_route_noalloc_matches_forward_debug(moe, wl):
         torch.cuda.synchronize()
         assert torch.equal(idx, idx_ref), (wl.name, call)
         np.testing.assert_allclose(w.cpu().numpy(), w_ref.cpu().numpy(), rtol=W_RTOL, atol=0)
+        # and against the oracle's routing of the same tokens
+        ref = oracle_layer(wl, li, experts=[])
+        xh, ih, wh = x.cpu().numpy(), idx.cpu().numpy(), w.cpu().numpy()
+        for t in range(T):
+            x64 = xh[t].astype(np.float64)
+            xin = oracle.rmsnorm(x64, wl.rms_eps) if wl.prenorm_residual else x64
+            check_route(wl, ref.cfg, ref.router_w, ref.router_b, xin, ih[t], wh[t],
+                        where=f"noalloc {wl.name} call {call} t={t}")
     layer.close()
 
 
