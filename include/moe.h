@@ -185,10 +185,21 @@ moe_status moe_profile_read(moe_handle *h, int32_t *n_calls, float *stage_ms);
 /* Waits for the device, then reads and clears the handle's device error
  * word.  Kernels never wait without bound: a wait that runs out (a pipeline
  * stage, or a grid-wide barrier of the T == 1 kernel) sets a flag bit and the
- * kernel returns early; that call's output is then invalid.  *flags = the bits
- * seen (0: none); returns MOE_ERR_CUDA when any was set, after resetting the
- * handle's barrier state so that later calls are valid again. */
+ * kernel returns early.  That call's output is invalid, and so is the output of
+ * every later call on the handle until this function has reset the handle's
+ * barrier and call counters.  *flags = the bits seen (0: none); returns
+ * MOE_ERR_CUDA when any was set, after that reset, so that later calls are
+ * valid again. */
 moe_status moe_device_error(moe_handle *h, uint32_t *flags);
+
+/* Diagnosis and testing of the bounded waits (not a step of the method).
+ * Moves the handle's device call counter ahead of its grid-barrier counters,
+ * so that the next T == 1 call on the single-kernel decode path finds its first
+ * grid barrier unreachable: that call's waits run out (after about 0.5 s), it
+ * sets the device error word and returns without writing y.  moe_device_error
+ * then reports the flag and resets the counters.  Waits for the device first.
+ * MOE_ERR_UNSUPPORTED if T == 1 calls on the handle do not use that kernel. */
+moe_status moe_debug_stall_next_call(moe_handle *h);
 
 /* 1 if T == 1 calls on this handle run the single persistent decode kernel
  * (a cooperative launch; weights streamed from HBM into registers;

@@ -18,6 +18,7 @@ __all__ = [
     "lib", "library_path", "moe_init", "moe_forward", "moe_forward_debug", "moe_forward_host",
     "moe_destroy", "moe_last_error", "moe_workspace_bytes", "moe_abi_version",
     "moe_profile_start", "moe_profile_read", "moe_route_noalloc", "moe_device_error",
+    "moe_debug_stall_next_call",
     "moe_uses_streaming_decode", "moe_uses_tensor_cores",
 ]
 
@@ -89,6 +90,8 @@ def lib():
         L.moe_profile_read.restype = C.c_int
         L.moe_device_error.argtypes = [vp, C.POINTER(C.c_uint32)]
         L.moe_device_error.restype = C.c_int
+        L.moe_debug_stall_next_call.argtypes = [vp]
+        L.moe_debug_stall_next_call.restype = C.c_int
         L.moe_uses_streaming_decode.argtypes = [vp]
         L.moe_uses_streaming_decode.restype = i32
         L.moe_uses_tensor_cores.argtypes = [vp]
@@ -188,11 +191,19 @@ def moe_route_noalloc(cfg: MoeConfig, router_w, router_bias, x, T: int, topk_idx
         raise MoeError(status, "moe_route_noalloc", "rejected (see moe.h for the limits)")
 
 
-def moe_device_error(handle: int) -> int:
-    """Device error flags since the last check (0 = none); raises if any."""
+def moe_device_error(handle: int, check: bool = True) -> int:
+    """Device error flags since the last check (0 = none); raises if any, unless
+    check is False (the flags are then returned; the handle is reset either way)."""
     f = C.c_uint32()
-    _check(lib().moe_device_error(handle, C.byref(f)), "moe_device_error")
+    st = lib().moe_device_error(handle, C.byref(f))
+    if check or st != MOE_ERR_CUDA or f.value == 0:
+        _check(st, "moe_device_error")
     return f.value
+
+
+def moe_debug_stall_next_call(handle: int) -> None:
+    """Make the next T == 1 call on the decode kernel time out (tests of the bounded waits)."""
+    _check(lib().moe_debug_stall_next_call(handle), "moe_debug_stall_next_call")
 
 
 def moe_uses_streaming_decode(handle: int) -> bool:

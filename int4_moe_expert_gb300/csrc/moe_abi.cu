@@ -269,7 +269,7 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, int32_t max_tok
     p.sh_scale = d.n_shared ? w->shared_scale : nullptr;
     moe::carve_workspace(d, h->ws_base, &p.ws);
     e = cudaMemset(h->ws_base, 0, h->ws_bytes);
-    if (e == cudaSuccess) e = moe::prepare_kernels(d);
+    if (e == cudaSuccess) e = moe::prepare_kernels(p.d);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) { free_handle(h); return cuda_fail(e, "workspace init"); }
     *out = h;
@@ -349,16 +349,31 @@ moe_status moe_device_error(moe_handle *h, uint32_t *flags) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = cudaMemcpy(&v, h->p.ws.err, sizeof(v), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess && v) {
-        // a kernel gave up part-way: start the barrier and work counters
-        // afresh so the next call is consistent again
-        e = cudaMemset(h->p.ws.err, 0, sizeof(unsigned));
-        if (e == cudaSuccess) e = cudaMemset(h->p.ws.counters, 0, 16 * sizeof(unsigned));
-        if (e == cudaSuccess) e = cudaMemset(h->p.ws.claims, 0, moe::kClaimWords * sizeof(unsigned));
+        // a kernel gave up part-way: start the barrier counters and the call
+        // counter afresh so that the next call is consistent again (until this
+        // reset, every call on the handle is invalid)
+        e = cudaMemset(h->p.ws.counters, 0, 16 * sizeof(unsigned));
+        if (e == cudaSuccess) e = cudaMemset(h->p.ws.err, 0, sizeof(unsigned));
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
     }
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
     *flags = v;
     if (v) return fail(MOE_ERR_CUDA, "a kernel gave up waiting (flags 0x%x)", v);
+    return MOE_OK;
+}
+
+moe_status moe_debug_stall_next_call(moe_handle *h) {
+    if (!h) return fail(MOE_ERR_INVALID, "handle is NULL");
+    if (!h->p.d.fast_decode) return fail(MOE_ERR_UNSUPPORTED, "T == 1 calls on this handle do not use the decode kernel");
+    // counters[7] is the number of the handle's last call; every barrier target of the next
+    // call is that number + 1 times the grid, which the barrier counters (at most the calls
+    // so far times the grid) then cannot reach
+    unsigned calls = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&calls, h->p.ws.counters + 7, sizeof(calls), cudaMemcpyDeviceToHost);
+    calls += 1000u;
+    if (e == cudaSuccess) e = cudaMemcpy(h->p.ws.counters + 7, &calls, sizeof(calls), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "moving the call counter");
     return MOE_OK;
 }
 
@@ -370,7 +385,7 @@ moe_status moe_trace_read(moe_handle *h, uint64_t *out, int32_t capacity_blocks,
     if (!h || !out || !n_blocks || capacity_blocks < 0) return fail(MOE_ERR_INVALID, "NULL argument or negative capacity");
     if (!h->p.d.trace || !h->p.d.fast_decode)
         return fail(MOE_ERR_UNSUPPORTED, "the handle records no trace (MOE_FLAG_TRACE and the decode kernel needed)");
-    const int g = moe::decode_grid_blocks();
+    const int g = moe::decode_grid_blocks(h->p.d);
     const int n = g < capacity_blocks ? g : capacity_blocks;
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess && n > 0)

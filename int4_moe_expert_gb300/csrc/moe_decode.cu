@@ -816,9 +816,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     mark(6);
 }
 
-int g_sms = 0;
-int g_blocks = 0;   // co-resident blocks the cooperative launch uses
-
 constexpr int kMaxCplH = 8;   // H up to 8192
 constexpr int kMaxCplI = 2;   // I up to 2048 (digits of more chunks do not fit in registers)
 
@@ -860,7 +857,7 @@ cudaError_t attr_t() {
 
 }  // namespace
 
-int decode_grid_blocks() { return g_blocks; }
+int decode_grid_blocks(const Dims &d) { return d.dec_grid; }
 
 bool decode_fast_supported(const Dims &d) {
     if (d.n_group != 1 || d.score_func != MOE_SCORE_SIGMOID) return false;   // routing variants: generic path
@@ -872,28 +869,33 @@ bool decode_fast_supported(const Dims &d) {
     return fused_shape(d).smem <= (size_t)kSmemBudget;
 }
 
-cudaError_t prepare_decode_fast(const Dims &d) {
-    if (!decode_fast_supported(d)) return cudaSuccess;
-    int dev = 0, coop = 0;
+// Kernel attributes and this GPU's grid (one block per SM) for a handle; a GPU
+// without cooperative launch, or with too few SMs for the slots, runs the
+// generic kernels instead (d.fast_decode cleared).
+cudaError_t prepare_decode_fast(Dims &d) {
+    d.dec_grid = 0;
+    if (!d.fast_decode) return cudaSuccess;
+    int dev = 0, coop = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-    if (e == cudaSuccess && !coop) e = cudaErrorNotSupported;
+    if (e != cudaSuccess) return e;
+    // every slot needs at least one half-block in the down phase
+    if (!coop || 2 * sms < d.K + d.n_shared) {
+        d.fast_decode = 0;
+        return cudaSuccess;
+    }
     // every instantiation gets the same (largest) shared-memory limit, so
     // handles of different shapes coexist
     const int b = (d.I / 32 + 31) / 32;
-    if (e == cudaSuccess) {
-        switch (cpl_h(d) * 16 + b) {
+    switch (cpl_h(d) * 16 + b) {
 #define MOE_ATTR(A, B) case A * 16 + B: e = attr_t<A, B>(); break;
-            MOE_ATTR(1, 1) MOE_ATTR(2, 1) MOE_ATTR(3, 1) MOE_ATTR(4, 1) MOE_ATTR(6, 1) MOE_ATTR(8, 1)
-            MOE_ATTR(1, 2) MOE_ATTR(2, 2) MOE_ATTR(3, 2) MOE_ATTR(4, 2) MOE_ATTR(6, 2) MOE_ATTR(8, 2)
+        MOE_ATTR(1, 1) MOE_ATTR(2, 1) MOE_ATTR(3, 1) MOE_ATTR(4, 1) MOE_ATTR(6, 1) MOE_ATTR(8, 1)
+        MOE_ATTR(1, 2) MOE_ATTR(2, 2) MOE_ATTR(3, 2) MOE_ATTR(4, 2) MOE_ATTR(6, 2) MOE_ATTR(8, 2)
 #undef MOE_ATTR
-            default: e = cudaErrorInvalidValue;
-        }
+        default: e = cudaErrorInvalidValue;
     }
-    // every slot needs at least one half-block in the down phase
-    if (e == cudaSuccess && 2 * g_sms < d.K + d.n_shared) e = cudaErrorNotSupported;
-    g_blocks = g_sms;
+    if (e == cudaSuccess) d.dec_grid = sms;
     return e;
 }
 
@@ -906,7 +908,8 @@ cudaError_t launch_decode_fast(const Params &p, const float *x, float *y, cudaSt
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(g_blocks > 0 ? g_blocks : 148);
+    if (p.d.dec_grid < 1) return cudaErrorInvalidConfiguration;
+    cfg.gridDim = dim3(p.d.dec_grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = s.smem;
     cfg.stream = st;

@@ -26,6 +26,7 @@ struct Dims {
     int fast_decode;    // T == 1 runs the streaming kernels (moe_decode.cu)
     int mma;            // T > 1 runs the tensor-core expert kernels (H, I, I_sh multiples of 128)
     int trace;          // MOE_FLAG_TRACE: the decode kernel records its timeline
+    int dec_grid;       // blocks of the decode launch (the GPU's SM count; 0 before prepare)
 };
 
 // Device workspace owned by a handle.  Vectors marked "perm" are stored in
@@ -52,9 +53,7 @@ struct Workspace {
     int *n_items;        // [1]
     float *lpart;        // [S, T, E] tiled router: logits of each of a call's S k-ranges
     float *sspart;       // [S, T] tiled router: sums of squares of each k-range
-    // decode (T == 1) streaming path
-    unsigned *claims;    // [kClaimWords] work counters: [0] gate/up units, [1 + j] down rows of
-                         // slot j; each call's last barrier is followed by their reset to 0
+    // decode (T == 1) single-kernel path (moe_decode.cu)
     unsigned *err;       // [4] device error word: bounded waits that ran out
     float *dpart;        // [kMaxSlots, H] down outputs per slot (times the routing weight)
     float *dscore;       // [2, E] decode router: sigmoid | selection score (sigmoid + bias)
@@ -71,7 +70,6 @@ inline int max_items(int T, int K, int E, int n_shared, int item = kItemTokens) 
 }
 bool mma_supported(const Dims &d);
 bool tc_supported(const Dims &d);   // int4 experts on the tensor-core path: tcgen05 for large T
-constexpr int kClaimWords = 64;  // >= 1 + kMaxSlots
 constexpr int kTraceBlocks = 1024;   // decode blocks the trace buffer holds
 
 // Everything a kernel needs, passed by value.
@@ -91,7 +89,7 @@ size_t workspace_bytes(const Dims &d);
 void carve_workspace(const Dims &d, void *base, Workspace *ws);
 
 // Per-config kernel attributes (dynamic shared memory limits); once per handle.
-cudaError_t prepare_kernels(const Dims &d);
+cudaError_t prepare_kernels(Dims &d);
 
 constexpr int kStages = 4;   // router, gate/up, down, combine
 
@@ -100,8 +98,8 @@ constexpr int kStages = 4;   // router, gate/up, down, combine
 // call; ws.counters[7] counts the calls (read and advanced on the device, so
 // the launch has no per-call host state and can be captured in a graph).
 bool decode_fast_supported(const Dims &d);
-cudaError_t prepare_decode_fast(const Dims &d);
-int decode_grid_blocks();   // blocks of the decode launch (0 before prepare)
+cudaError_t prepare_decode_fast(Dims &d);   // sets d.dec_grid, or clears d.fast_decode for this GPU
+int decode_grid_blocks(const Dims &d);      // blocks of the decode launch (0 before prepare)
 cudaError_t launch_decode_fast(const Params &p, const float *x, float *y, cudaStream_t st, cudaEvent_t *ev,
                                bool want_counts);
 

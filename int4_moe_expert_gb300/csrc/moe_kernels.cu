@@ -1431,6 +1431,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
     __shared__ __align__(8) unsigned long long s_bar[kTcS];
     __shared__ uint32_t s_taddr;
     __shared__ int s_fail;
+    __shared__ int s_last_commit;    // the last stage whose MMAs were committed (-1: none)
     const int item = blockIdx.x;
     if (item >= *p.ws.n_items) return;
     const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
@@ -1450,6 +1451,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
     }
     if (tid == 0) {
         s_fail = 0;
+        s_last_commit = -1;
         for (int i = 0; i < kTcS; i++)
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar[i])) : "memory");
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1558,6 +1560,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
                     tc_mma(taddr + kTcTok * t, tc_desc(st + t * kTcATile + 256 * ks), bd, acc);
             }
             tc_commit(smem_u32(&s_bar[kb % kTcS]));
+            s_last_commit = kb;
         }
         return fail;
     };
@@ -1572,6 +1575,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
     // the last commit covers every MMA this block issued
     const int last = nkb - 1;
     if (!failed && !mbar_wait(smem_u32(&s_bar[last % kTcS]), (uint32_t)(last / kTcS) & 1u)) s_fail = 1;
+    __syncthreads();
+    // after a wait that ran out, MMAs already committed may still be writing the accumulators:
+    // wait (bounded) for the last commit, which covers all of them, before the columns are freed
+    if (s_fail && tid == 0 && s_last_commit >= 0)
+        mbar_wait(smem_u32(&s_bar[s_last_commit % kTcS]), (uint32_t)(s_last_commit / kTcS) & 1u);
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (s_fail) {
@@ -1735,7 +1743,6 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
     ws->inv = reinterpret_cast<int *>(take(P * sizeof(int)));
     ws->slot_expert = reinterpret_cast<int *>(take(d.E * sizeof(int)));
     ws->n_slots = reinterpret_cast<int *>(take(sizeof(int)));
-    ws->claims = reinterpret_cast<unsigned *>(take(kClaimWords * sizeof(unsigned)));
     ws->err = reinterpret_cast<unsigned *>(take(4 * sizeof(unsigned)));
     ws->dpart = reinterpret_cast<float *>(take((size_t)kMaxSlots * d.H * sizeof(float)));
     ws->dscore = reinterpret_cast<float *>(take(2 * (size_t)d.E * sizeof(float)));
@@ -1769,7 +1776,7 @@ bool mma_supported(const Dims &d) {
            (!d.n_shared || d.I_sh % 128 == 0);
 }
 
-cudaError_t prepare_kernels(const Dims &d) {
+cudaError_t prepare_kernels(Dims &d) {
     const int smem = (int)router_smem_bytes(d);
     cudaError_t e = cudaFuncSetAttribute(router_gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)

@@ -8,6 +8,7 @@ set); per token max|y - y_ref| / max|y_ref| <= 2e-3; routing weights within
 1e-4 relative per expert id.
 """
 import dataclasses
+import time
 
 import numpy as np
 import pytest
@@ -508,6 +509,39 @@ def test_nan_input_decode_path(moe):
     y, idx, w = layer.forward_debug(x)
     torch.cuda.synchronize()
     assert torch.isfinite(y).all()
+    assert moe.moe_device_error(layer.handle) == 0
+    layer.close()
+
+
+def test_decode_wait_runs_out_and_recovers(moe):
+    """A grid barrier of the decode kernel that cannot complete: every wait gives up after its
+    bound (no fault, no hang), the call returns, moe_device_error reports the grid flag and
+    resets the handle, and the next call matches the oracle again."""
+    wl = synth.WORKLOADS["tiny"]
+    li = synth.layer_inputs(wl)
+    layer = upload(moe, wl, li, 1)
+    assert moe.moe_uses_streaming_decode(layer.handle)
+    ref = oracle_layer(wl, li)
+    x = synth.tokens(wl, T=1, stream=61)
+    y, idx, w = layer.forward_debug(torch.from_numpy(x).cuda())
+    check_token(wl, ref, x[0], y.cpu().numpy()[0], idx.cpu().numpy()[0], w.cpu().numpy()[0],
+                where="before the stall")
+    assert moe.moe_device_error(layer.handle) == 0
+    moe.moe_debug_stall_next_call(layer.handle)
+    y_stale = torch.full((1, wl.H), 123.0, device="cuda")
+    t0 = time.perf_counter()
+    moe.moe_forward(layer.handle, torch.from_numpy(x).cuda(), 1, y_stale)
+    torch.cuda.synchronize()
+    waited = time.perf_counter() - t0
+    flags = moe.moe_device_error(layer.handle, check=False)
+    assert flags & 8, flags                                  # the grid-barrier flag
+    assert waited < 10.0, waited                             # bounded: gave up, did not hang
+    assert moe.moe_device_error(layer.handle) == 0           # reset by the previous read
+    for s in range(3):
+        x = synth.tokens(wl, T=1, stream=62 + s)
+        y, idx, w = layer.forward_debug(torch.from_numpy(x).cuda())
+        check_token(wl, ref, x[0], y.cpu().numpy()[0], idx.cpu().numpy()[0], w.cpu().numpy()[0],
+                    where=f"after the reset, call {s}")
     assert moe.moe_device_error(layer.handle) == 0
     layer.close()
 
