@@ -202,11 +202,16 @@ moe_status moe_device_error(moe_handle *h, uint32_t *flags);
 moe_status moe_debug_stall_next_call(moe_handle *h);
 
 /* 1 if T == 1 calls on this handle run the single persistent decode kernel
- * (a cooperative launch; weights streamed from HBM into registers;
- * fixed-point activations and dp4a), 0 if they use the generic kernels
- * (shapes outside its limits: H, I multiples of 32, I == I_shared,
- * I <= 2048, H <= 8192, E <= 1024, K + n_shared <= 32; and the routing
- * variants: n_group > 1 or the softmax score). */
+ * (one block per SM, all of them resident together, meeting at grid-wide
+ * barriers; weights streamed from HBM into registers; fixed-point activations
+ * and dp4a), 0 if they use the generic kernels (shapes outside its limits: H,
+ * I multiples of 32, I == I_shared, I <= 2048, H <= 8192, E <= 1024,
+ * K + n_shared <= 32; the routing variants: n_group > 1 or the softmax score;
+ * int8 or group-64 weights).  The kernel is launched so that it may start
+ * while the previous kernel on the stream ends (programmatic dependent launch:
+ * it reads only weights and pointer tables before that kernel is complete).
+ * It needs every SM: while other work holds SMs, its barrier waits can run
+ * out, which moe_device_error then reports. */
 int32_t moe_uses_streaming_decode(const moe_handle *h);
 
 /* 1 if T > 1 calls on this handle run the experts on the tensor cores

@@ -1,6 +1,6 @@
 // Decode (T == 1): the whole MoE step as one persistent kernel.
 //
-// One block per SM (a cooperative launch, so every block is resident), eight
+// One block per SM (all resident together: one block fills an SM), eight
 // warps.  The step's four parts run as phases separated by grid-wide
 // barriers:
 //   phase 0  one batch of loads (x chunk and this block's two router rows);
@@ -301,12 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     const int G = gridDim.x, nw = G * kWarps, gw = blockIdx.x * kWarps + warp;
     const unsigned kFull = 0xffffffffu;
     unsigned *bar1 = p.ws.counters + 4, *bar2 = p.ws.counters + 5, *bar3 = p.ws.counters + 6;
-    // this call's number on the handle: the previous call's + 1, kept in device memory (so a
-    // captured graph replays correctly); block 0 advances it once every block is past
-    // barrier 2, i.e. after every block has read it.  Only thread 0 uses it.
     unsigned *epoch = p.ws.counters + 7;
-    const unsigned gen = tid == 0 ? *reinterpret_cast<volatile unsigned *>(epoch) + 1u : 0u;
-    const unsigned target = gen * (unsigned)G;
     const bool fullH = (C % 32) == 0, fullI = (Cd % 32) == 0;
     // timeline (MOE_FLAG_TRACE): block b's record of MOE_TRACE_SLOTS global-timer readings
     const bool trace = p.d.trace != 0 && blockIdx.x < kTraceBlocks;
@@ -314,9 +309,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     auto mark = [&](int slot) {
         if (trace && tid == 0) tr[slot] = now_ns();
     };
-    if (trace && tid < MOE_TRACE_SLOTS) tr[tid] = 0ull;
-    mark(0);
-    if (tid == 0) s_flags[2] = 0;     // routing not known yet (read after the first __syncthreads)
 
     // ---- gate/up units: unit u < U_sh is row u of the shared expert, unit U_sh + v is row
     // v mod I of slot v / I.  The shared expert's units go to warps 1..7 (their share
@@ -375,19 +367,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         if (has0) bias0 = __ldg(p.router_b + e0);
         if (has1) bias1 = __ldg(p.router_b + e0 + 1);
     }
+    // Before the wait for the preceding grid (programmatic dependent launch): only reads of
+    // data no call writes -- this block's chunk of its two router rows, the biases, every
+    // expert's slab and scale pointers (for the slot tables after routing; E <= 4 x kThreads)
+    // and, if it is the shared expert's, the warp's first unit.  These overlap the previous
+    // kernel's tail when calls follow one another on a stream.
     if (tid < C) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(x + (size_t)tid * 32);
         const float4 *w0 = reinterpret_cast<const float4 *>(p.router_w + (size_t)(has0 ? e0 : 0) * H + (size_t)tid * 32);
         const float4 *w1 = reinterpret_cast<const float4 *>(p.router_w + (size_t)(has1 ? e0 + 1 : 0) * H + (size_t)tid * 32);
 #pragma unroll
         for (int k = 0; k < 8; k++) {
-            const float4 f = __ldg(x4 + k);
-            xv[4 * k] = f.x; xv[4 * k + 1] = f.y; xv[4 * k + 2] = f.z; xv[4 * k + 3] = f.w;
             u0[k] = has0 ? __ldg(w0 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
             u1[k] = has1 ? __ldg(w1 + k) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    // every expert's slab and scale pointers, for the slot tables after routing (E <= 4 x kThreads)
     const uint8_t *pt_slab[kPtab];
     const float *pt_scale[kPtab];
 #pragma unroll
@@ -396,10 +389,30 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         pt_slab[i] = e < E ? p.slabs[e] : nullptr;
         pt_scale[i] = e < E ? p.scales[e] : nullptr;
     }
-    // the first unit's loads go out now if it is the shared expert's (routing not needed)
     if (u_first.pos < 0) {
         load_gu(u_first, wa, sga, sua);
         loaded = true;
+    }
+    // x (possibly the previous call's output) and the handle's workspace (the previous call on
+    // this handle uses it) only after the preceding grid has completed and its writes are
+    // visible; the next call may then be launched (its blocks start as these exit)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // this call's number on the handle: the previous call's + 1, kept in device memory (so a
+    // captured graph replays correctly); block 0 advances it once every block is past
+    // barrier 2, i.e. after every block has read it.  Only thread 0 uses it.
+    const unsigned gen = tid == 0 ? *reinterpret_cast<volatile unsigned *>(epoch) + 1u : 0u;
+    const unsigned target = gen * (unsigned)G;
+    if (trace && tid < MOE_TRACE_SLOTS) tr[tid] = 0ull;
+    mark(0);
+    if (tid == 0) s_flags[2] = 0;     // routing not known yet (read after the first __syncthreads)
+    if (tid < C) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(x + (size_t)tid * 32);
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+            const float4 f = __ldg(x4 + k);
+            xv[4 * k] = f.x; xv[4 * k + 1] = f.y; xv[4 * k + 2] = f.z; xv[4 * k + 3] = f.w;
+        }
     }
     if (tid < C) {
 #pragma unroll
@@ -870,18 +883,17 @@ bool decode_fast_supported(const Dims &d) {
 }
 
 // Kernel attributes and this GPU's grid (one block per SM) for a handle; a GPU
-// without cooperative launch, or with too few SMs for the slots, runs the
-// generic kernels instead (d.fast_decode cleared).
+// with too few SMs for the slots runs the generic kernels instead (d.fast_decode
+// cleared).
 cudaError_t prepare_decode_fast(Dims &d) {
     d.dec_grid = 0;
     if (!d.fast_decode) return cudaSuccess;
-    int dev = 0, coop = 0, sms = 0;
+    int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
     if (e != cudaSuccess) return e;
     // every slot needs at least one half-block in the down phase
-    if (!coop || 2 * sms < d.K + d.n_shared) {
+    if (2 * sms < d.K + d.n_shared) {
         d.fast_decode = 0;
         return cudaSuccess;
     }
@@ -899,14 +911,23 @@ cudaError_t prepare_decode_fast(Dims &d) {
     return e;
 }
 
-// One cooperative launch for the whole T == 1 step.  ev (optional): ev[0],
+// One launch for the whole T == 1 step.  ev (optional): ev[0],
 // ev[1] before the kernel, ev[2..4] after it (stage 1 = the fused kernel).
 cudaError_t launch_decode_fast(const Params &p, const float *x, float *y, cudaStream_t st, cudaEvent_t *ev,
                                bool want_counts) {
     const FusedShape s = fused_shape(p.d);
+    // programmatic stream serialisation: the kernel may be launched before the previous kernel
+    // on the stream ends (its blocks take each SM as the previous kernel's block there exits),
+    // and waits for that kernel (griddepcontrol.wait) before it reads x or the workspace.  The
+    // grid is one block per SM and the blocks meet at grid barriers, so all of them must be
+    // resident together: true on a GPU this call has to itself (one block fills an SM's
+    // registers); a cooperative launch would guarantee it but is never started early (measured
+    // on the GLM-5.2 layer, calls back to back: 44.0 us per call cooperative, 40.7 us with the
+    // early launch).  When other work holds SMs, a block that cannot start makes the barrier
+    // waits run out (bounded), and the call reports it through moe_device_error.
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     if (p.d.dec_grid < 1) return cudaErrorInvalidConfiguration;
     cfg.gridDim = dim3(p.d.dec_grid);
