@@ -50,7 +50,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 
 /* y = x + moe(rmsnorm(x)) instead of y = moe(x). */
 #define MOE_FLAG_PRENORM_RESIDUAL 1u
@@ -86,7 +86,23 @@ typedef struct moe_config {
     int32_t score_func;    /* MOE_SCORE_SIGMOID (0) or MOE_SCORE_SOFTMAX (1) */
     int32_t expert_format; /* routed experts: MOE_FORMAT_INT4 (0), MOE_FORMAT_INT8 (1) or MOE_FORMAT_G64 (2) */
     int32_t shared_format; /* shared expert: MOE_FORMAT_INT4 (0), MOE_FORMAT_INT8 (1) or MOE_FORMAT_G64 (2) */
+    int32_t ep_size;       /* expert parallelism: ranks sharing the layer's experts (0 or 1: none) */
+    int32_t ep_rank;       /* this handle's rank, 0..ep_size-1 (see "Expert parallelism" below) */
 } moe_config;
+
+/* Expert parallelism (the reader.mx page, section 13, "五级专家驻留": disjoint
+ * expert sets on the GPUs of one tier).  With ep_size = W > 1, rank r owns the
+ * routed experts e with r*E/W <= e < (r+1)*E/W (integer division) and needs
+ * only their slab and scale pointers (the others may be NULL); the shared
+ * expert belongs to rank 0 (other ranks may pass NULL for it).  Every rank
+ * runs the whole router (replicated router weights), so all ranks agree on the
+ * selection, and moe_forward writes the rank's partial output
+ *     y_r = sum over k with idx_k owned by r of w_k d_k
+ *           (+ d_shared, and + x under MOE_FLAG_PRENORM_RESIDUAL, on rank 0 only);
+ * the layer's y is the sum of y_r over the ranks: one all-reduce (or
+ * reduce-scatter) of y[T, H], which the caller runs (e.g. NCCL, summing in a
+ * fixed rank order).  EP handles take the generic kernels at every T (not the
+ * single-kernel decode path). */
 
 /* Weight formats of an expert slab:
  * INT4: gate [I, H/2] | up [I, H/2] | down [H, I/2] bytes, two values per byte

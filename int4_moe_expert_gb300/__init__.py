@@ -48,7 +48,8 @@ class MoeConfig(C.Structure):
                 ("moe_inter", C.c_int32), ("n_shared", C.c_int32), ("shared_inter", C.c_int32),
                 ("n_group", C.c_int32), ("norm_topk", C.c_int32), ("routed_scale", C.c_float),
                 ("rms_eps", C.c_float), ("flags", C.c_uint32), ("topk_group", C.c_int32),
-                ("score_func", C.c_int32), ("expert_format", C.c_int32), ("shared_format", C.c_int32)]
+                ("score_func", C.c_int32), ("expert_format", C.c_int32), ("shared_format", C.c_int32),
+                ("ep_size", C.c_int32), ("ep_rank", C.c_int32)]
 
 
 class MoeWeights(C.Structure):
@@ -220,12 +221,13 @@ def moe_destroy(handle: int) -> None:
 
 def make_config(H, E, K, I, n_shared=0, I_shared=0, routed_scale=1.0, norm_topk=1,
                 prenorm_residual=False, rms_eps=1e-5, n_group=1, trace=False, topk_group=1,
-                score_func=0, cuda_cores=False, expert_format=0, shared_format=0) -> MoeConfig:
+                score_func=0, cuda_cores=False, expert_format=0, shared_format=0, ep_size=1,
+                ep_rank=0) -> MoeConfig:
     flags = ((MOE_FLAG_PRENORM_RESIDUAL if prenorm_residual else 0) | (MOE_FLAG_TRACE if trace else 0) |
              (MOE_FLAG_CUDA_CORES if cuda_cores else 0))
     return MoeConfig(H, E, K, I, n_shared, I_shared if n_shared else 0, n_group, norm_topk,
                      float(routed_scale), float(rms_eps), flags, topk_group, score_func,
-                     expert_format, shared_format)
+                     expert_format, shared_format, ep_size, ep_rank)
 
 
 def moe_trace_read(handle: int, capacity_blocks: int = 1024):
@@ -244,7 +246,9 @@ class MoeLayer:
     Uploads host arrays (router [E,H] f32, bias [E] f32, slabs [E, nbytes] u8,
     scales [E, 2I+H] f32, optional shared slab/scale) into device tensors it
     owns, and holds a library handle that borrows them.  expert_rows (optional)
-    maps each expert to a row of slabs/scales, so experts may share storage.
+    maps each expert to a row of slabs/scales, so experts may share storage; a
+    None entry passes NULL for that expert (one another expert-parallel rank
+    computes).
     """
 
     def __init__(self, cfg: MoeConfig, router_w, router_b, slabs, scales, sh_slab=None,
@@ -273,8 +277,8 @@ class MoeLayer:
         sb = self.slabs.stride(0)
         cb = self.scales.stride(0) * 4
         rows = list(range(E)) if expert_rows is None else list(expert_rows)   # expert -> row
-        self._slab_ptrs = (C.c_void_p * E)(*[sp + r * sb for r in rows])
-        self._scale_ptrs = (C.c_void_p * E)(*[cp + r * cb for r in rows])
+        self._slab_ptrs = (C.c_void_p * E)(*[None if r is None else sp + r * sb for r in rows])
+        self._scale_ptrs = (C.c_void_p * E)(*[None if r is None else cp + r * cb for r in rows])
         self.weights = MoeWeights(_ptr(self.router_w), _ptr(self.router_b),
                                   C.cast(self._slab_ptrs, C.POINTER(C.c_void_p)),
                                   C.cast(self._scale_ptrs, C.POINTER(C.c_void_p)),

@@ -90,26 +90,33 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
         return fail(MOE_ERR_INVALID, "rms_eps must be finite and >= 0");
     if (max_tokens < 1 || max_tokens > kMaxTokens)
         return fail(MOE_ERR_INVALID, "max_tokens=%d: need 1..%d", max_tokens, kMaxTokens);
+    const int ep = c->ep_size == 0 ? 1 : c->ep_size;
+    if (ep < 1 || ep > c->n_experts || c->ep_rank < 0 || c->ep_rank >= ep)
+        return fail(MOE_ERR_INVALID, "ep_size=%d, ep_rank=%d: need 1 <= ep_size <= n_experts, 0 <= ep_rank < ep_size",
+                    c->ep_size, c->ep_rank);
     d->H = c->hidden;
     d->E = c->n_experts;
     d->K = c->top_k;
     d->I = c->moe_inter;
-    d->n_shared = c->n_shared;
-    d->I_sh = c->n_shared ? c->shared_inter : 0;
+    d->n_shared = (c->n_shared && c->ep_rank == 0) ? 1 : 0;   // the shared expert is rank 0's
+    d->I_sh = d->n_shared ? c->shared_inter : 0;
     d->I_max = d->I > d->I_sh ? d->I : d->I_sh;
     d->norm_topk = c->norm_topk;
     d->n_group = c->n_group;
     d->topk_group = c->n_group > 1 ? c->topk_group : 1;
     d->score_func = c->score_func;
     d->expert_fmt = c->expert_format;
-    d->shared_fmt = c->n_shared ? c->shared_format : MOE_FORMAT_INT4;
+    d->shared_fmt = d->n_shared ? c->shared_format : MOE_FORMAT_INT4;
     d->mma_fmt = (d->expert_fmt != MOE_FORMAT_INT4 || d->shared_fmt != MOE_FORMAT_INT4) ? 1 : 0;
     d->tc = moe::tc_supported(*d) ? 1 : 0;
     d->prenorm = (c->flags & MOE_FLAG_PRENORM_RESIDUAL) ? 1 : 0;
+    d->ep_lo = (int)((long long)c->ep_rank * c->n_experts / ep);
+    d->ep_hi = (int)((long long)(c->ep_rank + 1) * c->n_experts / ep);
+    d->resid = (d->prenorm && c->ep_rank == 0) ? 1 : 0;
     d->scale = c->routed_scale;
     d->eps = c->rms_eps;
     d->max_tokens = max_tokens;
-    d->fast_decode = moe::decode_fast_supported(*d) ? 1 : 0;
+    d->fast_decode = (ep == 1 && moe::decode_fast_supported(*d)) ? 1 : 0;
     d->mma = (moe::mma_supported(*d) && !(c->flags & MOE_FLAG_CUDA_CORES)) ? 1 : 0;
     d->trace = (c->flags & MOE_FLAG_TRACE) ? 1 : 0;
     return MOE_OK;
@@ -131,7 +138,7 @@ moe_status check_weights(const moe::Dims &d, const moe_weights *w) {
     if (!is_device_ptr(w->router_w) || !is_device_ptr(w->router_bias))
         return fail(MOE_ERR_INVALID, "router_w / router_bias are not device pointers");
     if (!w->expert_slab || !w->expert_scale) return fail(MOE_ERR_INVALID, "expert pointer arrays are NULL");
-    for (int e = 0; e < d.E; e++) {
+    for (int e = d.ep_lo; e < d.ep_hi; e++) {     // the experts this handle computes
         const void *s = w->expert_slab[e], *c = w->expert_scale[e];
         if (!s || !c) return fail(MOE_ERR_INVALID, "expert %d: NULL slab or scale", e);
         if (!aligned16(s) || !aligned16(c))
@@ -251,9 +258,10 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, int32_t max_tok
 
     void **host_tab = new (std::nothrow) void *[2 * (size_t)d.E];
     if (!host_tab) { free_handle(h); return fail(MOE_ERR_NOMEM, "host allocation failed"); }
-    for (int i = 0; i < d.E; i++) {
-        host_tab[i] = const_cast<uint8_t *>(w->expert_slab[i]);
-        host_tab[d.E + i] = const_cast<float *>(w->expert_scale[i]);
+    for (int i = 0; i < d.E; i++) {      // experts another rank computes: NULL (never read)
+        const bool own = i >= d.ep_lo && i < d.ep_hi;
+        host_tab[i] = own ? const_cast<uint8_t *>(w->expert_slab[i]) : nullptr;
+        host_tab[d.E + i] = own ? const_cast<float *>(w->expert_scale[i]) : nullptr;
     }
     e = cudaMemcpy(h->tables, host_tab, tbytes, cudaMemcpyHostToDevice);
     delete[] host_tab;

@@ -27,6 +27,8 @@ struct Dims {
     int mma;            // T > 1 runs the tensor-core expert kernels (H, I, I_sh multiples of 128)
     int trace;          // MOE_FLAG_TRACE: the decode kernel records its timeline
     int dec_grid;       // blocks of the decode launch (the GPU's SM count; 0 before prepare)
+    int ep_lo, ep_hi;   // routed experts this handle computes: [ep_lo, ep_hi) ([0, E) without expert parallelism)
+    int resid;          // add x to the output (pre-norm residual; rank 0 only under expert parallelism)
 };
 
 // Device workspace owned by a handle.  Vectors marked "perm" are stored in

@@ -260,7 +260,10 @@ __device__ void bucket_phase(const Params &p, int T, int *ismem) {
     const int span = (P + kWarps - 1) / kWarps, q0 = min(P, warp * span), q1 = min(P, q0 + span);
     for (int i = tid; i < kWarps * E; i += kThreads) wcnt[i] = 0;
     __syncthreads();
-    for (int q = q0 + lane; q < q1; q += 32) atomicAdd(&wcnt[warp * E + __ldcg(p.ws.topk_idx + q)], 1);
+    for (int q = q0 + lane; q < q1; q += 32) {
+        const int e = __ldcg(p.ws.topk_idx + q);
+        if (e >= p.d.ep_lo && e < p.d.ep_hi) atomicAdd(&wcnt[warp * E + e], 1);   // expert parallelism: own experts only
+    }
     __syncthreads();
     for (int e = tid; e < E; e += kThreads) {
         int s = 0;
@@ -329,7 +332,11 @@ __device__ void bucket_phase(const Params &p, int T, int *ismem) {
     const unsigned lt_mask = (1u << lane) - 1u;
     for (int base = q0; base < q1; base += 32) {
         const int q = base + lane;
-        const int e = q < q1 ? __ldcg(p.ws.topk_idx + q) : -1;
+        int e = q < q1 ? __ldcg(p.ws.topk_idx + q) : -1;
+        if (e >= 0 && (e < p.d.ep_lo || e >= p.d.ep_hi)) {   // another rank's expert: no position
+            p.ws.inv[q] = -1;
+            e = -1;
+        }
         const unsigned same = __match_any_sync(0xffffffffu, e);
         const int lrank = __popc(same & lt_mask);
         if (e >= 0) {
@@ -663,6 +670,7 @@ __global__ void __launch_bounds__(kThreads) gateup_decode_kernel(Params p) {
     int Is;
     if (slot < p.d.K) {
         const int e = p.ws.topk_idx[slot];
+        if (e < p.d.ep_lo || e >= p.d.ep_hi) return;   // another rank's expert (expert parallelism)
         slab = p.slabs[e];
         sc = p.scales[e];
         Is = p.d.I;
@@ -721,8 +729,9 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(Params p, const f
         const int j = threadIdx.x;
         if (j < K) {
             const int e = p.ws.topk_idx[j];
-            s_slab[j] = p.slabs[e];
-            s_sc[j] = p.scales[e];
+            const bool own = e >= p.d.ep_lo && e < p.d.ep_hi;   // expert parallelism: own experts only
+            s_slab[j] = own ? p.slabs[e] : nullptr;
+            s_sc[j] = own ? p.scales[e] : nullptr;
             s_w[j] = p.ws.topk_w[j];
         } else {
             s_slab[j] = p.sh_slab;
@@ -747,6 +756,7 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(Params p, const f
         int j, c, Ij;
         if (q < Qr) { j = q / C; c = q - j * C; Ij = I; }
         else { j = K; c = q - Qr; Ij = Ish; }
+        if (s_slab[j] == nullptr) continue;
         const size_t rbI = (size_t)(Ij >> 1);
         const uint8_t *d0 = s_slab[j] + 2 * (size_t)Ij * (size_t)(H >> 1) + (size_t)row0 * rbI + (size_t)c * 16;
         uint4 wv[RPW];
@@ -767,7 +777,7 @@ __global__ void __launch_bounds__(kThreads) down_decode_kernel(Params p, const f
         const float v = warp_sum(acc[r]);
         if (lane == r) {
             const int o = row0 + r;
-            y[o] = p.d.prenorm ? x[o] + v : v;
+            y[o] = p.d.resid ? x[o] + v : v;
         }
     }
 }
@@ -935,8 +945,10 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Params p, const float
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int k = 0; k < K; k++) {
         const int q = t * K + k;
+        const int pos = p.ws.inv[q];
+        if (pos < 0) continue;          // another rank's expert (expert parallelism)
         const float w = p.ws.topk_w[q];
-        const float4 d = __ldg(reinterpret_cast<const float4 *>(p.ws.dbuf + (size_t)p.ws.inv[q] * H + o));
+        const float4 d = __ldg(reinterpret_cast<const float4 *>(p.ws.dbuf + (size_t)pos * H + o));
         v.x = fmaf(w, d.x, v.x);
         v.y = fmaf(w, d.y, v.y);
         v.z = fmaf(w, d.z, v.z);
@@ -946,7 +958,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(Params p, const float
         const float4 d = __ldg(reinterpret_cast<const float4 *>(p.ws.dbuf + (size_t)(T * K + t) * H + o));
         v.x += d.x; v.y += d.y; v.z += d.z; v.w += d.w;
     }
-    if (p.d.prenorm) {
+    if (p.d.resid) {
         const float4 r = __ldg(reinterpret_cast<const float4 *>(x + (size_t)t * H + o));
         v.x += r.x; v.y += r.y; v.z += r.z; v.w += r.w;
     }
@@ -1956,6 +1968,7 @@ extern "C" moe_status moe_route_noalloc(const moe_config *cfg, const float *rout
     Dims d = {};
     d.H = cfg->hidden;
     d.E = cfg->n_experts;
+    d.ep_hi = d.E;
     d.K = cfg->top_k;
     d.norm_topk = cfg->norm_topk;
     d.n_group = cfg->n_group;

@@ -113,3 +113,29 @@ def selected_experts(wl, li, x, experts_hint=None):
         idx, _, _, _ = oracle.route(ref.cfg, ref.router_w, ref.router_b, xin)
         need.update(idx.tolist())
     return need
+
+
+def oracle_ep_partial(wl, li, x_t, lo: int, hi: int, rank0: bool, idx=None):
+    """One expert-parallel rank's partial output of token x_t, in double: the
+    selected experts with lo <= e < hi (routing weights over the whole
+    selection), plus the shared expert and the pre-norm residual on rank 0.
+    idx: a selection to use instead of the oracle's own (near-ties)."""
+    cfg = oracle.cfg_from_workload(wl)
+    x64 = np.asarray(x_t, dtype=np.float64)
+    xin = oracle.rmsnorm(x64, wl.rms_eps) if wl.prenorm_residual else x64
+    if idx is None:
+        idx, w, _, _ = oracle.route(cfg, li.router_w, li.router_b, xin)
+    else:
+        w = oracle.weights_for(cfg, li.router_w, xin, idx)
+    y = np.zeros(wl.H, dtype=np.float64)
+    for e, we in zip(np.asarray(idx).tolist(), np.asarray(w).tolist()):
+        if lo <= e < hi:
+            d, _ = oracle.expert(wl.H, wl.I, li.slabs[e], li.scales[e], xin, wl.expert_format)
+            y += we * d
+    if rank0:
+        if wl.n_shared:
+            d, _ = oracle.expert(wl.H, wl.I_shared, li.sh_slab, li.sh_scale, xin, wl.shared_format)
+            y += d
+        if wl.prenorm_residual:
+            y += x64
+    return y

@@ -1,6 +1,7 @@
 """The C-ABI library loads, exports every symbol include/moe.h declares, and
 rejects bad configurations and arguments on the host (no GPU needed)."""
 import ctypes as C
+import os
 import re
 from pathlib import Path
 
@@ -36,10 +37,31 @@ def test_library_exports_every_declared_symbol(moe):
         assert hasattr(L, name), name
 
 
-def test_config_struct_layout_matches_header(moe):
-    # fifteen 4-byte fields, no padding
-    assert C.sizeof(moe.MoeConfig) == 60
-    assert C.sizeof(moe.MoeWeights) == 6 * C.sizeof(C.c_void_p)
+def test_config_struct_layout_matches_header(moe, tmp_path):
+    """The ctypes structs have the header's size and field offsets (a C program
+    compiled against include/moe.h prints them)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    fields = {"moe_config": moe.MoeConfig, "moe_weights": moe.MoeWeights}
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "moe.h"', 'int main(void) {']
+    for cname, py in fields.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.run(["gcc", "-I", inc, str(src), "-o", str(exe)], check=True)
+    out = dict(l.rsplit(" ", 1) for l in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                          text=True).stdout.splitlines())
+    for cname, py in fields.items():
+        assert int(out[f"{cname} size"]) == C.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert int(out[f"{cname} {f}"]) == getattr(py, f).offset, (cname, f)
 
 
 def test_workspace_bytes_validates_config(moe):
@@ -121,7 +143,7 @@ def test_null_arguments_are_errors_not_crashes(moe):
 
 
 def test_abi_version(moe):
-    assert moe.moe_abi_version() == 3
+    assert moe.moe_abi_version() == 4
 
 
 def test_product_path_does_not_reference_the_oracle():
