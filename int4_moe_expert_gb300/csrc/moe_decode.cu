@@ -278,7 +278,93 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4 *p) {   // weights: read
     return v;
 }
 
-template <int CPLH, int CPLI>
+// Routing variants, warp 0 of a block (all E scores written): s_sig[e] = the expert's gate
+// value (sigmoid, or the softmax probability), s_key[e] = the order key of its selection
+// score, 0 never (a removed entry); each lane's best key among experts lane + 32 i.
+//   softmax family: g = exp(l - max l) / sum exp(l - max l), selection by g;
+//   group-limited sigmoid: a group's score is the sum of its two best (sigma + bias),
+//   the topk_group best groups are kept (a tie to the lower group) and the others'
+//   experts rank below every kept one (score -inf).
+__device__ __forceinline__ void route_variant_keys(const Params &p, int E, int lane, unsigned *s_key,
+                                                float *s_sig, unsigned &best, int &bidx) {
+    const unsigned kFull = 0xffffffffu;
+    const bool softmax = p.d.score_func == MOE_SCORE_SOFTMAX;
+    float *s_ch = reinterpret_cast<float *>(s_key);    // choices as floats until the keys replace them
+    float lmax = -INFINITY;
+    for (int e0 = lane; e0 < E; e0 += 32 * kKeyBatch) {
+        float c[kKeyBatch], sgv[kKeyBatch];
+#pragma unroll
+        for (int i = 0; i < kKeyBatch; i++) {
+            const int e = e0 + 32 * i;
+            c[i] = e < E ? __ldcg(p.ws.dscore + E + e) : 0.0f;
+            sgv[i] = (e < E && !softmax) ? __ldcg(p.ws.dscore + e) : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < kKeyBatch; i++) {
+            const int e = e0 + 32 * i;
+            if (e < E) {
+                s_ch[e] = c[i];
+                s_sig[e] = sgv[i];
+                lmax = fmaxf(lmax, c[i]);
+            }
+        }
+    }
+    if (softmax) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(kFull, lmax, o));
+        float z = 0.0f;
+        for (int e = lane; e < E; e += 32) {
+            const float v = expf(s_ch[e] - lmax);
+            s_sig[e] = v;
+            z += v;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(kFull, z, o);
+        for (int e = lane; e < E; e += 32) {
+            const float g = s_sig[e] / z;
+            s_sig[e] = g;
+            s_ch[e] = isnan(g) ? -INFINITY : g;
+        }
+    }
+    __syncwarp();
+    if (p.d.n_group > 1) {
+        const int G = p.d.n_group, m = E / G;
+        float gsc = -INFINITY;
+        if (lane < G) {
+            float b1 = -INFINITY, b2 = -INFINITY;
+            for (int i = 0; i < m; i++) {
+                const float v = s_ch[lane * m + i];
+                if (v > b1) { b2 = b1; b1 = v; }
+                else if (v > b2) b2 = v;
+            }
+            gsc = m > 1 ? b1 + b2 : b1;
+        }
+        unsigned keep = 0u;
+        bool taken = false;
+        for (int r = 0; r < p.d.topk_group; r++) {
+            const unsigned k = (lane < G && !taken) ? order_key(gsc) : 0u;
+            const unsigned mx = __reduce_max_sync(kFull, k);
+            const unsigned g = __reduce_min_sync(kFull, (k == mx && lane < G && !taken) ? (unsigned)lane : 0xffffffffu);
+            keep |= 1u << g;
+            if (lane == (int)g) taken = true;
+        }
+        __syncwarp();
+        for (int e = lane; e < E; e += 32)
+            if (!((keep >> (e / m)) & 1u)) s_ch[e] = -INFINITY;
+        __syncwarp();
+    }
+    for (int e = lane; e < E; e += 32) {
+        const unsigned k = order_key(s_ch[e]);
+        s_key[e] = k;
+        if (k > best) { best = k; bidx = e; }
+    }
+    __syncwarp();
+}
+
+// RV = 0: the sigmoid + bias router with plain top-K (GLM-5.2, n_group == 1).  RV = 1: the
+// routing variants (Edge0 article section 七; reader.mx section 03): group-limited selection
+// (n_group > 1, sigmoid family) and the softmax family; only warp 0's selection differs.
+template <int CPLH, int CPLI, int RV>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, const float *__restrict__ x,
                                                                    float *__restrict__ y, FusedShape sh,
                                                                    int want_counts) {
@@ -461,6 +547,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     const float r = d.prenorm ? 1.0f / sqrtf(ss / (float)H + d.eps) : 1.0f;
     auto put_score = [&](int e, float raw, float bias) {
         const float l = raw * r;
+        if constexpr (RV != 0) {
+            if (d.score_func == MOE_SCORE_SOFTMAX) {   // the routing warps take the softmax
+                p.ws.logits[e] = l;
+                p.ws.dscore[E + e] = l;
+                return;
+            }
+        }
         const float sg = 1.0f / (1.0f + expf(-l));
         float c = sg + bias + 0.0f;   // + 0: no negative zero
         if (isnan(c)) c = -INFINITY;
@@ -553,6 +646,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         // (the scores of up to kKeyBatch x 32 experts are requested together: one round trip)
         unsigned best = 0u;
         int bidx = 0x7fffffff;
+        if constexpr (RV != 0) {
+            route_variant_keys(p, E, lane, s_key, s_sig, best, bidx);
+        } else
         for (int e0 = lane; e0 < E; e0 += 32 * kKeyBatch) {
             float c[kKeyBatch], sgv[kKeyBatch];
 #pragma unroll
@@ -592,7 +688,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         float sum = sg;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-        const float mw = d.norm_topk ? d.scale * sg / (sum + 1e-20f) : d.scale * sg;
+        float den = sum + 1e-20f;
+        if constexpr (RV != 0) {
+            if (d.score_func == MOE_SCORE_SOFTMAX) den = sum;   // the softmax family: no epsilon
+        }
+        const float mw = d.norm_topk ? d.scale * sg / den : d.scale * sg;
         if (lane < K) {
             s_slab[lane] = s_pslab[me];
             s_scale[lane] = s_pscale[me];
@@ -840,38 +940,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
 constexpr int kMaxCplH = 8;   // H up to 8192
 constexpr int kMaxCplI = 2;   // I up to 2048 (digits of more chunks do not fit in registers)
 
-template <int A, int B>
+template <int A, int B, int RV>
 cudaError_t launch_t(cudaLaunchConfig_t &cfg, const Params &p, const float *x, float *y, const FusedShape &s,
                      int counts) {
-    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<A, B>, p, x, y, s, counts);
+    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<A, B, RV>, p, x, y, s, counts);
 }
 
-template <int B>
+template <int B, int RV>
 cudaError_t launch_h(int a, cudaLaunchConfig_t &cfg, const Params &p, const float *x, float *y,
                      const FusedShape &s, int counts) {
     switch (a) {
-        case 1: return launch_t<1, B>(cfg, p, x, y, s, counts);
-        case 2: return launch_t<2, B>(cfg, p, x, y, s, counts);
-        case 3: return launch_t<3, B>(cfg, p, x, y, s, counts);
-        case 4: return launch_t<4, B>(cfg, p, x, y, s, counts);
-        case 6: return launch_t<6, B>(cfg, p, x, y, s, counts);
-        case 8: return launch_t<8, B>(cfg, p, x, y, s, counts);
+        case 1: return launch_t<1, B, RV>(cfg, p, x, y, s, counts);
+        case 2: return launch_t<2, B, RV>(cfg, p, x, y, s, counts);
+        case 3: return launch_t<3, B, RV>(cfg, p, x, y, s, counts);
+        case 4: return launch_t<4, B, RV>(cfg, p, x, y, s, counts);
+        case 6: return launch_t<6, B, RV>(cfg, p, x, y, s, counts);
+        case 8: return launch_t<8, B, RV>(cfg, p, x, y, s, counts);
     }
     return cudaErrorInvalidValue;
 }
+
+// the routing-variant instantiation (group-limited or softmax selection)
+int route_variant(const Dims &d) { return (d.n_group > 1 || d.score_func == MOE_SCORE_SOFTMAX) ? 1 : 0; }
 
 int cpl_h(const Dims &d) {
     const int c = (d.H / 32 + 31) / 32;
     return c == 5 ? 6 : (c == 7 ? 8 : c);       // instantiated: 1, 2, 3, 4, 6, 8
 }
 
-template <int A, int B>
+template <int A, int B, int RV>
 cudaError_t attr_t() {
-    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<A, B>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<A, B, RV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBudget);
     int nb = 0;
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, decode_fused_kernel<A, B>, kThreads, kSmemBudget);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, decode_fused_kernel<A, B, RV>, kThreads, kSmemBudget);
     if (e == cudaSuccess && nb < 1) e = cudaErrorInvalidConfiguration;
     return e;
 }
@@ -881,7 +984,6 @@ cudaError_t attr_t() {
 int decode_grid_blocks(const Dims &d) { return d.dec_grid; }
 
 bool decode_fast_supported(const Dims &d) {
-    if (d.n_group != 1 || d.score_func != MOE_SCORE_SIGMOID) return false;   // routing variants: generic path
     if (d.mma_fmt) return false;                                             // int8 experts: tensor-core kernels
     if (d.H % kDnRows != 0 || d.H % 32 != 0 || d.I % 32 != 0) return false;
     if (d.n_shared && d.I_sh != d.I) return false;
@@ -908,8 +1010,9 @@ cudaError_t prepare_decode_fast(Dims &d) {
     // every instantiation gets the same (largest) shared-memory limit, so
     // handles of different shapes coexist
     const int b = (d.I / 32 + 31) / 32;
-    switch (cpl_h(d) * 16 + b) {
-#define MOE_ATTR(A, B) case A * 16 + B: e = attr_t<A, B>(); break;
+    switch (cpl_h(d) * 32 + b * 2 + route_variant(d)) {
+#define MOE_ATTR(A, B) case A * 32 + B * 2: e = attr_t<A, B, 0>(); break; \
+                       case A * 32 + B * 2 + 1: e = attr_t<A, B, 1>(); break;
         MOE_ATTR(1, 1) MOE_ATTR(2, 1) MOE_ATTR(3, 1) MOE_ATTR(4, 1) MOE_ATTR(6, 1) MOE_ATTR(8, 1)
         MOE_ATTR(1, 2) MOE_ATTR(2, 2) MOE_ATTR(3, 2) MOE_ATTR(4, 2) MOE_ATTR(6, 2) MOE_ATTR(8, 2)
 #undef MOE_ATTR
@@ -950,8 +1053,11 @@ cudaError_t launch_decode_fast(const Params &p, const float *x, float *y, cudaSt
     if (e != cudaSuccess) return e;
     const int b = (p.d.I / 32 + 31) / 32;
     const int counts = want_counts ? 1 : 0;
-    e = b == 1 ? launch_h<1>(cpl_h(p.d), cfg, p, x, y, s, counts)
-               : launch_h<2>(cpl_h(p.d), cfg, p, x, y, s, counts);
+    const int a = cpl_h(p.d);
+    if (route_variant(p.d))
+        e = b == 1 ? launch_h<1, 1>(a, cfg, p, x, y, s, counts) : launch_h<2, 1>(a, cfg, p, x, y, s, counts);
+    else
+        e = b == 1 ? launch_h<1, 0>(a, cfg, p, x, y, s, counts) : launch_h<2, 0>(a, cfg, p, x, y, s, counts);
     for (int i = 2; ev && e == cudaSuccess && i < 5; i++) e = cudaEventRecord(ev[i], st);
     return e;
 }

@@ -248,7 +248,7 @@ def test_tcgen05_path_large_batches(moe, kw):
 @pytest.mark.parametrize("name", ["group8", "softmax_renorm", "olmoe_softmax"])
 def test_routing_variants(moe, name):
     wl, li, layer = layer_for(moe, name, 64)
-    assert not moe.moe_uses_streaming_decode(layer.handle)     # the generic T == 1 kernels
+    assert moe.moe_uses_streaming_decode(layer.handle)         # T == 1: the single-kernel path
     assert moe.moe_uses_tensor_cores(layer.handle)
     for T in (1, 5, 40):
         run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=200 + T), f"{name} T={T}")
@@ -380,6 +380,12 @@ def small_workload(**kw):
     dict(n_group=4, topk_group=2),                     # group-limited, CUDA-core batched kernels
     dict(score_func=1),                                # softmax top-k, renormalised
     dict(score_func=1, norm_topk=0, n_shared=0, I_shared=0),   # softmax, probability as weight
+    # routing variants on the single-kernel decode path (I_shared == I)
+    dict(n_group=4, topk_group=2, I_shared=32),                # group-limited
+    dict(n_group=8, topk_group=3, E=64, K=8, I_shared=32),     # 8 experts per group, K > a group
+    dict(n_group=32, topk_group=1, E=64, K=2, I_shared=32),    # 2 experts per group, one group kept
+    dict(score_func=1, I_shared=32),                           # softmax, renormalised
+    dict(score_func=1, E=300, K=32, H=96, n_shared=0, I_shared=0),   # softmax, E > 256, K = 32
     # T > 1 on the tensor cores (H, I, I_shared multiples of 128)
     dict(H=384, I=128, I_shared=256, E=40, K=8),       # 256-row down tiles half used; I_sh != I
     dict(H=256, I=256, n_shared=0, I_shared=0, E=8, K=8),   # E == K: 37 tokens on every expert
