@@ -90,6 +90,10 @@ __device__ __forceinline__ void dp4a_us(int &acc, uint32_t nib, uint32_t dig) {
     asm("dp4a.u32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"(nib), "r"(dig));
 }
 
+__device__ __forceinline__ void dp4a_ss(int &acc, uint32_t w, uint32_t dig) {
+    asm("dp4a.s32.s32 %0, %1, %2, %0;" : "+r"(acc) : "r"(w), "r"(dig));
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int m) {
     return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
 }
@@ -162,6 +166,24 @@ __device__ __forceinline__ void dot_rows(const uint4 (&w)[NR], const uint4 (&dig
             for (int rr = 0; rr < NR; rr++) dp4a_us(lo[rr][p], l[rr], dl);
 #pragma unroll
             for (int rr = 0; rr < NR; rr++) dp4a_us(hi[rr][p], h[rr], dh);
+        }
+    }
+}
+
+// int8 rows (one signed byte per weight, natural order): lo[rr][p] += the plane-p sums of NR
+// rows of one 32-value chunk (w[rr][0..1]: the chunk's 32 bytes).  The digit words hold the
+// even and the odd elements of 8 consecutive values apart (the int4 nibble order above); a
+// byte permute puts the digits of elements 4 jw .. 4 jw + 3 in order again.
+template <int NR>
+__device__ __forceinline__ void dot8_rows(const uint4 (&w)[NR][2], const uint4 (&dig)[kQ], int (&lo)[NR][kPlanes]) {
+#pragma unroll
+    for (int jw = 0; jw < 8; jw++) {
+#pragma unroll
+        for (int p = 0; p < kPlanes; p++) {
+            const uint32_t de = word_of(dig[2 * p], jw >> 1), dd = word_of(dig[2 * p + 1], jw >> 1);
+            const uint32_t dn = __byte_perm(de, dd, (jw & 1) ? 0x7362 : 0x5140);
+#pragma unroll
+            for (int rr = 0; rr < NR; rr++) dp4a_ss(lo[rr][p], word_of(w[rr][jw >> 2], jw & 3), dn);
         }
     }
 }
@@ -361,10 +383,14 @@ __device__ __forceinline__ void route_variant_keys(const Params &p, int E, int l
     __syncwarp();
 }
 
-// RV = 0: the sigmoid + bias router with plain top-K (GLM-5.2, n_group == 1).  RV = 1: the
-// routing variants (Edge0 article section 七; reader.mx section 03): group-limited selection
-// (n_group > 1, sigmoid family) and the softmax family; only warp 0's selection differs.
-template <int CPLH, int CPLI, int RV>
+// V = 0: the sigmoid + bias router with plain top-K (GLM-5.2, n_group == 1), int4 experts.
+// V = 1: the routing variants (Edge0 article section 七; reader.mx section 03): group-limited
+// selection (n_group > 1, sigmoid family) and the softmax family; only warp 0's selection
+// differs.  V = 2: any of those routers, and int8 routed and/or shared experts (reader.mx
+// section 03, the OLMoE engine; section 06/07, the GLM engine's int8 shared expert): an int8
+// unit's rows are twice as long, so it is streamed in two column segments of about half the
+// chunks each (the same registers as an int4 unit), its partial sums carried between them.
+template <int CPLH, int CPLI, int V>
 __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, const float *__restrict__ x,
                                                                    float *__restrict__ y, FusedShape sh,
                                                                    int want_counts) {
@@ -437,7 +463,53 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             su = __ldg(scale + Ij + o);
         }
     };
-    uint4 wa[2 * CPLH], wb[2 * CPLH];
+    // V == 2: a gate/up step is one segment of a unit (int4 units: one segment, the whole rows;
+    // int8 units: two, chunks [0, SEG) and [SEG, CPLH) of each row, 2 uint4 per chunk)
+    constexpr int SEG = (CPLH + 1) / 2;
+    constexpr int NBUF = V == 2 ? 2 * (CPLH > 2 * SEG ? CPLH : 2 * SEG) : 2 * CPLH;
+    const bool r8 = V == 2 && d.expert_fmt == MOE_FORMAT_INT8;
+    const bool s8 = V == 2 && d.shared_fmt == MOE_FORMAT_INT8;
+    struct Step { Unit u; int seg; };
+    auto is8 = [&](const Unit &u) { return u.pos < 0 ? s8 : r8; };
+    auto next_step = [&](Step st) -> Step {
+        if (is8(st.u) && st.seg == 0) return Step{st.u, 1};
+        return Step{next_unit(st.u), 0};
+    };
+    auto load_step = [&](Step st, uint4 (&w)[NBUF], float &sg, float &su) {
+        const int o = st.u.o;
+        const int Ij = st.u.pos < 0 ? d.I_sh : d.I;
+        const uint8_t *slab = st.u.pos < 0 ? p.sh_slab : s_slab[st.u.pos];
+        const float *scale = st.u.pos < 0 ? p.sh_scale : s_scale[st.u.pos];
+        if (!is8(st.u)) {
+            const uint4 *g = reinterpret_cast<const uint4 *>(slab + (size_t)o * sh.rowbytes) + lane;
+            const uint4 *up = reinterpret_cast<const uint4 *>(slab + (size_t)(Ij + o) * sh.rowbytes) + lane;
+#pragma unroll
+            for (int k = 0; k < CPLH; k++) {
+                if (fullH || lane + 32 * k < C) {
+                    w[k] = ldg_stream(g + 32 * k);
+                    w[NBUF / 2 + k] = ldg_stream(up + 32 * k);
+                }
+            }
+        } else {                          // int8 rows: H bytes, chunk c at bytes 32 c .. 32 c + 31
+            const uint4 *g = reinterpret_cast<const uint4 *>(slab + (size_t)o * H);
+            const uint4 *up = reinterpret_cast<const uint4 *>(slab + (size_t)(Ij + o) * H);
+#pragma unroll
+            for (int t = 0; t < SEG; t++) {
+                const int k = st.seg * SEG + t, c = lane + 32 * k;
+                if (k < CPLH && (fullH || c < C)) {
+                    w[2 * t] = ldg_stream(g + 2 * c);
+                    w[2 * t + 1] = ldg_stream(g + 2 * c + 1);
+                    w[NBUF / 2 + 2 * t] = ldg_stream(up + 2 * c);
+                    w[NBUF / 2 + 2 * t + 1] = ldg_stream(up + 2 * c + 1);
+                }
+            }
+        }
+        if (lane == 0) {
+            sg = __ldg(scale + o);
+            su = __ldg(scale + Ij + o);
+        }
+    };
+    uint4 wa[NBUF], wb[NBUF];
     float sga = 0.0f, sua = 0.0f, sgb = 0.0f, sub = 0.0f;
     bool loaded = false;          // wa holds the warp's first unit
 
@@ -530,7 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     }
     __syncthreads();
     if (u_first.pos < 0) {
-        load_gu(u_first, wa, sga, sua);
+        if constexpr (V == 2) load_step(Step{u_first, 0}, wa, sga, sua);
+        else load_gu(u_first, wa, sga, sua);
         loaded = true;
     }
     amax = 0.0f;
@@ -547,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     const float r = d.prenorm ? 1.0f / sqrtf(ss / (float)H + d.eps) : 1.0f;
     auto put_score = [&](int e, float raw, float bias) {
         const float l = raw * r;
-        if constexpr (RV != 0) {
+        if constexpr (V != 0) {
             if (d.score_func == MOE_SCORE_SOFTMAX) {   // the routing warps take the softmax
                 p.ws.logits[e] = l;
                 p.ws.dscore[E + e] = l;
@@ -646,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         // (the scores of up to kKeyBatch x 32 experts are requested together: one round trip)
         unsigned best = 0u;
         int bidx = 0x7fffffff;
-        if constexpr (RV != 0) {
+        if constexpr (V != 0) {
             route_variant_keys(p, E, lane, s_key, s_sig, best, bidx);
         } else
         for (int e0 = lane; e0 < E; e0 += 32 * kKeyBatch) {
@@ -689,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
         float den = sum + 1e-20f;
-        if constexpr (RV != 0) {
+        if constexpr (V != 0) {
             if (d.score_func == MOE_SCORE_SOFTMAX) den = sum;   // the softmax family: no epsilon
         }
         const float mw = d.norm_topk ? d.scale * sg / den : d.scale * sg;
@@ -776,6 +849,65 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     };
     // the next unit's loads are in flight while this one is computed; the loop is kept
     // rolled (its body is large: unrolling it only grows the instruction footprint)
+    if constexpr (V == 2) {
+        int lo2[2][kPlanes], hi2[2][kPlanes];    // a unit's sums, carried between its segments
+        auto step_compute = [&](Step st, const uint4 (&w2)[NBUF], float sg, float su) {
+            const bool i8 = is8(st.u);
+            if (st.seg == 0) {
+#pragma unroll
+                for (int rr = 0; rr < 2; rr++)
+#pragma unroll
+                    for (int q = 0; q < kPlanes; q++) { lo2[rr][q] = i8 ? 0 : corr[q]; hi2[rr][q] = 0; }
+            }
+            if (!i8) {
+#pragma unroll
+                for (int k = 0; k < CPLH; k++) {
+                    if (fullH || lane + 32 * k < C) {
+                        uint4 dig[kQ];
+#pragma unroll
+                        for (int q = 0; q < kQ; q++) dig[q] = lds128(xdig_a + (uint32_t)(q * C * 16 + 512 * k));
+                        const uint4 w[2] = {w2[k], w2[NBUF / 2 + k]};
+                        dot_rows<2>(w, dig, lo2, hi2);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int t = 0; t < SEG; t++) {
+                    const int k = st.seg * SEG + t;
+                    if (k < CPLH && (fullH || lane + 32 * k < C)) {
+                        uint4 dig[kQ];
+#pragma unroll
+                        for (int q = 0; q < kQ; q++) dig[q] = lds128(xdig_a + (uint32_t)(q * C * 16 + 512 * k));
+                        const uint4 w[2][2] = {{w2[2 * t], w2[2 * t + 1]}, {w2[NBUF / 2 + 2 * t], w2[NBUF / 2 + 2 * t + 1]}};
+                        dot8_rows<2>(w, dig, lo2);
+                    }
+                }
+            }
+            if (i8 && st.seg == 0) return;       // the unit's second segment follows
+            const int slot = st.u.pos < 0 ? K : st.u.pos;
+            float v[2] = {planes_lh_to_float(lo2[0], hi2[0]), planes_lh_to_float(lo2[1], hi2[1])};
+            const float tot = reduce_scatter<2>(v, lane);
+            const float up = __shfl_down_sync(kFull, tot, 16);
+            if (lane == 0) p.ws.h[(size_t)slot * d.I_max + st.u.o] = silu_mul(tot * s_x * sg, up * s_x * su);
+        };
+        if (!loaded && u_first.pos < K) {
+            if (!wait_routing()) return;
+            load_step(Step{u_first, 0}, wa, sga, sua);
+        }
+#pragma unroll 1
+        for (Step st = {u_first, 0}, sn; st.u.pos < K; st = sn) {
+            sn = next_step(st);
+            if (sn.u.pos < K) {
+                if (sn.u.pos >= 0 && !wait_routing()) return;
+                load_step(sn, wb, sgb, sub);
+            }
+            step_compute(st, wa, sga, sua);
+#pragma unroll
+            for (int k = 0; k < NBUF; k++) wa[k] = wb[k];
+            sga = sgb;
+            sua = sub;
+        }
+    } else {
     if (!loaded && u_first.pos < K) {
         if (!wait_routing()) return;
         load_gu(u_first, wa, sga, sua);
@@ -797,6 +929,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             if (i < 32) tr[8 + i] = now_ns();
         }
     }
+    }
 
     // ---- down: half-block hb (warps 4 hb .. 4 hb + 3) serves slot j; warp wl of the slot's
     // nwj warps takes row blocks wl, wl + nwj, ...  The first unit's loads go out before
@@ -807,10 +940,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     const int j = hbg % J;
     const int wl = (hbg / J) * 4 + (warp & 3);
     const int nwj = 4 * ((2 * G - 1 - j) / J + 1);
-    const uint8_t *dslab = s_slab[j] + (size_t)d.I * d.H;
+    // V == 2: an int8 slot's down rows (I bytes) are streamed one chunk (2 uint4 per row) per step
+    constexpr int NBD = V == 2 ? (kDnRows * CPLI > 2 * kDnRows ? kDnRows * CPLI : 2 * kDnRows) : kDnRows * CPLI;
+    const bool j8 = j == K ? s8 : r8;
+    const uint8_t *dslab = s_slab[j] + (size_t)(j8 ? 2 : 1) * d.I * d.H;
     const float *sd = s_scale[j] + 2 * d.I;
     const bool dn_writer = (lane & 7) == 0;                // lane l ends with row l / 8
-    auto load_dn = [&](int rb, uint4 (&w)[kDnRows * CPLI], float &sc) {
+    auto load_dn8 = [&](int rb, int kc, uint4 (&w)[NBD], float &sc) {
+        const int c = lane + 32 * kc;
+        if (fullI || c < Cd) {
+#pragma unroll
+            for (int rr = 0; rr < kDnRows; rr++) {
+                const uint4 *row = reinterpret_cast<const uint4 *>(dslab + (size_t)(rb * kDnRows + rr) * d.I);
+                w[2 * rr] = ldg_stream(row + 2 * c);
+                w[2 * rr + 1] = ldg_stream(row + 2 * c + 1);
+            }
+        }
+        if (dn_writer) sc = __ldg(sd + rb * kDnRows + (lane >> 3));
+    };
+    auto load_dn = [&](int rb, uint4 (&w)[NBD], float &sc) {
         const uint4 *src = reinterpret_cast<const uint4 *>(dslab + (size_t)rb * kDnRows * sh.drowbytes) + lane;
 #pragma unroll
         for (int rr = 0; rr < kDnRows; rr++)
@@ -819,9 +967,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
                 if (fullI || lane + 32 * k < Cd) w[rr * CPLI + k] = ldg_stream(src + rr * (sh.drowbytes / 16) + 32 * k);
         if (dn_writer) sc = __ldg(sd + rb * kDnRows + (lane >> 3));
     };
-    uint4 da[kDnRows * CPLI], db[kDnRows * CPLI];
+    uint4 da[NBD], db[NBD];
     float sca = 0.0f, scb = 0.0f;
-    if (wl < sh.RB) load_dn(wl, da, sca);
+    if (wl < sh.RB) {
+        if (V == 2 && j8) load_dn8(wl, 0, da, sca);
+        else load_dn(wl, da, sca);
+    }
 
     // ---- barrier 2: every SwiGLU activation is written ------------------------------------
     if (!grid_barrier(bar2, target, p.ws.err, s_flags + 1)) return;
@@ -890,7 +1041,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             for (int q = 0; q < kQ; q++) hdig[k][q] = make_uint4(0u, 0u, 0u, 0u);
         }
     }
-    auto dn_compute = [&](int rb, const uint4 (&w2)[kDnRows * CPLI], float sc) {
+    auto dn_compute = [&](int rb, const uint4 (&w2)[NBD], float sc) {
         int lo[kDnRows][kPlanes], hi[kDnRows][kPlanes];
 #pragma unroll
         for (int rr = 0; rr < kDnRows; rr++)
@@ -911,13 +1062,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         const float tot = reduce_scatter<kDnRows>(v, lane);
         if (dn_writer) p.ws.dpart[(size_t)j * H + rb * kDnRows + (lane >> 3)] = tot * coef_j * sc;
     };
+    if (V == 2 && j8) {
+        // int8 down rows: steps (rb, chunk kc), the sums of a row block carried over its chunks
+        int lo8[kDnRows][kPlanes], hi8[kDnRows][kPlanes];
+#pragma unroll 1
+        for (int rb = wl, kc = 0; rb < sh.RB;) {
+            const int kn = kc + 1 < CPLI ? kc + 1 : 0, rn = kc + 1 < CPLI ? rb : rb + nwj;
+            if (rn < sh.RB) load_dn8(rn, kn, db, scb);
+            if (kc == 0) {
+#pragma unroll
+                for (int rr = 0; rr < kDnRows; rr++)
+#pragma unroll
+                    for (int q = 0; q < kPlanes; q++) { lo8[rr][q] = 0; hi8[rr][q] = 0; }
+            }
+#pragma unroll
+            for (int k = 0; k < CPLI; k++) {
+                if (k == kc && (fullI || lane + 32 * k < Cd)) {
+                    const uint4 w[kDnRows][2] = {{da[0], da[1]}, {da[2], da[3]}, {da[4], da[5]}, {da[6], da[7]}};
+                    dot8_rows<kDnRows>(w, hdig[k], lo8);
+                }
+            }
+            if (kc + 1 == CPLI) {
+                float v[kDnRows];
+#pragma unroll
+                for (int rr = 0; rr < kDnRows; rr++) v[rr] = planes_lh_to_float(lo8[rr], hi8[rr]);
+                const float tot = reduce_scatter<kDnRows>(v, lane);
+                if (dn_writer) p.ws.dpart[(size_t)j * H + rb * kDnRows + (lane >> 3)] = tot * coef_j * sca;
+            }
+#pragma unroll
+            for (int k = 0; k < NBD; k++) da[k] = db[k];
+            sca = scb;
+            rb = rn;
+            kc = kn;
+        }
+    } else
 #pragma unroll 1
     for (int rb = wl; rb < sh.RB; rb += nwj) {
         const int rn = rb + nwj;
         if (rn < sh.RB) load_dn(rn, db, scb);             // in flight during this unit
         dn_compute(rb, da, sca);
 #pragma unroll
-        for (int k = 0; k < kDnRows * CPLI; k++) da[k] = db[k];
+        for (int k = 0; k < NBD; k++) da[k] = db[k];
         sca = scb;
         if (trace && warp == 0 && lane == 0) {
             const int i = (rb - wl) / nwj;
@@ -940,41 +1125,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
 constexpr int kMaxCplH = 8;   // H up to 8192
 constexpr int kMaxCplI = 2;   // I up to 2048 (digits of more chunks do not fit in registers)
 
-template <int A, int B, int RV>
+template <int A, int B, int V>
 cudaError_t launch_t(cudaLaunchConfig_t &cfg, const Params &p, const float *x, float *y, const FusedShape &s,
                      int counts) {
-    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<A, B, RV>, p, x, y, s, counts);
+    return cudaLaunchKernelEx(&cfg, decode_fused_kernel<A, B, V>, p, x, y, s, counts);
 }
 
-template <int B, int RV>
+template <int B, int V>
 cudaError_t launch_h(int a, cudaLaunchConfig_t &cfg, const Params &p, const float *x, float *y,
                      const FusedShape &s, int counts) {
     switch (a) {
-        case 1: return launch_t<1, B, RV>(cfg, p, x, y, s, counts);
-        case 2: return launch_t<2, B, RV>(cfg, p, x, y, s, counts);
-        case 3: return launch_t<3, B, RV>(cfg, p, x, y, s, counts);
-        case 4: return launch_t<4, B, RV>(cfg, p, x, y, s, counts);
-        case 6: return launch_t<6, B, RV>(cfg, p, x, y, s, counts);
-        case 8: return launch_t<8, B, RV>(cfg, p, x, y, s, counts);
+        case 1: return launch_t<1, B, V>(cfg, p, x, y, s, counts);
+        case 2: return launch_t<2, B, V>(cfg, p, x, y, s, counts);
+        case 3: return launch_t<3, B, V>(cfg, p, x, y, s, counts);
+        case 4: return launch_t<4, B, V>(cfg, p, x, y, s, counts);
+        case 6: return launch_t<6, B, V>(cfg, p, x, y, s, counts);
+        case 8: return launch_t<8, B, V>(cfg, p, x, y, s, counts);
     }
     return cudaErrorInvalidValue;
 }
 
-// the routing-variant instantiation (group-limited or softmax selection)
-int route_variant(const Dims &d) { return (d.n_group > 1 || d.score_func == MOE_SCORE_SOFTMAX) ? 1 : 0; }
+// the instantiation a handle needs: 2 with an int8 expert, 1 for the routing variants
+// (group-limited or softmax selection), else 0
+int kernel_variant(const Dims &d) {
+    if (d.mma_fmt) return 2;
+    return (d.n_group > 1 || d.score_func == MOE_SCORE_SOFTMAX) ? 1 : 0;
+}
 
 int cpl_h(const Dims &d) {
     const int c = (d.H / 32 + 31) / 32;
     return c == 5 ? 6 : (c == 7 ? 8 : c);       // instantiated: 1, 2, 3, 4, 6, 8
 }
 
-template <int A, int B, int RV>
+template <int A, int B, int V>
 cudaError_t attr_t() {
-    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<A, B, RV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<A, B, V>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBudget);
     int nb = 0;
     if (e == cudaSuccess)
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, decode_fused_kernel<A, B, RV>, kThreads, kSmemBudget);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, decode_fused_kernel<A, B, V>, kThreads, kSmemBudget);
     if (e == cudaSuccess && nb < 1) e = cudaErrorInvalidConfiguration;
     return e;
 }
@@ -984,7 +1173,8 @@ cudaError_t attr_t() {
 int decode_grid_blocks(const Dims &d) { return d.dec_grid; }
 
 bool decode_fast_supported(const Dims &d) {
-    if (d.mma_fmt) return false;                                             // int8 experts: tensor-core kernels
+    // int4 and int8 experts (int4 affine group-64 runs on the tensor-core kernels)
+    if (d.expert_fmt == MOE_FORMAT_G64 || (d.n_shared && d.shared_fmt == MOE_FORMAT_G64)) return false;                                             // int8 experts: tensor-core kernels
     if (d.H % kDnRows != 0 || d.H % 32 != 0 || d.I % 32 != 0) return false;
     if (d.n_shared && d.I_sh != d.I) return false;
     if (d.K + d.n_shared > kMaxSlots || d.K + d.n_shared > 32 || d.E > 1024) return false;
@@ -1010,9 +1200,10 @@ cudaError_t prepare_decode_fast(Dims &d) {
     // every instantiation gets the same (largest) shared-memory limit, so
     // handles of different shapes coexist
     const int b = (d.I / 32 + 31) / 32;
-    switch (cpl_h(d) * 32 + b * 2 + route_variant(d)) {
-#define MOE_ATTR(A, B) case A * 32 + B * 2: e = attr_t<A, B, 0>(); break; \
-                       case A * 32 + B * 2 + 1: e = attr_t<A, B, 1>(); break;
+    switch (cpl_h(d) * 16 + b * 4 + kernel_variant(d)) {
+#define MOE_ATTR(A, B) case A * 16 + B * 4: e = attr_t<A, B, 0>(); break; \
+                       case A * 16 + B * 4 + 1: e = attr_t<A, B, 1>(); break; \
+                       case A * 16 + B * 4 + 2: e = attr_t<A, B, 2>(); break;
         MOE_ATTR(1, 1) MOE_ATTR(2, 1) MOE_ATTR(3, 1) MOE_ATTR(4, 1) MOE_ATTR(6, 1) MOE_ATTR(8, 1)
         MOE_ATTR(1, 2) MOE_ATTR(2, 2) MOE_ATTR(3, 2) MOE_ATTR(4, 2) MOE_ATTR(6, 2) MOE_ATTR(8, 2)
 #undef MOE_ATTR
@@ -1054,10 +1245,11 @@ cudaError_t launch_decode_fast(const Params &p, const float *x, float *y, cudaSt
     const int b = (p.d.I / 32 + 31) / 32;
     const int counts = want_counts ? 1 : 0;
     const int a = cpl_h(p.d);
-    if (route_variant(p.d))
-        e = b == 1 ? launch_h<1, 1>(a, cfg, p, x, y, s, counts) : launch_h<2, 1>(a, cfg, p, x, y, s, counts);
-    else
-        e = b == 1 ? launch_h<1, 0>(a, cfg, p, x, y, s, counts) : launch_h<2, 0>(a, cfg, p, x, y, s, counts);
+    switch (kernel_variant(p.d)) {
+        case 0: e = b == 1 ? launch_h<1, 0>(a, cfg, p, x, y, s, counts) : launch_h<2, 0>(a, cfg, p, x, y, s, counts); break;
+        case 1: e = b == 1 ? launch_h<1, 1>(a, cfg, p, x, y, s, counts) : launch_h<2, 1>(a, cfg, p, x, y, s, counts); break;
+        default: e = b == 1 ? launch_h<1, 2>(a, cfg, p, x, y, s, counts) : launch_h<2, 2>(a, cfg, p, x, y, s, counts);
+    }
     for (int i = 2; ev && e == cudaSuccess && i < 5; i++) e = cudaEventRecord(ev[i], st);
     return e;
 }

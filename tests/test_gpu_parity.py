@@ -274,7 +274,10 @@ def test_routing_variant_selection_differs_from_plain(moe):
 def test_int8_experts_olmoe_engine(moe):
     """All routed experts int8, softmax top-8, probability as weight (the OLMoE engine)."""
     wl, li, layer = layer_for(moe, "olmoe_int8", 64)
-    assert moe.moe_uses_tensor_cores(layer.handle) and not moe.moe_uses_streaming_decode(layer.handle)
+    # T == 1 on the single-kernel path (int8 rows in two column segments), T > 1 on tensor cores
+    assert moe.moe_uses_tensor_cores(layer.handle) and moe.moe_uses_streaming_decode(layer.handle)
+    for s in range(8):
+        run_and_check(moe, wl, li, layer, synth.tokens(wl, T=1, stream=400 + s), f"olmoe_int8 T=1 s={s}")
     for T in (1, 5, 40):
         run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=300 + T), f"olmoe_int8 T={T}")
 
@@ -284,6 +287,9 @@ def test_int8_shared_expert_glm(moe):
     wl = synth.WORKLOADS["glm_int8_shared"]
     li = synth.layer_inputs(wl)
     layer = upload(moe, wl, li, 4)
+    assert moe.moe_uses_streaming_decode(layer.handle)
+    for s in range(8):
+        run_and_check(moe, wl, li, layer, synth.tokens(wl, T=1, stream=410 + s), f"glm_int8_shared T=1 s={s}")
     for T in (1, 3):
         run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=310 + T), f"glm_int8_shared T={T}")
     layer.close()
@@ -303,6 +309,12 @@ def test_g64_experts_35b_layer(moe):
     dict(H=128, I=128, I_shared=256, E=8, K=2, expert_format=1, shared_format=1),
     dict(H=256, I=128, I_shared=128, E=8, K=2, shared_format=1),            # int4 routed, int8 shared
     dict(H=384, I=256, n_shared=0, I_shared=0, E=6, K=6, expert_format=1),  # E == K, half-used down tiles
+    # T == 1 on the single-kernel path (I_shared == I)
+    dict(H=384, I=256, I_shared=256, E=16, K=4, expert_format=1, shared_format=1),   # one chunk per lane
+    dict(H=3072, I=384, I_shared=384, E=16, K=4, expert_format=1, shared_format=1),  # 3 chunks: segments 2 + 1
+    dict(H=256, I=2048, I_shared=2048, E=4, K=2, expert_format=1, shared_format=1),  # down rows in 2 steps
+    dict(H=512, I=256, I_shared=256, E=32, K=4, expert_format=1, score_func=1, n_group=1),  # int8, softmax
+    dict(H=512, I=256, I_shared=256, E=32, K=4, shared_format=1, n_group=4, topk_group=2),  # group-limited
 ])
 def test_int8_edge_configs(moe, kw):
     wl = small_workload(**kw)
