@@ -61,6 +61,23 @@ extern "C" {
  * where the tensor-core kernels apply (for comparisons at small T). */
 #define MOE_FLAG_CUDA_CORES 4u
 
+/* Checked build of the path (bounds and invariants, in place of a memory
+ * checker): every call on the handle runs one more kernel after the step that
+ * verifies the call's routing and buckets -- each top-K index in [0, E) and
+ * distinct within its token, each routing weight finite, and where the call
+ * built buckets (T > 1, or T == 1 off the single-kernel decode path) counts
+ * that are the running differences of the offsets, every pair of an expert the
+ * handle computes at a position within its expert's range with perm and inv
+ * inverse to each other there, and every other pair without a position.  A
+ * failed check sets MOE_DEVICE_ERR_CHECK in the device error word (see
+ * moe_device_error); the output of that call is not to be trusted. */
+#define MOE_FLAG_DEBUG_CHECKS 8u
+
+/* Bits of the device error word (moe_device_error). */
+#define MOE_DEVICE_ERR_GRID 8u     /* a grid-wide wait of the decode kernel ran out */
+#define MOE_DEVICE_ERR_CHECK 16u   /* a check of MOE_FLAG_DEBUG_CHECKS failed */
+#define MOE_DEVICE_ERR_TC 32u      /* a pipeline wait of the tcgen05 expert kernel ran out */
+
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID = 1,      /* bad argument or config; nothing was launched */
@@ -216,6 +233,25 @@ moe_status moe_device_error(moe_handle *h, uint32_t *flags);
  * then reports the flag and resets the counters.  Waits for the device first.
  * MOE_ERR_UNSUPPORTED if T == 1 calls on the handle do not use that kernel. */
 moe_status moe_debug_stall_next_call(moe_handle *h);
+
+/* Testing of MOE_FLAG_DEBUG_CHECKS (not steps of the method).
+ * moe_debug_check runs the checking kernel on `stream` over the routing and
+ * buckets the handle's last call of T tokens left in its workspace (the
+ * handle's flag is not needed); a failure sets MOE_DEVICE_ERR_CHECK and
+ * *first_pair (after moe_device_error's wait: read it with moe_device_error)
+ * -- see moe_debug_check_result.  moe_debug_set_topk overwrites one top-K
+ * index of the workspace (pair = t * K + k, 0 <= pair < max_tokens * K) with
+ * `expert` (any value: the checking kernel never uses an index it has not
+ * checked), so that a test can make a check fail without running a step on
+ * bad data.  Both wait for the device; MOE_ERR_INVALID on bad arguments. */
+moe_status moe_debug_check(moe_handle *h, int32_t T);
+moe_status moe_debug_set_topk(moe_handle *h, int32_t pair, int32_t expert);
+/* After a failed check: *pair = a failing pair (t * K + k; or P + e for an
+ * expert e's count, P = T * K), *code = which check (1 index range, 2 weight,
+ * 3 repeated index, 4 position of another rank's pair, 5 position, 6 count or
+ * offset, 7 owned-pair total); 0 / -1 when no check failed.  Call it before
+ * moe_device_error (which clears the record). */
+moe_status moe_debug_check_result(moe_handle *h, int32_t *pair, int32_t *code);
 
 /* 1 if T == 1 calls on this handle run the single persistent decode kernel
  * (one block per SM, all of them resident together, meeting at grid-wide

@@ -19,6 +19,13 @@ __all__ = [
     "moe_destroy", "moe_last_error", "moe_workspace_bytes", "moe_abi_version",
     "moe_profile_start", "moe_profile_read", "moe_route_noalloc", "moe_device_error",
     "moe_debug_stall_next_call",
+    "moe_debug_check",
+    "moe_debug_set_topk",
+    "moe_debug_check_result",
+    "MOE_FLAG_DEBUG_CHECKS",
+    "MOE_DEVICE_ERR_GRID",
+    "MOE_DEVICE_ERR_CHECK",
+    "MOE_DEVICE_ERR_TC",
     "moe_uses_streaming_decode", "moe_uses_tensor_cores",
 ]
 
@@ -26,6 +33,8 @@ MOE_OK, MOE_ERR_INVALID, MOE_ERR_CUDA, MOE_ERR_NOMEM, MOE_ERR_UNSUPPORTED = 0, 1
 MOE_FLAG_PRENORM_RESIDUAL = 1
 MOE_FLAG_TRACE = 2
 MOE_FLAG_CUDA_CORES = 4
+MOE_FLAG_DEBUG_CHECKS = 8
+MOE_DEVICE_ERR_GRID, MOE_DEVICE_ERR_CHECK, MOE_DEVICE_ERR_TC = 8, 16, 32
 MOE_TRACE_SLOTS = 64
 MOE_SCORE_SIGMOID, MOE_SCORE_SOFTMAX = 0, 1
 MOE_FORMAT_INT4, MOE_FORMAT_INT8, MOE_FORMAT_G64 = 0, 1, 2
@@ -93,6 +102,12 @@ def lib():
         L.moe_device_error.restype = C.c_int
         L.moe_debug_stall_next_call.argtypes = [vp]
         L.moe_debug_stall_next_call.restype = C.c_int
+        L.moe_debug_check.argtypes = [vp, C.c_int32]
+        L.moe_debug_check.restype = C.c_int
+        L.moe_debug_set_topk.argtypes = [vp, C.c_int32, C.c_int32]
+        L.moe_debug_set_topk.restype = C.c_int
+        L.moe_debug_check_result.argtypes = [vp, C.POINTER(C.c_int32), C.POINTER(C.c_int32)]
+        L.moe_debug_check_result.restype = C.c_int
         L.moe_uses_streaming_decode.argtypes = [vp]
         L.moe_uses_streaming_decode.restype = i32
         L.moe_uses_tensor_cores.argtypes = [vp]
@@ -202,6 +217,23 @@ def moe_device_error(handle: int, check: bool = True) -> int:
     return f.value
 
 
+def moe_debug_check(handle: int, T: int) -> None:
+    """Run the routing/bucket checks over the handle's last call of T tokens."""
+    _check(lib().moe_debug_check(handle, T), "moe_debug_check")
+
+
+def moe_debug_set_topk(handle: int, pair: int, expert: int) -> None:
+    """Overwrite one top-K index of the workspace (test hook for the checks)."""
+    _check(lib().moe_debug_set_topk(handle, pair, expert), "moe_debug_set_topk")
+
+
+def moe_debug_check_result(handle: int):
+    """(failing pair, check code) of the last failed check, (-1, 0) if none."""
+    pair, code = C.c_int32(0), C.c_int32(0)
+    _check(lib().moe_debug_check_result(handle, C.byref(pair), C.byref(code)), "moe_debug_check_result")
+    return pair.value, code.value
+
+
 def moe_debug_stall_next_call(handle: int) -> None:
     """Make the next T == 1 call on the decode kernel time out (tests of the bounded waits)."""
     _check(lib().moe_debug_stall_next_call(handle), "moe_debug_stall_next_call")
@@ -222,9 +254,9 @@ def moe_destroy(handle: int) -> None:
 def make_config(H, E, K, I, n_shared=0, I_shared=0, routed_scale=1.0, norm_topk=1,
                 prenorm_residual=False, rms_eps=1e-5, n_group=1, trace=False, topk_group=1,
                 score_func=0, cuda_cores=False, expert_format=0, shared_format=0, ep_size=1,
-                ep_rank=0) -> MoeConfig:
+                ep_rank=0, debug_checks=False) -> MoeConfig:
     flags = ((MOE_FLAG_PRENORM_RESIDUAL if prenorm_residual else 0) | (MOE_FLAG_TRACE if trace else 0) |
-             (MOE_FLAG_CUDA_CORES if cuda_cores else 0))
+             (MOE_FLAG_CUDA_CORES if cuda_cores else 0) | (MOE_FLAG_DEBUG_CHECKS if debug_checks else 0))
     return MoeConfig(H, E, K, I, n_shared, I_shared if n_shared else 0, n_group, norm_topk,
                      float(routed_scale), float(rms_eps), flags, topk_group, score_func,
                      expert_format, shared_format, ep_size, ep_rank)

@@ -21,6 +21,8 @@ struct moe_handle {
     cudaEvent_t *prof_ev;   // [prof_max][kStages + 1]
     int prof_max;           // calls to record
     int prof_n;             // calls recorded so far
+    int last_T;             // tokens of the last call, and whether it built buckets (checks)
+    bool last_buckets;
 };
 
 namespace {
@@ -84,7 +86,7 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
     if (c->norm_topk != 0 && c->norm_topk != 1)
         return fail(MOE_ERR_INVALID, "norm_topk=%d: need 0 or 1", c->norm_topk);
     if (!isfinite(c->routed_scale)) return fail(MOE_ERR_INVALID, "routed_scale is not finite");
-    if (c->flags & ~(MOE_FLAG_PRENORM_RESIDUAL | MOE_FLAG_TRACE | MOE_FLAG_CUDA_CORES))
+    if (c->flags & ~(MOE_FLAG_PRENORM_RESIDUAL | MOE_FLAG_TRACE | MOE_FLAG_CUDA_CORES | MOE_FLAG_DEBUG_CHECKS))
         return fail(MOE_ERR_INVALID, "unknown flags 0x%x", c->flags);
     if ((c->flags & MOE_FLAG_PRENORM_RESIDUAL) && !(c->rms_eps >= 0.0f && isfinite(c->rms_eps)))
         return fail(MOE_ERR_INVALID, "rms_eps must be finite and >= 0");
@@ -119,6 +121,7 @@ moe_status check_config(const moe_config *c, int32_t max_tokens, moe::Dims *d) {
     d->fast_decode = (ep == 1 && moe::decode_fast_supported(*d)) ? 1 : 0;
     d->mma = (moe::mma_supported(*d) && !(c->flags & MOE_FLAG_CUDA_CORES)) ? 1 : 0;
     d->trace = (c->flags & MOE_FLAG_TRACE) ? 1 : 0;
+    d->debug_checks = (c->flags & MOE_FLAG_DEBUG_CHECKS) ? 1 : 0;
     return MOE_OK;
 }
 
@@ -203,6 +206,12 @@ moe_status run(moe_handle *h, const float *x, int32_t T, float *y, int32_t *topk
     if (h->prof_ev && h->prof_n < h->prof_max) ev = h->prof_ev + (size_t)(h->prof_n++) * (moe::kStages + 1);
     e = moe::launch_forward(h->p, x, T, y, st, counts != nullptr, ev);
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    h->last_T = T;
+    h->last_buckets = moe::buckets_built(h->p.d, T, counts != nullptr);
+    if (h->p.d.debug_checks) {
+        e = moe::launch_checks(h->p, T, h->last_buckets, st);
+        if (e != cudaSuccess) return cuda_fail(e, "check kernel launch");
+    }
     if (debug) {
         const size_t nk = (size_t)T * h->p.d.K;
         e = cudaMemcpyAsync(topk_idx, h->p.ws.topk_idx, nk * sizeof(int32_t), cudaMemcpyDeviceToDevice, st);
@@ -361,12 +370,43 @@ moe_status moe_device_error(moe_handle *h, uint32_t *flags) {
         // counter afresh so that the next call is consistent again (until this
         // reset, every call on the handle is invalid)
         e = cudaMemset(h->p.ws.counters, 0, 16 * sizeof(unsigned));
-        if (e == cudaSuccess) e = cudaMemset(h->p.ws.err, 0, sizeof(unsigned));
+        if (e == cudaSuccess) e = cudaMemset(h->p.ws.err, 0, 4 * sizeof(unsigned));
         if (e == cudaSuccess) e = cudaDeviceSynchronize();
     }
     if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
     *flags = v;
     if (v) return fail(MOE_ERR_CUDA, "a kernel gave up waiting (flags 0x%x)", v);
+    return MOE_OK;
+}
+
+moe_status moe_debug_check(moe_handle *h, int32_t T) {
+    if (!h) return fail(MOE_ERR_INVALID, "handle is NULL");
+    if (T < 1 || T > h->p.d.max_tokens) return fail(MOE_ERR_INVALID, "T=%d: need 1..max_tokens", T);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = moe::launch_checks(h->p, T, T == h->last_T && h->last_buckets, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "check kernel");
+    return MOE_OK;
+}
+
+moe_status moe_debug_set_topk(moe_handle *h, int32_t pair, int32_t expert) {
+    if (!h) return fail(MOE_ERR_INVALID, "handle is NULL");
+    if (pair < 0 || (long long)pair >= (long long)h->p.d.max_tokens * h->p.d.K)
+        return fail(MOE_ERR_INVALID, "pair=%d: need 0..max_tokens*K-1", pair);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(h->p.ws.topk_idx + pair, &expert, sizeof(expert), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "writing the top-K index");
+    return MOE_OK;
+}
+
+moe_status moe_debug_check_result(moe_handle *h, int32_t *pair, int32_t *code) {
+    if (!h || !pair || !code) return fail(MOE_ERR_INVALID, "NULL argument");
+    unsigned v[4] = {0, 0, 0, 0};
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(v, h->p.ws.err, sizeof(v), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the check record");
+    *pair = v[1] ? (int32_t)(v[1] - 1) : -1;
+    *code = v[1] ? (int32_t)v[2] : 0;
     return MOE_OK;
 }
 

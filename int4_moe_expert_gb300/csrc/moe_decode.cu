@@ -75,7 +75,7 @@ constexpr int kKeyBatch = 8;   // score loads a routing lane has in flight at on
 static_assert(kMaxSlots * 16 % 16 == 0 && kSwWords >= kMaxSlots, "shared-memory carving");
 static_assert(kPtab * kThreads >= 1024, "pointer staging covers the largest expert count");
 
-enum : unsigned { kErrGrid = 8u };
+enum : unsigned { kErrGrid = MOE_DEVICE_ERR_GRID };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -29,6 +29,7 @@ struct Dims {
     int dec_grid;       // blocks of the decode launch (the GPU's SM count; 0 before prepare)
     int ep_lo, ep_hi;   // routed experts this handle computes: [ep_lo, ep_hi) ([0, E) without expert parallelism)
     int resid;          // add x to the output (pre-norm residual; rank 0 only under expert parallelism)
+    int debug_checks;   // MOE_FLAG_DEBUG_CHECKS: a checking kernel after every call
 };
 
 // Device workspace owned by a handle.  Vectors marked "perm" are stored in
@@ -88,6 +89,11 @@ struct Params {
 };
 
 size_t workspace_bytes(const Dims &d);
+
+// MOE_FLAG_DEBUG_CHECKS: the routing / bucket checks over the state of a call of T tokens
+// (buckets: whether that call built them, buckets_built below).
+cudaError_t launch_checks(const Params &p, int T, bool buckets, cudaStream_t st);
+bool buckets_built(const Dims &d, int T, bool want_counts);
 void carve_workspace(const Dims &d, void *base, Workspace *ws);
 
 // Per-config kernel attributes (dynamic shared memory limits); once per handle.

@@ -1374,7 +1374,7 @@ constexpr int kTcBTile = kTcTok * kTcKB * 2;       // the item's f16 activations
 constexpr int kTcSlot = kTcTiles * kTcATile + kTcBTile;
 constexpr size_t kTcSmem = (size_t)kTcS * kTcSlot + 1024;
 constexpr int kTcCols = kTcTiles * kTcTok;         // tensor-memory columns: one f32 accumulator per tile
-constexpr unsigned kErrTc = 32u;
+constexpr unsigned kErrTc = MOE_DEVICE_ERR_TC;
 // kind::f16: D f32 (bits 4-5 = 1), A and B f16 (0), both K-major (0), N >> 3 at bit 17, M >> 4 at bit 24
 constexpr uint32_t kTcIdesc = (1u << 4) | ((uint32_t)(kTcTok >> 3) << 17) | ((128u >> 4) << 24);
 constexpr unsigned long long kTcWaitNs = 500ull * 1000 * 1000;
@@ -1812,6 +1812,64 @@ cudaError_t prepare_kernels(Dims &d) {
     return e;
 }
 
+// ---------------------------------------------------------------------------
+// Checked build (MOE_FLAG_DEBUG_CHECKS): routing and bucket invariants of a call
+// ---------------------------------------------------------------------------
+
+constexpr unsigned kErrCheck = MOE_DEVICE_ERR_CHECK;
+
+// One block.  Every index is range-checked before it is used as an address, so
+// any workspace contents are safe to check.  A failure ORs kErrCheck into
+// err[0] and records (pair + 1, code) in err[1], err[2] (the first to claim).
+__global__ void __launch_bounds__(kThreads) check_kernel(Params p, int T, int buckets) {
+    const int K = p.d.K, E = p.d.E, P = T * K;
+    const int *idx = p.ws.topk_idx;
+    __shared__ int s_owned;
+    if (threadIdx.x == 0) s_owned = 0;
+    __syncthreads();
+    auto fail = [&](int where, int code) {
+        atomicOr(p.ws.err, kErrCheck);
+        if (atomicCAS(p.ws.err + 1, 0u, (unsigned)where + 1u) == 0u) p.ws.err[2] = (unsigned)code;
+    };
+    int owned = 0;
+    for (int q = threadIdx.x; q < P; q += blockDim.x) {
+        const int e = idx[q];
+        if (e < 0 || e >= E) { fail(q, 1); continue; }
+        if (!isfinite(p.ws.topk_w[q])) fail(q, 2);
+        const int t0 = q - q % K;
+        for (int q2 = t0; q2 < q; q2++)
+            if (idx[q2] == e) fail(q, 3);
+        if (!buckets) continue;
+        const bool own = e >= p.d.ep_lo && e < p.d.ep_hi;
+        const int pos = p.ws.inv[q];
+        if (!own) {
+            if (pos != -1) fail(q, 4);
+            continue;
+        }
+        owned++;
+        const int lo = p.ws.off[e], hi = p.ws.off[e + 1];
+        if (pos < 0 || pos >= P || pos < lo || pos >= hi || p.ws.perm[pos] != q) fail(q, 5);
+    }
+    if (!buckets) return;
+    atomicAdd(&s_owned, owned);
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int c = p.ws.cnt[e], lo = p.ws.off[e], hi = p.ws.off[e + 1];
+        if (c < 0 || hi - lo != c || (e == 0 && lo != 0) || hi > P) fail(P + e, 6);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && p.ws.off[E] != s_owned) fail(P + E, 7);
+}
+
+bool buckets_built(const Dims &d, int T, bool want_counts) {
+    if (T == 1 && d.fast_decode) return false;
+    return T > 1 || want_counts || (d.mma && d.mma_fmt);
+}
+
+cudaError_t launch_checks(const Params &p, int T, bool buckets, cudaStream_t st) {
+    check_kernel<<<1, kThreads, 0, st>>>(p, T, buckets ? 1 : 0);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_forward(const Params &p0, const float *x, int T, float *y, cudaStream_t st,
                            bool want_buckets, cudaEvent_t *ev) {
     // this call's tensor-core work items: 128 tokens on the tcgen05 kernel (T >= kTcMinT),
@@ -1822,7 +1880,7 @@ cudaError_t launch_forward(const Params &p0, const float *x, int T, float *y, cu
     if (T == 1 && d.fast_decode) return launch_decode_fast(p, x, y, st, ev, want_buckets);
     const size_t smem = router_smem_bytes(d);
     const bool mma_all = d.mma && (T > 1 || d.mma_fmt);   // the tensor-core expert kernels
-    const int buckets = (T > 1 || want_buckets || mma_all) ? 1 : 0;
+    const int buckets = buckets_built(d, T, want_buckets) ? 1 : 0;
     cudaError_t e = cudaSuccess;
     auto mark = [&](int i) {
         if (ev && e == cudaSuccess) e = cudaEventRecord(ev[i], st);

@@ -94,7 +94,7 @@ def test_workspace_bytes_validates_config(moe):
         moe.make_config(6144, 256, 8, 2048, 1, 2048, routed_scale=float("inf")),
     ]
     unknown_flag = moe.make_config(6144, 256, 8, 2048, 1, 2048)
-    unknown_flag.flags = 8
+    unknown_flag.flags = 16
     bad.append(unknown_flag)
     for cfg in bad:
         assert moe.moe_workspace_bytes(cfg, 1) == 0
