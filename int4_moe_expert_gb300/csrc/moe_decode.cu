@@ -49,6 +49,7 @@
 // 8 warps per SM: per-warp units loaded into registers ran at 5.8 TB/s, the
 // same units through cp.async or 1-D bulk copies into shared memory at
 // 5.0-5.1 TB/s, with or without compute.)
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
@@ -97,6 +98,10 @@ __device__ __forceinline__ void dp4a_ss(int &acc, uint32_t w, uint32_t dig) {
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int m) {
     return m == 0 ? v.x : m == 1 ? v.y : m == 2 ? v.z : v.w;
 }
+
+// (s, b) of an int4 affine group (float16 pair, s in the low half of the word)
+__device__ __forceinline__ float g64_s(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))); }
+__device__ __forceinline__ float g64_b(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
 
 __device__ __forceinline__ float planes_lh_to_float(const int (&lo)[kPlanes], const int (&hi)[kPlanes]) {
     float r = 0.0f;
@@ -469,13 +474,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     constexpr int NBUF = V == 2 ? 2 * (CPLH > 2 * SEG ? CPLH : 2 * SEG) : 2 * CPLH;
     const bool r8 = V == 2 && d.expert_fmt == MOE_FORMAT_INT8;
     const bool s8 = V == 2 && d.shared_fmt == MOE_FORMAT_INT8;
+    // V == 2, int4 affine group-64 (Edge0 article section 三): int4 rows of unsigned nibbles u and
+    // one (s, b) pair per 64 inputs; a chunk (32 inputs) contributes s sum(u X) + b sum(X)
+    const bool rg = V == 2 && d.expert_fmt == MOE_FORMAT_G64;
+    const bool sgf = V == 2 && d.shared_fmt == MOE_FORMAT_G64;
+    auto isg = [&](const Unit &u) { return u.pos < 0 ? sgf : rg; };
     struct Step { Unit u; int seg; };
     auto is8 = [&](const Unit &u) { return u.pos < 0 ? s8 : r8; };
     auto next_step = [&](Step st) -> Step {
         if (is8(st.u) && st.seg == 0) return Step{st.u, 1};
         return Step{next_unit(st.u), 0};
     };
-    auto load_step = [&](Step st, uint4 (&w)[NBUF], float &sg, float &su) {
+    auto load_step = [&](Step st, uint4 (&w)[NBUF], float &sg, float &su, uint32_t (&pr)[2 * CPLH]) {
         const int o = st.u.o;
         const int Ij = st.u.pos < 0 ? d.I_sh : d.I;
         const uint8_t *slab = st.u.pos < 0 ? p.sh_slab : s_slab[st.u.pos];
@@ -504,11 +514,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
                 }
             }
         }
-        if (lane == 0) {
+        if (isg(st.u)) {                  // the chunks' (s, b) pairs; no per-row scale
+            const uint32_t *pw = reinterpret_cast<const uint32_t *>(scale);
+            const int ng = H / 64;
+#pragma unroll
+            for (int k = 0; k < CPLH; k++) {
+                const int c = lane + 32 * k;
+                if (fullH || c < C) {
+                    pr[k] = __ldg(pw + (size_t)o * ng + (c >> 1));
+                    pr[CPLH + k] = __ldg(pw + (size_t)(Ij + o) * ng + (c >> 1));
+                }
+            }
+        } else if (lane == 0) {
             sg = __ldg(scale + o);
             su = __ldg(scale + Ij + o);
         }
     };
+    uint32_t pra[2 * CPLH], prb[2 * CPLH];   // V == 2, group-64 units: (s, b) pairs of the buffered unit
     uint4 wa[NBUF], wb[NBUF];
     float sga = 0.0f, sua = 0.0f, sgb = 0.0f, sub = 0.0f;
     bool loaded = false;          // wa holds the warp's first unit
@@ -602,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     }
     __syncthreads();
     if (u_first.pos < 0) {
-        if constexpr (V == 2) load_step(Step{u_first, 0}, wa, sga, sua);
+        if constexpr (V == 2) load_step(Step{u_first, 0}, wa, sga, sua, pra);
         else load_gu(u_first, wa, sga, sua);
         loaded = true;
     }
@@ -851,8 +873,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     // rolled (its body is large: unrolling it only grows the instruction footprint)
     if constexpr (V == 2) {
         int lo2[2][kPlanes], hi2[2][kPlanes];    // a unit's sums, carried between its segments
-        auto step_compute = [&](Step st, const uint4 (&w2)[NBUF], float sg, float su) {
+        auto step_compute = [&](Step st, const uint4 (&w2)[NBUF], float sg, float su, const uint32_t (&pr)[2 * CPLH]) {
             const bool i8 = is8(st.u);
+            if (isg(st.u)) {
+                float f[2] = {0.0f, 0.0f};
+#pragma unroll
+                for (int k = 0; k < CPLH; k++) {
+                    if (fullH || lane + 32 * k < C) {
+                        uint4 dig[kQ];
+#pragma unroll
+                        for (int q = 0; q < kQ; q++) dig[q] = lds128(xdig_a + (uint32_t)(q * C * 16 + 512 * k));
+                        int lo[2][kPlanes] = {}, hi[2][kPlanes] = {};
+                        const uint4 w[2] = {w2[k], w2[NBUF / 2 + k]};
+                        dot_rows<2>(w, dig, lo, hi);
+                        const int4 t = xdsum[lane + 32 * k];
+                        const float xs = fmaf((float)t.y, 256.0f, (float)t.x);     // sum of the chunk's X
+#pragma unroll
+                        for (int rr = 0; rr < 2; rr++) {
+                            const uint32_t pw = pr[rr * CPLH + k];
+                            f[rr] = fmaf(g64_s(pw), planes_lh_to_float(lo[rr], hi[rr]), fmaf(g64_b(pw), xs, f[rr]));
+                        }
+                    }
+                }
+                const float tot = reduce_scatter<2>(f, lane);
+                const float up = __shfl_down_sync(kFull, tot, 16);
+                const int slot = st.u.pos < 0 ? K : st.u.pos;
+                if (lane == 0) p.ws.h[(size_t)slot * d.I_max + st.u.o] = silu_mul(tot * s_x, up * s_x);
+                return;
+            }
             if (st.seg == 0) {
 #pragma unroll
                 for (int rr = 0; rr < 2; rr++)
@@ -892,18 +940,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
         };
         if (!loaded && u_first.pos < K) {
             if (!wait_routing()) return;
-            load_step(Step{u_first, 0}, wa, sga, sua);
+            load_step(Step{u_first, 0}, wa, sga, sua, pra);
         }
 #pragma unroll 1
         for (Step st = {u_first, 0}, sn; st.u.pos < K; st = sn) {
             sn = next_step(st);
             if (sn.u.pos < K) {
                 if (sn.u.pos >= 0 && !wait_routing()) return;
-                load_step(sn, wb, sgb, sub);
+                load_step(sn, wb, sgb, sub, prb);
             }
-            step_compute(st, wa, sga, sua);
+            step_compute(st, wa, sga, sua, pra);
 #pragma unroll
             for (int k = 0; k < NBUF; k++) wa[k] = wb[k];
+#pragma unroll
+            for (int k = 0; k < 2 * CPLH; k++) pra[k] = prb[k];
             sga = sgb;
             sua = sub;
         }
@@ -943,6 +993,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
     // V == 2: an int8 slot's down rows (I bytes) are streamed one chunk (2 uint4 per row) per step
     constexpr int NBD = V == 2 ? (kDnRows * CPLI > 2 * kDnRows ? kDnRows * CPLI : 2 * kDnRows) : kDnRows * CPLI;
     const bool j8 = j == K ? s8 : r8;
+    const bool jg = j == K ? sgf : rg;        // group-64 down rows: int4 layout, (s, b) per 64 inputs
     const uint8_t *dslab = s_slab[j] + (size_t)(j8 ? 2 : 1) * d.I * d.H;
     const float *sd = s_scale[j] + 2 * d.I;
     const bool dn_writer = (lane & 7) == 0;                // lane l ends with row l / 8
@@ -967,11 +1018,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
                 if (fullI || lane + 32 * k < Cd) w[rr * CPLI + k] = ldg_stream(src + rr * (sh.drowbytes / 16) + 32 * k);
         if (dn_writer) sc = __ldg(sd + rb * kDnRows + (lane >> 3));
     };
+    auto load_dpairs = [&](int rb, uint32_t (&pd)[kDnRows * CPLI]) {
+        const uint32_t *pw = reinterpret_cast<const uint32_t *>(s_scale[j]) + (size_t)2 * d.I * (H / 64);
+        const int ng = d.I / 64;
+#pragma unroll
+        for (int rr = 0; rr < kDnRows; rr++)
+#pragma unroll
+            for (int k = 0; k < CPLI; k++) {
+                const int c = lane + 32 * k;
+                if (fullI || c < Cd) pd[rr * CPLI + k] = __ldg(pw + (size_t)(rb * kDnRows + rr) * ng + (c >> 1));
+            }
+    };
+    uint32_t pda[kDnRows * CPLI], pdb[kDnRows * CPLI];   // V == 2, group-64 slot: pairs of the buffered unit
     uint4 da[NBD], db[NBD];
     float sca = 0.0f, scb = 0.0f;
     if (wl < sh.RB) {
         if (V == 2 && j8) load_dn8(wl, 0, da, sca);
         else load_dn(wl, da, sca);
+        if (V == 2 && jg) load_dpairs(wl, pda);
     }
 
     // ---- barrier 2: every SwiGLU activation is written ------------------------------------
@@ -1095,6 +1159,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fused_kernel(Params p, con
             rb = rn;
             kc = kn;
         }
+    } else if (V == 2 && jg) {
+        // group-64 down rows: per chunk, s sum(u X) + b sum(X) with the chunk's h digit sums
+        float xsh[CPLI];
+#pragma unroll
+        for (int k = 0; k < CPLI; k++) {
+            const int c = lane + 32 * k;
+            const uint4 t = (fullI || c < Cd) ? hd[kQ * Cd + c] : make_uint4(0u, 0u, 0u, 0u);
+            xsh[k] = fmaf((float)(int)t.y, 256.0f, (float)(int)t.x);
+        }
+#pragma unroll 1
+        for (int rb = wl; rb < sh.RB; rb += nwj) {
+            const int rn = rb + nwj;
+            if (rn < sh.RB) {
+                load_dn(rn, db, scb);
+                load_dpairs(rn, pdb);
+            }
+            float f[kDnRows] = {};
+#pragma unroll
+            for (int k = 0; k < CPLI; k++) {
+                if (fullI || lane + 32 * k < Cd) {
+                    int lo[kDnRows][kPlanes] = {}, hi[kDnRows][kPlanes] = {};
+                    uint4 w[kDnRows];
+#pragma unroll
+                    for (int rr = 0; rr < kDnRows; rr++) w[rr] = da[rr * CPLI + k];
+                    dot_rows<kDnRows>(w, hdig[k], lo, hi);
+#pragma unroll
+                    for (int rr = 0; rr < kDnRows; rr++) {
+                        const uint32_t pw = pda[rr * CPLI + k];
+                        f[rr] = fmaf(g64_s(pw), planes_lh_to_float(lo[rr], hi[rr]), fmaf(g64_b(pw), xsh[k], f[rr]));
+                    }
+                }
+            }
+            const float tot = reduce_scatter<kDnRows>(f, lane);
+            if (dn_writer) p.ws.dpart[(size_t)j * H + rb * kDnRows + (lane >> 3)] = tot * coef_j;
+#pragma unroll
+            for (int k = 0; k < NBD; k++) da[k] = db[k];
+#pragma unroll
+            for (int k = 0; k < kDnRows * CPLI; k++) pda[k] = pdb[k];
+        }
     } else
 #pragma unroll 1
     for (int rb = wl; rb < sh.RB; rb += nwj) {
@@ -1172,9 +1275,7 @@ cudaError_t attr_t() {
 
 int decode_grid_blocks(const Dims &d) { return d.dec_grid; }
 
-bool decode_fast_supported(const Dims &d) {
-    // int4 and int8 experts (int4 affine group-64 runs on the tensor-core kernels)
-    if (d.expert_fmt == MOE_FORMAT_G64 || (d.n_shared && d.shared_fmt == MOE_FORMAT_G64)) return false;                                             // int8 experts: tensor-core kernels
+bool decode_fast_supported(const Dims &d) {                                             // int8 experts: tensor-core kernels
     if (d.H % kDnRows != 0 || d.H % 32 != 0 || d.I % 32 != 0) return false;
     if (d.n_shared && d.I_sh != d.I) return false;
     if (d.K + d.n_shared > kMaxSlots || d.K + d.n_shared > 32 || d.E > 1024) return false;

@@ -298,7 +298,10 @@ def test_int8_shared_expert_glm(moe):
 def test_g64_experts_35b_layer(moe):
     """The 35B-class layer with int4 affine group-64 experts (routed and shared)."""
     wl, li, layer = layer_for(moe, "g64_35b", 64)
-    assert moe.moe_uses_tensor_cores(layer.handle) and not moe.moe_uses_streaming_decode(layer.handle)
+    # T == 1 on the single-kernel path (per-chunk s sum(u X) + b sum(X)), T > 1 on tensor cores
+    assert moe.moe_uses_tensor_cores(layer.handle) and moe.moe_uses_streaming_decode(layer.handle)
+    for s in range(8):
+        run_and_check(moe, wl, li, layer, synth.tokens(wl, T=1, stream=420 + s), f"g64_35b T=1 s={s}")
     for T in (1, 5, 40):
         run_and_check(moe, wl, li, layer, synth.tokens(wl, T=T, stream=320 + T), f"g64_35b T={T}")
 
@@ -315,6 +318,9 @@ def test_g64_experts_35b_layer(moe):
     dict(H=256, I=2048, I_shared=2048, E=4, K=2, expert_format=1, shared_format=1),  # down rows in 2 steps
     dict(H=512, I=256, I_shared=256, E=32, K=4, expert_format=1, score_func=1, n_group=1),  # int8, softmax
     dict(H=512, I=256, I_shared=256, E=32, K=4, shared_format=1, n_group=4, topk_group=2),  # group-limited
+    dict(H=256, I=128, I_shared=128, E=8, K=2, expert_format=2, shared_format=2),    # group-64 throughout
+    dict(H=384, I=256, I_shared=256, E=16, K=4, expert_format=2, shared_format=1),   # group-64 + int8 shared
+    dict(H=3072, I=384, I_shared=384, E=16, K=4, expert_format=2, score_func=1),     # 3 chunks per lane
 ])
 def test_int8_edge_configs(moe, kw):
     wl = small_workload(**kw)
