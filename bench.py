@@ -41,9 +41,10 @@ METRIC = "MoE-layer decode tokens/s and achieved HBM GB/s vs ~8 TB/s (GLM-5.2 sh
 N_X = 16                      # distinct token batches rotated through the steps
 FLUSH_BYTES = 256 << 20       # > 129 MB L2
 # committed ncu traffic summaries: dominant kernel -> (summary file, the source it was taken from)
+# committed ncu DRAM summaries per (dominant kernel, workload, tokens per step)
 TRAFFIC_FILES = {
-    "fused": ("traffic_decode_fused_glm_decode.txt", "moe_decode.cu"),
-    "gate_up": ("traffic_gateup_batched_glm.txt", "moe_kernels.cu"),
+    ("fused", "glm_decode", 1): ("traffic_decode_fused_glm_decode.txt", "moe_decode.cu"),
+    ("gate_up", "glm_batched", 512): ("traffic_gateup_batched_glm.txt", "moe_kernels.cu"),
 }
 
 
@@ -193,11 +194,13 @@ def binding_roofline(hbm_frac: float, tensor_frac: float) -> str:
     return "tensor" if tensor_frac >= hbm_frac else "hbm"
 
 
-def recorded_traffic(kind: str):
+def recorded_traffic(kind: str, workload: str, T: int):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary (already scaled to the bench workload), or None when the kernel
-    source changed since the capture."""
-    name, src_name = TRAFFIC_FILES[kind]
+    summary of this workload, or None when there is none or the kernel source
+    changed since the capture."""
+    if (kind, workload, T) not in TRAFFIC_FILES:
+        return None
+    name, src_name = TRAFFIC_FILES[(kind, workload, T)]
     f = ROOT / "profiles" / name
     if not f.exists():
         return None
@@ -378,7 +381,7 @@ def run_ours(args, rank, world, local_rank, dist_on):
         # dominant (only) kernel: the whole step; its bytes are the step's bytes
         dom_kind = "fused"
         dom_name = ("decode_fused_kernel: router + top-k + gate/up + SwiGLU + down + combine, "
-                    "one cooperative launch, T=1")
+                    "one launch (programmatic dependent launch), T=1")
         dom_bytes = bytes_step
         dom_ms = total_ms / K
         units = wl.K + wl.n_shared
@@ -448,7 +451,7 @@ def run_ours(args, rank, world, local_rank, dist_on):
                 "peak_kind": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy)" if peak_kind == "measured" else peak_kind,
                 "unit": "GB/s",
                 "frac": round(achieved / peak, 4),
-                "traffic": recorded_traffic(dom_kind),
+                "traffic": recorded_traffic(dom_kind, wl.name, T),
                 "algorithmic_bytes_per_launch": int(dom_bytes),
                 "experts_per_launch": units,
                 "launch_ms": round(dom_ms, 6),

@@ -64,3 +64,14 @@ def test_cpu_baseline_times_all_cores_and_one():
     assert out["kind"] == "oracle" and out["cores"] == cores and out["value"] > 0
     assert out["single_core"]["cores"] == 1 and out["single_core"]["value"] > 0
     assert oracle.threads() == cores          # the thread count is restored
+
+
+def test_recorded_traffic_is_per_workload():
+    """A committed DRAM summary is used only for the workload and token count it was
+    captured on, and only while the kernel source is the captured one."""
+    import bench
+    assert bench.recorded_traffic("fused", "group8", 1) is None
+    assert bench.recorded_traffic("gate_up", "glm_batched_t16", 16) is None
+    for (kind, wl, T), (name, _) in bench.TRAFFIC_FILES.items():
+        v = bench.recorded_traffic(kind, wl, T)
+        assert v is None or v > 0, (kind, wl, T, name)
