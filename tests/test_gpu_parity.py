@@ -85,6 +85,23 @@ def test_decode_glm(moe):
     print(f"glm decode worst rel err {worst:.3e}")
 
 
+@pytest.mark.parametrize("kw", [
+    dict(H=8192, I=2048, I_shared=2048, E=32, K=8),                  # the largest rows the kernel takes
+    dict(H=8192, I=2048, I_shared=2048, E=32, K=8, shared_format=1),  # ... with an int8 shared expert
+    dict(H=8192, I=2048, I_shared=2048, E=64, K=16, n_group=8, topk_group=4),  # 17 slots, group-limited
+])
+def test_decode_largest_shapes(moe, kw):
+    """The single-kernel decode path at its largest hidden size (8192: eight chunks per lane)
+    and intermediate size (2048: two chunks per lane), for each instantiation."""
+    wl = small_workload(**kw)
+    li = synth.layer_inputs(wl)
+    layer = upload(moe, wl, li, 1)
+    assert moe.moe_uses_streaming_decode(layer.handle)
+    for s_ in range(4):
+        run_and_check(moe, wl, li, layer, synth.tokens(wl, T=1, stream=500 + s_), f"{kw} s={s_}")
+    layer.close()
+
+
 @pytest.mark.parametrize("name", ["tiny", "olmoe", "glm_decode"])
 def test_streaming_decode_path_is_used(moe, name):
     wl, li, layer = layer_for(moe, name, 1 if name == "glm_decode" else 64)
