@@ -216,6 +216,51 @@ def recorded_traffic(kind: str, workload: str, T: int):
     return float(kv["traffic_bytes_per_launch"])
 
 
+
+def kernel_span_stats(moe, cfg, copies, xs, y, T, stream, wl):
+    """Kernel-only time of the decode step: the kernel's own global-timer trace (a handle
+    with MOE_FLAG_TRACE over the same weights, one per layer copy), from the first block's
+    start (past the wait for the previous kernel) to the last block's end, calls back to back
+    in the bench's rotation; the event-timed step adds the launch and the gap between calls."""
+    import ctypes as C
+    import numpy as np
+    import torch
+    tcfg = moe.MoeConfig.from_buffer_copy(cfg)
+    tcfg.flags |= moe.MOE_FLAG_TRACE
+    traced = [moe.MoeLayer(tcfg, c.router_w, c.router_b, c.slabs, c.scales, c.sh_slab, c.sh_scale,
+                           max_tokens=T) for c in copies]
+    spans, gaps = [], []
+    try:
+        for rep in range(8):
+            for i in range(3 * len(traced)):
+                moe.moe_forward(traced[i % len(traced)].handle, xs[i % len(xs)], T, y, stream)
+            torch.cuda.synchronize()
+            recs = []
+            for t in traced:
+                tr = moe.moe_trace_read(t.handle).astype(np.int64)
+                st, en = tr[:, 0], tr[:, 6]
+                if (st > 0).all() and (en > 0).all():
+                    recs.append((int(st.min()), int(en.max())))
+            recs.sort()
+            for (a0, a1), (b0, _) in zip(recs, recs[1:]):
+                spans.append((a1 - a0) / 1e3)
+                gaps.append((b0 - a1) / 1e3)
+        for t in traced:
+            assert moe.moe_device_error(t.handle) == 0
+    finally:
+        for t in traced:
+            t.close()
+    if not spans:
+        return None
+    span = statistics.median(spans)
+    b = step_bytes(wl, T, wl.K)
+    return {"median_us": round(span, 2), "gap_median_us": round(statistics.median(gaps), 2),
+            "hbm_frac_of_span": round(b / (span * 1e-6) / 1e9 / measured_peaks()[0], 4),
+            "note": ("first block start (past the wait for the previous kernel) to last block end, "
+                     "from the kernel's global-timer trace (a traced handle per layer copy, same "
+                     "weights), calls back to back; gap = last block end to the next call's first "
+                     "block start (launch + wait)")}
+
 # --------------------------------------------------------------------------- our arm
 
 def run_ours(args, rank, world, local_rank, dist_on):
@@ -326,9 +371,10 @@ def run_ours(args, rank, world, local_rank, dist_on):
                               "earlier measurements")}
     assert moe.moe_device_error(layer.handle) == 0
 
-    # One cooperative launch per step on the decode path (the step events
-    # bracket exactly that kernel); otherwise router, gate/up, down (+ combine).
+    # One launch per step on the decode path (the step events bracket exactly that kernel);
+    # otherwise router, gate/up, down (+ combine).
     fused = T == 1 and moe.moe_uses_streaming_decode(layer.handle)
+    kernel_span = kernel_span_stats(moe, cfg, copies, xs, y, T, stream, wl) if fused else None
     # launches per step: the fused kernel; or router, gate/up, down; or router (+ activation
     # conversion when T > 8), gate/up, down, combine
     # (T == 1 with an int8 expert runs the tensor-core flow: router, gate/up, down, combine)
@@ -417,6 +463,7 @@ def run_ours(args, rank, world, local_rank, dist_on):
             "ms_per_step": round(ms_per_step, 6),
             "step_time_distribution": step_stats,
             "step_time_flushed": flushed_stats,
+            "kernel_span": kernel_span,
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
