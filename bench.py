@@ -722,7 +722,7 @@ def run_stack(args, rank, world, local_rank, dist_on):
                 "routed_experts_per_layer": wl.K,
             },
             "roofline": {
-                "kernel": ("decode_fused_kernel: one cooperative launch per layer, T=1" if fused else
+                "kernel": ("decode_fused_kernel: one launch per layer (programmatic dependent launch), T=1" if fused else
                            "per-layer kernels, T=1"),
                 "bound": "hbm",
                 "achieved": round(achieved, 1),

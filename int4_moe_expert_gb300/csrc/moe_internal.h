@@ -101,7 +101,7 @@ cudaError_t prepare_kernels(Dims &d);
 
 constexpr int kStages = 4;   // router, gate/up, down, combine
 
-// Decode path (moe_decode.cu): T == 1 as one persistent cooperative kernel.
+// Decode path (moe_decode.cu): T == 1 as one persistent kernel (one block per SM, all resident).
 // ws.counters[4..6] are its grid barriers: they only grow, by gridDim per
 // call; ws.counters[7] counts the calls (read and advanced on the device, so
 // the launch has no per-call host state and can be captured in a graph).
