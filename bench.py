@@ -373,13 +373,14 @@ def run_ours(args, rank, world, local_rank, dist_on):
 
     # One launch per step on the decode path (the step events bracket exactly that kernel);
     # otherwise router, gate/up, down (+ combine).
-    fused = T == 1 and moe.moe_uses_streaming_decode(layer.handle)
-    kernel_span = kernel_span_stats(moe, cfg, copies, xs, y, T, stream, wl) if fused else None
+    # (up to moe_streaming_decode_max_tokens tokens: one single-token decode step per token)
+    fused = T <= moe.moe_streaming_decode_max_tokens(layer.handle)
+    kernel_span = kernel_span_stats(moe, cfg, copies, xs, y, T, stream, wl) if fused and T == 1 else None
     # launches per step: the fused kernel; or router, gate/up, down; or router (+ activation
     # conversion when T > 8), gate/up, down, combine
     # (T == 1 with an int8 expert runs the tensor-core flow: router, gate/up, down, combine)
     t1_tensor = T == 1 and (wl.expert_format != 0 or (wl.n_shared and wl.shared_format != 0))
-    kernels_per_step = 1 if fused else ((4 if t1_tensor else 3) if T == 1 else (4 if T <= 8 else 5))
+    kernels_per_step = T if fused else ((4 if t1_tensor else 3) if T == 1 else (4 if T <= 8 else 5))
     stage_ms, n_calls, event_ms = None, 0, 0.0
     if not fused:
         # Per-kernel times: the same steps again with the library recording an
@@ -427,7 +428,7 @@ def run_ours(args, rank, world, local_rank, dist_on):
         # dominant (only) kernel: the whole step; its bytes are the step's bytes
         dom_kind = "fused"
         dom_name = ("decode_fused_kernel: router + top-k + gate/up + SwiGLU + down + combine, "
-                    "one launch (programmatic dependent launch), T=1")
+                    "one launch (programmatic dependent launch) per token, T=%d" % T)
         dom_bytes = bytes_step
         dom_ms = total_ms / K
         units = wl.K + wl.n_shared
@@ -441,7 +442,7 @@ def run_ours(args, rank, world, local_rank, dist_on):
                      (gateup_bytes(wl.H, wl.I_shared, wl.shared_format) if wl.n_shared else 0))
         dom_ms = stage_ms["gate_up"] - event_ms
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
-    tensor = T > 1 and moe.moe_uses_tensor_cores(layer.handle)
+    tensor = T > 1 and not fused and moe.moe_uses_tensor_cores(layer.handle)
     if tensor:
         # gate/up on the tensor cores: 2 FLOP per weight per (token, expert) pair
         tc5 = T >= 256 and wl.expert_format == 0 and (not wl.n_shared or wl.shared_format == 0)

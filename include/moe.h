@@ -266,6 +266,14 @@ moe_status moe_debug_check_result(moe_handle *h, int32_t *pair, int32_t *code);
  * out, which moe_device_error then reports. */
 int32_t moe_uses_streaming_decode(const moe_handle *h);
 
+/* Calls of up to this many tokens on h run one single-kernel decode step per
+ * token, one after another on the stream (each step streams only its own
+ * experts; below this size that is faster than the batched kernels, whose
+ * per-call work is too small to keep the tensor cores fed).  0 when h does
+ * not use the single-kernel decode path.  moe_forward_debug with
+ * expert_counts always takes the batched kernels for T > 1. */
+int32_t moe_streaming_decode_max_tokens(const moe_handle *h);
+
 /* 1 if T > 1 calls on this handle run the experts on the tensor cores
  * (exact int4 weights times f16 activations, f32 accumulation: tcgen05.mma
  * with tensor-memory accumulators for T >= 256 with int4 experts, mma.sync

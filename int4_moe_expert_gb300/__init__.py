@@ -26,7 +26,7 @@ __all__ = [
     "MOE_DEVICE_ERR_GRID",
     "MOE_DEVICE_ERR_CHECK",
     "MOE_DEVICE_ERR_TC",
-    "moe_uses_streaming_decode", "moe_uses_tensor_cores",
+    "moe_uses_streaming_decode", "moe_streaming_decode_max_tokens", "moe_uses_tensor_cores",
 ]
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_CUDA, MOE_ERR_NOMEM, MOE_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
@@ -110,6 +110,8 @@ def lib():
         L.moe_debug_check_result.restype = C.c_int
         L.moe_uses_streaming_decode.argtypes = [vp]
         L.moe_uses_streaming_decode.restype = i32
+        L.moe_streaming_decode_max_tokens.argtypes = [vp]
+        L.moe_streaming_decode_max_tokens.restype = i32
         L.moe_uses_tensor_cores.argtypes = [vp]
         L.moe_uses_tensor_cores.restype = i32
         L.moe_route_noalloc.argtypes = [C.POINTER(MoeConfig), vp, vp, vp, i32, vp, vp, vp]
@@ -241,6 +243,11 @@ def moe_debug_stall_next_call(handle: int) -> None:
 
 def moe_uses_streaming_decode(handle: int) -> bool:
     return bool(lib().moe_uses_streaming_decode(handle))
+
+
+def moe_streaming_decode_max_tokens(handle: int) -> int:
+    """Calls of up to this many tokens run one single-kernel decode step per token (0: none)."""
+    return int(lib().moe_streaming_decode_max_tokens(handle))
 
 
 def moe_uses_tensor_cores(handle: int) -> bool:

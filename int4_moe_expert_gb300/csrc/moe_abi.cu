@@ -427,6 +427,10 @@ moe_status moe_debug_stall_next_call(moe_handle *h) {
 
 int32_t moe_uses_streaming_decode(const moe_handle *h) { return h ? h->p.d.fast_decode : 0; }
 
+int32_t moe_streaming_decode_max_tokens(const moe_handle *h) {
+    return (h && h->p.d.fast_decode) ? moe::decode_loop_max_tokens() : 0;
+}
+
 int32_t moe_uses_tensor_cores(const moe_handle *h) { return h ? h->p.d.mma : 0; }
 
 moe_status moe_trace_read(moe_handle *h, uint64_t *out, int32_t capacity_blocks, int32_t *n_blocks) {

@@ -94,6 +94,7 @@ size_t workspace_bytes(const Dims &d);
 // (buckets: whether that call built them, buckets_built below).
 cudaError_t launch_checks(const Params &p, int T, bool buckets, cudaStream_t st);
 bool buckets_built(const Dims &d, int T, bool want_counts);
+int decode_loop_max_tokens();   // calls of up to this many tokens run one decode step per token
 void carve_workspace(const Dims &d, void *base, Workspace *ws);
 
 // Per-config kernel attributes (dynamic shared memory limits); once per handle.

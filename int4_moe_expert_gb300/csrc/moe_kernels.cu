@@ -26,6 +26,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+// Tokens up to which a call on a single-kernel-decode handle runs one step per token instead of the
+// batched kernels (measured on the GLM-5.2 layer: see the design notes)
+constexpr int kDecodeLoopMaxT = 6;
 constexpr int kGemvMaxT = 8;       // router GEMV handles up to this many tokens
 constexpr int kGemvAhead = 4;      // router GEMV: row steps (32 lanes x 16 bytes) loaded at once
 constexpr int kRouterBlocks = 456;  // tiled router: aim for 3 blocks per SM (split-K over H)
@@ -1860,8 +1863,16 @@ __global__ void __launch_bounds__(kThreads) check_kernel(Params p, int T, int bu
     if (threadIdx.x == 0 && p.ws.off[E] != s_owned) fail(P + E, 7);
 }
 
+// A few tokens on a handle with the single-kernel decode path: one single-token step per token,
+// each streaming only its own experts (up to kDecodeLoopMaxT tokens).
+bool decode_loop(const Dims &d, int T, bool want_counts) {
+    return d.fast_decode && T >= 1 && (T == 1 || (T <= kDecodeLoopMaxT && !want_counts));
+}
+
+int decode_loop_max_tokens() { return kDecodeLoopMaxT; }
+
 bool buckets_built(const Dims &d, int T, bool want_counts) {
-    if (T == 1 && d.fast_decode) return false;
+    if (decode_loop(d, T, want_counts)) return false;
     return T > 1 || want_counts || (d.mma && d.mma_fmt);
 }
 
@@ -1878,6 +1889,21 @@ cudaError_t launch_forward(const Params &p0, const float *x, int T, float *y, cu
     p.item_tok = mma_item_tokens(p0.d, T);
     const Dims &d = p.d;
     if (T == 1 && d.fast_decode) return launch_decode_fast(p, x, y, st, ev, want_buckets);
+    if (decode_loop(d, T, want_buckets)) {
+        // token t: x, y and its top-K record at offset t (the steps run one after another on the
+        // stream, each started early by the programmatic dependent launch)
+        cudaError_t e = cudaSuccess;
+        if (ev) e = cudaEventRecord(ev[0], st);
+        if (e == cudaSuccess && ev) e = cudaEventRecord(ev[1], st);
+        for (int t = 0; t < T && e == cudaSuccess; t++) {
+            Params pt = p;
+            pt.ws.topk_idx += (size_t)t * d.K;
+            pt.ws.topk_w += (size_t)t * d.K;
+            e = launch_decode_fast(pt, x + (size_t)t * d.H, y + (size_t)t * d.H, st, nullptr, false);
+        }
+        for (int i = 2; ev && e == cudaSuccess && i < 5; i++) e = cudaEventRecord(ev[i], st);
+        return e;
+    }
     const size_t smem = router_smem_bytes(d);
     const bool mma_all = d.mma && (T > 1 || d.mma_fmt);   // the tensor-core expert kernels
     const int buckets = buckets_built(d, T, want_buckets) ? 1 : 0;

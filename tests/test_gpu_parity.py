@@ -85,6 +85,29 @@ def test_decode_glm(moe):
     print(f"glm decode worst rel err {worst:.3e}")
 
 
+def test_decode_loop_small_batches(moe):
+    """T = 2..max on a single-kernel handle: one decode step per token (each token's output and
+    routing record at its own offset), bit-identical to the same tokens one call at a time,
+    and against the oracle; one more token takes the batched kernels."""
+    wl, li, layer = layer_for(moe, "glm_decode", 8)
+    tmax = moe.moe_streaming_decode_max_tokens(layer.handle)
+    assert tmax >= 2
+    ref = oracle_layer(wl, li)
+    for T in (2, 3, tmax):
+        x = synth.tokens(wl, T=T, stream=600 + T)
+        xd = torch.from_numpy(x).cuda()
+        y, idx, w = layer.forward_debug(xd)
+        singles = [layer.forward_debug(xd[t:t + 1]) for t in range(T)]
+        torch.cuda.synchronize()
+        for t in range(T):
+            assert torch.equal(y[t], singles[t][0][0]) and torch.equal(idx[t], singles[t][1][0])
+            check_token(wl, ref, x[t], y[t].cpu().numpy(), idx[t].cpu().numpy(), w[t].cpu().numpy(),
+                        where=f"glm loop T={T} t={t}")
+    x = synth.tokens(wl, T=tmax + 1, stream=700)
+    run_and_check(moe, wl, li, layer, x, f"glm batched T={tmax + 1}")
+    assert moe.moe_device_error(layer.handle) == 0
+
+
 @pytest.mark.parametrize("kw", [
     dict(H=8192, I=2048, I_shared=2048, E=32, K=8),                  # the largest rows the kernel takes
     dict(H=8192, I=2048, I_shared=2048, E=32, K=8, shared_format=1),  # ... with an int8 shared expert
