@@ -15,6 +15,7 @@ struct moe_handle {
     void *ws_base;
     size_t ws_bytes;
     void *tables;        // device copies of the per-expert pointer arrays
+    void *tmaps;         // tcgen05 path: tensor maps of the weights and activations (or NULL)
     float *x_stage;      // device staging for moe_forward_host
     float *y_stage;
     int device;
@@ -175,6 +176,7 @@ void free_handle(moe_handle *h) {
     free_events(h);
     if (h->ws_base) cudaFree(h->ws_base);
     if (h->tables) cudaFree(h->tables);
+    if (h->tmaps) cudaFree(h->tmaps);
     if (h->x_stage) cudaFree(h->x_stage);
     if (h->y_stage) cudaFree(h->y_stage);
     delete h;
@@ -273,8 +275,7 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, int32_t max_tok
         host_tab[d.E + i] = own ? const_cast<float *>(w->expert_scale[i]) : nullptr;
     }
     e = cudaMemcpy(h->tables, host_tab, tbytes, cudaMemcpyHostToDevice);
-    delete[] host_tab;
-    if (e != cudaSuccess) { free_handle(h); return cuda_fail(e, "table upload"); }
+    if (e != cudaSuccess) { delete[] host_tab; free_handle(h); return cuda_fail(e, "table upload"); }
 
     moe::Params &p = h->p;
     p.d = d;
@@ -285,6 +286,17 @@ moe_status moe_init(const moe_config *cfg, const moe_weights *w, int32_t max_tok
     p.sh_slab = d.n_shared ? w->shared_slab : nullptr;
     p.sh_scale = d.n_shared ? w->shared_scale : nullptr;
     moe::carve_workspace(d, h->ws_base, &p.ws);
+    const size_t nmaps = moe::tc_map_count(d);
+    if (nmaps) {
+        e = cudaMalloc(&h->tmaps, nmaps * moe::kTmapBytes);
+        if (e != cudaSuccess) { h->tmaps = nullptr; delete[] host_tab; free_handle(h); return cuda_fail(e, "tensor-map cudaMalloc"); }
+        p.tmaps = h->tmaps;
+        e = moe::upload_tc_maps(p, reinterpret_cast<const uint8_t *const *>(host_tab), h->tmaps);
+        if (e != cudaSuccess) { delete[] host_tab; free_handle(h); return cuda_fail(e, "tensor-map encoding"); }
+    } else {
+        p.tmaps = nullptr;
+    }
+    delete[] host_tab;
     e = cudaMemset(h->ws_base, 0, h->ws_bytes);
     if (e == cudaSuccess) e = moe::prepare_kernels(p.d);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();

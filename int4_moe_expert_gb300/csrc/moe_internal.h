@@ -51,7 +51,10 @@ struct Workspace {
     float *dbuf;         // [(maxT*K + maxT), H] unweighted down outputs (T > 1)
     // T > 1 tensor-core path: f16 activations in mma order (mma_pos in moe_kernels.cu)
     uint16_t *x16;       // [maxT, H] pre-normed x
-    uint16_t *h16;       // [(maxT*K + maxT), I_max] SwiGLU activations, rows as h
+    uint16_t *h16;       // [(maxT*K + maxT), I_max] SwiGLU activations, rows as h (tcgen05 path:
+                         //   the item-blocked layout of moe_kernels.cu, tc_act_index)
+    uint16_t *xp16;      // tcgen05 gate/up: every work item's x16 rows in that layout (permute_x16_kernel)
+    int tc_items;        // work items the tcgen05 layouts hold (0 without that path)
     int *items;          // [2 * max_items] (slot, first token) of every work item (item_tok tokens)
     int *n_items;        // [1]
     float *lpart;        // [S, T, E] tiled router: logits of each of a call's S k-ranges
@@ -73,6 +76,15 @@ inline int max_items(int T, int K, int E, int n_shared, int item = kItemTokens) 
 }
 bool mma_supported(const Dims &d);
 bool tc_supported(const Dims &d);   // int4 experts on the tensor-core path: tcgen05 for large T
+// tcgen05 path (T >= its minimum): tensor maps of every expert's weights, kTmapBytes each,
+// encoded once by moe_init: [2e] gate/up rows and [2e + 1] down rows of routed expert e
+// ([2E], [2E + 1]: the shared expert)
+constexpr int kTmapBytes = 128;
+bool tc_maps_needed(const Dims &d);
+size_t tc_map_count(const Dims &d);
+struct Params;
+// host_slabs: the routed experts' slab pointers (NULL: another rank's expert, no map)
+cudaError_t upload_tc_maps(const Params &p, const uint8_t *const *host_slabs, void *dev);
 constexpr int kTraceBlocks = 1024;   // decode blocks the trace buffer holds
 
 // Everything a kernel needs, passed by value.
@@ -86,6 +98,7 @@ struct Params {
     const float *sh_scale;
     Workspace ws;
     int item_tok;                   // this call: tokens per tensor-core work item
+    const void *tmaps;              // tcgen05 path: device array of tensor maps (tc_map_count), else NULL
 };
 
 size_t workspace_bytes(const Dims &d);

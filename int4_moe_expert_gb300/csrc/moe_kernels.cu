@@ -12,11 +12,15 @@
 // "chunk-permuted" order so that one 16-byte weight load (32 int4 values)
 // meets its 32 activations as eight float4 loads that are contiguous across
 // the lanes of a warp; see perm_pos.
+#include <cuda.h>           // CUtensorMap and its enums (the encoder is resolved at run time)
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <math.h>
 #include <stdint.h>
 
+#include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "moe_internal.h"
 
@@ -1365,33 +1369,38 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
 // ---------------------------------------------------------------------------
 
 constexpr int kTcTok = 128;                        // tokens of a work item on this path (MMA N)
-constexpr int kTcTiles = 4;                        // 128-row weight tiles per block (one accumulator each)
-constexpr int kTcRows = 128 * kTcTiles;            // weight rows per block (gate/up: half gate, half up)
-constexpr int kTcKB = 32;                          // reduction elements per stage
-constexpr int kTcS = 4;                            // ring slots
-constexpr int kTcLag = 2;                          // stage kb waits for the MMAs of stage kb - kTcLag
-constexpr int kTcKAhead = 4;                       // stages of int4 rows in registers ahead
-constexpr int kTcSBO = kTcKB / 8 * 128;            // bytes between 8-row groups of an operand
-constexpr int kTcATile = 128 * kTcKB * 2;          // one 128-row f16 weight tile of a stage
-constexpr int kTcBTile = kTcTok * kTcKB * 2;       // the item's f16 activations of a stage
-constexpr int kTcSlot = kTcTiles * kTcATile + kTcBTile;
-constexpr size_t kTcSmem = (size_t)kTcS * kTcSlot + 1024;
-constexpr int kTcCols = kTcTiles * kTcTok;         // tensor-memory columns: one f32 accumulator per tile
+constexpr int kTcTiles = 2;                        // 128-row weight tiles per block (one accumulator each)
+constexpr int kTcRows = 128 * kTcTiles;            // weight rows per block (gate/up: the gate and up rows of 128 outputs)
+constexpr int kTcKB = 64;                          // reduction elements per stage
+constexpr int kTcS = 6;                            // activation ring slots (shared memory)
+constexpr int kTcSA = 4;                           // A ring slots (tensor memory)
+constexpr int kTcRawB = 64;                        // bytes of a weight row per tensor copy (two stages)
+constexpr int kTcR = 6;                            // raw ring slots (two stages each)
+constexpr int kTcBGroup = kTcTok * 16;             // activations: one 8-element k-group of the item's rows
+constexpr int kTcBTile = kTcBGroup * (kTcKB / 8);  // the item's f16 activations of a stage (one copy)
+constexpr int kTcRawBox = 128;                     // weight rows of one tensor copy (box height)
+constexpr int kTcRawSlot = kTcRows * kTcRawB;      // the block's int4 rows of two stages
+constexpr int kTcACols = kTcTiles * (kTcKB / 2);   // A columns per stage (two f16 per 32-bit column)
+constexpr int kTcCols = 512;                       // allocation: accumulators + the A ring
+constexpr int kTcDq0 = 3;                          // warps: 0 MMA, 1 weight copies, 2 activation copies, 3.. dequant
+constexpr int kTcWarps = kTcDq0 + kTcRows / 32;
+constexpr int kTcThreads = 32 * kTcWarps;
+constexpr size_t kTcSmem = (size_t)kTcS * kTcBTile + (size_t)kTcR * kTcRawSlot + 1024;
 constexpr unsigned kErrTc = MOE_DEVICE_ERR_TC;
 // kind::f16: D f32 (bits 4-5 = 1), A and B f16 (0), both K-major (0), N >> 3 at bit 17, M >> 4 at bit 24
 constexpr uint32_t kTcIdesc = (1u << 4) | ((uint32_t)(kTcTok >> 3) << 17) | ((128u >> 4) << 24);
 constexpr unsigned long long kTcWaitNs = 500ull * 1000 * 1000;
-static_assert(kTcSmem <= 227 * 1024, "the ring fits one block's shared memory");
-static_assert(kTcS >= kTcLag + 1 && kTcLag >= 1, "activations are fetched kTcS - kTcLag stages ahead");
+static_assert(kTcSmem + 1024 <= 227 * 1024, "both rings and the static arrays fit one block's shared memory");
+static_assert(kTcS > kTcSA && kTcSA >= 2, "a commit barrier's phase is never two ahead of its waiters");
+static_assert(kTcTiles * kTcTok + kTcSA * kTcACols <= kTcCols, "accumulators and the A ring fit the allocation");
+static_assert(kTcRawB == 2 * (kTcKB / 2) && kTcRawSlot == 2 * kTcRawBox * kTcRawB, "a raw slot is two copies of two stages");
+static_assert(kTcRows / 32 == 8 && kTcDq0 % 4 == 3, "eight dequantising warps cover each lane quarter of each tile once");
 
-__device__ __forceinline__ uint64_t tc_desc(uint32_t saddr) {   // no-swizzle K-major operand
-    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(128 >> 4) << 16) |
-           ((uint64_t)(kTcSBO >> 4) << 32) | (1ull << 46);
-}
-__device__ __forceinline__ void tc_mma(uint32_t taddr, uint64_t ad, uint64_t bd, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-                 ::"r"(taddr), "l"(ad), "l"(bd), "r"(kTcIdesc), "r"(acc) : "memory");
+// no-swizzle K-major operand descriptor: core matrices of 8 rows x 16 bytes, lbo bytes apart
+// along K, sbo bytes apart per 8 rows
+__device__ __forceinline__ uint64_t tc_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)(lbo >> 4) << 16) |
+           ((uint64_t)(sbo >> 4) << 32) | (1ull << 46);
 }
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
@@ -1417,6 +1426,22 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
         if (tc_now() - t0 > kTcWaitNs) return false;
     }
 }
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// this thread's arrival, announcing `bytes` of tensor copies that complete the phase
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// 2-D tensor copy global -> shared (box of the tensor map at element x, row y; rows outside the
+// tensor read as zeros), counted on the mbarrier
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *map, int x, int y, uint32_t bar) {
+    asm volatile("cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                 ::"r"(dst), "l"(map), "r"(x), "r"(y), "r"(bar) : "memory");
+}
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
     uint32_t r[16];
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -1427,26 +1452,52 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
 #pragma unroll
     for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
-// weights: volatile, so the loads are issued where written (kTcKAhead stages before use)
-__device__ __forceinline__ uint4 ld_stream_v(const void *ptr) {
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
     uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(ptr));
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
     return v;
 }
-__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+
+__device__ __forceinline__ void tc_mma_ta(uint32_t dtaddr, uint32_t ataddr, uint64_t bd, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}"
+                 ::"r"(dtaddr), "r"(ataddr), "l"(bd), "r"(kTcIdesc), "r"(acc) : "memory");
+}
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+                 "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+                   "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+                   "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+                   "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+// contiguous copy global -> shared (16-byte aligned, a multiple of 16 bytes), counted on the mbarrier
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+// The tcgen05 path's activations, [stage][item][k-group][row][8 f16]: one stage (kTcKB elements)
+// of one work item's kTcTok rows is one contiguous kTcBTile block, already in the operand layout
+// (k-group j at j kTcBGroup, row n at 16 n).  Gate/up reads xp16 (written by permute_x16_kernel);
+// down reads h16 (written by the gate/up epilogue of the same item).
+__device__ __forceinline__ size_t tc_act_index(int stage, int item, int cap) {   // in f16 elements
+    return ((size_t)stage * (size_t)cap + (size_t)item) * (size_t)(kTcBTile / 2);
 }
 
 template <bool GU>
-__global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T) {
+__global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int T) {
     extern __shared__ __align__(1024) unsigned char tc_smem[];
-    __shared__ int s_brow[kTcTok], s_orow[kTcTok];
-    __shared__ __align__(8) unsigned long long s_bar[kTcS];
+    __shared__ int s_orow[kTcTok];
+    __shared__ __align__(8) unsigned long long s_rfull[kTcR];   // a raw slot's int4 rows have landed
+    __shared__ __align__(8) unsigned long long s_rempty[kTcR];  // the dequantising warps are done with a raw slot
+    __shared__ __align__(8) unsigned long long s_bfull[kTcS];   // an activation slot has landed
+    __shared__ __align__(8) unsigned long long s_mdone[kTcS];   // a stage's MMAs are done (commit)
+    __shared__ __align__(8) unsigned long long s_afull[kTcSA];  // a stage's A columns are written
     __shared__ uint32_t s_taddr;
     __shared__ int s_fail;
-    __shared__ int s_last_commit;    // the last stage whose MMAs were committed (-1: none)
+    __shared__ int s_last_commit, s_r_issued, s_b_issued;   // for the bounded drain after a failure
     const int item = blockIdx.x;
     if (item >= *p.ws.n_items) return;
     const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
@@ -1461,14 +1512,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
     if (tid < kTcTok) {
         int tok = 0, row = -1;
         if (tid < nt) slot_token(p, s, T, n0 + tid, &tok, &row);
-        s_brow[tid] = GU ? tok : row;
         s_orow[tid] = row;
     }
     if (tid == 0) {
         s_fail = 0;
         s_last_commit = -1;
-        for (int i = 0; i < kTcS; i++)
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(&s_bar[i])) : "memory");
+        s_r_issued = -1;
+        s_b_issued = -1;
+        for (int i = 0; i < kTcR; i++) {
+            mbar_init(smem_u32(&s_rfull[i]), 1);
+            mbar_init(smem_u32(&s_rempty[i]), kTcRows / 32);
+        }
+        for (int i = 0; i < kTcS; i++) {
+            mbar_init(smem_u32(&s_bfull[i]), 1);
+            mbar_init(smem_u32(&s_mdone[i]), 1);
+        }
+        for (int i = 0; i < kTcSA; i++) mbar_init(smem_u32(&s_afull[i]), kTcRows / 32);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -1479,168 +1538,171 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t taddr = s_taddr;
+    volatile int *fail = &s_fail;
 
     const int Kd = GU ? H : Is;
-    const int nkb = Kd / kTcKB;
-    const size_t arb = (size_t)(Kd >> 1);
-    const uint8_t *abase = GU ? s.slab : s.slab + 2 * (size_t)Is * (size_t)(H >> 1);
-    const uint16_t *act = GU ? p.ws.x16 : p.ws.h16;
-    const size_t ald = GU ? (size_t)H : (size_t)p.d.I_max;
+    const int nkb = Kd / kTcKB, nq = Kd / (2 * kTcRawB);
+    const int cap = p.ws.tc_items;
     const uint32_t sbase = (smem_u32(tc_smem) + 1023u) & ~1023u;
-    // weights: thread piece i covers 16 bytes (four words, k-groups 4 piece .. + 3) of row lr
-    constexpr int kAP = kTcRows * (kTcKB / 2) / 16 / kThreads;    // 16-byte pieces per thread per stage
-    constexpr int kRowPcs = kTcKB / 2 / 16;                        // 16-byte pieces per row per stage
-    const uint4 *asrc[kAP];
-    uint32_t adst[kAP];
-    bool aok[kAP];
+    const uint32_t rbase = sbase + (uint32_t)(kTcS * kTcBTile);
+    if (warp == 0) {
+        // MMA issue: stage kb once its A columns and activations are in; the commit frees both
+        if (lane == 0) {
+            for (int kb = 0; kb < nkb; kb++) {
+                if (*fail) break;
+                if (!mbar_wait(smem_u32(&s_afull[kb % kTcSA]), (uint32_t)(kb / kTcSA) & 1u) ||
+                    !mbar_wait(smem_u32(&s_bfull[kb % kTcS]), (uint32_t)(kb / kTcS) & 1u)) {
+                    *fail = 1;
+                    break;
+                }
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t st = sbase + (uint32_t)((kb % kTcS) * kTcBTile);
+                const uint32_t a0 = taddr + (uint32_t)(kTcTiles * kTcTok + (kb % kTcSA) * kTcACols);
 #pragma unroll
-    for (int i = 0; i < kAP; i++) {
-        const int c = tid + i * kThreads, lr = c / kRowPcs, piece = c % kRowPcs;
-        // gate/up: rows [0, kTcRows / 2) are gate rows o0 + lr, the rest the matching up rows
-        const int ol = GU ? (lr < kTcRows / 2 ? lr : lr - kTcRows / 2) : lr;
-        const int gr = GU ? (lr < kTcRows / 2 ? o0 + ol : Is + o0 + ol) : o0 + lr;
-        aok[i] = o0 + ol < rows;
-        asrc[i] = reinterpret_cast<const uint4 *>(abase + (size_t)(aok[i] ? gr : 0) * arb) + piece;
-        const int t = lr >> 7, r = lr & 127;
-        adst[i] = (uint32_t)(t * kTcATile + ((r >> 3) * (kTcKB / 8) + piece * 4) * 128 + (r & 7) * 16);
-        static_assert(kTcKB / 2 / 16 * 4 <= kTcKB / 8, "a piece's four k-groups lie inside the stage");
-    }
-    // activations: thread piece i covers 8 f16 (k-group j) of token n
-    constexpr int kBP = kTcTok * (kTcKB / 8) / kThreads;
-    const uint16_t *bsrc[kBP];
-    uint32_t bdst[kBP];
-    bool bok[kBP];
+                for (int ks = 0; ks < kTcKB / 16; ks++) {     // K 16 per MMA: 8 A columns, two k-groups of B
+                    const uint64_t bd = tc_desc(st + 2 * kTcBGroup * ks, kTcBGroup, 128);
+                    const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
 #pragma unroll
-    for (int i = 0; i < kBP; i++) {
-        const int c = tid + i * kThreads, n = c / (kTcKB / 8), j = c % (kTcKB / 8);
-        bok[i] = n < ((nt + 7) & ~7);
-        bsrc[i] = act + (size_t)s_brow[n < nt ? n : 0] * ald + j * 8;
-        bdst[i] = (uint32_t)(kTcTiles * kTcATile + ((n >> 3) * (kTcKB / 8) + j) * 128 + (n & 7) * 16);
-    }
-    auto slot_addr = [&](int kb) { return sbase + (uint32_t)((kb % kTcS) * kTcSlot); };
-    auto issue_b = [&](int kb) {
-        if (kb < nkb) {
-            const uint32_t st = slot_addr(kb);
-#pragma unroll
-            for (int i = 0; i < kBP; i++)
-                if (bok[i]) cp_async16(st + bdst[i], bsrc[i] + (size_t)kb * kTcKB);
+                    for (int t = 0; t < kTcTiles; t++)
+                        tc_mma_ta(taddr + kTcTok * t, a0 + (uint32_t)(t * (kTcKB / 2) + 8 * ks), bd, acc);
+                }
+                tc_commit(smem_u32(&s_mdone[kb % kTcS]));
+                s_last_commit = kb;
+            }
+            // the last commit covers every MMA of the block
+            const int last = nkb - 1;
+            if (!*fail && !mbar_wait(smem_u32(&s_mdone[last % kTcS]), (uint32_t)(last / kTcS) & 1u)) *fail = 1;
         }
-        cp_async_commit();
-    };
-    uint4 ar[kTcKAhead][kAP];
-    auto load_a = [&](uint4 (&r)[kAP], int kb) {
-        if (kb < nkb) {
-#pragma unroll
-            for (int i = 0; i < kAP; i++)
-                r[i] = aok[i] ? ld_stream_v(asrc[i] + (kTcKB / 32) * kb) : make_uint4(0u, 0u, 0u, 0u);
+    } else if (warp == 1) {
+        // weight copies: raw slot q % kTcR (stages 2q, 2q + 1 of the block's rows) once the
+        // dequantising warps are done with its previous use
+        if (lane == 0) {
+            const int me = s.base >= 0 ? p.ws.slot_expert[slot] : p.d.E;
+            const void *wmap = static_cast<const unsigned char *>(p.tmaps) + (size_t)(2 * me + (GU ? 0 : 1)) * kTmapBytes;
+            const int wy0 = o0, wy1 = GU ? Is + o0 : o0 + kTcRawBox;
+            for (int q = 0; q < nq; q++) {
+                if (*fail) break;
+                if (q >= kTcR && !mbar_wait(smem_u32(&s_rempty[q % kTcR]), (uint32_t)((q - kTcR) / kTcR) & 1u)) {
+                    *fail = 1;
+                    break;
+                }
+                const uint32_t bar = smem_u32(&s_rfull[q % kTcR]);
+                const uint32_t dst = rbase + (uint32_t)((q % kTcR) * kTcRawSlot);
+                mbar_expect_tx(bar, kTcRawSlot);
+                tma_load_2d(dst, wmap, q * kTcRawB, wy0, bar);
+                tma_load_2d(dst + kTcRawBox * kTcRawB, wmap, q * kTcRawB, wy1, bar);
+                s_r_issued = q;
+            }
         }
-    };
+    } else if (warp == 2) {
+        // activation copies: slot kb % kTcS once the MMAs of its previous use are done
+        if (lane == 0) {
+            const uint16_t *act = GU ? p.ws.xp16 : p.ws.h16;
+            for (int kb = 0; kb < nkb; kb++) {
+                if (*fail) break;
+                if (kb >= kTcS && !mbar_wait(smem_u32(&s_mdone[kb % kTcS]), (uint32_t)((kb - kTcS) / kTcS) & 1u)) {
+                    *fail = 1;
+                    break;
+                }
+                const uint32_t bar = smem_u32(&s_bfull[kb % kTcS]);
+                mbar_expect_tx(bar, kTcBTile);
+                bulk_load(sbase + (uint32_t)((kb % kTcS) * kTcBTile), act + tc_act_index(kb, item, cap), kTcBTile, bar);
+                s_b_issued = kb;
+            }
+        }
+    } else {
+        // dequantisation: thread = weight row r = 32 (warp % 4) + lane of tile t (the warp's own
+        // tensor-memory lanes; gate/up: tile 0 the gate rows, tile 1 the up rows).  Raw rows are 64
+        // bytes apart with the copy's 64-byte swizzle: 16-byte chunk c of row lr at c ^ ((lr >> 1) & 3).
+        const int t = (warp - kTcDq0) >> 2;
+        const int lr = t * 128 + 32 * (warp & 3) + lane;
+        const uint32_t rrow = (uint32_t)(lr * kTcRawB), rsw = (uint32_t)((lr >> 1) & 3);
+        const uint32_t tcol = taddr + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTcTiles * kTcTok + t * (kTcKB / 2));
+        for (int kb = 0; kb < nkb; kb++) {
+            if (__any_sync(0xffffffffu, *fail != 0)) break;
+            const int q = kb >> 1;
+            bool ok = mbar_wait(smem_u32(&s_rfull[q % kTcR]), (uint32_t)(q / kTcR) & 1u);
+            if (ok && kb >= kTcSA)   // the A slot's previous stage has been consumed
+                ok = mbar_wait(smem_u32(&s_mdone[(kb - kTcSA) % kTcS]), (uint32_t)((kb - kTcSA) / kTcS) & 1u);
+            if (!__all_sync(0xffffffffu, ok)) {
+                *fail = 1;
+                break;
+            }
+            // this row's 64 values -> 32 f16 pairs (mma order) -> the stage's A columns
+            const uint32_t rs = rbase + (uint32_t)((q % kTcR) * kTcRawSlot) + rrow;
+            const uint32_t c0 = (uint32_t)(2 * (kb & 1));
+            const uint4 wa = lds128(rs + ((c0 ^ rsw) << 4));
+            const uint4 wb = lds128(rs + (((c0 + 1) ^ rsw) << 4));
+            const uint32_t w8[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+            uint32_t h32[32];
 #pragma unroll
-    for (int k = 0; k < kTcKAhead; k++) load_a(ar[k], k);
-#pragma unroll
-    for (int k = 0; k < kTcS - kTcLag; k++) issue_b(k);
-    // stage kb: wait for the MMAs of stage kb - kTcLag (their slot takes the activations of
-    // stage kb + kTcS - kTcLag; completion in order also frees this stage's slot, last used by
-    // kb - kTcS),
-    // dequantise the weights of stage kb into its slot, then one thread issues the MMAs
-    auto step = [&](int kb, uint4 (&r)[kAP]) -> bool {   // true: give up (block-uniform)
-        const uint32_t st = slot_addr(kb);
-        if (kb >= kTcLag &&
-            !mbar_wait(smem_u32(&s_bar[(kb - kTcLag) % kTcS]), (uint32_t)((kb - kTcLag) / kTcS) & 1u))
-            s_fail = 1;
-#pragma unroll
-        for (int i = 0; i < kAP; i++) {
-            const uint32_t w4[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
-#pragma unroll
-            for (int m = 0; m < 4; m++) {            // word m = k-group 4 piece + m: 128 bytes further
+            for (int m = 0; m < 8; m++) {
                 uint32_t h[4];
-                int4x8_to_f16x2(w4[m], h);
-                sts128(st + adst[i] + 128 * m, h[0], h[1], h[2], h[3]);
+                int4x8_to_f16x2(w8[m], h);
+#pragma unroll
+                for (int c = 0; c < 4; c++) h32[4 * m + c] = h[c];
+            }
+            tc_st32(tcol + (uint32_t)((kb % kTcSA) * kTcACols), h32);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(smem_u32(&s_afull[kb % kTcSA]));
+                if (kb & 1) mbar_arrive(smem_u32(&s_rempty[q % kTcR]));   // both stages of raw slot q read
             }
         }
-        issue_b(kb + kTcS - kTcLag);
-        load_a(r, kb + kTcKAhead);
-        cp_async_wait<kTcS - kTcLag>();            // activations of stage kb have landed
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncthreads();
-        const bool fail = s_fail != 0;             // the same in every thread until the next barrier
-        if (tid == 0 && !fail) {
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-#pragma unroll
-            for (int ks = 0; ks < kTcKB / 16; ks++) {     // K 16 per MMA: two core matrices
-                const uint64_t bd = tc_desc(st + kTcTiles * kTcATile + 256 * ks);
-                const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-#pragma unroll
-                for (int t = 0; t < kTcTiles; t++)
-                    tc_mma(taddr + kTcTok * t, tc_desc(st + t * kTcATile + 256 * ks), bd, acc);
-            }
-            tc_commit(smem_u32(&s_bar[kb % kTcS]));
-            s_last_commit = kb;
-        }
-        return fail;
-    };
-    bool failed = false;
-#pragma unroll 1
-    for (int kb0 = 0; kb0 < nkb && !failed; kb0 += kTcKAhead) {
-#pragma unroll
-        for (int k = 0; k < kTcKAhead; k++)
-            if (kb0 + k < nkb && !failed) failed = step(kb0 + k, ar[k]);
     }
-    cp_async_wait<0>();
-    // the last commit covers every MMA this block issued
-    const int last = nkb - 1;
-    if (!failed && !mbar_wait(smem_u32(&s_bar[last % kTcS]), (uint32_t)(last / kTcS) & 1u)) s_fail = 1;
     __syncthreads();
-    // after a wait that ran out, MMAs already committed may still be writing the accumulators:
-    // wait (bounded) for the last commit, which covers all of them, before the columns are freed
-    if (s_fail && tid == 0 && s_last_commit >= 0)
-        mbar_wait(smem_u32(&s_bar[s_last_commit % kTcS]), (uint32_t)(s_last_commit / kTcS) & 1u);
+    if (s_fail && tid == 0) {
+        // after a wait that ran out: copies still in flight land before the block's shared memory
+        // is released, and MMAs already committed finish before the columns are freed (the last
+        // issue into each slot; every wait bounded)
+        for (int q = max(0, s_r_issued - kTcR + 1); q <= s_r_issued; q++)
+            mbar_wait(smem_u32(&s_rfull[q % kTcR]), (uint32_t)(q / kTcR) & 1u);
+        for (int k = max(0, s_b_issued - kTcS + 1); k <= s_b_issued; k++)
+            mbar_wait(smem_u32(&s_bfull[k % kTcS]), (uint32_t)(k / kTcS) & 1u);
+        if (s_last_commit >= 0)
+            mbar_wait(smem_u32(&s_mdone[s_last_commit % kTcS]), (uint32_t)(s_last_commit / kTcS) & 1u);
+    }
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (s_fail) {
         if (tid == 0) atomicOr(p.ws.err, kErrTc);
-    } else {
-        // TMEM lane = row of a tile; warp w reads lanes 32 (w % 4) ..; accumulator t at column
-        // kTcTok t, token n at + n
-        // warp w: lane quarter q4 of the tiles hw, hw + 2, ... (gate/up: gate tile hw with up
-        // tile hw + kTcTiles / 2)
-        const int q4 = warp & 3, hw = warp >> 2;
+    } else if (warp >= kTcDq0) {
+        // warp w: lane quarter w % 4; gate/up: tokens 64 hw .. + 63 of the gate tile and the up tile;
+        // down: tile hw, all tokens (hw = 0 for warps 3-6, 1 for 7-10)
+        const int q4 = warp & 3, hw = (warp - kTcDq0) >> 2;
         const uint32_t trow = taddr + ((uint32_t)(32 * q4) << 16);
         if (GU) {
+            const int o = o0 + 32 * q4 + lane;     // gate row o and up row o
+            const bool ok = o < Is;
+            const float sg = ok ? s.sc[o] : 0.0f, su = ok ? s.sc[Is + o] : 0.0f;
+            const int pos = mma_pos(o);
+            // h of this item in the down kernel's activation layout: stage pos / kTcKB, k-group, element
+            uint16_t *hp = p.ws.h16 + tc_act_index(pos / kTcKB, item, cap) + (size_t)((pos >> 3) & 7) * (kTcBGroup / 2) + (pos & 7);
 #pragma unroll 1
-            for (int t = hw; t < kTcTiles / 2; t += 2) {
-                const int o = o0 + 128 * t + 32 * q4 + lane;     // gate row o and up row o
-                const bool ok = o < Is;
-                const float sg = ok ? s.sc[o] : 0.0f, su = ok ? s.sc[Is + o] : 0.0f;
-                const int pos = mma_pos(o);
-#pragma unroll 1
-                for (int c = 0; c < kTcTok / 16; c++) {
-                    float g[16], u[16];
-                    tc_ld16(trow + kTcTok * t + 16 * c, g);
-                    tc_ld16(trow + kTcTok * (t + kTcTiles / 2) + 16 * c, u);
+            for (int c = 4 * hw; c < 4 * hw + kTcTok / 32; c++) {
+                float g[16], u[16];
+                tc_ld16(trow + 16 * c, g);
+                tc_ld16(trow + kTcTok + 16 * c, u);
 #pragma unroll
-                    for (int i = 0; i < 16; i++) {
-                        const int n = 16 * c + i;
-                        if (ok && n < nt)
-                            p.ws.h16[(size_t)s_orow[n] * p.d.I_max + pos] = f2h_bits(silu_mul(sg * g[i], su * u[i]));
-                    }
+                for (int i = 0; i < 16; i++) {
+                    const int n = 16 * c + i;
+                    if (ok && n < nt) hp[n * 8] = f2h_bits(silu_mul(sg * g[i], su * u[i]));
                 }
             }
         } else {
+            const int o = o0 + 128 * hw + 32 * q4 + lane;
+            const float sd = o < H ? s.sc[2 * Is + o] : 0.0f;
 #pragma unroll 1
-            for (int t = hw; t < kTcTiles; t += 2) {
-                const int o = o0 + 128 * t + 32 * q4 + lane;     // row of tile t
-                const float sd = o < H ? s.sc[2 * Is + o] : 0.0f;
-#pragma unroll 1
-                for (int c = 0; c < kTcTok / 16; c++) {
-                    float v[16];
-                    tc_ld16(trow + kTcTok * t + 16 * c, v);
-                    if (o < H) {
+            for (int c = 0; c < kTcTok / 16; c++) {
+                float v[16];
+                tc_ld16(trow + kTcTok * hw + 16 * c, v);
+                if (o < H) {
 #pragma unroll
-                        for (int i = 0; i < 16; i++) {
-                            const int n = 16 * c + i;
-                            if (n < nt) p.ws.dbuf[(size_t)s_orow[n] * H + o] = sd * v[i];
-                        }
+                    for (int i = 0; i < 16; i++) {
+                        const int n = 16 * c + i;
+                        if (n < nt) p.ws.dbuf[(size_t)s_orow[n] * H + o] = sd * v[i];
                     }
                 }
             }
@@ -1650,6 +1712,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_expert_kernel(Params p, int T)
     __syncthreads();
     if (warp == 0)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "n"(kTcCols) : "memory");
+}
+
+// tcgen05 gate/up activations: xp16 holds, for every work item, the x16 rows of its tokens in the
+// layout above (stage, item, k-group, row).  Block: one item x 32 of its rows x the k-groups of
+// slice blockIdx.z; rows past the item's tokens stay unwritten (their accumulator columns are
+// never read).
+constexpr int kPermSlices = 8;
+__global__ void __launch_bounds__(kThreads) permute_x16_kernel(Params p, int T) {
+    const int item = blockIdx.x;
+    if (item >= *p.ws.n_items) return;
+    const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
+    const SlotInfo s = slot_info(p, T, slot);
+    if (!s.valid) return;
+    const int n = blockIdx.y * 32 + (threadIdx.x & 31);
+    if (n0 + n >= s.n) return;
+    int tok = 0, row = 0;
+    slot_token(p, s, T, n0 + n, &tok, &row);
+    const int H = p.d.H, warp = threadIdx.x >> 5, cap = p.ws.tc_items;
+    const uint4 *src = reinterpret_cast<const uint4 *>(p.ws.x16 + (size_t)tok * H);
+    uint4 *dst = reinterpret_cast<uint4 *>(p.ws.xp16);
+    for (int g = blockIdx.z * kWarps + warp; g < H / 8; g += kWarps * kPermSlices)
+        dst[(tc_act_index(g / (kTcKB / 8), item, cap) + (size_t)(g % (kTcKB / 8)) * (kTcBGroup / 2)) / 8 + n] =
+            __ldcg(src + g);
 }
 
 template <bool GU, int FR, int FS>
@@ -1687,7 +1772,8 @@ template <bool GU>
 void launch_mma_phase(const Params &p, int T, dim3 grid, cudaStream_t st) {
     if (p.item_tok == kTcTok) {
         const dim3 g(grid.x, GU ? (p.d.I_max + kTcRows / 2 - 1) / (kTcRows / 2) : (p.d.H + kTcRows - 1) / kTcRows);
-        tc_expert_kernel<GU><<<g, kThreads, kTcSmem, st>>>(p, T);
+        if (GU) permute_x16_kernel<<<dim3(grid.x, kTcTok / 32, kPermSlices), kThreads, 0, st>>>(p, T);
+        tc_expert_kernel<GU><<<g, kTcThreads, kTcSmem, st>>>(p, T);
         return;
     }
     switch (fmt_pair(p.d)) {
@@ -1766,7 +1852,13 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
     ws->dbuf = reinterpret_cast<float *>(take((P + T) * d.H * sizeof(float)));
     const bool mma = d.mma != 0 && (T > 1 || d.mma_fmt);
     ws->x16 = reinterpret_cast<uint16_t *>(take(mma ? T * d.H * sizeof(uint16_t) : 0));
-    ws->h16 = reinterpret_cast<uint16_t *>(take(mma ? (P + T) * d.I_max * sizeof(uint16_t) : 0));
+    // tcgen05 path: h16 and xp16 also in the item-blocked activation layout of tc_act_index
+    // (tc_items work items of kTcTok rows); h16 is row-major on the other paths
+    const bool tcp = tc_maps_needed(d);
+    ws->tc_items = tcp ? max_items((int)T, d.K, d.E, d.n_shared, kTcTok) : 0;
+    const size_t tc_h = (size_t)ws->tc_items * kTcTok * d.I_max, rm_h = (P + T) * d.I_max;
+    ws->h16 = reinterpret_cast<uint16_t *>(take(!mma ? 0 : (tc_h > rm_h ? tc_h : rm_h) * sizeof(uint16_t)));
+    ws->xp16 = reinterpret_cast<uint16_t *>(take((size_t)ws->tc_items * kTcTok * d.H * sizeof(uint16_t)));
     ws->items = reinterpret_cast<int *>(
         take(mma ? 2 * (size_t)max_items((int)T, d.K, d.E, d.n_shared) * sizeof(int) : 0));
     ws->n_items = reinterpret_cast<int *>(take(sizeof(int)));
@@ -1784,6 +1876,48 @@ void carve_workspace(const Dims &d, void *base, Workspace *ws) {
 bool tc_supported(const Dims &d) {
     const bool int4_only = d.expert_fmt == MOE_FORMAT_INT4 && (!d.n_shared || d.shared_fmt == MOE_FORMAT_INT4);
     return kUseTc && int4_only;
+}
+
+bool tc_maps_needed(const Dims &d) { return d.mma && d.tc && d.max_tokens >= kTcMinT; }
+
+size_t tc_map_count(const Dims &d) { return tc_maps_needed(d) ? 2 * (size_t)d.E + 2 : 0; }
+
+cudaError_t upload_tc_maps(const Params &p, const uint8_t *const *host_slabs, void *dev) {
+    static_assert(sizeof(CUtensorMap) == kTmapBytes, "tensor-map size");
+    const Dims &d = p.d;
+    const size_t n = tc_map_count(d);
+    if (n == 0) return cudaSuccess;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    std::vector<CUtensorMap> m(n);
+    std::memset(m.data(), 0, n * sizeof(CUtensorMap));
+    // weights, uint8 [rows, cols]: boxes of kTcRawB bytes (two stages) x kTcRawBox rows, stored with
+    // the 64-byte swizzle (16-byte chunk c of box row r at chunk c ^ ((r >> 1) & 3)); rows past the
+    // tensor read as zeros.  Gate/up: rows [0, 2 Is) of H / 2 bytes; down: rows [0, H) of Is / 2
+    // bytes after them.
+    bool ok = true;
+    auto map2d = [&](size_t i, const void *base, uint64_t cols, uint64_t rows) {
+        const cuuint64_t dims[2] = {cols, rows};
+        const cuuint64_t strides[1] = {cols};
+        const cuuint32_t box[2] = {(cuuint32_t)kTcRawB, (cuuint32_t)kTcRawBox};
+        const cuuint32_t es[2] = {1, 1};
+        ok = ok && encode(&m[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    auto weights = [&](size_t i, const uint8_t *slab, int Is) {
+        map2d(2 * i, slab, (uint64_t)d.H / 2, 2 * (uint64_t)Is);
+        map2d(2 * i + 1, slab + (size_t)Is * d.H, (uint64_t)Is / 2, (uint64_t)d.H);
+    };
+    for (int x = 0; x < d.E; x++)
+        if (host_slabs[x]) weights((size_t)x, host_slabs[x], d.I);
+    if (d.n_shared) weights((size_t)d.E, p.sh_slab, d.I_sh);
+    if (!ok) return cudaErrorInvalidValue;
+    return cudaMemcpy(dev, m.data(), n * sizeof(CUtensorMap), cudaMemcpyHostToDevice);
 }
 
 bool mma_supported(const Dims &d) {
@@ -1888,6 +2022,7 @@ cudaError_t launch_forward(const Params &p0, const float *x, int T, float *y, cu
     Params p = p0;
     p.item_tok = mma_item_tokens(p0.d, T);
     const Dims &d = p.d;
+    if (p.item_tok == kTcTok && !p.tmaps) return cudaErrorInvalidValue;   // the tcgen05 kernels read tensor maps
     if (T == 1 && d.fast_decode) return launch_decode_fast(p, x, y, st, ev, want_buckets);
     if (decode_loop(d, T, want_buckets)) {
         // token t: x, y and its top-K record at offset t (the steps run one after another on the

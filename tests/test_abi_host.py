@@ -116,11 +116,22 @@ def test_workspace_bytes_validates_config(moe):
 def test_workspace_grows_linearly_in_max_tokens(moe):
     """The workspace is per-token buffers (h, down outputs, f16 activations, routing) plus
     the tiled router's partial logits, which are bounded in rows (split count x tokens):
-    about 0.4 MB per token on the GLM layer from 64 tokens up, never a quadratic term."""
-    glm = moe.make_config(6144, 256, 8, 2048, 1, 2048, 2.5)
-    sizes = {T: moe.moe_workspace_bytes(glm, T) for T in (64, 512, 4096, 16384)}
+    about 0.4 MB per token on the GLM layer from 64 tokens up, never a quadratic term.
+    Handles for 256 tokens or more add the tcgen05 path's item-blocked f16 activations:
+    128 rows of H + I values for each work item a call can have (T K / 128 full items, one
+    partial item per expert, the shared expert's items)."""
+    H, E, K, I = 6144, 256, 8, 2048
+    glm = moe.make_config(H, E, K, I, 1, I, 2.5)
+    sizes = {T: moe.moe_workspace_bytes(glm, T) for T in (64, 255, 256, 512, 4096, 16384)}
+
+    def tc_blocks(T):
+        items = T * K // 128 + min(E, T * K) + (T + 127) // 128 + 1
+        return items * 128 * (H + I) * 2
+
     for T, b in sizes.items():
-        assert 0 < b / T < 420_000, (T, b)
+        extra = tc_blocks(T) if T >= 256 else 0
+        assert 0 < (b - extra) / T < 420_000, (T, b, extra)
+    assert sizes[255] + tc_blocks(256) - 2 * 256 * (K + 1) * I < sizes[256]
     assert sizes[512] < sizes[4096] < sizes[16384]
 
 
