@@ -1372,17 +1372,16 @@ constexpr int kTcTok = 128;                        // tokens of a work item on t
 constexpr int kTcTiles = 2;                        // 128-row weight tiles per block (one accumulator each)
 constexpr int kTcRows = 128 * kTcTiles;            // weight rows per block (gate/up: the gate and up rows of 128 outputs)
 constexpr int kTcKB = 64;                          // reduction elements per stage
-constexpr int kTcS = 6;                            // activation ring slots (shared memory)
-constexpr int kTcSA = 4;                           // A ring slots (tensor memory)
+constexpr int kTcS = 4;                            // stage slots: activations (shared memory) and A (tensor memory)
 constexpr int kTcRawB = 64;                        // bytes of a weight row per tensor copy (two stages)
-constexpr int kTcR = 6;                            // raw ring slots (two stages each)
+constexpr int kTcR = 8;                            // raw ring slots (two stages each)
 constexpr int kTcBGroup = kTcTok * 16;             // activations: one 8-element k-group of the item's rows
 constexpr int kTcBTile = kTcBGroup * (kTcKB / 8);  // the item's f16 activations of a stage (one copy)
 constexpr int kTcRawBox = 128;                     // weight rows of one tensor copy (box height)
 constexpr int kTcRawSlot = kTcRows * kTcRawB;      // the block's int4 rows of two stages
 constexpr int kTcACols = kTcTiles * (kTcKB / 2);   // A columns per stage (two f16 per 32-bit column)
 constexpr int kTcCols = 512;                       // allocation: accumulators + the A ring
-constexpr int kTcDq0 = 3;                          // warps: 0 MMA, 1 weight copies, 2 activation copies, 3.. dequant
+constexpr int kTcDq0 = 4;                          // warps: 0, 1 MMA (tile 0, 1), 2 weight copies, 3 activation copies, 4.. dequant
 constexpr int kTcWarps = kTcDq0 + kTcRows / 32;
 constexpr int kTcThreads = 32 * kTcWarps;
 constexpr size_t kTcSmem = (size_t)kTcS * kTcBTile + (size_t)kTcR * kTcRawSlot + 1024;
@@ -1391,10 +1390,10 @@ constexpr unsigned kErrTc = MOE_DEVICE_ERR_TC;
 constexpr uint32_t kTcIdesc = (1u << 4) | ((uint32_t)(kTcTok >> 3) << 17) | ((128u >> 4) << 24);
 constexpr unsigned long long kTcWaitNs = 500ull * 1000 * 1000;
 static_assert(kTcSmem + 1024 <= 227 * 1024, "both rings and the static arrays fit one block's shared memory");
-static_assert(kTcS > kTcSA && kTcSA >= 2, "a commit barrier's phase is never two ahead of its waiters");
-static_assert(kTcTiles * kTcTok + kTcSA * kTcACols <= kTcCols, "accumulators and the A ring fit the allocation");
+static_assert(kTcTiles == 2, "one MMA-issuing warp per tile: warps 0 and 1");
+static_assert(kTcTiles * kTcTok + kTcS * kTcACols <= kTcCols, "accumulators and the A ring fit the allocation");
 static_assert(kTcRawB == 2 * (kTcKB / 2) && kTcRawSlot == 2 * kTcRawBox * kTcRawB, "a raw slot is two copies of two stages");
-static_assert(kTcRows / 32 == 8 && kTcDq0 % 4 == 3, "eight dequantising warps cover each lane quarter of each tile once");
+static_assert(kTcRows / 32 == 8 && kTcDq0 % 4 == 0, "eight dequantising warps cover each lane quarter of each tile once");
 
 // no-swizzle K-major operand descriptor: core matrices of 8 rows x 16 bytes, lbo bytes apart
 // along K, sbo bytes apart per 8 rows
@@ -1492,12 +1491,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
     __shared__ int s_orow[kTcTok];
     __shared__ __align__(8) unsigned long long s_rfull[kTcR];   // a raw slot's int4 rows have landed
     __shared__ __align__(8) unsigned long long s_rempty[kTcR];  // the dequantising warps are done with a raw slot
-    __shared__ __align__(8) unsigned long long s_bfull[kTcS];   // an activation slot has landed
-    __shared__ __align__(8) unsigned long long s_mdone[kTcS];   // a stage's MMAs are done (commit)
-    __shared__ __align__(8) unsigned long long s_afull[kTcSA];  // a stage's A columns are written
+    __shared__ __align__(8) unsigned long long s_bfull[kTcS];   // a stage's activation copy has landed
+    __shared__ __align__(8) unsigned long long s_full[kTcS];    // a stage's A columns are written and its activations landed
+    __shared__ __align__(8) unsigned long long s_mdone[kTcS];   // a stage's MMAs of both tiles are done (two commits)
+    __shared__ __align__(8) unsigned long long s_drain[kTcTiles];   // all MMAs an issuing thread made are done
     __shared__ uint32_t s_taddr;
     __shared__ int s_fail;
-    __shared__ int s_last_commit, s_r_issued, s_b_issued;   // for the bounded drain after a failure
+    __shared__ int s_r_issued, s_b_issued, s_b_landed;   // for the bounded drain after a failure
     const int item = blockIdx.x;
     if (item >= *p.ws.n_items) return;
     const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
@@ -1516,18 +1516,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
     }
     if (tid == 0) {
         s_fail = 0;
-        s_last_commit = -1;
         s_r_issued = -1;
         s_b_issued = -1;
+        s_b_landed = -1;
         for (int i = 0; i < kTcR; i++) {
             mbar_init(smem_u32(&s_rfull[i]), 1);
             mbar_init(smem_u32(&s_rempty[i]), kTcRows / 32);
         }
         for (int i = 0; i < kTcS; i++) {
             mbar_init(smem_u32(&s_bfull[i]), 1);
-            mbar_init(smem_u32(&s_mdone[i]), 1);
+            mbar_init(smem_u32(&s_full[i]), kTcRows / 32 + 1);   // eight warps + the activation producer
+            mbar_init(smem_u32(&s_mdone[i]), kTcTiles);
         }
-        for (int i = 0; i < kTcSA; i++) mbar_init(smem_u32(&s_afull[i]), kTcRows / 32);
+        for (int i = 0; i < kTcTiles; i++) mbar_init(smem_u32(&s_drain[i]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 0) {
@@ -1545,35 +1546,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
     const int cap = p.ws.tc_items;
     const uint32_t sbase = (smem_u32(tc_smem) + 1023u) & ~1023u;
     const uint32_t rbase = sbase + (uint32_t)(kTcS * kTcBTile);
-    if (warp == 0) {
-        // MMA issue: stage kb once its A columns and activations are in; the commit frees both
+    if (warp < kTcTiles) {
+        // MMA issue, tile t = warp: stage kb once its A columns and activations are in; the two
+        // tiles' commits together free the stage's slots.  Each tile accumulates in stage order.
         if (lane == 0) {
+            const int t = warp;
+            bool issued = false;
             for (int kb = 0; kb < nkb; kb++) {
                 if (*fail) break;
-                if (!mbar_wait(smem_u32(&s_afull[kb % kTcSA]), (uint32_t)(kb / kTcSA) & 1u) ||
-                    !mbar_wait(smem_u32(&s_bfull[kb % kTcS]), (uint32_t)(kb / kTcS) & 1u)) {
+                if (!mbar_wait(smem_u32(&s_full[kb % kTcS]), (uint32_t)(kb / kTcS) & 1u)) {
                     *fail = 1;
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
                 const uint32_t st = sbase + (uint32_t)((kb % kTcS) * kTcBTile);
-                const uint32_t a0 = taddr + (uint32_t)(kTcTiles * kTcTok + (kb % kTcSA) * kTcACols);
+                const uint32_t a0 = taddr + (uint32_t)(kTcTiles * kTcTok + (kb % kTcS) * kTcACols + t * (kTcKB / 2));
 #pragma unroll
-                for (int ks = 0; ks < kTcKB / 16; ks++) {     // K 16 per MMA: 8 A columns, two k-groups of B
-                    const uint64_t bd = tc_desc(st + 2 * kTcBGroup * ks, kTcBGroup, 128);
-                    const uint32_t acc = (kb > 0 || ks > 0) ? 1u : 0u;
-#pragma unroll
-                    for (int t = 0; t < kTcTiles; t++)
-                        tc_mma_ta(taddr + kTcTok * t, a0 + (uint32_t)(t * (kTcKB / 2) + 8 * ks), bd, acc);
-                }
+                for (int ks = 0; ks < kTcKB / 16; ks++)      // K 16 per MMA: 8 A columns, two k-groups of B
+                    tc_mma_ta(taddr + kTcTok * t, a0 + (uint32_t)(8 * ks), tc_desc(st + 2 * kTcBGroup * ks, kTcBGroup, 128),
+                              (kb > 0 || ks > 0) ? 1u : 0u);
                 tc_commit(smem_u32(&s_mdone[kb % kTcS]));
-                s_last_commit = kb;
+                issued = true;
             }
-            // the last commit covers every MMA of the block
-            const int last = nkb - 1;
-            if (!*fail && !mbar_wait(smem_u32(&s_mdone[last % kTcS]), (uint32_t)(last / kTcS) & 1u)) *fail = 1;
+            // every MMA this thread issued is done before the block moves on (bounded)
+            if (issued) {
+                tc_commit(smem_u32(&s_drain[t]));
+                if (!mbar_wait(smem_u32(&s_drain[t]), 0u)) *fail = 1;
+            }
         }
-    } else if (warp == 1) {
+    } else if (warp == kTcTiles) {
         // weight copies: raw slot q % kTcR (stages 2q, 2q + 1 of the block's rows) once the
         // dequantising warps are done with its previous use
         if (lane == 0) {
@@ -1594,13 +1595,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
                 s_r_issued = q;
             }
         }
-    } else if (warp == 2) {
-        // activation copies: slot kb % kTcS once the MMAs of its previous use are done
+    } else if (warp == kTcTiles + 1) {
+        // activation copies: slot kb % kTcS once the MMAs of its previous use are done; the copy
+        // of stage kb - 1 is waited for after stage kb's is issued (two in flight), then reported
+        // on that stage's full barrier
         if (lane == 0) {
             const uint16_t *act = GU ? p.ws.xp16 : p.ws.h16;
-            for (int kb = 0; kb < nkb; kb++) {
-                if (*fail) break;
+            auto land = [&](int k) {          // false: the wait ran out
+                if (!mbar_wait(smem_u32(&s_bfull[k % kTcS]), (uint32_t)(k / kTcS) & 1u)) return false;
+                s_b_landed = k;
+                mbar_arrive(smem_u32(&s_full[k % kTcS]));
+                return true;
+            };
+            bool ok = true;
+            for (int kb = 0; kb < nkb && ok; kb++) {
+                if (*fail) { ok = false; break; }
                 if (kb >= kTcS && !mbar_wait(smem_u32(&s_mdone[kb % kTcS]), (uint32_t)((kb - kTcS) / kTcS) & 1u)) {
+                    ok = false;
                     *fail = 1;
                     break;
                 }
@@ -1608,7 +1619,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
                 mbar_expect_tx(bar, kTcBTile);
                 bulk_load(sbase + (uint32_t)((kb % kTcS) * kTcBTile), act + tc_act_index(kb, item, cap), kTcBTile, bar);
                 s_b_issued = kb;
+                if (kb >= 1 && !land(kb - 1)) { ok = false; *fail = 1; }
             }
+            if (ok && !land(nkb - 1)) *fail = 1;
         }
     } else {
         // dequantisation: thread = weight row r = 32 (warp % 4) + lane of tile t (the warp's own
@@ -1622,8 +1635,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
             if (__any_sync(0xffffffffu, *fail != 0)) break;
             const int q = kb >> 1;
             bool ok = mbar_wait(smem_u32(&s_rfull[q % kTcR]), (uint32_t)(q / kTcR) & 1u);
-            if (ok && kb >= kTcSA)   // the A slot's previous stage has been consumed
-                ok = mbar_wait(smem_u32(&s_mdone[(kb - kTcSA) % kTcS]), (uint32_t)((kb - kTcSA) / kTcS) & 1u);
+            if (ok && kb >= kTcS)    // the A slot's previous stage has been consumed
+                ok = mbar_wait(smem_u32(&s_mdone[kb % kTcS]), (uint32_t)((kb - kTcS) / kTcS) & 1u);
             if (!__all_sync(0xffffffffu, ok)) {
                 *fail = 1;
                 break;
@@ -1642,12 +1655,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
 #pragma unroll
                 for (int c = 0; c < 4; c++) h32[4 * m + c] = h[c];
             }
-            tc_st32(tcol + (uint32_t)((kb % kTcSA) * kTcACols), h32);
+            tc_st32(tcol + (uint32_t)((kb % kTcS) * kTcACols), h32);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
             if (lane == 0) {
-                mbar_arrive(smem_u32(&s_afull[kb % kTcSA]));
+                mbar_arrive(smem_u32(&s_full[kb % kTcS]));
                 if (kb & 1) mbar_arrive(smem_u32(&s_rempty[q % kTcR]));   // both stages of raw slot q read
             }
         }
@@ -1655,14 +1668,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
     __syncthreads();
     if (s_fail && tid == 0) {
         // after a wait that ran out: copies still in flight land before the block's shared memory
-        // is released, and MMAs already committed finish before the columns are freed (the last
-        // issue into each slot; every wait bounded)
+        // is released (every wait bounded); the MMA threads already waited for their own MMAs
         for (int q = max(0, s_r_issued - kTcR + 1); q <= s_r_issued; q++)
             mbar_wait(smem_u32(&s_rfull[q % kTcR]), (uint32_t)(q / kTcR) & 1u);
-        for (int k = max(0, s_b_issued - kTcS + 1); k <= s_b_issued; k++)
+        for (int k = s_b_landed + 1; k <= s_b_issued; k++)
             mbar_wait(smem_u32(&s_bfull[k % kTcS]), (uint32_t)(k / kTcS) & 1u);
-        if (s_last_commit >= 0)
-            mbar_wait(smem_u32(&s_mdone[s_last_commit % kTcS]), (uint32_t)(s_last_commit / kTcS) & 1u);
     }
     __syncthreads();
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -1670,7 +1680,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
         if (tid == 0) atomicOr(p.ws.err, kErrTc);
     } else if (warp >= kTcDq0) {
         // warp w: lane quarter w % 4; gate/up: tokens 64 hw .. + 63 of the gate tile and the up tile;
-        // down: tile hw, all tokens (hw = 0 for warps 3-6, 1 for 7-10)
+        // down: tile hw, all tokens (hw = 0 for warps 4-7, 1 for 8-11)
         const int q4 = warp & 3, hw = (warp - kTcDq0) >> 2;
         const uint32_t trow = taddr + ((uint32_t)(32 * q4) << 16);
         if (GU) {
