@@ -1492,12 +1492,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
     __shared__ __align__(8) unsigned long long s_rfull[kTcR];   // a raw slot's int4 rows have landed
     __shared__ __align__(8) unsigned long long s_rempty[kTcR];  // the dequantising warps are done with a raw slot
     __shared__ __align__(8) unsigned long long s_bfull[kTcS];   // a stage's activation copy has landed
-    __shared__ __align__(8) unsigned long long s_full[kTcS];    // a stage's A columns are written and its activations landed
+    __shared__ __align__(8) unsigned long long s_full[kTcS];    // a stage's A columns are written (eight warps)
     __shared__ __align__(8) unsigned long long s_mdone[kTcS];   // a stage's MMAs of both tiles are done (two commits)
     __shared__ __align__(8) unsigned long long s_drain[kTcTiles];   // all MMAs an issuing thread made are done
     __shared__ uint32_t s_taddr;
     __shared__ int s_fail;
-    __shared__ int s_r_issued, s_b_issued, s_b_landed;   // for the bounded drain after a failure
+    __shared__ int s_r_issued, s_b_issued;   // for the bounded drain after a failure
     const int item = blockIdx.x;
     if (item >= *p.ws.n_items) return;
     const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
@@ -1518,14 +1518,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
         s_fail = 0;
         s_r_issued = -1;
         s_b_issued = -1;
-        s_b_landed = -1;
         for (int i = 0; i < kTcR; i++) {
             mbar_init(smem_u32(&s_rfull[i]), 1);
             mbar_init(smem_u32(&s_rempty[i]), kTcRows / 32);
         }
         for (int i = 0; i < kTcS; i++) {
             mbar_init(smem_u32(&s_bfull[i]), 1);
-            mbar_init(smem_u32(&s_full[i]), kTcRows / 32 + 1);   // eight warps + the activation producer
+            mbar_init(smem_u32(&s_full[i]), kTcRows / 32);
             mbar_init(smem_u32(&s_mdone[i]), kTcTiles);
         }
         for (int i = 0; i < kTcTiles; i++) mbar_init(smem_u32(&s_drain[i]), 1);
@@ -1552,20 +1551,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
         if (lane == 0) {
             const int t = warp;
             bool issued = false;
+            // everything but the slot is fixed: the B descriptor of slot j and k-step ks is the
+            // slot-0 descriptor plus the byte offset / 16 in its start-address field (shared
+            // addresses stay below 2^18, so the field cannot carry), the A column likewise
+            const uint64_t bd0 = tc_desc(sbase, kTcBGroup, 128);
+            const uint32_t dt = taddr + (uint32_t)(kTcTok * t);
+            const uint32_t at0 = taddr + (uint32_t)(kTcTiles * kTcTok + t * (kTcKB / 2));
             for (int kb = 0; kb < nkb; kb++) {
                 if (*fail) break;
-                if (!mbar_wait(smem_u32(&s_full[kb % kTcS]), (uint32_t)(kb / kTcS) & 1u)) {
+                const int j = kb % kTcS;
+                const uint64_t bd = bd0 + (uint64_t)((j * kTcBTile) >> 4);
+                const uint32_t at = at0 + (uint32_t)(j * kTcACols);
+                if (!mbar_wait(smem_u32(&s_full[j]), (uint32_t)(kb / kTcS) & 1u) ||
+                    !mbar_wait(smem_u32(&s_bfull[j]), (uint32_t)(kb / kTcS) & 1u)) {
                     *fail = 1;
                     break;
                 }
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t st = sbase + (uint32_t)((kb % kTcS) * kTcBTile);
-                const uint32_t a0 = taddr + (uint32_t)(kTcTiles * kTcTok + (kb % kTcS) * kTcACols + t * (kTcKB / 2));
+                tc_mma_ta(dt, at, bd, kb > 0 ? 1u : 0u);      // K 16 per MMA: 8 A columns, two k-groups of B
 #pragma unroll
-                for (int ks = 0; ks < kTcKB / 16; ks++)      // K 16 per MMA: 8 A columns, two k-groups of B
-                    tc_mma_ta(taddr + kTcTok * t, a0 + (uint32_t)(8 * ks), tc_desc(st + 2 * kTcBGroup * ks, kTcBGroup, 128),
-                              (kb > 0 || ks > 0) ? 1u : 0u);
-                tc_commit(smem_u32(&s_mdone[kb % kTcS]));
+                for (int ks = 1; ks < kTcKB / 16; ks++)
+                    tc_mma_ta(dt, at + (uint32_t)(8 * ks), bd + (uint64_t)((2 * kTcBGroup * ks) >> 4), 1u);
+                tc_commit(smem_u32(&s_mdone[j]));
                 issued = true;
             }
             // every MMA this thread issued is done before the block moves on (bounded)
@@ -1596,22 +1603,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
             }
         }
     } else if (warp == kTcTiles + 1) {
-        // activation copies: slot kb % kTcS once the MMAs of its previous use are done; the copy
-        // of stage kb - 1 is waited for after stage kb's is issued (two in flight), then reported
-        // on that stage's full barrier
+        // activation copies: slot kb % kTcS once the MMAs of its previous use are done
         if (lane == 0) {
             const uint16_t *act = GU ? p.ws.xp16 : p.ws.h16;
-            auto land = [&](int k) {          // false: the wait ran out
-                if (!mbar_wait(smem_u32(&s_bfull[k % kTcS]), (uint32_t)(k / kTcS) & 1u)) return false;
-                s_b_landed = k;
-                mbar_arrive(smem_u32(&s_full[k % kTcS]));
-                return true;
-            };
-            bool ok = true;
-            for (int kb = 0; kb < nkb && ok; kb++) {
-                if (*fail) { ok = false; break; }
+            for (int kb = 0; kb < nkb; kb++) {
+                if (*fail) break;
                 if (kb >= kTcS && !mbar_wait(smem_u32(&s_mdone[kb % kTcS]), (uint32_t)((kb - kTcS) / kTcS) & 1u)) {
-                    ok = false;
                     *fail = 1;
                     break;
                 }
@@ -1619,9 +1616,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
                 mbar_expect_tx(bar, kTcBTile);
                 bulk_load(sbase + (uint32_t)((kb % kTcS) * kTcBTile), act + tc_act_index(kb, item, cap), kTcBTile, bar);
                 s_b_issued = kb;
-                if (kb >= 1 && !land(kb - 1)) { ok = false; *fail = 1; }
             }
-            if (ok && !land(nkb - 1)) *fail = 1;
         }
     } else {
         // dequantisation: thread = weight row r = 32 (warp % 4) + lane of tile t (the warp's own
@@ -1631,23 +1626,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
         const int lr = t * 128 + 32 * (warp & 3) + lane;
         const uint32_t rrow = (uint32_t)(lr * kTcRawB), rsw = (uint32_t)((lr >> 1) & 3);
         const uint32_t tcol = taddr + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(kTcTiles * kTcTok + t * (kTcKB / 2));
-        for (int kb = 0; kb < nkb; kb++) {
-            if (__any_sync(0xffffffffu, *fail != 0)) break;
-            const int q = kb >> 1;
-            bool ok = mbar_wait(smem_u32(&s_rfull[q % kTcR]), (uint32_t)(q / kTcR) & 1u);
-            if (ok && kb >= kTcS)    // the A slot's previous stage has been consumed
-                ok = mbar_wait(smem_u32(&s_mdone[kb % kTcS]), (uint32_t)((kb - kTcS) / kTcS) & 1u);
-            if (!__all_sync(0xffffffffu, ok)) {
-                *fail = 1;
-                break;
-            }
-            // this row's 64 values -> 32 f16 pairs (mma order) -> the stage's A columns
+        // this row's 64 values of stage k -> 32 f16 pairs (mma order), once its raw slot has landed;
+        // false: the wait ran out (warp-uniform)
+        uint32_t h32[32];
+        auto convert = [&](int k) -> bool {
+            const int q = k >> 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&s_rfull[q % kTcR]), (uint32_t)(q / kTcR) & 1u)))
+                return false;
             const uint32_t rs = rbase + (uint32_t)((q % kTcR) * kTcRawSlot) + rrow;
-            const uint32_t c0 = (uint32_t)(2 * (kb & 1));
+            const uint32_t c0 = (uint32_t)(2 * (k & 1));
             const uint4 wa = lds128(rs + ((c0 ^ rsw) << 4));
             const uint4 wb = lds128(rs + (((c0 + 1) ^ rsw) << 4));
             const uint32_t w8[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
-            uint32_t h32[32];
 #pragma unroll
             for (int m = 0; m < 8; m++) {
                 uint32_t h[4];
@@ -1655,13 +1645,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
 #pragma unroll
                 for (int c = 0; c < 4; c++) h32[4 * m + c] = h[c];
             }
+            if (k & 1) {                        // both stages of raw slot q are read
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&s_rempty[q % kTcR]));
+            }
+            return true;
+        };
+        // stage kb: its pairs are already in registers; once the A slot's previous stage has been
+        // consumed they go to tensor memory and the stage is reported, then stage kb + 1 is converted
+        // (off the path from a commit to the next MMAs)
+        bool ok = convert(0);
+        if (!ok) *fail = 1;
+        for (int kb = 0; kb < nkb && ok; kb++) {
+            if (__any_sync(0xffffffffu, *fail != 0)) break;
+            if (kb >= kTcS &&
+                !__all_sync(0xffffffffu, mbar_wait(smem_u32(&s_mdone[kb % kTcS]), (uint32_t)((kb - kTcS) / kTcS) & 1u))) {
+                *fail = 1;
+                break;
+            }
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             tc_st32(tcol + (uint32_t)((kb % kTcS) * kTcACols), h32);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(smem_u32(&s_full[kb % kTcS]));
-                if (kb & 1) mbar_arrive(smem_u32(&s_rempty[q % kTcR]));   // both stages of raw slot q read
+            if (lane == 0) mbar_arrive(smem_u32(&s_full[kb % kTcS]));
+            if (kb + 1 < nkb && !convert(kb + 1)) {
+                *fail = 1;
+                break;
             }
         }
     }
@@ -1671,7 +1681,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
         // is released (every wait bounded); the MMA threads already waited for their own MMAs
         for (int q = max(0, s_r_issued - kTcR + 1); q <= s_r_issued; q++)
             mbar_wait(smem_u32(&s_rfull[q % kTcR]), (uint32_t)(q / kTcR) & 1u);
-        for (int k = s_b_landed + 1; k <= s_b_issued; k++)
+        for (int k = max(0, s_b_issued - kTcS + 1); k <= s_b_issued; k++)
             mbar_wait(smem_u32(&s_bfull[k % kTcS]), (uint32_t)(k / kTcS) & 1u);
     }
     __syncthreads();
