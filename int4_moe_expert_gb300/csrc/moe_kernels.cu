@@ -1351,21 +1351,31 @@ __global__ void __launch_bounds__(kThreads, 2) mma_expert_kernel(Params p, int T
 // accumulators in tensor memory).
 //
 // One block = one work item (a slot and up to kTcTok of its tokens) x kTcTiles
-// 128-row weight tiles, one f32 accumulator each in tensor memory (gate/up: the
-// gate rows and the up rows of 256 outputs; down: 512 output rows).  Measured on this GPU, one tcgen05.mma of M 128, K 16
-// occupies the SM's tensor core ~36 ns for any N up to 128, so the items are 128
-// tokens wide (N 128 reaches the dense f16 peak; N 32 only a quarter of it).
-// The reduction runs in stages of kTcKB elements through a kTcS-slot ring in
-// shared memory: the threads dequantise the int4 rows (loaded into registers
-// kTcKAhead stages ahead) into f16 operand tiles of the slot, the activations
-// arrive by cp.async kTcS - kTcLag stages ahead straight in the layout the tensor core
-// reads, and one thread issues kTcTiles x (kTcKB / 16) MMAs and commits them to the
-// slot's mbarrier, which frees the slot.  Operands are K-major without swizzle:
-// core matrices of 8 rows x 16 bytes, 128 bytes apart along K and
-// kTcKB / 8 * 128 bytes apart per 8 rows.  The K order inside every 8-element
-// group is the mma order of the activations (0 4 1 5 2 6 3 7), exactly the order
-// of int4x8_to_f16x2's pairs.  Every wait is bounded; a block that gives up sets
-// kErrTc and still frees its tensor memory.
+// 128-row weight tiles (gate/up: the gate rows and the up rows of 128 outputs;
+// down: 256 output rows), one 128 x 128 f32 accumulator each in tensor memory.
+// Measured on this GPU, one M 128 x K 16 MMA occupies the SM's tensor core
+// ~33-36 ns for any N up to 128, so the items are 128 tokens wide.  The
+// reduction runs in stages of kTcKB elements, each warp with one role:
+//   warps 0, 1   issue the MMAs of tile 0 / 1 (one thread each, in stage order,
+//                so every accumulator sums in a fixed order) with A, the
+//                dequantised weights, in tensor memory and B, the activations,
+//                in shared memory; each stage's two commits free its slots;
+//   warp 2       copies the block's raw int4 rows, two stages at a time, by 2-D
+//                tensor copies (64-byte rows, 64-byte swizzle) into a kTcR-slot
+//                ring;
+//   warp 3       copies a stage's activations, already in the operand layout
+//                (tc_act_index), by one contiguous bulk copy into a kTcS-slot ring;
+//   warps 4-11   dequantise: thread = weight row, 64 int4 of a stage -> 32 f16
+//                pairs -> tcgen05.st into the stage's A columns (lane = row, column
+//                c = the pair of K positions 2c, 2c + 1).
+// Full/empty mbarriers connect the roles.  The issuing thread's code between MMAs
+// is kept to one 64-bit add (measured: a single thread issues at the tensor
+// core's rate only when descriptors are precomputed).  Operands are K-major
+// without swizzle: core matrices of 8 rows x 16 bytes; the K order inside every
+// 8-element group is the mma order of the activations (0 4 1 5 2 6 3 7), exactly
+// the order of int4x8_to_f16x2's pairs.  Every wait is bounded; a block that
+// gives up sets kErrTc, waits (bounded) for its copies in flight and its MMAs,
+// and still frees its tensor memory.
 // ---------------------------------------------------------------------------
 
 constexpr int kTcTok = 128;                        // tokens of a work item on this path (MMA N)
@@ -1774,7 +1784,8 @@ inline int fmt_pair(const Dims &d) { return d.expert_fmt * 3 + (d.n_shared ? d.s
 
 constexpr bool kUseTc = true;   // int4 experts on tcgen05 for large T (else always the mma.sync kernel)
 // tcgen05 from this many tokens per call: it wins where the 128-token items are full (measured
-// on the GLM layer: gate/up 0.68 vs 0.78 ms at T 512; at T <= 64 the mma.sync kernel is faster)
+// on the GLM layer at T 512: gate/up 0.42 vs 0.78 ms, down 0.24 vs 0.40 ms against the mma.sync
+// kernel; at T <= 64 the mma.sync kernel is faster)
 constexpr int kTcMinT = 256;
 
 // Tokens of a tensor-core work item for a call of T tokens: 128 on tcgen05; on the
