@@ -377,10 +377,13 @@ def run_ours(args, rank, world, local_rank, dist_on):
     fused = T <= moe.moe_streaming_decode_max_tokens(layer.handle)
     kernel_span = kernel_span_stats(moe, cfg, copies, xs, y, T, stream, wl) if fused and T == 1 else None
     # launches per step: the fused kernel; or router, gate/up, down; or router (+ activation
-    # conversion when T > 8), gate/up, down, combine
+    # conversion when T > 8), gate/up, down, combine; the tcgen05 path (T >= 256, int4) adds the
+    # copy of the activations into its item-blocked layout
     # (T == 1 with an int8 expert runs the tensor-core flow: router, gate/up, down, combine)
     t1_tensor = T == 1 and (wl.expert_format != 0 or (wl.n_shared and wl.shared_format != 0))
-    kernels_per_step = T if fused else ((4 if t1_tensor else 3) if T == 1 else (4 if T <= 8 else 5))
+    tc5 = (T >= 256 and not fused and wl.expert_format == 0 and (not wl.n_shared or wl.shared_format == 0)
+           and bool(moe.moe_uses_tensor_cores(layer.handle)))
+    kernels_per_step = T if fused else ((4 if t1_tensor else 3) if T == 1 else (4 if T <= 8 else 5) + (1 if tc5 else 0))
     stage_ms, n_calls, event_ms = None, 0, 0.0
     if not fused:
         # Per-kernel times: the same steps again with the library recording an
@@ -445,9 +448,9 @@ def run_ours(args, rank, world, local_rank, dist_on):
     tensor = T > 1 and not fused and moe.moe_uses_tensor_cores(layer.handle)
     if tensor:
         # gate/up on the tensor cores: 2 FLOP per weight per (token, expert) pair
-        tc5 = T >= 256 and wl.expert_format == 0 and (not wl.n_shared or wl.shared_format == 0)
-        dom_name = (("tc_expert_kernel<GU>: gate/up + SwiGLU on tcgen05 (f16 operands in shared memory, "
-                     "f32 accumulators in tensor memory), T=%d") if tc5 else
+        dom_name = (("tc_expert_kernel<GU>: gate/up + SwiGLU on tcgen05 (warp-specialised: dequantised weights "
+                     "in tensor memory as A, activations by bulk copy in shared memory, f32 accumulators in "
+                     "tensor memory), T=%d") if tc5 else
                     "mma_expert_kernel<GU>: gate/up + SwiGLU on the tensor cores (mma.sync f16), T=%d") % T
         dom_flops = T * (wl.K * 4 * wl.I * wl.H + wl.n_shared * 4 * wl.I_shared * wl.H)
         tpeak, tpeak_kind = measured_tensor_peak()
@@ -537,7 +540,8 @@ def run_ours(args, rank, world, local_rank, dist_on):
                              "frac": round(achieved / peak, 4), "algorithmic_bytes_per_launch": int(dom_bytes)},
                 "note": ("peak: the measured cuBLAS bf16 rate (f16 runs at the same rate); on this GPU "
                          "mma.sync reaches ~600 TFLOP/s in a register-only loop, and one tcgen05.mma of "
-                         "M 128 x K 16 costs ~36 ns per SM for any N <= 128 (2.19 PFLOP/s at N 128)"),
+                         "M 128 x K 16 costs ~33-36 ns per SM for any N <= 128 when issued back to back "
+                         "(2.2 PFLOP/s at N 128)"),
             }
         if stage_ms is not None:
             out["stages_ms"] = {k: round(v, 6) for k, v in stage_ms.items()}

@@ -1508,14 +1508,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tc_expert_kernel(Params p, int 
     __shared__ uint32_t s_taddr;
     __shared__ int s_fail;
     __shared__ int s_r_issued, s_b_issued;   // for the bounded drain after a failure
-    const int item = blockIdx.x;
+    const int item = blockIdx.y;      // row blocks of one item run together: its activations and
+                                       // (items of one expert are adjacent) its weights stay in L2
     if (item >= *p.ws.n_items) return;
     const int slot = p.ws.items[2 * item], n0 = p.ws.items[2 * item + 1];
     const SlotInfo s = slot_info(p, T, slot);
     if (!s.valid) return;
     const int H = p.d.H, Is = s.Is;
     const int rows = GU ? Is : H;
-    const int o0 = blockIdx.y * (GU ? kTcRows / 2 : kTcRows);
+    const int o0 = blockIdx.x * (GU ? kTcRows / 2 : kTcRows);
     if (o0 >= rows) return;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nt = min(kTcTok, s.n - n0);
@@ -1802,7 +1803,7 @@ int mma_item_tokens(const Dims &d, int T) {
 template <bool GU>
 void launch_mma_phase(const Params &p, int T, dim3 grid, cudaStream_t st) {
     if (p.item_tok == kTcTok) {
-        const dim3 g(grid.x, GU ? (p.d.I_max + kTcRows / 2 - 1) / (kTcRows / 2) : (p.d.H + kTcRows - 1) / kTcRows);
+        const dim3 g(GU ? (p.d.I_max + kTcRows / 2 - 1) / (kTcRows / 2) : (p.d.H + kTcRows - 1) / kTcRows, grid.x);
         if (GU) permute_x16_kernel<<<dim3(grid.x, kTcTok / 32, kPermSlices), kThreads, 0, st>>>(p, T);
         tc_expert_kernel<GU><<<g, kTcThreads, kTcSmem, st>>>(p, T);
         return;
