@@ -168,7 +168,11 @@ typedef struct moe_handle moe_handle;
 
 /* Validates cfg and weights, allocates the handle's device workspace (sized
  * for max_tokens tokens per call) on the current device, and returns the
- * handle in *out.  On error *out is NULL and nothing stays allocated. */
+ * handle in *out.  On error *out is NULL and nothing stays allocated.  With
+ * int4 experts and max_tokens >= 256 it also encodes a tensor-copy map of
+ * every expert slab (the batched tensor-core path reads the weights through
+ * them), so the weight buffers must stay where they are while the handle
+ * lives, as for every other borrowed pointer. */
 moe_status moe_init(const moe_config *cfg, const moe_weights *w, int32_t max_tokens,
                     moe_handle **out);
 
